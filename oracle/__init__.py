@@ -1,0 +1,183 @@
+"""fp64 CPU oracle for sparse sink decode attention and its index builder.
+
+TEST INFRASTRUCTURE ONLY.  The only code that may import this package is the
+test suite (``tests/``), the smoke check in ``__graft_entry__.py`` and the
+CPU-baseline / reference leg of ``bench.py``.  The product library never
+imports, links or calls it, and it imports nothing from the product package.
+
+The arithmetic lives in ``sda_oracle.c`` (plain C, double precision, one
+OpenMP loop over (token, head)); this module only compiles it with gcc on
+first use and marshals NumPy arrays through ctypes.
+
+What it computes follows the docstring of ``paged_decode.py`` quoted on the
+sglang PR 28392 summary page ("为 AMD V4 内核添加 ATOM 来源注释", section
+"关键源码片段": caller convention, returns, numerics):
+
+    x_j = softmax_scale * <q[t,h,:], kv[S_j,:]>
+    out[t,h,:] = sum_j e^{x_j} kv[S_j,:] / (e^{sink_h} + sum_j e^{x_j})
+
+with S = kv_indices[kv_indptr[t]:kv_indptr[t+1]].  The pins that tie this to
+the pages and to mathematics, not to itself, are in ``tests/test_oracle.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sda_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_ERRORS = {1: "bad shape", 2: "bad kv_indptr", 3: "slot out of range", 4: "out of memory"}
+
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_f32p = ctypes.POINTER(ctypes.c_float)
+_f64p = ctypes.POINTER(ctypes.c_double)
+
+
+def build(force: bool = False, src: str = _SRC, dst: str = _LIB) -> str:
+    """Compile the C oracle into a shared library (gcc, -O2, OpenMP)."""
+    if not force and os.path.exists(dst) and os.path.getmtime(dst) >= os.path.getmtime(src):
+        return dst
+    tmp = dst + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, dst)
+    return dst
+
+
+def _bind(lib):
+    lib.oracle_sda_decode.restype = ctypes.c_int
+    lib.oracle_sda_decode.argtypes = [
+        _u16p, _u16p, ctypes.c_int64, _i32p, ctypes.c_int64, _i32p, _f32p, ctypes.c_float,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int, _f64p]
+    lib.oracle_build_indices.restype = ctypes.c_int
+    lib.oracle_build_indices.argtypes = [
+        _i32p, _i32p, _i32p, _i32p, _i32p, _i32p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int64, ctypes.c_int64, _i32p, ctypes.c_int64, _i32p, _i32p]
+    lib.oracle_validate_indices.restype = ctypes.c_int
+    lib.oracle_validate_indices.argtypes = [
+        _i32p, ctypes.c_int64, _i32p, ctypes.c_int, ctypes.c_int64, _i32p]
+    lib.oracle_num_threads.restype = ctypes.c_int
+    lib.oracle_num_threads.argtypes = []
+    return lib
+
+
+def load(path: str | None = None):
+    """Return the ctypes handle of the oracle library, compiling it if needed."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def _ptr(a: np.ndarray, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _as(a, dtype) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a), dtype=dtype)
+
+
+def num_threads(lib=None) -> int:
+    """Threads the oracle's OpenMP loop uses (OMP_NUM_THREADS or all cores)."""
+    return int((lib or load()).oracle_num_threads())
+
+
+def bf16_bits(x) -> np.ndarray:
+    """View a bf16 array (uint16 bit patterns or a torch bf16 tensor) as uint16."""
+    if hasattr(x, "detach"):  # torch tensor
+        import torch
+
+        x = x.detach().cpu().contiguous().view(torch.int16).numpy()
+    return _as(np.asarray(x).view(np.uint16), np.uint16)
+
+
+def sda_decode(q_bits, kv_bits, kv_indices, kv_indptr, attn_sink, softmax_scale,
+               tokens=None, lib=None) -> np.ndarray:
+    """fp64 sparse sink decode attention.
+
+    q_bits [N,H,D] and kv_bits [P,D] are bf16 bit patterns (uint16).  Returns
+    float64 [len(tokens) or N, H, D].  ``softmax_scale`` is rounded to fp32,
+    as the CUDA entry point receives it.
+    """
+    lib = lib or load()
+    q = _as(q_bits, np.uint16)
+    kv = _as(kv_bits, np.uint16)
+    N, H, D = q.shape
+    assert kv.ndim == 2 and kv.shape[1] == D
+    idx = _as(kv_indices, np.int32)
+    ptr = _as(kv_indptr, np.int32)
+    sink = _as(attn_sink, np.float32)
+    assert ptr.shape == (N + 1,) and sink.shape == (H,)
+    if tokens is None:
+        tok = None
+        n_tok = N
+    else:
+        tok = _as(tokens, np.int32)
+        n_tok = int(tok.size)
+    out = np.zeros((n_tok, H, D), dtype=np.float64)
+    idx_arg = idx if idx.size else np.zeros(1, np.int32)
+    rc = lib.oracle_sda_decode(_ptr(q, ctypes.c_uint16), _ptr(kv, ctypes.c_uint16), kv.shape[0],
+                               _ptr(idx_arg, ctypes.c_int32), idx.size, _ptr(ptr, ctypes.c_int32),
+                               _ptr(sink, ctypes.c_float), float(np.float32(softmax_scale)),
+                               N, H, D, None if tok is None else _ptr(tok, ctypes.c_int32), n_tok,
+                               _ptr(out, ctypes.c_double))
+    if rc != 0:
+        raise ValueError(f"oracle_sda_decode: {_ERRORS.get(rc, rc)}")
+    return out
+
+
+def build_indices(state_slot, swa_len, swa_head, comp_indptr, comp_block, comp_slot, win,
+                  k_per_block, swa_pages, total_pages, capacity=None, lib=None):
+    """Reference index builder.  Returns (kv_indices[:indptr[N]], kv_indptr, status)."""
+    lib = lib or load()
+    ss = _as(state_slot, np.int32)
+    N = int(ss.size)
+    sl = _as(swa_len, np.int32)
+    sh = _as(swa_head, np.int32)
+    cp = _as(comp_indptr, np.int32)
+    cb = _as(comp_block, np.int32)
+    cs = _as(comp_slot, np.int32)
+    assert cb.size == cs.size and cp.size == N + 1
+    if capacity is None:
+        capacity = N * int(win) + int(cb.size)
+    out = np.full(max(int(capacity), 1), -1, dtype=np.int32)
+    ptr = np.zeros(N + 1, dtype=np.int32)
+    st = np.zeros(1, dtype=np.int32)
+    one = np.zeros(1, np.int32)
+    rc = lib.oracle_build_indices(
+        _ptr(ss if N else one, ctypes.c_int32), _ptr(sl if N else one, ctypes.c_int32),
+        _ptr(sh if N else one, ctypes.c_int32), _ptr(cp, ctypes.c_int32),
+        _ptr(cb if cb.size else one, ctypes.c_int32), _ptr(cs if cs.size else one, ctypes.c_int32),
+        cb.size, N, int(win), int(k_per_block), int(swa_pages), int(total_pages),
+        _ptr(out, ctypes.c_int32), int(capacity), _ptr(ptr, ctypes.c_int32),
+        _ptr(st, ctypes.c_int32))
+    if rc != 0:
+        raise ValueError(f"oracle_build_indices: {_ERRORS.get(rc, rc)}")
+    return out[: ptr[N]].copy(), ptr, int(st[0])
+
+
+def validate_indices(kv_indices, kv_indptr, total_pages, lib=None):
+    """Reference index validation.  Returns (flags, n_bad_slots)."""
+    lib = lib or load()
+    idx = _as(kv_indices, np.int32)
+    ptr = _as(kv_indptr, np.int32)
+    st = np.zeros(2, dtype=np.int32)
+    one = np.zeros(1, np.int32)
+    rc = lib.oracle_validate_indices(_ptr(idx if idx.size else one, ctypes.c_int32), idx.size,
+                                     _ptr(ptr, ctypes.c_int32), ptr.size - 1, int(total_pages),
+                                     _ptr(st, ctypes.c_int32))
+    if rc != 0:
+        raise ValueError(f"oracle_validate_indices: {_ERRORS.get(rc, rc)}")
+    return int(st[0]), int(st[1])

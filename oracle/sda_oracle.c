@@ -1,0 +1,255 @@
+/*
+ * sda_oracle.c -- plain, slow, fp64 CPU oracle for sparse sink decode attention
+ * over a unified KV pool, and for the ragged index builder in front of it.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this code.  It shares nothing with the
+ * CUDA library: no header, helper, constant or table.  Status-bit values that
+ * both sides report are fixed by the documented contract, not by shared code.
+ *
+ * Sources (all from the sglang pull-request summary page "为 AMD V4 内核添加
+ * ATOM 来源注释" (sglang PR 28392), section "关键源码片段", the docstring of
+ * paged_decode.py):
+ *   - caller convention, unified_kv: one [total_pages, D] bf16 table, page
+ *     size 1; slots [0, swa_pages) are SWA entries state_slot*win + ring,
+ *     slots [swa_pages, ...) are compressed entries block_id*K_PER_BLOCK +
+ *     slot_in_block (offset by swa_pages);
+ *   - caller convention, kv_indices / kv_indptr: token t attends over
+ *     kv_indices[kv_indptr[t] : kv_indptr[t+1]]; every entry is a valid slot;
+ *     padded tokens get an empty slice;
+ *   - caller convention, attn_sink: per-head learnable softmax denominator bias;
+ *   - returns: out [N, H, D] in q's dtype (here returned in fp64);
+ *   - numerics: online softmax in the log2 domain with the sink merged as a
+ *     virtual key.  The log2 form is the same function as the natural-log form
+ *     written below (2^(x*log2 e) = e^x), so the oracle uses the plain
+ *     definition with libm exp() in double precision.
+ *
+ * Readings where the page is silent (each also listed in the design notes):
+ *   - the sink is a natural-log logit that is NOT multiplied by softmax_scale;
+ *     its value vector is zero (a "virtual key" that only adds e^sink to the
+ *     denominator);
+ *   - empty slice with a finite sink -> 0 (follows from the definition);
+ *     empty slice with sink = -inf (0/0) -> 0;
+ *   - sink = +inf -> 0 for every token;
+ *   - duplicated slots each count once per occurrence.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bf16 bit pattern -> double, exactly (bf16 is the top half of an fp32). */
+static double bf16_bits_to_double(uint16_t b) {
+  uint32_t u = ((uint32_t)b) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* Return codes of the oracle entry points. */
+#define ORACLE_OK 0
+#define ORACLE_BAD_SHAPE 1
+#define ORACLE_BAD_INDPTR 2
+#define ORACLE_BAD_SLOT 3
+#define ORACLE_NO_MEMORY 4
+
+/*
+ * Sparse decode attention with an attention sink, fp64.
+ *
+ * q           [N, H, D] bf16 bits
+ * unified_kv  [total_pages, D] bf16 bits; row s is both key and value
+ * kv_indices  [total_indices] int32
+ * kv_indptr   [N + 1] int32, non-decreasing, within [0, total_indices]
+ * attn_sink   [H] fp32 (may be +-inf)
+ * softmax_scale  fp32, applied to the q.k dot product only
+ * tokens      optional list of n_tokens token ids to evaluate (NULL = all N,
+ *             in which case n_tokens must equal N)
+ * out         [n_tokens, H, D] fp64, row i belongs to token tokens[i]
+ *
+ * For token t, head h, with S = kv_indices[kv_indptr[t] : kv_indptr[t+1]]:
+ *   x_j = softmax_scale * sum_d q[t,h,d] * kv[S_j, d]
+ *   M   = max(sink_h, max_j x_j)
+ *   Z   = e^(sink_h - M) + sum_j e^(x_j - M)
+ *   out = sum_j e^(x_j - M) * kv[S_j, :] / Z
+ * The whole input is validated first; nothing out of range is ever read.
+ */
+int oracle_sda_decode(const uint16_t* q, const uint16_t* unified_kv, int64_t total_pages,
+                      const int32_t* kv_indices, int64_t total_indices,
+                      const int32_t* kv_indptr, const float* attn_sink, float softmax_scale,
+                      int N, int H, int D, const int32_t* tokens, int n_tokens, double* out) {
+  if (N < 0 || H <= 0 || D <= 0 || total_pages <= 0 || total_indices < 0 || n_tokens < 0)
+    return ORACLE_BAD_SHAPE;
+  if (tokens == NULL && n_tokens != N) return ORACLE_BAD_SHAPE;
+  for (int t = 0; t < N; ++t) {
+    if (kv_indptr[t] < 0 || kv_indptr[t + 1] < kv_indptr[t] || kv_indptr[t + 1] > total_indices)
+      return ORACLE_BAD_INDPTR;
+  }
+  for (int i = 0; i < n_tokens; ++i) {
+    int t = tokens ? tokens[i] : i;
+    if (t < 0 || t >= N) return ORACLE_BAD_SHAPE;
+    for (int32_t e = kv_indptr[t]; e < kv_indptr[t + 1]; ++e)
+      if (kv_indices[e] < 0 || (int64_t)kv_indices[e] >= total_pages) return ORACLE_BAD_SLOT;
+  }
+  const double scale = (double)softmax_scale;
+  int failed = 0;
+
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+  for (int i = 0; i < n_tokens; ++i) {
+    for (int h = 0; h < H; ++h) {
+      const int t = tokens ? tokens[i] : i;
+      const int32_t begin = kv_indptr[t];
+      const int32_t len = kv_indptr[t + 1] - begin;
+      const double sink = (double)attn_sink[h];
+      double* o = out + ((size_t)i * H + h) * D;
+      for (int d = 0; d < D; ++d) o[d] = 0.0;
+      if (sink == INFINITY) continue;        /* reading: an infinite sink absorbs all mass */
+      double* x = (double*)malloc(sizeof(double) * (len > 0 ? len : 1));
+      if (!x) {
+#pragma omp atomic write
+        failed = 1;
+        continue;
+      }
+      const uint16_t* qh = q + ((size_t)t * H + h) * D;
+      /* logits */
+      double M = sink;
+      for (int32_t j = 0; j < len; ++j) {
+        const uint16_t* row = unified_kv + (size_t)kv_indices[begin + j] * D;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += bf16_bits_to_double(qh[d]) * bf16_bits_to_double(row[d]);
+        x[j] = scale * dot;
+        if (x[j] > M) M = x[j];
+      }
+      if (M == -INFINITY) {                  /* empty slice and sink = -inf: 0/0, reading -> 0 */
+        free(x);
+        continue;
+      }
+      /* denominator: the sink's term plus one term per listed slot */
+      double Z = exp(sink - M);
+      for (int32_t j = 0; j < len; ++j) Z += exp(x[j] - M);
+      /* numerator: probability-weighted sum of the value rows (the same rows) */
+      for (int32_t j = 0; j < len; ++j) {
+        const double w = exp(x[j] - M) / Z;
+        const uint16_t* row = unified_kv + (size_t)kv_indices[begin + j] * D;
+        for (int d = 0; d < D; ++d) o[d] += w * bf16_bits_to_double(row[d]);
+      }
+      free(x);
+    }
+  }
+  return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
+}
+
+/*
+ * Index builder: packs, per token, its SWA ring slots and its compressed-cache
+ * slots into one ragged list (the "index scatter" the same page names
+ * write_v4_paged_decode_indices; its inputs are not on the page -- reading:
+ * the plainest inputs that produce the two slot formulas of the docstring).
+ *
+ * state_slot [N]        < 0 marks a padded token (empty slice, not an error)
+ * swa_len    [N]        number of valid ring entries, 0..win
+ * swa_head   [N]        ring position of the newest entry, 0..win-1
+ * comp_indptr [N + 1]   token t's compressed entries are
+ * comp_block / comp_slot  [comp_indptr[t], comp_indptr[t+1])
+ * Emission order (reading): SWA entries oldest -> newest, ring position
+ * (swa_head - swa_len + 1 + j) mod win, as slot state_slot*win + ring; then
+ * compressed entries in input order as swa_pages + block*k_per_block + slot.
+ * Tokens with any bad field get an empty slice and raise a status bit:
+ *   1  swa_len outside [0, win]
+ *   2  swa_head outside [0, win) while swa_len > 0
+ *   4  comp_indptr decreasing, or outside [0, comp_total]
+ *   8  a compressed entry with block < 0 or slot outside [0, k_per_block)
+ *   16 an emitted slot outside its region (SWA slot >= swa_pages, or
+ *      compressed slot >= total_pages)
+ *   32 the packed list would exceed `capacity`; then every slice is empty
+ * kv_indptr[0] = 0 and kv_indptr is the prefix sum of the emitted lengths.
+ */
+int oracle_build_indices(const int32_t* state_slot, const int32_t* swa_len, const int32_t* swa_head,
+                         const int32_t* comp_indptr, const int32_t* comp_block,
+                         const int32_t* comp_slot, int64_t comp_total, int N, int win,
+                         int k_per_block, int64_t swa_pages, int64_t total_pages,
+                         int32_t* kv_indices, int64_t capacity, int32_t* kv_indptr,
+                         int32_t* status) {
+  if (N < 0 || win <= 0 || k_per_block <= 0 || swa_pages < 0 || total_pages <= 0 ||
+      swa_pages > total_pages || capacity < 0 || comp_total < 0)
+    return ORACLE_BAD_SHAPE;
+  int32_t flags = 0;
+  int64_t* len = (int64_t*)calloc((size_t)(N > 0 ? N : 1), sizeof(int64_t));
+  if (!len) return ORACLE_NO_MEMORY;
+  for (int t = 0; t < N; ++t) {
+    if (state_slot[t] < 0) continue;          /* padded token */
+    int32_t bad = 0;
+    const int32_t n_swa = swa_len[t];
+    if (n_swa < 0 || n_swa > win) bad |= 1;
+    else if (n_swa > 0 && (swa_head[t] < 0 || swa_head[t] >= win)) bad |= 2;
+    else if (n_swa > 0 && (int64_t)state_slot[t] * win + win > swa_pages) bad |= 16;
+    const int32_t c0 = comp_indptr[t], c1 = comp_indptr[t + 1];
+    if (c0 < 0 || c1 < c0 || (int64_t)c1 > comp_total) bad |= 4;
+    else {
+      for (int32_t e = c0; e < c1; ++e) {
+        if (comp_block[e] < 0 || comp_slot[e] < 0 || comp_slot[e] >= k_per_block) { bad |= 8; continue; }
+        const int64_t s = swa_pages + (int64_t)comp_block[e] * k_per_block + comp_slot[e];
+        if (s >= total_pages) bad |= 16;
+      }
+    }
+    flags |= bad;
+    if (!bad) len[t] = (int64_t)n_swa + (c1 - c0);
+  }
+  int64_t total = 0;
+  for (int t = 0; t < N; ++t) total += len[t];
+  if (total > capacity) {
+    flags |= 32;
+    for (int t = 0; t < N; ++t) len[t] = 0;
+  }
+  kv_indptr[0] = 0;
+  int64_t pos = 0;
+  for (int t = 0; t < N; ++t) {
+    if (len[t] > 0) {
+      const int32_t n_swa = swa_len[t];
+      for (int32_t j = 0; j < n_swa; ++j) {
+        const int32_t ring = (int32_t)((((int64_t)swa_head[t] - n_swa + 1 + j) % win + win) % win);
+        kv_indices[pos++] = (int32_t)((int64_t)state_slot[t] * win + ring);
+      }
+      for (int32_t e = comp_indptr[t]; e < comp_indptr[t + 1]; ++e)
+        kv_indices[pos++] = (int32_t)(swa_pages + (int64_t)comp_block[e] * k_per_block + comp_slot[e]);
+    }
+    kv_indptr[t + 1] = (int32_t)pos;
+  }
+  free(len);
+  *status = flags;
+  return ORACLE_OK;
+}
+
+/*
+ * Index validation (the docstring's requirement that every entry is a valid
+ * slot and that kv_indptr is a true prefix sum).  status[0] bits:
+ *   1 kv_indptr decreasing somewhere;  2 kv_indptr outside [0, total_indices];
+ *   4 some entry of kv_indices outside [0, total_pages).
+ * status[1] = number of entries of kv_indices[0 : total_indices] out of range.
+ */
+int oracle_validate_indices(const int32_t* kv_indices, int64_t total_indices,
+                            const int32_t* kv_indptr, int N, int64_t total_pages,
+                            int32_t* status) {
+  if (N < 0 || total_indices < 0 || total_pages <= 0) return ORACLE_BAD_SHAPE;
+  int32_t flags = 0;
+  for (int t = 0; t <= N; ++t) {
+    if (kv_indptr[t] < 0 || (int64_t)kv_indptr[t] > total_indices) flags |= 2;
+    if (t < N && kv_indptr[t + 1] < kv_indptr[t]) flags |= 1;
+  }
+  int64_t n_bad = 0;
+  for (int64_t e = 0; e < total_indices; ++e)
+    if (kv_indices[e] < 0 || (int64_t)kv_indices[e] >= total_pages) ++n_bad;
+  if (n_bad) flags |= 4;
+  status[0] = flags;
+  status[1] = (int32_t)(n_bad > INT32_MAX ? INT32_MAX : n_bad);
+  return ORACLE_OK;
+}

@@ -1,0 +1,287 @@
+"""Seeded synthetic workloads for sparse sink decode attention.
+
+This module only draws random inputs; it holds none of the attention or
+index-building arithmetic, so that both the CUDA path and the CPU oracle can
+be fed the very same inputs without sharing any of the method's code.
+
+Shapes, sizes and value distributions follow the five benchmark workloads
+of the project (tiny, H=16, ragged H=64, H=128, long-tail H=64); the
+per-workload recipe is written next to each generator.  Everything is seeded:
+index lists, q and attn_sink come from NumPy's PCG64 on the host (so they are
+identical on every machine); the big unified KV pool is drawn with torch's
+seeded generator directly on the target device (it is gigabytes) and copied
+back only where a CPU consumer needs rows of it.
+
+Per-token slot lists are drawn first; the index-builder descriptors
+(state_slot / swa_len / swa_head + compressed (block, slot) pairs) are then
+the plain inverse of how the slot ids are laid out in the pool:
+SWA slot = state_slot * win + ring, compressed slot = swa_pages +
+block * k_per_block + slot_in_block.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+import torch
+
+SEED_BASE = 20261202
+K_PER_BLOCK = 64
+WIN = 128
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    N: int
+    H: int
+    D: int
+    total_pages: int
+    softmax_scale: float
+    q: torch.Tensor              # [N, H, D] bf16 (device)
+    unified_kv: torch.Tensor     # [total_pages, D] bf16 (device)
+    attn_sink: torch.Tensor      # [H] fp32 (device)
+    kv_indices: np.ndarray       # [sum L] int32, the intended packed lists
+    kv_indptr: np.ndarray        # [N + 1] int32
+    # index-builder descriptors (host, int32)
+    state_slot: np.ndarray
+    swa_len: np.ndarray
+    swa_head: np.ndarray
+    comp_indptr: np.ndarray
+    comp_block: np.ndarray
+    comp_slot: np.ndarray
+    win: int
+    k_per_block: int
+    swa_pages: int
+    recipe: str = ""
+
+    @property
+    def lengths(self) -> np.ndarray:
+        return np.diff(self.kv_indptr)
+
+    @property
+    def total_len(self) -> int:
+        return int(self.kv_indptr[-1] - self.kv_indptr[0])
+
+    def q_bits(self) -> np.ndarray:
+        return bf16_to_bits(self.q)
+
+    def kv_rows_for(self, tokens=None):
+        """Host copy of the pool restricted to the rows the given tokens read.
+
+        Returns (kv_bits [R, D] uint16, kv_indices remapped into [0, R),
+        kv_indptr rebased for the selected tokens, token order).  Pools of at
+        most 256 MiB are copied whole (indices unchanged).
+        """
+        ptr = self.kv_indptr.astype(np.int64)
+        if tokens is None:
+            tokens = np.arange(self.N)
+        tokens = np.asarray(tokens, dtype=np.int64)
+        pieces = [self.kv_indices[ptr[t]:ptr[t + 1]] for t in tokens]
+        lens = np.array([len(p) for p in pieces], dtype=np.int64)
+        sub_idx = np.concatenate(pieces) if len(pieces) else np.zeros(0, np.int32)
+        sub_ptr = np.zeros(len(tokens) + 1, dtype=np.int32)
+        sub_ptr[1:] = np.cumsum(lens)
+        if self.unified_kv.numel() * 2 <= (256 << 20):
+            return bf16_to_bits(self.unified_kv), sub_idx.astype(np.int32), sub_ptr
+        uniq, inv = np.unique(sub_idx, return_inverse=True)
+        rows = self.unified_kv.index_select(
+            0, torch.from_numpy(uniq.astype(np.int64)).to(self.unified_kv.device))
+        return bf16_to_bits(rows), inv.astype(np.int32), sub_ptr
+
+    def builder_inputs(self, device):
+        def t(a):
+            return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+        return dict(state_slot=t(self.state_slot), swa_len=t(self.swa_len),
+                    swa_head=t(self.swa_head), comp_indptr=t(self.comp_indptr),
+                    comp_block=t(self.comp_block), comp_slot=t(self.comp_slot))
+
+
+def bf16_to_bits(x: torch.Tensor) -> np.ndarray:
+    return x.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def _to_bf16(a: np.ndarray, device) -> torch.Tensor:
+    # fp32 -> bf16 with round-to-nearest-even (torch's conversion)
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).to(device)
+
+
+def random_pool(total_pages: int, D: int, seed: int, device, chunk_rows: int = 1 << 20):
+    """[total_pages, D] bf16 ~ N(0,1) drawn with torch's seeded generator on `device`."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    out = torch.empty((total_pages, D), dtype=torch.bfloat16, device=dev)
+    for r0 in range(0, total_pages, chunk_rows):
+        r1 = min(total_pages, r0 + chunk_rows)
+        out[r0:r1] = torch.randn((r1 - r0, D), generator=g, device=dev, dtype=torch.float32)
+    return out
+
+
+def _descriptors(lists, swa_parts, swa_pages, win, kpb):
+    """Builder descriptors that reproduce `lists` (SWA part first, then compressed)."""
+    N = len(lists)
+    state_slot = np.full(N, -1, np.int32)
+    swa_len = np.zeros(N, np.int32)
+    swa_head = np.zeros(N, np.int32)
+    comp_ptr = np.zeros(N + 1, np.int64)
+    blocks, slots = [], []
+    for t, (lst, sp) in enumerate(zip(lists, swa_parts)):
+        if sp is None:                      # padded token
+            comp_ptr[t + 1] = comp_ptr[t]
+            continue
+        state, n_swa, head = sp
+        state_slot[t] = state
+        swa_len[t] = n_swa
+        swa_head[t] = head
+        comp = np.asarray(lst[n_swa:], dtype=np.int64) - swa_pages
+        b, s = np.divmod(comp, kpb)
+        blocks.append(b)
+        slots.append(s)
+        comp_ptr[t + 1] = comp_ptr[t] + len(comp)
+    cb = np.concatenate(blocks).astype(np.int32) if blocks else np.zeros(0, np.int32)
+    cs = np.concatenate(slots).astype(np.int32) if slots else np.zeros(0, np.int32)
+    return state_slot, swa_len, swa_head, comp_ptr.astype(np.int32), cb, cs
+
+
+def _ring(state, n_swa, head, win):
+    """SWA slots of one state, oldest -> newest (head = newest ring position)."""
+    pos = (head - n_swa + 1 + np.arange(n_swa)) % win
+    return state * win + pos
+
+
+def _assemble(name, N, H, D, P, lists, swa_parts, swa_pages, sink_sigma, seed, device, recipe,
+              win=WIN, kpb=K_PER_BLOCK, q_rng=None):
+    rng = q_rng
+    q = _to_bf16(rng.standard_normal((N, H, D), dtype=np.float32), device)
+    sink = torch.from_numpy((rng.standard_normal(H) * sink_sigma).astype(np.float32)).to(device)
+    lens = np.array([len(x) for x in lists], dtype=np.int64)
+    ptr = np.zeros(N + 1, np.int64)
+    ptr[1:] = np.cumsum(lens)
+    idx = (np.concatenate([np.asarray(x, np.int64) for x in lists]) if lens.sum()
+           else np.zeros(0, np.int64)).astype(np.int32)
+    desc = _descriptors(lists, swa_parts, swa_pages, win, kpb)
+    kv = random_pool(P, D, seed + 7919, device)
+    return Workload(name=name, N=N, H=H, D=D, total_pages=P, softmax_scale=1.0 / math.sqrt(D),
+                    q=q, unified_kv=kv, attn_sink=sink, kv_indices=idx,
+                    kv_indptr=ptr.astype(np.int32), state_slot=desc[0], swa_len=desc[1],
+                    swa_head=desc[2], comp_indptr=desc[3], comp_block=desc[4], comp_slot=desc[5],
+                    win=win, k_per_block=kpb, swa_pages=swa_pages, recipe=recipe)
+
+
+def tiny(device="cpu", seed=SEED_BASE + 0):
+    """N=4, H=8, D=64, pool 4096; lengths {0,1,17,64} in random order, slots
+    uniform without replacement; sink ~ N(0,1); scale 1/sqrt(D)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    N, H, D, P = 4, 8, 64, 4096
+    lens = rng.permutation(np.array([0, 1, 17, 64]))
+    lists, swa = [], []
+    for L in lens:
+        lists.append(rng.choice(P, int(L), replace=False))
+        swa.append(None if L == 0 else (0, 0, 0))
+    return _assemble("tiny N=4 H=8 D=64", N, H, D, P, lists, swa, 0, 1.0, seed, device,
+                     tiny.__doc__, q_rng=rng)
+
+
+def _swa_plus_random(rng, N, P, comp_lens, zero_tokens=()):
+    swa_pages = N * WIN
+    lists, swa = [], []
+    zero = set(int(z) for z in zero_tokens)
+    for t in range(N):
+        if t in zero:
+            lists.append(np.zeros(0, np.int64))
+            swa.append(None)
+            continue
+        head = int(rng.integers(0, WIN))
+        ring = _ring(t, WIN, head, WIN)
+        comp = swa_pages + rng.choice(P - swa_pages, int(comp_lens[t]), replace=False)
+        lists.append(np.concatenate([ring, comp]))
+        swa.append((t, WIN, head))
+    return lists, swa, swa_pages
+
+
+def h16(device="cpu", seed=SEED_BASE + 1):
+    """N=64, H=16, D=512, pool 2^20 (first 8192 slots = SWA region, 64 states x
+    win 128); each token: its 128 ring slots + 512 compressed slots uniform
+    without replacement from the rest (L=640); sink ~ N(0,1)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    N, H, D, P = 64, 16, 512, 1 << 20
+    lists, swa, swa_pages = _swa_plus_random(rng, N, P, np.full(N, 512))
+    return _assemble("N=64 H=16 D=512 L=640", N, H, D, P, lists, swa, swa_pages, 1.0, seed, device,
+                     h16.__doc__, q_rng=rng)
+
+
+def ragged_h64(device="cpu", seed=SEED_BASE + 2):
+    """N=256, H=64, D=512, pool 2^21 (SWA region 256 x 128); 26 tokens (10%,
+    seeded choice) zero-length padding; the others 128 ring slots + U{0..2048}
+    compressed slots; sink ~ N(0,1)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    N, H, D, P = 256, 64, 512, 1 << 21
+    zero = rng.choice(N, int(round(0.1 * N)), replace=False)
+    comp_lens = rng.integers(0, 2049, size=N)
+    lists, swa, swa_pages = _swa_plus_random(rng, N, P, comp_lens, zero)
+    return _assemble("N=256 H=64 D=512 ragged", N, H, D, P, lists, swa, swa_pages, 1.0, seed, device,
+                     ragged_h64.__doc__, q_rng=rng)
+
+
+def h128(device="cpu", seed=SEED_BASE + 3):
+    """N=1024, H=128, D=512, pool 2^21 (SWA region 1024 x 128); each token 128
+    ring slots + 512 random compressed slots (L=640); sink ~ N(0,1)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    N, H, D, P = 1024, 128, 512, 1 << 21
+    lists, swa, swa_pages = _swa_plus_random(rng, N, P, np.full(N, 512))
+    return _assemble("N=1024 H=128 D=512 L=640", N, H, D, P, lists, swa, swa_pages, 1.0, seed,
+                     device, h128.__doc__, q_rng=rng)
+
+
+def longtail_h64(device="cpu", seed=SEED_BASE + 4):
+    """N=512, H=64, D=512, pool 2^22 slots (4 GiB), no SWA region; L_t =
+    round(2^u), u ~ U[0,13] (log-uniform in [1, 8192]), except token 1 with
+    L=65536; even tokens read contiguous runs of 64 slots (whole compressed
+    blocks at distinct random block ids, last run truncated), odd tokens read
+    uniform random slots without replacement; sink ~ N(0, 2^2)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    N, H, D, P = 512, 64, 512, 1 << 22
+    lens = np.rint(2.0 ** rng.uniform(0.0, 13.0, size=N)).astype(np.int64)
+    lens[1] = 65536
+    lists, swa = [], []
+    n_blocks = P // K_PER_BLOCK
+    for t in range(N):
+        L = int(lens[t])
+        if t % 2 == 0:
+            nb = -(-L // K_PER_BLOCK)
+            blocks = rng.choice(n_blocks, nb, replace=False)
+            lst = (blocks[:, None] * K_PER_BLOCK + np.arange(K_PER_BLOCK)[None, :]).reshape(-1)[:L]
+        else:
+            lst = rng.choice(P, L, replace=False)
+        lists.append(lst)
+        swa.append((0, 0, 0))
+    return _assemble("N=512 H=64 D=512 long-tail", N, H, D, P, lists, swa, 0, 2.0, seed, device,
+                     longtail_h64.__doc__, q_rng=rng)
+
+
+GENERATORS = [tiny, h16, ragged_h64, h128, longtail_h64]
+CONFIG_NAMES = ["tiny", "h16", "ragged_h64", "h128", "longtail_h64"]
+
+
+def config(i: int, device="cpu") -> Workload:
+    """Workload i (0..4) with its fixed seed SEED_BASE + i."""
+    return GENERATORS[i](device=device, seed=SEED_BASE + i)
+
+
+def random_small(seed: int, N: int, H: int, D: int, P: int, lengths, sink_sigma=1.0,
+                 device="cpu", duplicates=False) -> Workload:
+    """Small random case for parity sweeps: given per-token lengths, slots drawn
+    uniformly (with replacement if `duplicates`), q/kv/sink normal."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lists, swa = [], []
+    for L in lengths:
+        L = int(L)
+        if duplicates:
+            lists.append(rng.integers(0, P, size=L))
+        else:
+            lists.append(rng.choice(P, L, replace=False))
+        swa.append((0, 0, 0))
+    return _assemble(f"random N={N} H={H} D={D}", N, H, D, P, lists, swa, 0, sink_sigma,
+                     seed, device, "random_small", q_rng=rng)

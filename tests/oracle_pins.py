@@ -1,0 +1,295 @@
+"""Pins that tie the fp64 oracle to the pages and to mathematics (CPU only).
+
+Each pin checks the oracle against something other than itself: a library
+routine (torch's scaled-dot-product attention and softmax in float64), a
+closed form, an invariant, or a hand-worked example of the slot formulas.
+The functions take an oracle library handle so that the mutation tests can
+run the same pins against deliberately broken builds of the oracle.
+
+Source of the definitions: the docstring of paged_decode.py quoted on the
+sglang PR 28392 summary page ("为 AMD V4 内核添加 ATOM 来源注释", section
+"关键源码片段"): caller convention (unified_kv, kv_indices, kv_indptr,
+attn_sink, softmax_scale), returns, numerics.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def bf16_bits(a: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def bits_to_f64(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def random_case(rng, N, H, D, P, lens, dup=False, sink_sigma=1.0):
+    q = bf16_bits(rng.standard_normal((N, H, D)))
+    kv = bf16_bits(rng.standard_normal((P, D)))
+    lists = [rng.integers(0, P, L) if dup else rng.choice(P, L, replace=False) for L in lens]
+    ptr = np.zeros(N + 1, np.int32)
+    ptr[1:] = np.cumsum([len(x) for x in lists])
+    idx = np.concatenate(lists).astype(np.int32) if ptr[-1] else np.zeros(0, np.int32)
+    sink = (rng.standard_normal(H) * sink_sigma).astype(np.float32)
+    return q, kv, idx, ptr, sink
+
+
+def sdpa_reference(q, kv, idx, ptr, sink, scale):
+    """Attention with a sink written as ordinary softmax attention (torch SDPA,
+    float64) over the listed keys plus one extra all-zero key/value row whose
+    logit is biased by attn_sink[h] through an additive mask."""
+    N, H, D = q.shape
+    qf = torch.from_numpy(bits_to_f64(q))
+    kvf = torch.from_numpy(bits_to_f64(kv))
+    sink_t = torch.from_numpy(np.asarray(sink, np.float64))
+    out = torch.zeros((N, H, D), dtype=torch.float64)
+    for t in range(N):
+        rows = kvf[torch.from_numpy(idx[ptr[t]:ptr[t + 1]].astype(np.int64))]
+        L = rows.shape[0]
+        keys = torch.cat([rows, torch.zeros(1, D, dtype=torch.float64)], 0)
+        keys = keys.unsqueeze(0).expand(H, L + 1, D)
+        mask = torch.zeros(H, 1, L + 1, dtype=torch.float64)
+        mask[:, 0, L] = sink_t
+        out[t] = F.scaled_dot_product_attention(qf[t].unsqueeze(1), keys, keys, attn_mask=mask,
+                                                scale=float(np.float32(scale)))[:, 0, :]
+    return out.numpy()
+
+
+def logits(q, kv, idx, ptr, t, h, scale):
+    rows = bits_to_f64(kv[idx[ptr[t]:ptr[t + 1]]])
+    return float(np.float32(scale)) * rows @ bits_to_f64(q[t, h])
+
+
+# ----------------------------------------------------------------------------- pins
+def pin_sdpa(lib):
+    """Random small cases (empty, short and full-tile lists) vs torch SDPA fp64."""
+    rng = np.random.default_rng(11)
+    for N, H, D, P in [(1, 1, 8, 50), (4, 3, 16, 300), (6, 8, 64, 4096), (3, 2, 128, 900)]:
+        lens = rng.integers(0, 70, N)
+        lens[0] = 0
+        q, kv, idx, ptr, sink = random_case(rng, N, H, D, P, lens)
+        scale = rng.uniform(0.05, 0.5)
+        got = oracle.sda_decode(q, kv, idx, ptr, sink, scale, lib=lib)
+        ref = sdpa_reference(q, kv, idx, ptr, sink, scale)
+        np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def pin_sink_minus_inf_is_softmax(lib):
+    """attn_sink -> -inf reduces to ordinary softmax attention (torch.softmax)."""
+    rng = np.random.default_rng(12)
+    N, H, D, P = 3, 4, 32, 500
+    q, kv, idx, ptr, _ = random_case(rng, N, H, D, P, [5, 40, 1])
+    sink = np.full(H, -np.inf, np.float32)
+    scale = 0.2
+    got = oracle.sda_decode(q, kv, idx, ptr, sink, scale, lib=lib)
+    for t in range(N):
+        v = torch.from_numpy(bits_to_f64(kv[idx[ptr[t]:ptr[t + 1]]]))
+        for h in range(H):
+            x = torch.from_numpy(logits(q, kv, idx, ptr, t, h, scale))
+            ref = torch.softmax(x, 0) @ v
+            np.testing.assert_allclose(got[t, h], ref.numpy(), rtol=0, atol=1e-12)
+
+
+def pin_single_slot(lib):
+    """One slot: out = v * e^x / (e^x + e^sink) = v * logistic(x - sink)."""
+    rng = np.random.default_rng(13)
+    N, H, D, P = 5, 6, 64, 256
+    q, kv, idx, ptr, sink = random_case(rng, N, H, D, P, [1] * N, sink_sigma=2.0)
+    scale = 0.125
+    got = oracle.sda_decode(q, kv, idx, ptr, sink, scale, lib=lib)
+    for t in range(N):
+        v = bits_to_f64(kv[idx[ptr[t]]])
+        for h in range(H):
+            x = logits(q, kv, idx, ptr, t, h, scale)[0]
+            w = 1.0 / (1.0 + math.exp(float(sink[h]) - x))
+            np.testing.assert_allclose(got[t, h], w * v, rtol=1e-13, atol=1e-14)
+
+
+def pin_duplicate_adds_ln2(lib):
+    """A slot listed twice weighs like one occurrence with its logit + ln 2."""
+    rng = np.random.default_rng(14)
+    D, P, H = 32, 100, 3
+    q = bf16_bits(rng.standard_normal((1, H, D)))
+    kv = bf16_bits(rng.standard_normal((P, D)))
+    sink = rng.standard_normal(H).astype(np.float32)
+    s = 17
+    idx = np.array([s, s], np.int32)
+    ptr = np.array([0, 2], np.int32)
+    scale = 0.3
+    got = oracle.sda_decode(q, kv, idx, ptr, sink, scale, lib=lib)
+    v = bits_to_f64(kv[s])
+    for h in range(H):
+        x = logits(q, kv, idx[:1], np.array([0, 1], np.int32), 0, h, scale)[0]
+        w = 1.0 / (1.0 + math.exp(float(sink[h]) - (x + math.log(2.0))))
+        np.testing.assert_allclose(got[0, h], w * v, rtol=1e-13, atol=1e-14)
+
+
+def pin_zero_length(lib):
+    """Empty slice -> exactly +0.0, with a finite sink and with sink = -inf."""
+    rng = np.random.default_rng(15)
+    q, kv, idx, ptr, sink = random_case(rng, 3, 4, 16, 64, [0, 3, 0])
+    sink[1] = -np.inf
+    out = oracle.sda_decode(q, kv, idx, ptr, sink, 0.25, lib=lib)
+    assert np.all(out[0] == 0.0) and np.all(out[2] == 0.0)
+    assert not np.signbit(out[0]).any()
+
+
+def pin_permutation(lib):
+    """Order within a token's list does not change the result."""
+    rng = np.random.default_rng(16)
+    q, kv, idx, ptr, sink = random_case(rng, 2, 4, 64, 2000, [200, 37])
+    a = oracle.sda_decode(q, kv, idx, ptr, sink, 0.125, lib=lib)
+    idx2 = idx.copy()
+    for t in range(2):
+        idx2[ptr[t]:ptr[t + 1]] = rng.permutation(idx[ptr[t]:ptr[t + 1]])
+    b = oracle.sda_decode(q, kv, idx2, ptr, sink, 0.125, lib=lib)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
+
+
+def pin_sink_factor(lib):
+    """out(sink) = out(-inf) * Zk / (Zk + e^sink), Zk = sum_j e^{x_j}."""
+    rng = np.random.default_rng(17)
+    q, kv, idx, ptr, sink = random_case(rng, 2, 3, 32, 400, [9, 50])
+    scale = 0.2
+    with_sink = oracle.sda_decode(q, kv, idx, ptr, sink, scale, lib=lib)
+    no_sink = oracle.sda_decode(q, kv, idx, ptr, np.full(3, -np.inf, np.float32), scale, lib=lib)
+    for t in range(2):
+        for h in range(3):
+            x = logits(q, kv, idx, ptr, t, h, scale)
+            zk = np.exp(x).sum()
+            f = zk / (zk + math.exp(float(sink[h])))
+            np.testing.assert_allclose(with_sink[t, h], no_sink[t, h] * f, rtol=1e-12, atol=1e-14)
+
+
+def pin_scale_zero(lib):
+    """softmax_scale = 0: every logit is 0, out = sum_j v_j / (L + e^sink)."""
+    rng = np.random.default_rng(18)
+    q, kv, idx, ptr, sink = random_case(rng, 2, 2, 16, 300, [4, 33])
+    got = oracle.sda_decode(q, kv, idx, ptr, sink, 0.0, lib=lib)
+    for t in range(2):
+        v = bits_to_f64(kv[idx[ptr[t]:ptr[t + 1]]])
+        L = v.shape[0]
+        for h in range(2):
+            ref = v.sum(0) / (L + math.exp(float(sink[h])))
+            np.testing.assert_allclose(got[t, h], ref, rtol=1e-13, atol=1e-14)
+
+
+def pin_convexity(lib):
+    """Weights are non-negative and sum to < 1: |out| <= max_j |kv[S_j, d]|."""
+    rng = np.random.default_rng(19)
+    q, kv, idx, ptr, sink = random_case(rng, 4, 4, 64, 3000, [1, 10, 100, 640])
+    got = oracle.sda_decode(q, kv, idx, ptr, sink, 1 / 8, lib=lib)
+    for t in range(4):
+        bound = np.abs(bits_to_f64(kv[idx[ptr[t]:ptr[t + 1]]])).max(0)
+        assert np.all(np.abs(got[t]) <= bound[None, :] + 1e-12)
+
+
+def pin_hard_attention_limit(lib):
+    """Huge scale: the softmax becomes an argmax; with sink -inf out -> v_argmax."""
+    rng = np.random.default_rng(20)
+    q, kv, idx, ptr, _ = random_case(rng, 1, 2, 16, 200, [12])
+    sink = np.full(2, -np.inf, np.float32)
+    got = oracle.sda_decode(q, kv, idx, ptr, sink, 1e4, lib=lib)
+    for h in range(2):
+        x = logits(q, kv, idx, ptr, 0, h, 1e4)
+        j = int(np.argmax(x))
+        np.testing.assert_allclose(got[0, h], bits_to_f64(kv[idx[j]]), rtol=0, atol=1e-12)
+
+
+def pin_sink_plus_inf(lib):
+    """sink = +inf absorbs all the mass (reading): out = 0."""
+    rng = np.random.default_rng(21)
+    q, kv, idx, ptr, sink = random_case(rng, 2, 2, 16, 100, [3, 0])
+    sink[:] = np.inf
+    assert np.all(oracle.sda_decode(q, kv, idx, ptr, sink, 0.5, lib=lib) == 0.0)
+
+
+def pin_token_subset(lib):
+    """Evaluating a subset of tokens gives exactly the same rows."""
+    rng = np.random.default_rng(22)
+    q, kv, idx, ptr, sink = random_case(rng, 5, 2, 16, 100, [3, 0, 7, 1, 9])
+    full = oracle.sda_decode(q, kv, idx, ptr, sink, 0.5, lib=lib)
+    sub = oracle.sda_decode(q, kv, idx, ptr, sink, 0.5, tokens=[4, 0, 2], lib=lib)
+    assert np.array_equal(sub, full[[4, 0, 2]])
+
+
+def read_golden_builder():
+    vals = {}
+    with open(os.path.join(GOLDEN, "build_indices_example.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            k, v = line.split(":", 1)
+            vals[k.strip()] = [int(x) for x in v.split()]
+    return vals
+
+
+def pin_builder_golden(lib):
+    """Hand-worked example of the two slot formulas (golden fixture)."""
+    g = read_golden_builder()
+    idx, ptr, st = oracle.build_indices(
+        g["state_slot"], g["swa_len"], g["swa_head"], g["comp_indptr"], g["comp_block"],
+        g["comp_slot"], g["win"][0], g["k_per_block"][0], g["swa_pages"][0], g["total_pages"][0],
+        lib=lib)
+    assert idx.tolist() == g["kv_indices"], (idx.tolist(), g["kv_indices"])
+    assert ptr.tolist() == g["kv_indptr"]
+    assert st == g["status"][0]
+
+
+def pin_builder_ring_closed_form(lib):
+    """A full ring with newest entry at `head` lists the state's win slots, oldest
+    first: state*win + (head+1), ..., state*win + head (mod win)."""
+    win, N = 8, 5
+    heads = np.array([0, 3, 7, 5, 1], np.int32)
+    idx, ptr, st = oracle.build_indices(np.arange(N), np.full(N, win), heads, np.zeros(N + 1),
+                                        [], [], win, 4, N * win, N * win, lib=lib)
+    assert st == 0 and ptr.tolist() == [0, 8, 16, 24, 32, 40]
+    for t in range(N):
+        expect = [t * win + (heads[t] + 1 + j) % win for j in range(win)]
+        assert idx[ptr[t]:ptr[t + 1]].tolist() == expect
+
+
+def pin_builder_capacity(lib):
+    """Over-capacity output: status bit 32 and every slice empty."""
+    idx, ptr, st = oracle.build_indices([0, 1], [2, 2], [1, 1], [0, 0, 0], [], [], 4, 4, 8, 8,
+                                        capacity=3, lib=lib)
+    assert st == 32 and ptr.tolist() == [0, 0, 0] and idx.size == 0
+
+
+def pin_validate(lib):
+    """Validation flags: decreasing indptr, indptr out of range, bad slots (counted)."""
+    assert oracle.validate_indices([0, 1, 2], [0, 1, 3], 3, lib=lib) == (0, 0)
+    assert oracle.validate_indices([0, 5, 2, -1], [0, 2, 4], 3, lib=lib) == (4, 2)
+    assert oracle.validate_indices([0, 1], [0, 2, 1], 3, lib=lib) == (1, 0)
+    assert oracle.validate_indices([0, 1], [0, 3], 3, lib=lib) == (2, 0)
+    assert oracle.validate_indices([2, 3], [0, 2], 3, lib=lib) == (4, 1)  # slot == total_pages
+
+
+DECODE_PINS = [pin_sdpa, pin_sink_minus_inf_is_softmax, pin_single_slot, pin_duplicate_adds_ln2,
+               pin_zero_length, pin_permutation, pin_sink_factor, pin_scale_zero, pin_convexity,
+               pin_hard_attention_limit, pin_sink_plus_inf, pin_token_subset]
+BUILDER_PINS = [pin_builder_golden, pin_builder_ring_closed_form, pin_builder_capacity]
+VALIDATE_PINS = [pin_validate]
+ALL_PINS = DECODE_PINS + BUILDER_PINS + VALIDATE_PINS
+
+
+def failing_pins(lib, pins=ALL_PINS):
+    """Names of the pins that fail (any exception counts) for this oracle build."""
+    bad = []
+    for p in pins:
+        try:
+            p(lib)
+        except Exception:  # noqa: BLE001 - a failing pin is the signal
+            bad.append(p.__name__)
+    return bad
