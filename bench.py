@@ -1,0 +1,402 @@
+"""Benchmark of the sparse sink decode attention hot path on one GB300.
+
+One step = the whole hot path over one batch: the index build
+(sda_build_indices: SWA ring slots + compressed slots -> ragged kv_indices)
+followed by the decode (sda_decode: device-side split plan, tensor-core
+attention kernel, log-sum-exp combine), replayed as one CUDA graph.
+
+Prints ONE JSON line.  Default workload: N=64 tokens, H=16, D=512, 640 slots
+per token (128 SWA ring slots + 512 random compressed slots) over a 2^20-slot
+pool.  `--config` picks another of the five workloads.
+
+  value     decode tokens/s with inputs resident in HBM (graph replays,
+            CUDA events, L2 flushed between steps)
+  e2e       the same metric through the public API from pinned host
+            buffers: H2D of q + index descriptors, build + decode, D2H of out
+  roofline  the attention kernel alone (events recorded around it by the
+            library's timing hook): algorithmic bytes / time vs measured HBM
+  cpu_baseline  the fp64 CPU oracle on the host cores (bounded sample)
+
+--impl reference times the fp64 CPU oracle instead (same config and metric).
+Under torchrun (N>1 GPUs) every rank runs its own copy of the workload
+(tokens are independent: weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from sink_sda_decode_gb300 import inputs  # noqa: E402
+
+METRIC = "decode tokens/s and gathered-KV GB/s; % of binding roofline (HBM vs bf16)"
+DEFAULT_CONFIG = 1
+L2_FLUSH_BYTES = 256 << 20
+HBM_FALLBACK_GBS = 6800.0
+BF16_FALLBACK_TFLOPS = 1900.0
+
+
+# ----------------------------------------------------------------------------- helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return HBM_FALLBACK_GBS, BF16_FALLBACK_TFLOPS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sink_sda_decode_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(config_name):
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary, only if it was taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(config_name)
+        if e and e.get("kernel_sources") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during timing."""
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def algorithmic_bytes(w):
+    """Bytes the method must move per decode: gathered KV rows + q + out +
+    kv_indices + kv_indptr."""
+    L = int(w.total_len)
+    return L * w.D * 2 + 2 * w.N * w.H * w.D * 2 + L * 4 + (w.N + 1) * 4
+
+
+def algorithmic_flops(w):
+    return 4 * w.H * w.D * int(w.total_len)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+class Step:
+    """Device-resident inputs and buffers of one hot-path step."""
+
+    def __init__(self, w, device):
+        import sink_sda_decode_gb300 as sda
+        self.sda = sda
+        self.w = w
+        self.dev = device
+        self.bi = w.builder_inputs(device)
+        self.capacity = w.N * w.win + int(w.comp_block.size)
+        self.kv_indices = torch.empty(max(self.capacity, 1), dtype=torch.int32, device=device)
+        self.kv_indptr = torch.empty(w.N + 1, dtype=torch.int32, device=device)
+        self.status = torch.empty(1, dtype=torch.int32, device=device)
+        self.out = torch.empty_like(w.q)
+        self.ws = torch.empty(sda.workspace_size(w.N, w.H, w.D, self.capacity), dtype=torch.uint8,
+                              device=device)
+
+    def run(self, q=None, bi=None, out=None, stream=None):
+        w = self.w
+        bi = bi or self.bi
+        self.sda.build_indices(**bi, win=w.win, k_per_block=w.k_per_block, swa_pages=w.swa_pages,
+                               total_pages=w.total_pages, capacity=self.capacity,
+                               kv_indices=self.kv_indices, kv_indptr=self.kv_indptr,
+                               status=self.status, stream=stream)
+        self.sda.decode(q if q is not None else w.q, w.unified_kv, self.kv_indices, self.kv_indptr,
+                        w.attn_sink, w.softmax_scale, out=self.out if out is None else out,
+                        workspace=self.ws, stream=stream)
+
+    # kernels of this library launched per step: 3 (index build) + plan + attention + combine
+    launches_per_step = 6
+
+
+def gpu_arm(args, w, device, ws, rank):
+    step = Step(w, device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(s):
+        for _ in range(max(args.warmup, 3)):
+            step.run(stream=s)
+    torch.cuda.current_stream(device).wait_stream(s)
+    torch.cuda.synchronize(device)
+    st = int(step.status.item())
+    if st != 0:
+        raise RuntimeError(f"index builder status {st}")
+    # whole step as one CUDA graph
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step.run(stream=s)
+    torch.cuda.synchronize(device)
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(device)
+
+    # ---- timed region 1: K graph replays, L2 flushed before each step
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    barrier()
+    with ClockSampler(torch.cuda.current_device() if device.index is None else device.index) as cs:
+        with torch.cuda.stream(s):
+            for a, b in evs:
+                flush.zero_()
+                a.record(s)
+                g.replay()
+                b.record(s)
+        barrier()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    ms_per_step = sum(step_ms) / len(step_ms)
+
+    # ---- timed region 2: the attention kernel alone (library timing hook)
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    barrier()
+    with torch.cuda.stream(s):
+        for a, b in kev:
+            flush.zero_()
+            step.sda.set_timing_events(a, b)
+            step.run(stream=s)
+        step.sda.set_timing_events(None, None)
+    barrier()
+    kernel_ms = sum(a.elapsed_time(b) for a, b in kev) / len(kev)
+
+    # ---- timed region 3: end to end from pinned host buffers
+    q_h = w.q.cpu().pin_memory()
+    bi_h = {k: v.cpu().pin_memory() for k, v in step.bi.items()}
+    out_h = torch.empty(w.q.shape, dtype=w.q.dtype, pin_memory=True)
+    h2d = q_h.numel() * q_h.element_size() + sum(v.numel() * v.element_size() for v in bi_h.values())
+    d2h = out_h.numel() * out_h.element_size()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    barrier()
+    with torch.cuda.stream(s):
+        for a, b in e2e_ev:
+            flush.zero_()
+            a.record(s)
+            q_d = q_h.to(device, non_blocking=True)
+            bi_d = {k: v.to(device, non_blocking=True) for k, v in bi_h.items()}
+            step.run(q=q_d, bi=bi_d, stream=s)
+            out_h.copy_(step.out, non_blocking=True)
+            b.record(s)
+    barrier()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / len(e2e_ev)
+    return dict(ms_per_step=ms_per_step, kernel_ms=kernel_ms, e2e_ms=e2e_ms, clocks=cs.summary(),
+                h2d=h2d, d2h=d2h, step=step)
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_inputs(w, tokens):
+    kv_bits, sub_idx, sub_ptr = w.kv_rows_for(tokens)
+    q_bits = w.q_bits()[np.asarray(tokens)]
+    return q_bits, kv_bits, sub_idx, sub_ptr, w.attn_sink.cpu().numpy()
+
+
+def oracle_sample(w, budget_tokens):
+    """Deterministic token sample whose slot count is about budget_tokens x mean L."""
+    rng = np.random.default_rng(0)
+    k = max(1, min(w.N, budget_tokens))
+    return np.sort(rng.choice(w.N, k, replace=False))
+
+
+def time_oracle(w, seconds, max_tokens):
+    import oracle
+    toks = oracle_sample(w, max_tokens)
+    args = oracle_inputs(w, toks)
+    done_tokens, t0 = 0, time.perf_counter()
+    passes = 0
+    while True:
+        oracle.sda_decode(*args, w.softmax_scale)
+        done_tokens += len(toks)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return done_tokens / el, oracle.num_threads(), toks, passes, el
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--config", default=inputs.CONFIG_NAMES[DEFAULT_CONFIG],
+                    choices=inputs.CONFIG_NAMES)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    ws, rank, local = dist_env()
+    cfg_idx = inputs.CONFIG_NAMES.index(args.config)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        w = inputs.config(cfg_idx, device="cuda" if torch.cuda.is_available() else "cpu")
+        import oracle
+        toks = oracle_sample(w, 16 if w.total_len > 200000 else w.N)
+        oargs = oracle_inputs(w, toks)
+        for _ in range(args.warmup):
+            oracle.sda_decode(*oargs, w.softmax_scale)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            oracle.sda_decode(*oargs, w.softmax_scale)
+        el = time.perf_counter() - t0
+        tps = len(toks) * args.steps / el
+        sample = f"{len(toks)} of {w.N} tokens per step"
+        line = {"metric": METRIC, "value": tps, "unit": "tokens/s", "impl": "reference",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": w.name, "N": w.N, "H": w.H, "D": w.D,
+                           "total_slots": w.total_len},
+                "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": oracle.num_threads(),
+                                 "kind": "oracle", "sample": sample},
+                "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if ws > 1:
+        torch.distributed.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    w = inputs.config(cfg_idx, device=device)
+    r = gpu_arm(args, w, device, ws, rank)
+
+    ms = torch.tensor([r["ms_per_step"], r["kernel_ms"], r["e2e_ms"]], device=device)
+    if ws > 1:
+        torch.distributed.all_reduce(ms, op=torch.distributed.ReduceOp.MAX)
+    ms_step, ms_kernel, ms_e2e = (float(x) for x in ms.cpu())
+    if rank != 0:
+        torch.distributed.destroy_process_group()
+        return
+
+    hbm, bf16, peak_src = peaks()
+    nbytes = algorithmic_bytes(w)
+    flops = algorithmic_flops(w)
+    tokens_total = w.N * ws
+    value = tokens_total / (ms_step * 1e-3)
+    achieved = nbytes / (ms_kernel * 1e-3) / 1e9
+    t_hbm = nbytes / (hbm * 1e9)
+    t_tc = flops / (bf16 * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "N": w.N, "H": w.H, "D": w.D,
+                   "total_slots": int(w.total_len), "pool_slots": w.total_pages,
+                   "step": "index build + decode (plan, attention, combine) as one CUDA graph",
+                   "l2": "flushed before every timed step (256 MiB write)",
+                   "parallelism": f"dp{ws} (independent token batches)"},
+        "gathered_kv_gbs": int(w.total_len) * w.D * 2 / (ms_step * 1e-3) / 1e9,
+        "roofline": {"bound": bound, "achieved": achieved,
+                     "peak": hbm if bound == "hbm" else bf16,
+                     "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+                     "frac": achieved / (hbm if bound == "hbm" else bf16),
+                     "traffic": ncu_traffic(args.config), "peak_source": peak_src,
+                     "kernel": "sda decode attention kernel", "kernel_ms": ms_kernel,
+                     "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+                     "step_frac_of_roofline": max(t_hbm, t_tc) / (ms_step * 1e-3)},
+        "e2e": {"value": tokens_total / (ms_e2e * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": Step.launches_per_step * args.steps,
+        "clocks": r["clocks"],
+    }
+    if not args.no_cpu_baseline and ws == 1:
+        tps, cores, toks, passes, el = time_oracle(w, args.cpu_seconds,
+                                                   16 if w.total_len > 200000 else w.N)
+        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": f"{len(toks)} of {w.N} tokens x {passes} passes, "
+                                          f"{el:.1f} s"}
+    print(json.dumps(line))
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,166 @@
+/*
+ * sda.h -- C ABI of libsda: sparse decode attention with a per-head attention
+ * sink over a unified KV pool, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the one documented by the docstring of paged_decode.py,
+ * quoted on the sglang PR 28392 summary page ("为 AMD V4 内核添加 ATOM 来源注释",
+ * section "关键源码片段"): caller convention, returns and numerics.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor arguments are raw DEVICE pointers into memory the caller
+ *     owns (e.g. torch tensors' data_ptr()).  The library never allocates,
+ *     frees or keeps them.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Every call only enqueues work on that stream: there is no
+ *     host synchronisation, no device-to-host read and no allocation, so the
+ *     calls can be captured into a CUDA graph.
+ *   - Host-side argument checks happen before anything is enqueued; on
+ *     failure nothing is enqueued and an error code is returned.
+ *     SDA_ERR_CUDA means a launch failed (cudaGetLastError() was not
+ *     cudaSuccess); the message is in sda_last_cuda_error().
+ *   - Errors found on the device never trap: they are written to status
+ *     words that the caller reads when it chooses.
+ */
+#ifndef SDA_H_
+#define SDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sda_status {
+  SDA_OK = 0,
+  SDA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer        */
+  SDA_ERR_UNSUPPORTED = 2, /* (H, D) outside the supported set                  */
+  SDA_ERR_CUDA = 3,        /* a CUDA call or launch failed                       */
+  SDA_ERR_WORKSPACE = 4    /* workspace smaller than sda_decode_workspace_size() */
+} sda_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* sda_strerror(sda_status status);
+
+/* Text of the last CUDA error seen by this library on the calling thread
+ * ("" if none).  Static thread-local storage; never NULL. */
+const char* sda_last_cuda_error(void);
+
+/* ABI version of this header (bumped on any signature change). */
+int sda_abi_version(void);
+
+/*
+ * Bytes of device workspace sda_decode needs for a call with these sizes on
+ * the CURRENT device (it depends on the device's SM count, which fixes how
+ * long token lists are split across CTAs).  Writes the size to *bytes.
+ * total_indices is the length of kv_indices.  Returns SDA_ERR_UNSUPPORTED for
+ * an (H, D) that sda_decode rejects, SDA_ERR_CUDA if no device is usable.
+ */
+sda_status sda_decode_workspace_size(int N, int H, int D, int64_t total_indices, size_t* bytes);
+
+/*
+ * Sparse decode attention with an attention sink (paged_decode.py docstring:
+ * caller convention, returns, numerics).
+ *
+ *   q            [N, H, D] bf16, contiguous, 16-byte aligned.
+ *   unified_kv   [total_pages, D] bf16, contiguous, 16-byte aligned; one row
+ *                (page size 1) is both the key and the value of a slot.
+ *                0 < total_pages < 2^31.
+ *   kv_indices   [total_indices] int32.  Token t attends over
+ *                kv_indices[kv_indptr[t] : kv_indptr[t+1]].  CONTRACT: every
+ *                entry inside those slices is a valid slot in
+ *                [0, total_pages) -- the kernels do not bounds-check slots
+ *                (check with sda_validate_indices when in doubt).
+ *   kv_indptr    [N + 1] int32, non-decreasing, within [0, total_indices];
+ *                kv_indptr[0] need not be 0.  A padded token has an empty
+ *                slice (kv_indptr[t+1] == kv_indptr[t]) and gets out = 0.
+ *   attn_sink    [H] fp32: per-head sink logit (natural-log units, not scaled
+ *                by softmax_scale); it adds e^sink to the softmax denominator
+ *                as a key whose value is zero.  May be -inf (no sink).
+ *   softmax_scale  multiplies q.k before the softmax.
+ *   out          [N, H, D] bf16 (q's dtype), written with round-to-nearest-
+ *                even; must not overlap the inputs.
+ *   workspace    device scratch of at least sda_decode_workspace_size()
+ *                bytes, 256-byte aligned; its contents need no
+ *                initialisation and are overwritten.  Two calls in flight
+ *                at the same time must use different workspaces.
+ *
+ * Supported: D in {64, 128, 256, 512}, 1 <= H <= 256 (D = 512 with
+ * H in {16, 32, 64, 128, 192, 256} takes the tensor-core path).
+ * N = 0 is a no-op.  Softmax is computed online in the log2 domain in fp32.
+ */
+sda_status sda_decode(const void* q, const void* unified_kv, int64_t total_pages,
+                      const int32_t* kv_indices, int64_t total_indices,
+                      const int32_t* kv_indptr, const float* attn_sink, float softmax_scale,
+                      int N, int H, int D, void* out, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
+/*
+ * Device-side error word of the last sda_decode that used `workspace`:
+ * copies one int32 (0 = fine, nonzero = a pipeline wait timed out and the
+ * affected outputs are unspecified) into *device_flag (device memory),
+ * ordered on `stream`.
+ */
+sda_status sda_decode_error_flag(const void* workspace, int32_t* device_flag, void* stream);
+
+/*
+ * Timing hook.  When both events are non-NULL, every later sda_decode made
+ * from the calling host thread records `before` on its stream immediately
+ * before its attention kernel and `after` immediately after it, so that the
+ * caller can time that kernel alone (cudaEventElapsedTime).  The events are
+ * cudaEvent_t handles created and owned by the caller.  NULL, NULL turns the
+ * hook off.  No effect on results.
+ */
+sda_status sda_set_timing_events(void* before, void* after);
+
+/*
+ * Index builder (the decode index scatter the docstring calls
+ * write_v4_paged_decode_indices; its inputs are not on the page, these are
+ * the plainest inputs that produce its two slot formulas).  Per token t:
+ *   - state_slot[t] < 0: padded token, empty slice (not an error);
+ *   - otherwise swa_len[t] SWA slots, oldest -> newest, ring position
+ *     (swa_head[t] - swa_len[t] + 1 + j) mod win, emitted as
+ *     state_slot[t] * win + ring;
+ *   - then its compressed entries e in [comp_indptr[t], comp_indptr[t+1]),
+ *     in input order, emitted as swa_pages + comp_block[e] * k_per_block +
+ *     comp_slot[e].
+ * kv_indptr [N + 1] receives the prefix sum (kv_indptr[0] = 0) and
+ * kv_indices [capacity] the packed slots.  All arrays are int32 device
+ * memory.  A token with a bad field gets an empty slice and sets bits of
+ * *status (device int32, overwritten):
+ *   1  swa_len outside [0, win]
+ *   2  swa_head outside [0, win) while swa_len > 0
+ *   4  comp_indptr decreasing or outside [0, comp_total]
+ *   8  a compressed entry with block < 0 or slot outside [0, k_per_block)
+ *   16 a slot outside its region (state_slot*win + win > swa_pages, or a
+ *      compressed slot >= total_pages)
+ *   32 the packed lists exceed `capacity`: then every slice is empty
+ * So every emitted slot is valid for sda_decode by construction.
+ * Host errors (SDA_ERR_INVALID_ARG): N < 0, win <= 0, k_per_block <= 0,
+ * swa_pages < 0, total_pages outside (0, 2^31), swa_pages > total_pages,
+ * capacity < 0 or > 2^31 - 1, a null pointer that would be read.
+ */
+sda_status sda_build_indices(const int32_t* state_slot, const int32_t* swa_len,
+                             const int32_t* swa_head, const int32_t* comp_indptr,
+                             const int32_t* comp_block, const int32_t* comp_slot,
+                             int64_t comp_total, int N, int win, int k_per_block,
+                             int64_t swa_pages, int64_t total_pages, int32_t* kv_indices,
+                             int64_t capacity, int32_t* kv_indptr, int32_t* status,
+                             void* stream);
+
+/*
+ * Checks the docstring's index contract on the device.  status [2] int32
+ * device memory receives: status[0] bits 1 = kv_indptr decreasing somewhere,
+ * 2 = kv_indptr outside [0, total_indices], 4 = some entry of
+ * kv_indices[0 : total_indices] outside [0, total_pages); status[1] = the
+ * number of such entries.
+ */
+sda_status sda_validate_indices(const int32_t* kv_indices, int64_t total_indices,
+                                const int32_t* kv_indptr, int N, int64_t total_pages,
+                                int32_t* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDA_H_ */

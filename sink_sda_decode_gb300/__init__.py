@@ -1,0 +1,194 @@
+"""Sparse decode attention with an attention sink over a unified KV pool (GB300).
+
+Thin Python binding of the C ABI in include/sda.h (libsda.so, built in this
+package directory).  The functions only check and marshal arguments: torch is
+used for device memory and streams, and every step of the computation runs in
+the library's CUDA kernels.  There is no CPU or PyTorch fallback; calling
+without the built library raises.
+
+    out = decode(q, unified_kv, kv_indices, kv_indptr, attn_sink, softmax_scale)
+
+computes, for every token t and head h, attention of q[t, h] over the rows
+unified_kv[kv_indices[kv_indptr[t]:kv_indptr[t+1]]] (each row is key and
+value), with attn_sink[h] as a key of value zero; see decode() for details.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+__all__ = ["decode", "workspace_size", "build_indices", "validate_indices", "decode_error_flag",
+           "decode_host", "set_timing_events", "library_path"]
+
+library_path = _lib.LIB_PATH
+
+
+def _stream_ptr(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _req(t: torch.Tensor, name: str, dtype, ndim=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def workspace_size(N: int, H: int, D: int, total_indices: int) -> int:
+    """Bytes of workspace decode() needs on the current CUDA device."""
+    lib = _lib.load()
+    n = ctypes.c_size_t(0)
+    _lib.check(lib.sda_decode_workspace_size(int(N), int(H), int(D), int(total_indices),
+                                             ctypes.byref(n)), "sda_decode_workspace_size")
+    return int(n.value)
+
+
+def decode(q: torch.Tensor, unified_kv: torch.Tensor, kv_indices: torch.Tensor,
+           kv_indptr: torch.Tensor, attn_sink: torch.Tensor, softmax_scale: float,
+           out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+           stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Sparse sink decode attention (paged_decode.py docstring semantics).
+
+    q [N, H, D] bf16; unified_kv [P, D] bf16 (one row = key and value of a
+    slot); kv_indices int32 (every listed entry must be a valid slot);
+    kv_indptr [N + 1] int32 (empty slice = padded token -> out 0); attn_sink
+    [H] fp32 sink logits; returns out [N, H, D] bf16.  `workspace` (uint8,
+    >= workspace_size(...) bytes) may be passed to keep the call free of
+    allocations, e.g. for CUDA-graph capture.  Asynchronous on `stream`.
+    """
+    lib = _lib.load()
+    _req(q, "q", torch.bfloat16, 3)
+    dev = q.device
+    _req(unified_kv, "unified_kv", torch.bfloat16, 2, dev)
+    _req(kv_indices, "kv_indices", torch.int32, 1, dev)
+    _req(kv_indptr, "kv_indptr", torch.int32, 1, dev)
+    _req(attn_sink, "attn_sink", torch.float32, 1, dev)
+    N, H, D = q.shape
+    if unified_kv.shape[1] != D:
+        raise ValueError("unified_kv row length must equal q's head dim")
+    if kv_indptr.numel() != N + 1 or attn_sink.numel() != H:
+        raise ValueError("kv_indptr must have N+1 entries and attn_sink H entries")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _req(out, "out", torch.bfloat16, 3, dev)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    with torch.cuda.device(dev):
+        need = workspace_size(N, H, D, kv_indices.numel())
+        if workspace is None:
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        else:
+            _req(workspace, "workspace", torch.uint8, 1, dev)
+        rc = lib.sda_decode(q.data_ptr(), unified_kv.data_ptr(), unified_kv.shape[0],
+                            kv_indices.data_ptr() if kv_indices.numel() else None,
+                            kv_indices.numel(), kv_indptr.data_ptr(), attn_sink.data_ptr(),
+                            float(softmax_scale), N, H, D, out.data_ptr(), workspace.data_ptr(),
+                            workspace.numel(), _stream_ptr(stream))
+    _lib.check(rc, "sda_decode")
+    return out
+
+
+def decode_error_flag(workspace: torch.Tensor, stream=None) -> int:
+    """Device error word of the last decode() on `workspace` (synchronises).
+
+    0 = fine; 1 = a pipeline wait timed out; 2 = kv_indptr was not a prefix
+    sum inside [0, len(kv_indices)] (nothing was computed)."""
+    lib = _lib.load()
+    flag = torch.zeros(1, dtype=torch.int32, device=workspace.device)
+    with torch.cuda.device(workspace.device):
+        _lib.check(lib.sda_decode_error_flag(workspace.data_ptr(), flag.data_ptr(),
+                                             _stream_ptr(stream)), "sda_decode_error_flag")
+    return int(flag.item())
+
+
+def set_timing_events(before: torch.cuda.Event | None, after: torch.cuda.Event | None) -> None:
+    """Record `before` / `after` around the attention kernel of every later
+    decode() on this thread (None, None turns it off).  Events must be
+    created with enable_timing=True."""
+    lib = _lib.load()
+    b = before.cuda_event if before is not None else None
+    a = after.cuda_event if after is not None else None
+    _lib.check(lib.sda_set_timing_events(b, a), "sda_set_timing_events")
+
+
+def build_indices(state_slot, swa_len, swa_head, comp_indptr, comp_block, comp_slot, *, win,
+                  k_per_block, swa_pages, total_pages, capacity=None, kv_indices=None,
+                  kv_indptr=None, status=None, stream=None):
+    """Pack SWA ring slots and compressed slots into ragged kv_indices.
+
+    Returns (kv_indices [capacity], kv_indptr [N+1], status [1]) int32 device
+    tensors; status bits are documented in include/sda.h (0 = all fine)."""
+    lib = _lib.load()
+    _req(state_slot, "state_slot", torch.int32, 1)
+    dev = state_slot.device
+    for name, t in (("swa_len", swa_len), ("swa_head", swa_head), ("comp_indptr", comp_indptr),
+                    ("comp_block", comp_block), ("comp_slot", comp_slot)):
+        _req(t, name, torch.int32, 1, dev)
+    N = state_slot.numel()
+    if capacity is None:
+        capacity = N * int(win) + comp_block.numel()
+    if kv_indices is None:
+        kv_indices = torch.empty(max(int(capacity), 1), dtype=torch.int32, device=dev)
+    if kv_indptr is None:
+        kv_indptr = torch.empty(N + 1, dtype=torch.int32, device=dev)
+    if status is None:
+        status = torch.empty(1, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        rc = lib.sda_build_indices(
+            state_slot.data_ptr(), swa_len.data_ptr(), swa_head.data_ptr(), comp_indptr.data_ptr(),
+            comp_block.data_ptr() if comp_block.numel() else None,
+            comp_slot.data_ptr() if comp_slot.numel() else None, comp_block.numel(), N, int(win),
+            int(k_per_block), int(swa_pages), int(total_pages), kv_indices.data_ptr(),
+            int(capacity), kv_indptr.data_ptr(), status.data_ptr(), _stream_ptr(stream))
+    _lib.check(rc, "sda_build_indices")
+    return kv_indices, kv_indptr, status
+
+
+def validate_indices(kv_indices, kv_indptr, total_pages, status=None, stream=None):
+    """Device check of the index contract; returns status [2] int32 (flags, n_bad)."""
+    lib = _lib.load()
+    _req(kv_indptr, "kv_indptr", torch.int32, 1)
+    dev = kv_indptr.device
+    _req(kv_indices, "kv_indices", torch.int32, 1, dev)
+    if status is None:
+        status = torch.empty(2, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        rc = lib.sda_validate_indices(kv_indices.data_ptr() if kv_indices.numel() else None,
+                                      kv_indices.numel(), kv_indptr.data_ptr(),
+                                      kv_indptr.numel() - 1, int(total_pages), status.data_ptr(),
+                                      _stream_ptr(stream))
+    _lib.check(rc, "sda_validate_indices")
+    return status
+
+
+def decode_host(q_host: torch.Tensor, unified_kv: torch.Tensor, kv_indices_host: torch.Tensor,
+                kv_indptr_host: torch.Tensor, attn_sink: torch.Tensor, softmax_scale: float,
+                out_host: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """End-to-end call from host buffers: copies q and the index lists to the
+    device (pinned host memory -> async copies), runs decode on the resident
+    pool and copies out back to the host.  Synchronises the stream."""
+    dev = unified_kv.device
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.stream(s):
+        q = q_host.to(dev, non_blocking=True)
+        idx = kv_indices_host.to(dev, non_blocking=True)
+        ptr = kv_indptr_host.to(dev, non_blocking=True)
+        out = decode(q, unified_kv, idx, ptr, attn_sink, softmax_scale, stream=s)
+        if out_host is None:
+            out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        out_host.copy_(out, non_blocking=True)
+    s.synchronize()
+    return out_host

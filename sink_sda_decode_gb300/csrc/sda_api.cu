@@ -1,0 +1,255 @@
+// sda_api.cu -- the extern "C" entry points of libsda (declared in
+// include/sda.h): host-side argument checks, kernel-variant choice, the
+// workspace layout, and the launches.  Nothing here allocates, synchronises
+// or reads device memory from the host.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "sda_internal.cuh"
+
+namespace sda {
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+thread_local cudaEvent_t g_ev_before = nullptr;
+thread_local cudaEvent_t g_ev_after = nullptr;
+
+void note_cuda_error(cudaError_t e, const char* where) {
+  std::snprintf(g_last_error, sizeof g_last_error, "%s: %s (%s)", where, cudaGetErrorName(e),
+                cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  std::once_flag once;
+  int num_sms = 0;
+  cudaError_t err = cudaSuccess;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+// SM count of the current device, queried once per device; also sets the
+// tensor-core kernels' shared-memory attribute on that device.
+cudaError_t device_sms(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  DeviceInfo& d = g_dev[dev];
+  std::call_once(d.once, [&]() {
+    d.err = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    for (int nh : {16, 32, 64})
+      if (d.err == cudaSuccess) d.err = umma_prepare(nh);
+  });
+  *sms = d.num_sms;
+  return d.err;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Optional A/B switch for tests: SDA_FORCE_VARIANT=simt forces the CUDA-core kernel.
+bool force_simt() {
+  const char* v = std::getenv("SDA_FORCE_VARIANT");
+  return v && std::strcmp(v, "simt") == 0;
+}
+
+}  // namespace
+
+bool choose_plan(int H, int D, int num_sms, LaunchPlan* lp) {
+  if (!(D == 64 || D == 128 || D == 256 || D == 512)) return false;
+  if (H < 1 || H > 256) return false;
+  lp->num_sms = num_sms;
+  const bool umma_shape = D == 512 && (H == 16 || H == 32 || H % 64 == 0);
+  if (umma_shape && !force_simt()) {
+    lp->variant = kUmma;
+    lp->nh = H < 64 ? H : 64;
+    lp->hg = H / lp->nh;
+    lp->grid = num_sms;  // one CTA per SM (about 200 KB of shared memory each)
+    lp->threads = 192;
+    lp->smem = umma_smem_bytes(lp->nh);
+  } else {
+    lp->variant = kSimt;
+    lp->nh = H;
+    lp->hg = 1;
+    lp->grid = num_sms * 4;
+    lp->threads = 256;
+    lp->smem = 0;
+  }
+  return true;
+}
+
+WsLayout workspace_layout(int N, int H, int D, int64_t total_indices, const LaunchPlan& lp) {
+  WsLayout L;
+  // Partial rows: fewer than 2 * grid / hg (pieces are >= T*hg/grid slots)
+  // and fewer than 2 * T / 64 + 1 (pieces are >= 64 slots); T <= total_indices.
+  int64_t p1 = 2 * ((int64_t)(lp.grid + lp.hg - 1) / lp.hg) + 2;
+  int64_t p2 = 2 * ((total_indices + kMinChunk - 1) / kMinChunk) + 2;
+  int64_t p_max = p1 < p2 ? p1 : p2;
+  int64_t s_max = p_max / 2 + 1;
+  if (s_max > N) s_max = N;
+  L.p_max = (int)p_max;
+  L.s_max = (int)s_max;
+  L.u_max = (int)((int64_t)lp.hg * ((int64_t)N + p_max));
+  size_t off = sizeof(WsHeader);
+  L.units_off = off;
+  off = align_up(off + (size_t)L.u_max * 16, 256);
+  L.split_off = off;
+  off = align_up(off + (size_t)(s_max > 0 ? s_max : 1) * 16, 256);
+  L.ml_off = off;
+  off = align_up(off + (size_t)p_max * H * 8, 256);
+  L.o_off = off;
+  off = align_up(off + (size_t)p_max * H * D * 4, 256);
+  L.total = off;
+  return L;
+}
+
+}  // namespace sda
+
+using namespace sda;
+
+extern "C" {
+
+const char* sda_strerror(sda_status status) {
+  switch (status) {
+    case SDA_OK: return "SDA_OK";
+    case SDA_ERR_INVALID_ARG: return "SDA_ERR_INVALID_ARG: invalid argument";
+    case SDA_ERR_UNSUPPORTED: return "SDA_ERR_UNSUPPORTED: unsupported (H, D)";
+    case SDA_ERR_CUDA: return "SDA_ERR_CUDA: a CUDA call failed";
+    case SDA_ERR_WORKSPACE: return "SDA_ERR_WORKSPACE: workspace too small or misaligned";
+    default: return "SDA: unknown status";
+  }
+}
+
+const char* sda_last_cuda_error(void) { return g_last_error; }
+
+int sda_abi_version(void) { return 1; }
+
+sda_status sda_decode_workspace_size(int N, int H, int D, int64_t total_indices, size_t* bytes) {
+  if (!bytes || N < 0 || total_indices < 0) return SDA_ERR_INVALID_ARG;
+  int sms = 0;
+  cudaError_t e = device_sms(&sms);
+  if (e != cudaSuccess) {
+    note_cuda_error(e, "sda_decode_workspace_size");
+    return SDA_ERR_CUDA;
+  }
+  LaunchPlan lp;
+  if (!choose_plan(H, D, sms, &lp)) return SDA_ERR_UNSUPPORTED;
+  *bytes = workspace_layout(N, H, D, total_indices, lp).total;
+  return SDA_OK;
+}
+
+sda_status sda_decode(const void* q, const void* unified_kv, int64_t total_pages,
+                      const int32_t* kv_indices, int64_t total_indices,
+                      const int32_t* kv_indptr, const float* attn_sink, float softmax_scale,
+                      int N, int H, int D, void* out, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  if (N < 0 || total_indices < 0 || total_indices > 0x7fffffffll) return SDA_ERR_INVALID_ARG;
+  if (total_pages <= 0 || total_pages > 0x7fffffffll) return SDA_ERR_INVALID_ARG;
+  LaunchPlan lp;
+  if (!choose_plan(H, D, 1, &lp)) return SDA_ERR_UNSUPPORTED;
+  if (N == 0) return SDA_OK;
+  if (!q || !unified_kv || !kv_indptr || !attn_sink || !out || !workspace) return SDA_ERR_INVALID_ARG;
+  if (total_indices > 0 && !kv_indices) return SDA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(unified_kv, 16) || !aligned(out, 16) || !aligned(kv_indptr, 4) ||
+      !aligned(attn_sink, 4) || (kv_indices && !aligned(kv_indices, 4)))
+    return SDA_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return SDA_ERR_WORKSPACE;
+  int sms = 0;
+  cudaError_t e = device_sms(&sms);
+  if (e != cudaSuccess) {
+    note_cuda_error(e, "sda_decode");
+    return SDA_ERR_CUDA;
+  }
+  choose_plan(H, D, sms, &lp);
+  const WsLayout L = workspace_layout(N, H, D, total_indices, lp);
+  if (workspace_bytes < L.total) return SDA_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  e = launch_plan(kv_indptr, N, total_indices, lp, workspace, L, st);
+  if (e == cudaSuccess && g_ev_before && g_ev_after) e = cudaEventRecord(g_ev_before, st);
+  if (e == cudaSuccess) {
+    if (lp.variant == kUmma)
+      e = launch_decode_umma(q, unified_kv, total_pages, kv_indices, attn_sink, softmax_scale, N, H,
+                             D, out, workspace, L, lp, st);
+    else
+      e = launch_decode_simt(q, unified_kv, kv_indices, attn_sink, softmax_scale, N, H, D, out,
+                             workspace, L, lp, st);
+  }
+  if (e == cudaSuccess && g_ev_before && g_ev_after) e = cudaEventRecord(g_ev_after, st);
+  if (e == cudaSuccess) e = launch_combine(attn_sink, N, H, D, out, workspace, L, sms, st);
+  if (e != cudaSuccess) {
+    note_cuda_error(e, "sda_decode");
+    return SDA_ERR_CUDA;
+  }
+  return SDA_OK;
+}
+
+sda_status sda_set_timing_events(void* before, void* after) {
+  if ((before == nullptr) != (after == nullptr)) return SDA_ERR_INVALID_ARG;
+  g_ev_before = static_cast<cudaEvent_t>(before);
+  g_ev_after = static_cast<cudaEvent_t>(after);
+  return SDA_OK;
+}
+
+sda_status sda_decode_error_flag(const void* workspace, int32_t* device_flag, void* stream) {
+  if (!workspace || !device_flag || !aligned(workspace, 256)) return SDA_ERR_INVALID_ARG;
+  const char* src = static_cast<const char*>(workspace) + offsetof(WsHeader, error);
+  cudaError_t e = cudaMemcpyAsync(device_flag, src, sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    note_cuda_error(e, "sda_decode_error_flag");
+    return SDA_ERR_CUDA;
+  }
+  return SDA_OK;
+}
+
+sda_status sda_build_indices(const int32_t* state_slot, const int32_t* swa_len,
+                             const int32_t* swa_head, const int32_t* comp_indptr,
+                             const int32_t* comp_block, const int32_t* comp_slot,
+                             int64_t comp_total, int N, int win, int k_per_block,
+                             int64_t swa_pages, int64_t total_pages, int32_t* kv_indices,
+                             int64_t capacity, int32_t* kv_indptr, int32_t* status,
+                             void* stream) {
+  if (N < 0 || win <= 0 || k_per_block <= 0 || swa_pages < 0 || total_pages <= 0 ||
+      total_pages > 0x7fffffffll || swa_pages > total_pages || capacity < 0 ||
+      capacity > 0x7fffffffll || comp_total < 0 || comp_total > 0x7fffffffll)
+    return SDA_ERR_INVALID_ARG;
+  if (!kv_indptr || !status) return SDA_ERR_INVALID_ARG;
+  if (N > 0 && (!state_slot || !swa_len || !swa_head || !comp_indptr)) return SDA_ERR_INVALID_ARG;
+  if (comp_total > 0 && (!comp_block || !comp_slot)) return SDA_ERR_INVALID_ARG;
+  if (capacity > 0 && !kv_indices) return SDA_ERR_INVALID_ARG;
+  cudaError_t e = launch_build_indices(state_slot, swa_len, swa_head, comp_indptr, comp_block,
+                                       comp_slot, comp_total, N, win, k_per_block, swa_pages,
+                                       total_pages, kv_indices, capacity, kv_indptr, status,
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    note_cuda_error(e, "sda_build_indices");
+    return SDA_ERR_CUDA;
+  }
+  return SDA_OK;
+}
+
+sda_status sda_validate_indices(const int32_t* kv_indices, int64_t total_indices,
+                                const int32_t* kv_indptr, int N, int64_t total_pages,
+                                int32_t* status, void* stream) {
+  if (N < 0 || total_indices < 0 || total_pages <= 0 || !kv_indptr || !status)
+    return SDA_ERR_INVALID_ARG;
+  if (total_indices > 0 && !kv_indices) return SDA_ERR_INVALID_ARG;
+  cudaError_t e = launch_validate(kv_indices, total_indices, kv_indptr, N, total_pages, status,
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    note_cuda_error(e, "sda_validate_indices");
+    return SDA_ERR_CUDA;
+  }
+  return SDA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,120 @@
+// sda_internal.cuh -- shared definitions of libsda's CUDA translation units:
+// the workspace layout, the work-unit descriptor and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/sda.h"
+
+namespace sda {
+
+// ---------------------------------------------------------------- work units
+//
+// A work unit is one piece of one token's slot list, for one group of heads.
+// Long lists are cut into pieces so that every CTA of a persistent grid gets
+// about the same number of slots ("split-L"); the pieces of a split token
+// each write an unnormalised partial (m, l, acc) that the combine kernel
+// merges with the sink.  Unsplit tokens are finished by the decode kernel.
+//
+// int4 layout: x = token, y = first index into kv_indices (absolute),
+//              z = number of slots, w = head_group | ((partial_row + 1) << 4)
+//              (partial_row + 1 == 0: the unit owns the whole token).
+struct UnitDesc {
+  int token, begin, len, meta;
+};
+__host__ __device__ inline int unit_head_group(int meta) { return meta & 15; }
+__host__ __device__ inline int unit_part_row(int meta) { return (meta >> 4) - 1; }
+__host__ __device__ inline int make_unit_meta(int head_group, int part_row) {
+  return head_group | ((part_row + 1) << 4);
+}
+
+// Workspace header (first 256 bytes of the workspace).
+struct WsHeader {
+  int n_units;   // number of valid UnitDesc entries
+  int n_split;   // number of split tokens (entries of the split list)
+  int n_parts;   // partial rows in use
+  int chunk;     // slots per piece chosen by the plan
+  int error;     // nonzero: a pipeline wait timed out
+  int pad[59];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+// Split list entry: x = token, y = first partial row, z = number of pieces.
+constexpr int kTileSlots = 64;     // slots per KV tile of the tensor-core kernel
+constexpr int kMinChunk = 64;      // smallest piece a list is cut into
+
+// Decode variants.
+enum Variant : int { kSimt = 0, kUmma = 1 };
+
+struct LaunchPlan {
+  Variant variant;
+  int nh;      // heads per CTA
+  int num_sms; // SMs of the device
+  int hg;      // head groups per token (H / nh)
+  int grid;    // persistent grid size
+  int threads; // threads per CTA
+  size_t smem; // dynamic shared memory bytes
+};
+
+struct WsLayout {
+  size_t units_off, split_off, ml_off, o_off, total;
+  int u_max, s_max, p_max;
+};
+
+// Picks the kernel variant and grid for (H, D) on a device with `num_sms` SMs.
+// Returns false if (H, D) is unsupported.
+bool choose_plan(int H, int D, int num_sms, LaunchPlan* lp);
+
+// Workspace layout for a plan.  p_max bounds the partial rows: a piece is
+// at least ceil(T * hg / grid) slots, so split tokens (L > chunk) use fewer
+// than 2 * L / chunk pieces each, and in total fewer than 2 * grid / hg.
+WsLayout workspace_layout(int N, int H, int D, int64_t total_indices, const LaunchPlan& lp);
+
+// ---------------------------------------------------------------- launchers
+// All launchers only enqueue; they return cudaGetLastError().
+cudaError_t launch_plan(const int32_t* kv_indptr, int N, int64_t total_indices,
+                        const LaunchPlan& lp, void* ws, const WsLayout& L, cudaStream_t st);
+cudaError_t launch_combine(const float* attn_sink, int N, int H, int D, void* out, void* ws,
+                           const WsLayout& L, int num_sms, cudaStream_t st);
+cudaError_t launch_decode_simt(const void* q, const void* kv, const int32_t* kv_indices,
+                               const float* attn_sink, float softmax_scale, int N, int H, int D,
+                               void* out, void* ws, const WsLayout& L, const LaunchPlan& lp,
+                               cudaStream_t st);
+cudaError_t launch_decode_umma(const void* q, const void* kv, int64_t total_pages,
+                               const int32_t* kv_indices, const float* attn_sink,
+                               float softmax_scale, int N, int H, int D, void* out, void* ws,
+                               const WsLayout& L, const LaunchPlan& lp, cudaStream_t st);
+size_t umma_smem_bytes(int nh);
+cudaError_t umma_prepare(int nh);  // one-time kernel attribute set-up
+
+cudaError_t launch_build_indices(const int32_t* state_slot, const int32_t* swa_len,
+                                 const int32_t* swa_head, const int32_t* comp_indptr,
+                                 const int32_t* comp_block, const int32_t* comp_slot,
+                                 int64_t comp_total, int N, int win, int k_per_block,
+                                 int64_t swa_pages, int64_t total_pages, int32_t* kv_indices,
+                                 int64_t capacity, int32_t* kv_indptr, int32_t* status,
+                                 cudaStream_t st);
+cudaError_t launch_validate(const int32_t* kv_indices, int64_t total_indices,
+                            const int32_t* kv_indptr, int N, int64_t total_pages,
+                            int32_t* status, cudaStream_t st);
+
+// ---------------------------------------------------------------- device helpers
+#ifdef __CUDACC__
+__device__ __forceinline__ float ex2_approx(float x) {
+  // hardware base-2 exponential (MUFU.EX2); ex2(-inf) = +0
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ int unit_position(int k, int cta, int grid) {
+  // "snake" order over a list sorted by decreasing size: CTA b takes
+  // positions b, 2G-1-b, 2G+b, 4G-1-b, ... so that big and small units pair up.
+  const int round = k >> 1;
+  return round * 2 * grid + ((k & 1) ? (2 * grid - 1 - cta) : cta);
+}
+#endif
+
+}  // namespace sda

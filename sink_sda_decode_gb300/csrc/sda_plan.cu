@@ -1,0 +1,231 @@
+// sda_plan.cu -- device-side work planning (split-L) and the log-sum-exp
+// combine of split tokens.
+//
+// The plan runs on the device because kv_indptr lives there and the decode
+// call must stay capturable in a CUDA graph (the reason the paged_decode.py
+// docstring gives for the whole design: no per-forward shape that depends on
+// host-side lengths).  Splitting long lists and merging the pieces is not on
+// the page; it is how the hot path fills all SMs when tokens are few or
+// lists are long.
+#include <cuda_bf16.h>
+
+#include "sda_internal.cuh"
+
+namespace sda {
+
+namespace {
+
+constexpr int kPlanThreads = 1024;
+constexpr int kBuckets = 33;  // bucket b holds units of length in [2^(b-1), 2^b); 0 = empty
+
+__device__ __forceinline__ int len_bucket(int len) { return len <= 0 ? 0 : 32 - __clz(len); }
+
+// Exclusive block-wide scan of one int per thread (1024 threads); returns the
+// prefix and stores the block total in *total (smem scratch of 32 ints).
+__device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sums[lane];
+    int s = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    warp_sums[lane] = s - w;  // exclusive warp offsets
+    if (lane == 31) *total = s;
+  }
+  __syncthreads();
+  const int r = warp_sums[warp] + x - v;
+  __syncthreads();
+  return r;
+}
+
+struct TokenSplit {
+  int len, pieces, piece_len;
+};
+
+__device__ __forceinline__ TokenSplit token_split(const int32_t* indptr, int t, int chunk) {
+  TokenSplit s;
+  int L = indptr[t + 1] - indptr[t];
+  s.len = L > 0 ? L : 0;
+  s.pieces = s.len == 0 ? 1 : (s.len + chunk - 1) / chunk;
+  const int even = (s.len + s.pieces - 1) / s.pieces;
+  s.piece_len = s.pieces == 1 ? s.len : ((even + kTileSlots - 1) / kTileSlots) * kTileSlots;
+  return s;
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+plan_kernel(const int32_t* __restrict__ indptr, int N, long long total_indices, int hg, int grid,
+            WsHeader* __restrict__ hdr, int4* __restrict__ units, int4* __restrict__ splits) {
+  __shared__ int warp_sums[32];
+  __shared__ int s_total[2];
+  __shared__ int bucket_count[kBuckets];
+  __shared__ int bucket_cursor[kBuckets];
+  __shared__ int s_chunk;
+
+  if (threadIdx.x < kBuckets) bucket_count[threadIdx.x] = 0;
+  // kv_indptr must be a true prefix sum inside [0, total_indices]; otherwise
+  // nothing is planned (out is left unwritten) and the error word reads 2, so
+  // that no kernel ever reads kv_indices out of bounds.
+  int bad = 0;
+  for (int t = threadIdx.x; t <= N; t += kPlanThreads) {
+    const int v = indptr[t];
+    if (v < 0 || (long long)v > total_indices || (t < N && indptr[t + 1] < v)) bad = 1;
+  }
+  if (__syncthreads_or(bad)) {
+    if (threadIdx.x == 0) {
+      hdr->n_units = 0;
+      hdr->n_split = 0;
+      hdr->n_parts = 0;
+      hdr->chunk = 0;
+      hdr->error = 2;
+    }
+    return;
+  }
+  if (threadIdx.x == 0) {
+    long long T = N > 0 ? (long long)indptr[N] - (long long)indptr[0] : 0;
+    if (T < 0) T = 0;
+    long long target = (T * hg + grid - 1) / grid;
+    long long chunk = ((target + kTileSlots - 1) / kTileSlots) * kTileSlots;
+    if (chunk < kMinChunk) chunk = kMinChunk;
+    if (chunk > (1ll << 30)) chunk = 1ll << 30;
+    s_chunk = (int)chunk;
+  }
+  __syncthreads();
+  const int chunk = s_chunk;
+
+  // pass 1: unit counts per length bucket
+  for (int t0 = 0; t0 < N; t0 += kPlanThreads) {
+    const int t = t0 + threadIdx.x;
+    if (t < N) {
+      TokenSplit s = token_split(indptr, t, chunk);
+      for (int k = 0; k < s.pieces; ++k) {
+        int plen = s.pieces == 1 ? s.len : min(s.piece_len, s.len - k * s.piece_len);
+        atomicAdd(&bucket_count[len_bucket(plen)], hg);
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int b = kBuckets - 1; b >= 0; --b) {  // longest pieces first
+      bucket_cursor[b] = acc;
+      acc += bucket_count[b];
+    }
+    hdr->n_units = acc;
+  }
+  __syncthreads();
+
+  // pass 2: emit units, partial rows and the split list
+  int part_carry = 0, split_carry = 0;
+  for (int t0 = 0; t0 < N; t0 += kPlanThreads) {
+    const int t = t0 + threadIdx.x;
+    TokenSplit s{0, 1, 0};
+    if (t < N) s = token_split(indptr, t, chunk);
+    const bool split = t < N && s.pieces > 1;
+    const int part_base = block_exclusive_scan(split ? s.pieces : 0, warp_sums, &s_total[0]) + part_carry;
+    const int split_idx = block_exclusive_scan(split ? 1 : 0, warp_sums, &s_total[1]) + split_carry;
+    if (t < N) {
+      const int begin = indptr[t];
+      for (int k = 0; k < s.pieces; ++k) {
+        const int plen = s.pieces == 1 ? s.len : min(s.piece_len, s.len - k * s.piece_len);
+        const int pos = atomicAdd(&bucket_cursor[len_bucket(plen)], hg);
+        const int row = split ? part_base + k : -1;
+        for (int g = 0; g < hg; ++g)
+          units[pos + g] = make_int4(t, begin + k * s.piece_len, plen, make_unit_meta(g, row));
+      }
+      if (split) splits[split_idx] = make_int4(t, part_base, s.pieces, 0);
+    }
+    part_carry += s_total[0];
+    split_carry += s_total[1];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    hdr->n_split = split_carry;
+    hdr->n_parts = part_carry;
+    hdr->chunk = chunk;
+    hdr->error = 0;
+  }
+}
+
+// Merge the pieces of each split token:
+//   M   = max(sink*log2e, max_k m_k)
+//   out = sum_k 2^(m_k - M) acc_k / (2^(sink*log2e - M) + sum_k 2^(m_k - M) l_k)
+// m_k, l_k, acc_k are the log2-domain running max, denominator and
+// unnormalised output of piece k (without the sink).
+__global__ void __launch_bounds__(128)
+combine_kernel(const float* __restrict__ attn_sink, int H, int D,
+               __nv_bfloat16* __restrict__ out, const WsHeader* __restrict__ hdr,
+               const int4* __restrict__ splits, const float2* __restrict__ part_ml,
+               const float* __restrict__ part_o) {
+  const int n_items = hdr->n_split * H;
+  for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
+    const int si = w / H, h = w % H;
+    const int4 sp = splits[si];
+    const int t = sp.x, row0 = sp.y, np = sp.z;
+    const float ms = attn_sink[h] * kLog2e;
+    float M = ms;
+    for (int k = 0; k < np; ++k) M = fmaxf(M, part_ml[(size_t)(row0 + k) * H + h].x);
+    const bool dead = (ms == INFINITY) || (M == -INFINITY);
+    float den = dead ? 1.f : ex2_approx(ms - M);
+    for (int k = 0; k < np; ++k) {
+      const float2 ml = part_ml[(size_t)(row0 + k) * H + h];
+      den += dead ? 0.f : ml.y * ex2_approx(ml.x - M);
+    }
+    for (int d0 = threadIdx.x * 4; d0 < D; d0 += blockDim.x * 4) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (!dead) {
+        for (int k = 0; k < np; ++k) {
+          const float wk = ex2_approx(part_ml[(size_t)(row0 + k) * H + h].x - M);
+          const float4 o = *reinterpret_cast<const float4*>(part_o + ((size_t)(row0 + k) * H + h) * D + d0);
+          acc.x += wk * o.x; acc.y += wk * o.y; acc.z += wk * o.z; acc.w += wk * o.w;
+        }
+      }
+      const float inv = dead ? 0.f : 1.f / den;
+      __nv_bfloat162 a = __floats2bfloat162_rn(acc.x * inv + 0.f, acc.y * inv + 0.f);
+      __nv_bfloat162 b = __floats2bfloat162_rn(acc.z * inv + 0.f, acc.w * inv + 0.f);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&a);
+      pk.y = *reinterpret_cast<uint32_t*>(&b);
+      *reinterpret_cast<uint2*>(out + ((size_t)t * H + h) * D + d0) = pk;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const int32_t* kv_indptr, int N, int64_t total_indices,
+                        const LaunchPlan& lp, void* ws, const WsLayout& L, cudaStream_t st) {
+  char* base = static_cast<char*>(ws);
+  plan_kernel<<<1, kPlanThreads, 0, st>>>(kv_indptr, N, (long long)total_indices, lp.hg, lp.grid,
+                                           reinterpret_cast<WsHeader*>(base),
+                                           reinterpret_cast<int4*>(base + L.units_off),
+                                           reinterpret_cast<int4*>(base + L.split_off));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float* attn_sink, int N, int H, int D, void* out, void* ws,
+                           const WsLayout& L, int num_sms, cudaStream_t st) {
+  if (L.s_max == 0) return cudaSuccess;
+  char* base = static_cast<char*>(ws);
+  int blocks = L.s_max * H;
+  if (blocks > num_sms * 8) blocks = num_sms * 8;
+  if (blocks < 1) blocks = 1;
+  combine_kernel<<<blocks, 128, 0, st>>>(attn_sink, H, D, static_cast<__nv_bfloat16*>(out),
+                                         reinterpret_cast<const WsHeader*>(base),
+                                         reinterpret_cast<const int4*>(base + L.split_off),
+                                         reinterpret_cast<const float2*>(base + L.ml_off),
+                                         reinterpret_cast<const float*>(base + L.o_off));
+  return cudaGetLastError();
+}
+
+}  // namespace sda

@@ -1,0 +1,105 @@
+"""GPU index builder and validator: bit-exact against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import oracle_pins
+import sink_sda_decode_gb300 as sda
+from sink_sda_decode_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a, np.int32)).cuda()
+
+
+def gpu_build(ss, sl, sh, cp, cb, cs, win, kpb, swa_pages, total_pages, capacity=None):
+    idx, ptr, st = sda.build_indices(dev(ss), dev(sl), dev(sh), dev(cp), dev(cb), dev(cs), win=win,
+                                     k_per_block=kpb, swa_pages=swa_pages, total_pages=total_pages,
+                                     capacity=capacity)
+    ptr_h = ptr.cpu().numpy()
+    return idx.cpu().numpy()[:ptr_h[-1]], ptr_h, int(st.item())
+
+
+def test_golden_example():
+    g = oracle_pins.read_golden_builder()
+    idx, ptr, st = gpu_build(g["state_slot"], g["swa_len"], g["swa_head"], g["comp_indptr"],
+                             g["comp_block"], g["comp_slot"], g["win"][0], g["k_per_block"][0],
+                             g["swa_pages"][0], g["total_pages"][0])
+    assert idx.tolist() == g["kv_indices"]
+    assert ptr.tolist() == g["kv_indptr"]
+    assert st == g["status"][0]
+
+
+@pytest.mark.parametrize("cfg", range(5), ids=inputs.CONFIG_NAMES)
+def test_workload_lists_bit_exact(cfg):
+    w = inputs.config(cfg, device="cuda")
+    args = (w.state_slot, w.swa_len, w.swa_head, w.comp_indptr, w.comp_block, w.comp_slot, w.win,
+            w.k_per_block, w.swa_pages, w.total_pages)
+    idx, ptr, st = gpu_build(*args)
+    assert st == 0
+    assert np.array_equal(ptr, w.kv_indptr)
+    assert np.array_equal(idx, w.kv_indices)
+    o_idx, o_ptr, o_st = oracle.build_indices(*args)
+    assert np.array_equal(idx, o_idx) and np.array_equal(ptr, o_ptr) and st == o_st
+
+
+def random_descriptors(rng, N, win, kpb, n_states, n_blocks, bad=True):
+    swa_pages = n_states * win
+    total_pages = swa_pages + n_blocks * kpb
+    ss = rng.integers(-1, n_states, N)
+    sl = rng.integers(0, win + 1, N)
+    sh = rng.integers(0, win, N)
+    cl = rng.integers(0, 40, N)
+    cp = np.zeros(N + 1, np.int64)
+    cp[1:] = np.cumsum(cl)
+    cb = rng.integers(0, n_blocks, cp[-1])
+    cs = rng.integers(0, kpb, cp[-1])
+    if bad:
+        k = rng.integers(0, N, 6)
+        sl[k[0]] = win + 1                      # bit 1
+        sh[k[1]] = win; sl[k[1]] = 3            # bit 2
+        ss[k[2]] = n_states + 2; sl[k[2]] = 1   # bit 16 (SWA slot outside its region)
+        if cp[-1] > 2:
+            cs[0] = kpb                         # bit 8
+            cb[1] = n_blocks                    # bit 16 (compressed slot >= total_pages)
+            cb[2] = -5                          # bit 8
+    return ss, sl, sh, cp.astype(np.int32), cb, cs, win, kpb, swa_pages, total_pages
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+@pytest.mark.parametrize("N", [1, 7, 1000, 5000])
+def test_random_descriptors_bit_exact(seed, N):
+    rng = np.random.default_rng(seed * 7919 + N)
+    args = random_descriptors(rng, N, win=16, kpb=8, n_states=max(N // 2, 1), n_blocks=300)
+    idx, ptr, st = gpu_build(*args)
+    o_idx, o_ptr, o_st = oracle.build_indices(*args)
+    assert st == o_st
+    assert np.array_equal(ptr, o_ptr)
+    assert np.array_equal(idx, o_idx)
+
+
+def test_capacity_overflow_and_empty_batch():
+    args = random_descriptors(np.random.default_rng(5), 50, 8, 4, 50, 10, bad=False)
+    total = oracle.build_indices(*args)[1][-1]
+    idx, ptr, st = gpu_build(*args, capacity=int(total) - 1)
+    assert st & 32 and np.all(ptr == 0)
+    e = np.zeros(0, np.int32)
+    idx, ptr, st = gpu_build(e, e, e, np.zeros(1, np.int32), e, e, 4, 4, 0, 10)
+    assert ptr.tolist() == [0] and st == 0
+
+
+def test_validate_matches_oracle():
+    rng = np.random.default_rng(3)
+    for _ in range(5):
+        n = int(rng.integers(1, 3000))
+        idx = rng.integers(-3, 1000, n).astype(np.int32)
+        ptr = np.sort(rng.integers(0, n + 1, 41)).astype(np.int32)
+        if rng.random() < 0.5:
+            ptr[5], ptr[6] = ptr[6] + 1, ptr[5]
+        if rng.random() < 0.3:
+            ptr[-1] = n + 4
+        st = sda.validate_indices(dev(idx), dev(ptr), 997).cpu().numpy()
+        assert tuple(int(x) for x in st) == oracle.validate_indices(idx, ptr, 997)
