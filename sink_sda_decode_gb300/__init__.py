@@ -119,9 +119,17 @@ def set_timing_events(before: torch.cuda.Event | None, after: torch.cuda.Event |
     decode() on this thread (None, None turns it off).  Events must be
     created with enable_timing=True."""
     lib = _lib.load()
-    b = before.cuda_event if before is not None else None
-    a = after.cuda_event if after is not None else None
-    _lib.check(lib.sda_set_timing_events(b, a), "sda_set_timing_events")
+    handles = []
+    for ev in (before, after):
+        if ev is None:
+            handles.append(None)
+            continue
+        if not ev.cuda_event:  # torch creates the CUDA event on its first record()
+            ev.record()
+        if not ev.cuda_event:
+            raise ValueError("could not create the CUDA event")
+        handles.append(ev.cuda_event)
+    _lib.check(lib.sda_set_timing_events(handles[0], handles[1]), "sda_set_timing_events")
 
 
 def build_indices(state_slot, swa_len, swa_head, comp_indptr, comp_block, comp_slot, *, win,

@@ -19,19 +19,19 @@ namespace {
 
 constexpr int kScanThreads = 1024;
 
-// One warp per token: check every field, write the length (0 if bad) to
-// kv_indptr[t + 1] (rewritten in place by the scan).
-__global__ void build_len_kernel(const int32_t* __restrict__ state_slot,
-                                 const int32_t* __restrict__ swa_len,
-                                 const int32_t* __restrict__ swa_head,
-                                 const int32_t* __restrict__ comp_indptr,
-                                 const int32_t* __restrict__ comp_block,
-                                 const int32_t* __restrict__ comp_slot, int64_t comp_total, int N,
-                                 int win, int k_per_block, int64_t swa_pages, int64_t total_pages,
-                                 int32_t* __restrict__ kv_indptr, int32_t* __restrict__ status) {
-  const int lane = threadIdx.x & 31;
-  const int warps = (gridDim.x * blockDim.x) >> 5;
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < N; t += warps) {
+constexpr int kTokThreads = 512;  // one CTA per token in the length and scatter passes
+
+// One CTA per token: check every field, write the length to kv_indptr[t + 1]
+// (rewritten in place by the scan), or -(status bits) if the token is bad.
+__global__ void __launch_bounds__(kTokThreads)
+build_len_kernel(const int32_t* __restrict__ state_slot, const int32_t* __restrict__ swa_len,
+                 const int32_t* __restrict__ swa_head, const int32_t* __restrict__ comp_indptr,
+                 const int32_t* __restrict__ comp_block, const int32_t* __restrict__ comp_slot,
+                 int64_t comp_total, int N, int win, int k_per_block, int64_t swa_pages,
+                 int64_t total_pages, int32_t* __restrict__ kv_indptr) {
+  pdl_wait();
+  pdl_trigger();
+  for (int t = blockIdx.x; t < N; t += gridDim.x) {
     int32_t bad = 0;
     int64_t len = 0;
     const int32_t ss = state_slot[t];
@@ -44,7 +44,8 @@ __global__ void build_len_kernel(const int32_t* __restrict__ state_slot,
       if (c0 < 0 || c1 < c0 || (int64_t)c1 > comp_total) {
         bad |= 4;
       } else {
-        for (int32_t e = c0 + lane; e < c1; e += 32) {
+#pragma unroll 4
+        for (int32_t e = c0 + threadIdx.x; e < c1; e += kTokThreads) {
           const int32_t b = comp_block[e], s = comp_slot[e];
           if (b < 0 || s < 0 || s >= k_per_block) bad |= 8;
           else if (swa_pages + (int64_t)b * k_per_block + s >= total_pages) bad |= 16;
@@ -52,33 +53,44 @@ __global__ void build_len_kernel(const int32_t* __restrict__ state_slot,
       }
       len = (int64_t)(n_swa > 0 ? n_swa : 0) + (c1 > c0 ? c1 - c0 : 0);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) bad |= __shfl_xor_sync(0xffffffffu, bad, o);
-    if (lane == 0) {
-      if (bad) atomicOr(status, bad);
-      kv_indptr[t + 1] = bad ? 0 : (int32_t)(len > 0x7fffffff ? 0x7fffffff : len);
-    }
+    __shared__ int s_bad;  // OR of every thread's findings for token t
+    if (threadIdx.x == 0) s_bad = 0;
+    __syncthreads();
+    if (bad) atomicOr(&s_bad, bad);
+    __syncthreads();
+    if (threadIdx.x == 0)
+      kv_indptr[t + 1] = s_bad ? -s_bad : (int32_t)(len > 0x7fffffff ? 0x7fffffff : len);
+    __syncthreads();
   }
 }
 
 // One CTA: in-place inclusive scan of the lengths in kv_indptr[1..N] (int64
-// running total), kv_indptr[0] = 0.  If the total exceeds capacity, every
-// slice is emptied and bit 32 is raised.
+// running total), kv_indptr[0] = 0; negative entries are bad tokens (empty
+// slice, their bits OR-ed into *status).  If the total exceeds capacity,
+// every slice is emptied and bit 32 is raised.  Writes *status.
 __global__ void __launch_bounds__(kScanThreads)
 build_scan_kernel(int N, int64_t capacity, int32_t* __restrict__ kv_indptr,
                   int32_t* __restrict__ status) {
   __shared__ long long warp_sums[32];
   __shared__ long long s_carry;
   __shared__ int s_over;
+  __shared__ int s_flags;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     s_carry = 0;
     s_over = 0;
+    s_flags = 0;
   }
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
   for (int t0 = 0; t0 < N; t0 += kScanThreads) {
     const int t = t0 + threadIdx.x;
     long long v = t < N ? kv_indptr[t + 1] : 0;
+    if (v < 0) {
+      atomicOr(&s_flags, (int)(-v));
+      v = 0;
+    }
     long long x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -108,37 +120,34 @@ build_scan_kernel(int N, int64_t capacity, int32_t* __restrict__ kv_indptr,
   }
   if (threadIdx.x == 0) kv_indptr[0] = 0;
   __syncthreads();
-  if (s_over) {
+  if (s_over)
     for (int t = threadIdx.x; t <= N; t += kScanThreads) kv_indptr[t] = 0;
-    if (threadIdx.x == 0) atomicOr(status, 32);
-  }
+  if (threadIdx.x == 0) *status = s_flags | (s_over ? 32 : 0);
 }
 
-// One warp per token: write its slots at kv_indices[kv_indptr[t] ...].
-__global__ void build_scatter_kernel(const int32_t* __restrict__ state_slot,
-                                     const int32_t* __restrict__ swa_len,
-                                     const int32_t* __restrict__ swa_head,
-                                     const int32_t* __restrict__ comp_indptr,
-                                     const int32_t* __restrict__ comp_block,
-                                     const int32_t* __restrict__ comp_slot, int N, int win,
-                                     int k_per_block, int64_t swa_pages,
-                                     const int32_t* __restrict__ kv_indptr,
-                                     int32_t* __restrict__ kv_indices) {
-  const int lane = threadIdx.x & 31;
-  const int warps = (gridDim.x * blockDim.x) >> 5;
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < N; t += warps) {
+// One CTA per token: write its slots at kv_indices[kv_indptr[t] ...].
+__global__ void __launch_bounds__(kTokThreads)
+build_scatter_kernel(const int32_t* __restrict__ state_slot, const int32_t* __restrict__ swa_len,
+                     const int32_t* __restrict__ swa_head, const int32_t* __restrict__ comp_indptr,
+                     const int32_t* __restrict__ comp_block, const int32_t* __restrict__ comp_slot,
+                     int N, int win, int k_per_block, int64_t swa_pages,
+                     const int32_t* __restrict__ kv_indptr, int32_t* __restrict__ kv_indices) {
+  pdl_wait();
+  pdl_trigger();
+  for (int t = blockIdx.x; t < N; t += gridDim.x) {
     const int32_t o0 = kv_indptr[t], o1 = kv_indptr[t + 1];
     if (o1 <= o0) continue;  // padded, bad or over capacity
     const int32_t ss = state_slot[t];
     const int32_t n_swa = swa_len[t];
     const int32_t head = swa_head[t];
-    for (int32_t j = lane; j < n_swa; j += 32) {
+    for (int32_t j = threadIdx.x; j < n_swa; j += kTokThreads) {
       int32_t ring = (int32_t)(((int64_t)head - n_swa + 1 + j) % win);
       if (ring < 0) ring += win;
       kv_indices[o0 + j] = (int32_t)((int64_t)ss * win + ring);
     }
     const int32_t c0 = comp_indptr[t], c1 = comp_indptr[t + 1];
-    for (int32_t e = c0 + lane; e < c1; e += 32)
+#pragma unroll 4
+    for (int32_t e = c0 + threadIdx.x; e < c1; e += kTokThreads)
       kv_indices[o0 + n_swa + (e - c0)] =
           (int32_t)(swa_pages + (int64_t)comp_block[e] * k_per_block + comp_slot[e]);
   }
@@ -181,23 +190,20 @@ cudaError_t launch_build_indices(const int32_t* state_slot, const int32_t* swa_l
                                  int64_t swa_pages, int64_t total_pages, int32_t* kv_indices,
                                  int64_t capacity, int32_t* kv_indptr, int32_t* status,
                                  cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
-  if (e != cudaSuccess) return e;
-  if (N == 0) {
-    return cudaMemsetAsync(kv_indptr, 0, sizeof(int32_t), st);
-  }
-  const int threads = 256;
-  int blocks = (int)(((int64_t)N * 32 + threads - 1) / threads);
-  if (blocks > 4096) blocks = 4096;
-  build_len_kernel<<<blocks, threads, 0, st>>>(state_slot, swa_len, swa_head, comp_indptr,
-                                               comp_block, comp_slot, comp_total, N, win,
-                                               k_per_block, swa_pages, total_pages, kv_indptr,
-                                               status);
-  build_scan_kernel<<<1, kScanThreads, 0, st>>>(N, capacity, kv_indptr, status);
-  build_scatter_kernel<<<blocks, threads, 0, st>>>(state_slot, swa_len, swa_head, comp_indptr,
-                                                   comp_block, comp_slot, N, win, k_per_block,
-                                                   swa_pages, kv_indptr, kv_indices);
-  return cudaGetLastError();
+  const int blocks = N < 65535 ? N : 65535;
+  cudaError_t e = cudaSuccess;
+  if (N > 0)
+    e = launch_pdl(build_len_kernel, dim3(blocks), dim3(kTokThreads), 0, st, state_slot, swa_len,
+                   swa_head, comp_indptr, comp_block, comp_slot, comp_total, N, win, k_per_block,
+                   swa_pages, total_pages, kv_indptr);
+  if (e == cudaSuccess)
+    e = launch_pdl(build_scan_kernel, dim3(1), dim3(kScanThreads), 0, st, N, capacity, kv_indptr,
+                   status);
+  if (e == cudaSuccess && N > 0)
+    e = launch_pdl(build_scatter_kernel, dim3(blocks), dim3(kTokThreads), 0, st, state_slot, swa_len,
+                   swa_head, comp_indptr, comp_block, comp_slot, N, win, k_per_block, swa_pages,
+                   (const int32_t*)kv_indptr, kv_indices);
+  return e;
 }
 
 cudaError_t launch_validate(const int32_t* kv_indices, int64_t total_indices,

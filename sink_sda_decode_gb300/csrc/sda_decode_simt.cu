@@ -84,6 +84,8 @@ decode_simt_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
                    float2* __restrict__ part_ml, float* __restrict__ part_o) {
   using S = LaneShape<D>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  pdl_wait();
+  pdl_trigger();
   const int n_units = hdr->n_units;
   for (int k = 0;; ++k) {
     const int pos = unit_position(k, blockIdx.x, gridDim.x);
@@ -171,12 +173,13 @@ cudaError_t launch_simt_d(const void* q, const void* kv, const int32_t* kv_indic
                           const float* attn_sink, float scale, int H, void* out, void* ws,
                           const WsLayout& L, const LaunchPlan& lp, cudaStream_t st) {
   char* base = static_cast<char*>(ws);
-  decode_simt_kernel<D><<<lp.grid, kSimtThreads, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kv), kv_indices,
-      attn_sink, scale * kLog2e, H, static_cast<__nv_bfloat16*>(out),
-      reinterpret_cast<const WsHeader*>(base), reinterpret_cast<const int4*>(base + L.units_off),
-      reinterpret_cast<float2*>(base + L.ml_off), reinterpret_cast<float*>(base + L.o_off));
-  return cudaGetLastError();
+  return launch_pdl(decode_simt_kernel<D>, dim3(lp.grid), dim3(kSimtThreads), 0, st,
+                    static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kv),
+                    kv_indices, attn_sink, scale * kLog2e, H, static_cast<__nv_bfloat16*>(out),
+                    reinterpret_cast<const WsHeader*>(base),
+                    reinterpret_cast<const int4*>(base + L.units_off),
+                    reinterpret_cast<float2*>(base + L.ml_off),
+                    reinterpret_cast<float*>(base + L.o_off));
 }
 
 }  // namespace

@@ -14,14 +14,18 @@
 //    token's slot list for NH <= 64 heads (H = 128 uses two CTAs per token).
 //    All heads of a token share each gathered KV row, so a row is read from
 //    HBM once per CTA.
-//  * Warp 0 gathers KV tiles of 64 slots with TMA tile::gather4 (four rows x
-//    128 bytes per instruction) into 128-byte-swizzled shared memory, two
-//    stages deep, and loads q[t] with plain tiled TMA.
-//  * Warp 1 issues tcgen05 MMAs:  S = Q K^T  (M = 64 padded heads, N = 64
-//    slots, K = 512) into TMEM, then  O^T += V^T P^T  (M = 128 rows of D,
-//    N = NH heads, K = 64 slots) into a TMEM accumulator.  The same shared
-//    tile is K (K-major operand) and V (MN-major operand).
-//  * Warps 2..5 read S rows from TMEM (one head per thread), run the online
+//  * Warps 0..3 load KV tiles of 64 slots: each 1 KB row is read by a whole
+//    warp as two contiguous 512-byte loads (32 x 16 B in flight per thread),
+//    then stored 128-byte-swizzled into one of two shared-memory stages.
+//    Whole-row loads keep DRAM accesses contiguous; TMA tile::gather4, which
+//    fetches 128 bytes of four rows per instruction, topped out near a third
+//    of HBM bandwidth on this GPU.
+//  * Warp 8 issues tcgen05 MMAs, event driven:  S = Q K^T  (M = 64 padded
+//    heads, N = 64 slots, K = 512) into TMEM, and  O^T += V^T P^T  (M = 128
+//    rows of D, N = NH heads, K = 64 slots) into a TMEM accumulator; the same
+//    shared tile is K (K-major operand) and V (MN-major operand).  It also
+//    loads q[t] with tiled TMA once the previous unit's last QK is done.
+//  * Warps 4..7 read S rows from TMEM (one head per thread), run the online
 //    softmax, write P (bf16) to shared memory, rescale O^T in TMEM only when
 //    a head's running max grows by more than 8 (2^8 headroom, so p <= 256),
 //    and finally normalise with the sink and write out (or, for a piece of a
@@ -49,8 +53,11 @@ constexpr int kPanelKV = kTileN * 128;     // bytes of one KV panel
 constexpr int kQBytes = kPanels * kPanelQ;     // 64 KB
 constexpr int kKVBytes = kPanels * kPanelKV;   // 64 KB per stage
 constexpr int kStages = 2;
-constexpr int kThreads = 192;              // 6 warps
-constexpr int kSoftmaxWarp0 = 2;           // warps 2..5: softmax / epilogue
+constexpr int kLoaderWarps = 4;            // warps 0..3: KV row loaders
+constexpr int kSoftmaxWarp0 = 4;           // warps 4..7: softmax / epilogue
+constexpr int kMmaWarp = 8;                // warp 8: MMA issuer + q loads
+constexpr int kThreads = 288;              // 9 warps
+constexpr int kRowsPerLoader = kTileSlots / kLoaderWarps;  // 16 rows of a tile per loader warp
 constexpr int kSoftmaxThreads = 128;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
@@ -96,6 +103,7 @@ struct Cfg {
 
 struct Params {
   const __nv_bfloat16* q;
+  const __nv_bfloat16* kv;
   const int32_t* kv_indices;
   const float* attn_sink;
   __nv_bfloat16* out;
@@ -140,10 +148,62 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, WsHeade
   }
 }
 
+// Walks the tiles of the units a CTA owns, in the same order in every role:
+// unit k of CTA b is unit_position(k, b, G); units without slots are skipped.
+struct TileCursor {
+  const int4* units;
+  int n_units;
+  int k;       // unit slot in the CTA's sequence
+  int4 u;      // current unit
+  int ntiles;  // tiles of the current unit
+  int i;       // tile within the unit
+  int g;       // tiles seen before this one (all units)
+  int nu;      // units with slots seen before this one
+  bool valid;
+  __device__ __forceinline__ int len() const { return u.z; }
+  __device__ __forceinline__ void seek() {
+    for (;; ++k) {
+      const int pos = unit_position(k, blockIdx.x, gridDim.x);
+      if (pos >= n_units) {
+        valid = false;
+        return;
+      }
+      u = units[pos];
+      if (u.z > 0) {
+        ntiles = (u.z + kTileN - 1) / kTileN;
+        i = 0;
+        valid = true;
+        return;
+      }
+    }
+  }
+  __device__ __forceinline__ void init(const int4* us, int n) {
+    units = us;
+    n_units = n;
+    k = 0;
+    g = 0;
+    nu = 0;
+    seek();
+  }
+  __device__ __forceinline__ void next() {
+    ++g;
+    if (++i == ntiles) {
+      ++nu;
+      ++k;
+      seek();
+    }
+  }
+  __device__ __forceinline__ void next_unit() {
+    g += ntiles - i;
+    ++nu;
+    ++k;
+    seek();
+  }
+};
+
 template <int NH>
 __global__ void __launch_bounds__(kThreads, 1)
-decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
-                   const __grid_constant__ CUtensorMap tmap_kv, const Params p) {
+decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q, const Params p) {
   using C = Cfg<NH>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -163,8 +223,8 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQFull), 1);
     mbar_init(bar(kBarQEmpty), 1);
-    mbar_init(bar(kBarKVFull0), 1);
-    mbar_init(bar(kBarKVFull1), 1);
+    mbar_init(bar(kBarKVFull0), kLoaderWarps);
+    mbar_init(bar(kBarKVFull1), kLoaderWarps);
     mbar_init(bar(kBarPVDone0), 1);
     mbar_init(bar(kBarPVDone1), 1);
     mbar_init(bar(kBarSFull0), 1);
@@ -178,9 +238,8 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmap_q);
-    tma_prefetch_desc(&tmap_kv);
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
@@ -188,133 +247,162 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // everything above overlaps the previous kernel (PDL); global memory only below
+  pdl_wait();
+  pdl_trigger();
   const int n_units = p.hdr->n_units;
   const int H = p.H;
 
-  if (warp == 0) {
-    // ===================================================== TMA producer
-    int g = 0, nu = 0, q_issued = 0;
+  if (warp < kLoaderWarps) {
+    // ===================================================== KV row loaders
+    // Warp w owns rows [16w, 16w+16) of every tile.  Each row (1 KB) is read
+    // by the whole warp as two 512-byte contiguous loads, so every thread
+    // keeps 32 x 16 B in flight; the loads of a tile are issued before the
+    // warp waits for the tile's shared-memory stage, and then stored into the
+    // 128-byte-swizzled K-major layout the MMAs read.  (Whole-row loads keep
+    // DRAM accesses contiguous; per-128-byte TMA gathers could not.)
+    const uint4* kv4 = reinterpret_cast<const uint4*>(p.kv);
+    TileCursor cur;
+    cur.init(p.units, n_units);
+    int my_slot = -1;  // lanes 0..15: slot of row 16w + lane of the current tile
+    auto fetch_slots = [&]() {
+      const int n = min(kTileN, cur.len() - cur.i * kTileN);
+      const int r = warp * kRowsPerLoader + lane;
+      my_slot = (lane < kRowsPerLoader && r < n) ? __ldg(p.kv_indices + cur.u.y + cur.i * kTileN + r) : -1;
+    };
+    if (cur.valid) fetch_slots();
     bool ok = true;
-    for (int k = 0; ok; ++k) {
-      const int pos = unit_position(k, blockIdx.x, gridDim.x);
-      if (pos >= n_units) break;
-      const int4 u = p.units[pos];
-      const int len = u.z;
-      if (len <= 0) continue;
-      const int hg = unit_head_group(u.w);
-      const int ntiles = (len + kTileN - 1) / kTileN;
-      if (lane == 0) {
-        if (nu >= 1) ok = wait_bar(bar(kBarQEmpty), (nu - 1) & 1, abort_flag, p.hdr);
-        if (ok) {
-          mbar_arrive_expect_tx(bar(kBarQFull), NH * 128 * kPanels);
-          const int qrow = u.x * H + hg * NH;
+    while (cur.valid && ok) {
+      const int g = cur.g, s = g & 1;
+      uint4 v[2 * kRowsPerLoader];
 #pragma unroll
-          for (int c = 0; c < kPanels; ++c) tma_load_2d(sQ + c * kPanelQ, &tmap_q, c * 64, qrow, bar(kBarQFull));
-          q_issued = nu + 1;
+      for (int r = 0; r < kRowsPerLoader; ++r) {
+        const int slot = __shfl_sync(0xffffffffu, my_slot, r);
+        if (slot >= 0) {
+          const uint4* src = kv4 + (size_t)slot * (kD / 8);
+          v[2 * r] = __ldcg(src + lane);
+          v[2 * r + 1] = __ldcg(src + 32 + lane);
+        } else {  // tail row of a partial tile: zeros (its p is forced to 0)
+          v[2 * r] = make_uint4(0, 0, 0, 0);
+          v[2 * r + 1] = make_uint4(0, 0, 0, 0);
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      for (int i = 0; i < ntiles && ok; ++i, ++g) {
-        const int s = g & 1;
-        const int base = u.y + i * kTileN;
-        const int n = min(kTileN, len - i * kTileN);
-        int i0 = lane < n ? __ldg(p.kv_indices + base + lane) : 0;
-        int i1 = lane + 32 < n ? __ldg(p.kv_indices + base + lane + 32) : 0;
-        const int first = __shfl_sync(0xffffffffu, i0, 0);
-        if (lane >= n) i0 = first;        // pad the tail with a valid row;
-        if (lane + 32 >= n) i1 = first;   // its probability is forced to 0
-        if (lane == 0 && g >= 2) ok = wait_bar(bar(kBarPVDone0 + s), ((g >> 1) - 1) & 1, abort_flag, p.hdr);
+      cur.next();
+      if (cur.valid) fetch_slots();  // next tile's slots, while this tile's rows are in flight
+      if (g >= 2) {
+        if (lane == 0) ok = wait_bar(bar(kBarPVDone0 + s), ((g >> 1) - 1) & 1, abort_flag, p.hdr);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        if (lane == 0) mbar_arrive_expect_tx(bar(kBarKVFull0 + s), kKVBytes);
-        __syncwarp();
-        const int g4 = lane & 15;
-        int y[4];
+      }
+      uint8_t* stage = smem + C::kOffKV + s * kKVBytes;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int row = 4 * g4 + r;
-          const int a = __shfl_sync(0xffffffffu, i0, row & 31);
-          const int b = __shfl_sync(0xffffffffu, i1, row & 31);
-          y[r] = row < 32 ? a : b;
-        }
-        const uint32_t dst0 = sKV + s * kKVBytes + g4 * 512;
-        const int c0 = (lane >> 4) * 4;
+      for (int r = 0; r < kRowsPerLoader; ++r) {
+        const int row = warp * kRowsPerLoader + r;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const int c = c0 + cc;
-          tma_gather4(dst0 + c * kPanelKV, &tmap_kv, c * 64, y[0], y[1], y[2], y[3], bar(kBarKVFull0 + s));
+        for (int h = 0; h < 2; ++h) {
+          const int q = h * 32 + lane;  // 16-byte chunk of the row, 0..63
+          const int c = q >> 3, k = q & 7;
+          *reinterpret_cast<uint4*>(stage + c * kPanelKV + (row >> 3) * 1024 + (row & 7) * 128 +
+                                    ((k ^ (row & 7)) << 4)) = v[2 * r + h];
         }
       }
-      ++nu;
+      fence_proxy_async_smem();  // generic-proxy stores -> read by the tensor cores
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarKVFull0 + s));
     }
-    // drain: make sure every copy this warp started has landed before exit
+  } else if (warp == kMmaWarp) {
+    // ===================================================== MMA issuer (+ q loads)
+    // Event driven: QK of tile gq is issued as soon as its KV tile has
+    // landed, PV of tile gp as soon as its P is written, and q of the next
+    // unit as soon as the previous unit's last QK is done -- none of them
+    // waits behind another, so a KV stage is released as early as possible.
     if (lane == 0) {
-      for (int gg = (g >= 2 ? g - 2 : 0); gg < g; ++gg)
-        drain_bar(bar(kBarKVFull0 + (gg & 1)), (gg >> 1) & 1, p.hdr);
-      if (q_issued >= 1) drain_bar(bar(kBarQFull), (q_issued - 1) & 1, p.hdr);
-    }
-  } else if (warp == 1) {
-    // ===================================================== MMA issuer
-    if (lane == 0) {
-      int g = 0, nu = 0;
-      bool ok = true;
-      auto issue_pv = [&](int gp, bool first, int nu_cur) -> bool {
-        const int sp = gp & 1;
-        if (!wait_bar(bar(kBarPFull0 + sp), (gp >> 1) & 1, abort_flag, p.hdr)) return false;
-        if (first && nu_cur >= 1)
-          if (!wait_bar(bar(kBarOEmpty), (nu_cur - 1) & 1, abort_flag, p.hdr)) return false;
-        tc_fence_after();
-        const uint32_t kvs = sKV + sp * kKVBytes;
-        const uint32_t ps = sP + sp * C::kPBytes;
+      TileCursor cq, cp, cql;
+      cq.init(p.units, n_units);
+      cp.init(p.units, n_units);
+      cql.init(p.units, n_units);
+      int q_issued = 0;
+      uint64_t t_last = globaltimer_ns();
+      uint32_t spins = 0;
+      while (cq.valid || cp.g < cq.g) {
+        bool did = false;
+        if (cql.valid && (cql.nu == 0 || mbar_test_wait(bar(kBarQEmpty), (cql.nu - 1) & 1))) {
+          mbar_arrive_expect_tx(bar(kBarQFull), NH * 128 * kPanels);
+          const int qrow = cql.u.x * H + unit_head_group(cql.u.w) * NH;
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            // A = V^T block b: rows d in [128b, 128b+128) = panels 2b, 2b+1 (MN-major);
-            //     K = slots [16kk, 16kk+16) = row groups 2kk, 2kk+1
-            const uint64_t a = sdesc_sw128(kvs + (2 * b) * kPanelKV + kk * 2048, kPanelKV, 1024);
-            // B = P^T: N = NH heads (rows), K = 16 slots at byte offset 32kk (K-major)
-            const uint64_t bd = sdesc_sw128(ps + kk * 32, 16, 1024);
-            mma_bf16(tmem + C::kOCol + b * NH, a, bd, C::kIdescPV, (first && kk == 0) ? 0u : 1u);
-          }
+          for (int c = 0; c < kPanels; ++c)
+            tma_load_2d(sQ + c * kPanelQ, &tmap_q, c * 64, qrow, bar(kBarQFull));
+          q_issued = cql.nu + 1;
+          cql.next_unit();
+          did = true;
         }
-        mma_commit(bar(kBarPVDone0 + sp));
-        return true;
-      };
-      for (int k = 0; ok; ++k) {
-        const int pos = unit_position(k, blockIdx.x, gridDim.x);
-        if (pos >= n_units) break;
-        const int4 u = p.units[pos];
-        const int len = u.z;
-        if (len <= 0) continue;
-        const int ntiles = (len + kTileN - 1) / kTileN;
-        ok = wait_bar(bar(kBarQFull), nu & 1, abort_flag, p.hdr);
-        for (int i = 0; i < ntiles && ok; ++i, ++g) {
-          const int s = g & 1;
-          ok = wait_bar(bar(kBarKVFull0 + s), (g >> 1) & 1, abort_flag, p.hdr);
-          if (ok && g >= 2) ok = wait_bar(bar(kBarSEmpty0 + s), ((g >> 1) - 1) & 1, abort_flag, p.hdr);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t kvs = sKV + s * kKVBytes;
+        if (cq.valid) {
+          const int g = cq.g, s = g & 1;
+          if (mbar_test_wait(bar(kBarKVFull0 + s), (g >> 1) & 1) &&
+              (g < 2 || mbar_test_wait(bar(kBarSEmpty0 + s), ((g >> 1) - 1) & 1)) &&
+              (cq.i != 0 || mbar_test_wait(bar(kBarQFull), cq.nu & 1))) {
+            tc_fence_after();
+            const uint32_t kvs = sKV + s * kKVBytes;
 #pragma unroll
-          for (int c = 0; c < kPanels; ++c) {
+            for (int c = 0; c < kPanels; ++c) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t a = sdesc_sw128(sQ + c * kPanelQ + kk * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(kvs + c * kPanelKV + kk * 32, 16, 1024);
-              mma_bf16(tmem + s * 64, a, bd, C::kIdescQK, (c | kk) ? 1u : 0u);
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t a = sdesc_sw128(sQ + c * kPanelQ + kk * 32, 16, 1024);
+                const uint64_t bd = sdesc_sw128(kvs + c * kPanelKV + kk * 32, 16, 1024);
+                mma_bf16(tmem + s * 64, a, bd, C::kIdescQK, (c | kk) ? 1u : 0u);
+              }
             }
+            mma_commit(bar(kBarSFull0 + s));
+            if (cq.i == cq.ntiles - 1) mma_commit(bar(kBarQEmpty));
+            cq.next();
+            did = true;
           }
-          mma_commit(bar(kBarSFull0 + s));
-          if (i == ntiles - 1) mma_commit(bar(kBarQEmpty));
-          if (i >= 1) ok = issue_pv(g - 1, i == 1, nu);
         }
-        if (ok) ok = issue_pv(g - 1, ntiles == 1, nu);
-        ++nu;
+        if (cp.g < cq.g) {
+          const int g = cp.g, s = g & 1;
+          const bool first = cp.i == 0;
+          if (mbar_test_wait(bar(kBarPFull0 + s), (g >> 1) & 1) &&
+              (!first || cp.nu == 0 || mbar_test_wait(bar(kBarOEmpty), (cp.nu - 1) & 1))) {
+            tc_fence_after();
+            const uint32_t kvs = sKV + s * kKVBytes;
+            const uint32_t ps = sP + s * C::kPBytes;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                // A = V^T block b: rows d in [128b, 128b+128) = panels 2b, 2b+1 (MN-major);
+                //     K = slots [16kk, 16kk+16) = row groups 2kk, 2kk+1
+                const uint64_t a = sdesc_sw128(kvs + (2 * b) * kPanelKV + kk * 2048, kPanelKV, 1024);
+                // B = P^T: N = NH heads (rows), K = 16 slots at byte offset 32kk (K-major)
+                const uint64_t bd = sdesc_sw128(ps + kk * 32, 16, 1024);
+                mma_bf16(tmem + C::kOCol + b * NH, a, bd, C::kIdescPV, (first && kk == 0) ? 0u : 1u);
+              }
+            }
+            mma_commit(bar(kBarPVDone0 + s));
+            cp.next();
+            did = true;
+          }
+        }
+        if (did) {
+          spins = 0;
+          continue;
+        }
+        __nanosleep(32);  // idle: leave issue slots to the softmax warp on this sub-partition
+        if ((++spins & 63u) == 0) {
+          if (*abort_flag) break;
+          const uint64_t now = globaltimer_ns();
+          if (spins == 64) t_last = now;  // first idle probe since the last issue
+          else if (now - t_last > kWaitTimeoutNs) {
+            *abort_flag = 1;
+            atomicExch(&p.hdr->error, 1);
+            break;
+          }
+        }
       }
-      // drain the tensor pipe before TMEM is released
+      // drain the tensor pipe and the last q copy before TMEM and smem go away
       mma_commit(bar(kBarDrain));
       drain_bar(bar(kBarDrain), 0, p.hdr);
+      if (q_issued >= 1) drain_bar(bar(kBarQFull), (q_issued - 1) & 1, p.hdr);
     }
     __syncwarp();
   } else {
@@ -446,6 +534,10 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         }
       }
       named_bar_sync(1, kSoftmaxThreads);
+      // The P buffers are idle here (the unit's last PV is done): each warp
+      // stages its 32 rows of D x 16 heads there, so that the bf16 output
+      // leaves as 16-byte stores (64 contiguous bytes per head).
+      __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + C::kOffP + q4 * 1024);
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
         const int d = b * 128 + q4 * 32 + lane;
@@ -455,10 +547,20 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
           tmem_ld16(tmem + lane_base + C::kOCol + b * NH + c * 16, ov);
           tmem_wait_ld();
           if (row < 0) {
-            __nv_bfloat16* o = p.out + ((size_t)t * H + hg * NH + c * 16) * kD + d;
-#pragma unroll
             // "+ 0.f" turns -0 into +0 when the factor is 0 (sink = +inf)
-            for (int e = 0; e < 16; ++e) o[(size_t)e * kD] = __float2bfloat16_rn(__uint_as_float(ov[e]) * s_fac[c * 16 + e] + 0.f);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              stage[e * 32 + lane] = __float2bfloat16_rn(__uint_as_float(ov[e]) * s_fac[c * 16 + e] + 0.f);
+            __syncwarp();
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2) {
+              const int chunk = lane + 32 * k2;  // 16 heads x 4 chunks of 8 d
+              const int hh = chunk >> 2, part = chunk & 3;
+              const uint4 v = *reinterpret_cast<const uint4*>(stage + hh * 32 + part * 8);
+              *reinterpret_cast<uint4*>(p.out + ((size_t)t * H + hg * NH + c * 16 + hh) * kD + b * 128 +
+                                        q4 * 32 + part * 8) = v;
+            }
+            __syncwarp();
           } else {
             float* o = p.part_o + ((size_t)row * H + hg * NH + c * 16) * kD + d;
 #pragma unroll
@@ -475,7 +577,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
 }
 
 // ------------------------------------------------------------------ host side
@@ -514,13 +616,14 @@ template <int NH>
 cudaError_t launch_nh(const void* q, const void* kv, int64_t total_pages, const int32_t* kv_indices,
                       const float* attn_sink, float scale, int N, int H, void* out, void* ws,
                       const WsLayout& L, const LaunchPlan& lp, cudaStream_t st) {
-  CUtensorMap tq, tkv;
-  if (!make_map_2d(&tq, q, kD, (uint64_t)N * H, 64, NH, CU_TENSOR_MAP_L2_PROMOTION_L2_128B) ||
-      !make_map_2d(&tkv, kv, kD, (uint64_t)total_pages, 64, 1, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
+  (void)total_pages;
+  CUtensorMap tq;
+  if (!make_map_2d(&tq, q, kD, (uint64_t)N * H, 64, NH, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
     return cudaErrorInvalidValue;
   char* base = static_cast<char*>(ws);
   Params p;
   p.q = static_cast<const __nv_bfloat16*>(q);
+  p.kv = static_cast<const __nv_bfloat16*>(kv);
   p.kv_indices = kv_indices;
   p.attn_sink = attn_sink;
   p.out = static_cast<__nv_bfloat16*>(out);
@@ -530,8 +633,8 @@ cudaError_t launch_nh(const void* q, const void* kv, int64_t total_pages, const 
   p.part_o = reinterpret_cast<float*>(base + L.o_off);
   p.qk_scale_log2 = scale * kLog2e;
   p.H = H;
-  decode_umma_kernel<NH><<<lp.grid, kThreads, Cfg<NH>::kSmem, st>>>(tq, tkv, p);
-  return cudaGetLastError();
+  return launch_pdl(decode_umma_kernel<NH>, dim3(lp.grid), dim3(kThreads), (size_t)Cfg<NH>::kSmem,
+                    st, tq, p);
 }
 
 }  // namespace

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/sda.h"
 
 namespace sda {
@@ -99,8 +101,36 @@ cudaError_t launch_validate(const int32_t* kv_indices, int64_t total_indices,
                             const int32_t* kv_indptr, int N, int64_t total_pages,
                             int32_t* status, cudaStream_t st);
 
+// Launch with programmatic dependent launch (PDL): the kernel may start while
+// the previous kernel on the stream is still running (once that kernel has
+// executed griddepcontrol.launch_dependents or exited).  Every kernel of this
+// library calls pdl_wait() before its first global-memory access, which
+// waits for the previous grid to complete and its writes to be visible, so
+// only prologues (barrier init, TMEM allocation, descriptor prefetch)
+// overlap.  Also valid inside CUDA-graph capture.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // ---------------------------------------------------------------- device helpers
 #ifdef __CUDACC__
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
   // hardware base-2 exponential (MUFU.EX2); ex2(-inf) = +0
   float y;

@@ -73,6 +73,8 @@ plan_kernel(const int32_t* __restrict__ indptr, int N, long long total_indices, 
   __shared__ int s_chunk;
 
   if (threadIdx.x < kBuckets) bucket_count[threadIdx.x] = 0;
+  pdl_wait();
+  pdl_trigger();
   // kv_indptr must be a true prefix sum inside [0, total_indices]; otherwise
   // nothing is planned (out is left unwritten) and the error word reads 2, so
   // that no kernel ever reads kv_indices out of bounds.
@@ -167,6 +169,7 @@ combine_kernel(const float* __restrict__ attn_sink, int H, int D,
                __nv_bfloat16* __restrict__ out, const WsHeader* __restrict__ hdr,
                const int4* __restrict__ splits, const float2* __restrict__ part_ml,
                const float* __restrict__ part_o) {
+  pdl_wait();
   const int n_items = hdr->n_split * H;
   for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
     const int si = w / H, h = w % H;
@@ -206,11 +209,10 @@ combine_kernel(const float* __restrict__ attn_sink, int H, int D,
 cudaError_t launch_plan(const int32_t* kv_indptr, int N, int64_t total_indices,
                         const LaunchPlan& lp, void* ws, const WsLayout& L, cudaStream_t st) {
   char* base = static_cast<char*>(ws);
-  plan_kernel<<<1, kPlanThreads, 0, st>>>(kv_indptr, N, (long long)total_indices, lp.hg, lp.grid,
-                                           reinterpret_cast<WsHeader*>(base),
-                                           reinterpret_cast<int4*>(base + L.units_off),
-                                           reinterpret_cast<int4*>(base + L.split_off));
-  return cudaGetLastError();
+  return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, kv_indptr, N,
+                    (long long)total_indices, lp.hg, lp.grid, reinterpret_cast<WsHeader*>(base),
+                    reinterpret_cast<int4*>(base + L.units_off),
+                    reinterpret_cast<int4*>(base + L.split_off));
 }
 
 cudaError_t launch_combine(const float* attn_sink, int N, int H, int D, void* out, void* ws,
@@ -218,14 +220,13 @@ cudaError_t launch_combine(const float* attn_sink, int N, int H, int D, void* ou
   if (L.s_max == 0) return cudaSuccess;
   char* base = static_cast<char*>(ws);
   int blocks = L.s_max * H;
-  if (blocks > num_sms * 8) blocks = num_sms * 8;
+  if (blocks > num_sms * 2) blocks = num_sms * 2;
   if (blocks < 1) blocks = 1;
-  combine_kernel<<<blocks, 128, 0, st>>>(attn_sink, H, D, static_cast<__nv_bfloat16*>(out),
-                                         reinterpret_cast<const WsHeader*>(base),
-                                         reinterpret_cast<const int4*>(base + L.split_off),
-                                         reinterpret_cast<const float2*>(base + L.ml_off),
-                                         reinterpret_cast<const float*>(base + L.o_off));
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(blocks), dim3(128), 0, st, attn_sink, H, D,
+                    static_cast<__nv_bfloat16*>(out), reinterpret_cast<const WsHeader*>(base),
+                    reinterpret_cast<const int4*>(base + L.split_off),
+                    reinterpret_cast<const float2*>(base + L.ml_off),
+                    reinterpret_cast<const float*>(base + L.o_off));
 }
 
 }  // namespace sda

@@ -260,3 +260,17 @@ def test_decode_host_e2e():
     out = sda.decode_host(q_h, w.unified_kv, idx_h, ptr_h, w.attn_sink, w.softmax_scale)
     assert not out.is_cuda
     parity.assert_parity(parity.compare(out, parity.run_oracle(w)), "host e2e")
+
+
+def test_timing_hook_records_around_the_kernel():
+    w = inputs.random_small(seed=19, N=8, H=64, D=512, P=30000, lengths=[640] * 8, device="cuda")
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    sda.set_timing_events(a, b)
+    try:
+        out = parity.run_gpu(w)
+    finally:
+        sda.set_timing_events(None, None)
+    torch.cuda.synchronize()
+    assert a.elapsed_time(b) > 0.0
+    parity.assert_parity(parity.compare(out, parity.run_oracle(w)), "timing hook")
