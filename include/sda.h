@@ -96,6 +96,36 @@ sda_status sda_decode(const void* q, const void* unified_kv, int64_t total_pages
                       void* stream);
 
 /*
+ * sda_decode without a workspace argument, for callers that cannot allocate
+ * device memory: hosts that give an operator only its input and output
+ * buffers and forbid it to allocate (e.g. an inference engine that owns all
+ * device memory under a fixed budget), or C callers with no device allocator
+ * of their own.  The paper has no counterpart; this is a service of this
+ * library.
+ *
+ * Same arguments, results and errors as sda_decode, except the workspace:
+ * the scratch memory is a fixed device array of SDA_NOALLOC_SCRATCH_BYTES
+ * (16 MiB) inside this library, which every GPU that loads the library holds
+ * until the process exits.  The call allocates and frees nothing.
+ *   - A call whose sda_decode_workspace_size() exceeds
+ *     SDA_NOALLOC_SCRATCH_BYTES returns SDA_ERR_WORKSPACE and enqueues
+ *     nothing (e.g. H = 16, D = 512 fits; H >= 64 at D = 512 on a GB300
+ *     does not: use sda_decode with a workspace of your own there).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture begins.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents.  Nothing in it has to start at zero (every call rewrites what
+ *     it reads), but two calls that overlap on the GPU -- on different
+ *     streams, or from different threads -- race on it: order them.
+ */
+#define SDA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+sda_status sda_decode_noalloc(const void* q, const void* unified_kv, int64_t total_pages,
+                              const int32_t* kv_indices, int64_t total_indices,
+                              const int32_t* kv_indptr, const float* attn_sink,
+                              float softmax_scale, int N, int H, int D, void* out, void* stream);
+
+/*
  * Device-side error word of the last sda_decode that used `workspace`:
  * copies one int32 (0 = fine, nonzero = a pipeline wait timed out and the
  * affected outputs are unspecified) into *device_flag (device memory),

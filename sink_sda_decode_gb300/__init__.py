@@ -21,7 +21,7 @@ import torch
 from . import _lib
 
 __all__ = ["decode", "workspace_size", "build_indices", "validate_indices", "decode_error_flag",
-           "decode_host", "set_timing_events", "library_path"]
+           "decode_host", "set_timing_events", "decode_noalloc", "library_path"]
 
 library_path = _lib.LIB_PATH
 
@@ -98,6 +98,34 @@ def decode(q: torch.Tensor, unified_kv: torch.Tensor, kv_indices: torch.Tensor,
                             float(softmax_scale), N, H, D, out.data_ptr(), workspace.data_ptr(),
                             workspace.numel(), _stream_ptr(stream))
     _lib.check(rc, "sda_decode")
+    return out
+
+
+def decode_noalloc(q: torch.Tensor, unified_kv: torch.Tensor, kv_indices: torch.Tensor,
+                   kv_indptr: torch.Tensor, attn_sink: torch.Tensor, softmax_scale: float,
+                   out: torch.Tensor, stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """decode() for callers that may not allocate device memory: `out` must be
+    given, and the scratch memory is the library's fixed 16 MiB device array
+    (calls that would need more raise; overlapping calls on the GPU race on
+    the shared array).  Asynchronous on `stream`."""
+    lib = _lib.load()
+    _req(q, "q", torch.bfloat16, 3)
+    dev = q.device
+    _req(unified_kv, "unified_kv", torch.bfloat16, 2, dev)
+    _req(kv_indices, "kv_indices", torch.int32, 1, dev)
+    _req(kv_indptr, "kv_indptr", torch.int32, 1, dev)
+    _req(attn_sink, "attn_sink", torch.float32, 1, dev)
+    _req(out, "out", torch.bfloat16, 3, dev)
+    N, H, D = q.shape
+    if out.shape != q.shape or kv_indptr.numel() != N + 1 or attn_sink.numel() != H:
+        raise ValueError("shape mismatch")
+    with torch.cuda.device(dev):
+        rc = lib.sda_decode_noalloc(q.data_ptr(), unified_kv.data_ptr(), unified_kv.shape[0],
+                                    kv_indices.data_ptr() if kv_indices.numel() else None,
+                                    kv_indices.numel(), kv_indptr.data_ptr(), attn_sink.data_ptr(),
+                                    float(softmax_scale), N, H, D, out.data_ptr(),
+                                    _stream_ptr(stream))
+    _lib.check(rc, "sda_decode_noalloc")
     return out
 
 
