@@ -14,22 +14,24 @@
 //    token's slot list for NH <= 64 heads (H = 128 uses two CTAs per token).
 //    All heads of a token share each gathered KV row, so a row is read from
 //    HBM once per CTA.
-//  * Warps 0..3 load KV tiles of 64 slots: each 1 KB row is read by a whole
-//    warp as two contiguous 512-byte loads (32 x 16 B in flight per thread),
-//    then stored 128-byte-swizzled into one of two shared-memory stages.
-//    Whole-row loads keep DRAM accesses contiguous; TMA tile::gather4, which
-//    fetches 128 bytes of four rows per instruction, topped out near a third
-//    of HBM bandwidth on this GPU.
-//  * Warp 8 issues tcgen05 MMAs, event driven:  S = Q K^T  (M = 64 padded
-//    heads, N = 64 slots, K = 512) into TMEM, and  O^T += V^T P^T  (M = 128
-//    rows of D, N = NH heads, K = 64 slots) into a TMEM accumulator; the same
-//    shared tile is K (K-major operand) and V (MN-major operand).  It also
-//    loads q[t] with tiled TMA once the previous unit's last QK is done.
-//  * Warps 4..7 read S rows from TMEM (one head per thread), run the online
-//    softmax, write P (bf16) to shared memory, rescale O^T in TMEM only when
-//    a head's running max grows by more than 8 (2^8 headroom, so p <= 256),
-//    and finally normalise with the sink and write out (or, for a piece of a
-//    split token, write the unnormalised partial for the combine kernel).
+//  * Warps 4..11 load KV tiles of 64 slots: each 1 KB row is read by a whole
+//    warp as two contiguous 512-byte loads (16 x 16 B in flight per thread,
+//    64 KB per SM), then stored 128-byte-swizzled into one of two
+//    shared-memory stages.  Whole-row loads keep DRAM accesses contiguous;
+//    TMA tile::gather4, which fetches 128 bytes of four rows per
+//    instruction, topped out near a third of HBM bandwidth on this GPU.
+//  * Warps 12 and 13 issue tcgen05 MMAs, event driven and apart, so that one
+//    waiting for the tensor pipe never delays the other:  S = Q K^T  (M = 64
+//    padded heads, N = 64 slots, K = 512) into TMEM by warp 12, which also
+//    loads q[t] with tiled TMA, and  O^T += V^T P^T  (M = 128 rows of D,
+//    N = NH heads, K = 64 slots) into a TMEM accumulator by warp 13; the
+//    same shared tile is K (K-major operand) and V (MN-major operand).
+//  * Warps 0..3 read S from TMEM (two heads per quad of threads), run the
+//    online softmax, write P (bf16) to shared memory, rescale O^T in TMEM
+//    only when a head's running max grows by more than 8 (2^8 headroom, so
+//    p <= 256), and finally normalise with the sink and write out through
+//    TMA stores (or, for a piece of a split token, write the unnormalised
+//    partial for the combine kernel).
 //  * Every mbarrier wait is bounded (2 s); on timeout the kernel raises the
 //    workspace error word, drains its own copies and returns.
 #include <cuda.h>
@@ -53,11 +55,13 @@ constexpr int kPanelKV = kTileN * 128;     // bytes of one KV panel
 constexpr int kQBytes = kPanels * kPanelQ;     // 64 KB
 constexpr int kKVBytes = kPanels * kPanelKV;   // 64 KB per stage
 constexpr int kStages = 2;
-constexpr int kLoaderWarps = 4;            // warps 0..3: KV row loaders
-constexpr int kSoftmaxWarp0 = 4;           // warps 4..7: softmax / epilogue
-constexpr int kMmaWarp = 8;                // warp 8: MMA issuer + q loads
-constexpr int kThreads = 288;              // 9 warps
-constexpr int kRowsPerLoader = kTileSlots / kLoaderWarps;  // 16 rows of a tile per loader warp
+constexpr int kSoftmaxWarp0 = 0;           // warps 0..3: softmax / epilogue (TMEM quadrants 0..3)
+constexpr int kLoaderWarp0 = 4;            // warps 4..11: KV row loaders
+constexpr int kLoaderWarps = 8;
+constexpr int kMmaWarp = 12;               // warp 12: QK issuer + q loads
+constexpr int kPvWarp = 13;                // warp 13: PV issuer
+constexpr int kThreads = 448;              // 14 warps (<= 128 registers per thread)
+constexpr int kRowsPerLoader = kTileSlots / kLoaderWarps;  // 8 rows of a tile per loader warp
 constexpr int kSoftmaxThreads = 128;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
@@ -77,6 +81,7 @@ enum Bar : int {
   kBarPFull1,
   kBarOEmpty,
   kBarDrain,
+  kBarDrainPv,
   kNumBars
 };
 
@@ -98,6 +103,7 @@ struct Cfg {
   static constexpr uint32_t kIdescQK = idesc_bf16_f32(64, 64, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, NH, true, false);
   static_assert(kOffP % 1024 == 0 && kPBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
+  static_assert(kNumBars * 8 <= kOffMisc - kOffBar, "mbarrier area");
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -203,7 +209,8 @@ struct TileCursor {
 
 template <int NH>
 __global__ void __launch_bounds__(kThreads, 1)
-decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q, const Params p) {
+decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                   const __grid_constant__ CUtensorMap tmap_out, const Params p) {
   using C = Cfg<NH>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -235,9 +242,11 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q, const Params p) {
     mbar_init(bar(kBarPFull1), 4);
     mbar_init(bar(kBarOEmpty), 4);
     mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarDrainPv), 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmap_q);
+    tma_prefetch_desc(&tmap_out);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
@@ -253,21 +262,21 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q, const Params p) {
   const int n_units = p.hdr->n_units;
   const int H = p.H;
 
-  if (warp < kLoaderWarps) {
+  if (warp >= kLoaderWarp0 && warp < kLoaderWarp0 + kLoaderWarps) {
     // ===================================================== KV row loaders
-    // Warp w owns rows [16w, 16w+16) of every tile.  Each row (1 KB) is read
-    // by the whole warp as two 512-byte contiguous loads, so every thread
-    // keeps 32 x 16 B in flight; the loads of a tile are issued before the
-    // warp waits for the tile's shared-memory stage, and then stored into the
-    // 128-byte-swizzled K-major layout the MMAs read.  (Whole-row loads keep
-    // DRAM accesses contiguous; per-128-byte TMA gathers could not.)
+    // Loader warp w owns rows [8w, 8w+8) of every 64-slot tile.  Each row
+    // (1 KB) is read by the whole warp as two contiguous 512-byte loads, so a
+    // thread keeps 16 x 16 B in flight and an SM 64 KB; the loads of a tile
+    // are issued before the warp waits for the tile's shared-memory stage,
+    // then stored into the 128-byte-swizzled K-major layout the MMAs read.
+    const int lw = warp - kLoaderWarp0;
     const uint4* kv4 = reinterpret_cast<const uint4*>(p.kv);
     TileCursor cur;
     cur.init(p.units, n_units);
-    int my_slot = -1;  // lanes 0..15: slot of row 16w + lane of the current tile
+    int my_slot = -1;  // lanes 0..7: slot of row 8w + lane of the current tile
     auto fetch_slots = [&]() {
       const int n = min(kTileN, cur.len() - cur.i * kTileN);
-      const int r = warp * kRowsPerLoader + lane;
+      const int r = lw * kRowsPerLoader + lane;
       my_slot = (lane < kRowsPerLoader && r < n) ? __ldg(p.kv_indices + cur.u.y + cur.i * kTileN + r) : -1;
     };
     if (cur.valid) fetch_slots();
@@ -297,7 +306,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q, const Params p) {
       uint8_t* stage = smem + C::kOffKV + s * kKVBytes;
 #pragma unroll
       for (int r = 0; r < kRowsPerLoader; ++r) {
-        const int row = warp * kRowsPerLoader + r;
+        const int row = lw * kRowsPerLoader + r;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int q = h * 32 + lane;  // 16-byte chunk of the row, 0..63
@@ -310,37 +319,40 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q, const Params p) {
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarKVFull0 + s));
     }
-  } else if (warp == kMmaWarp) {
-    // ===================================================== MMA issuer (+ q loads)
-    // Event driven: QK of tile gq is issued as soon as its KV tile has
-    // landed, PV of tile gp as soon as its P is written, and q of the next
-    // unit as soon as the previous unit's last QK is done -- none of them
-    // waits behind another, so a KV stage is released as early as possible.
+  } else if (warp == kMmaWarp || warp == kPvWarp) {
+    // ===================================================== MMA issuers
+    // Two threads issue tcgen05 MMAs, so that one waiting for the tensor
+    // pipe to accept its instructions never delays the other's reaction:
+    //  - warp 12, lane 0: q of each unit (tiled TMA, once the previous unit's
+    //    last QK is done) and S = Q K^T of every tile, as soon as the tile
+    //    has landed and its S buffer is free;
+    //  - warp 13, lane 0: O^T += V^T P^T of every tile as soon as its P is
+    //    written (its commit releases the KV stage and the P buffer).
+    // Each thread's commits track only its own MMAs.
     if (lane == 0) {
-      TileCursor cq, cp, cql;
+      const bool qk_role = warp == kMmaWarp;
+      TileCursor cq, cql;
       cq.init(p.units, n_units);
-      cp.init(p.units, n_units);
       cql.init(p.units, n_units);
       int q_issued = 0;
       uint64_t t_last = globaltimer_ns();
       uint32_t spins = 0;
-      while (cq.valid || cp.g < cq.g) {
+      while (cq.valid) {
         bool did = false;
-        if (cql.valid && (cql.nu == 0 || mbar_test_wait(bar(kBarQEmpty), (cql.nu - 1) & 1))) {
-          mbar_arrive_expect_tx(bar(kBarQFull), NH * 128 * kPanels);
-          const int qrow = cql.u.x * H + unit_head_group(cql.u.w) * NH;
+        const int g = cq.g, s = g & 1;
+        if (qk_role) {
+          if (cql.valid && (cql.nu == 0 || mbar_test_wait(bar(kBarQEmpty), (cql.nu - 1) & 1))) {
+            mbar_arrive_expect_tx(bar(kBarQFull), NH * 128 * kPanels);
+            const int qrow = cql.u.x * H + unit_head_group(cql.u.w) * NH;
 #pragma unroll
-          for (int c = 0; c < kPanels; ++c)
-            tma_load_2d(sQ + c * kPanelQ, &tmap_q, c * 64, qrow, bar(kBarQFull));
-          q_issued = cql.nu + 1;
-          cql.next_unit();
-          did = true;
-        }
-        if (cq.valid) {
-          const int g = cq.g, s = g & 1;
-          if (mbar_test_wait(bar(kBarKVFull0 + s), (g >> 1) & 1) &&
-              (g < 2 || mbar_test_wait(bar(kBarSEmpty0 + s), ((g >> 1) - 1) & 1)) &&
-              (cq.i != 0 || mbar_test_wait(bar(kBarQFull), cq.nu & 1))) {
+            for (int c = 0; c < kPanels; ++c)
+              tma_load_2d(sQ + c * kPanelQ, &tmap_q, c * 64, qrow, bar(kBarQFull));
+            q_issued = cql.nu + 1;
+            cql.next_unit();
+            did = true;
+          } else if (mbar_test_wait(bar(kBarKVFull0 + s), (g >> 1) & 1) &&
+                     (g < 2 || mbar_test_wait(bar(kBarSEmpty0 + s), ((g >> 1) - 1) & 1)) &&
+                     (cq.i != 0 || mbar_test_wait(bar(kBarQFull), cq.nu & 1))) {
             tc_fence_after();
             const uint32_t kvs = sKV + s * kKVBytes;
 #pragma unroll
@@ -357,12 +369,10 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q, const Params p) {
             cq.next();
             did = true;
           }
-        }
-        if (cp.g < cq.g) {
-          const int g = cp.g, s = g & 1;
-          const bool first = cp.i == 0;
+        } else {
+          const bool first = cq.i == 0;
           if (mbar_test_wait(bar(kBarPFull0 + s), (g >> 1) & 1) &&
-              (!first || cp.nu == 0 || mbar_test_wait(bar(kBarOEmpty), (cp.nu - 1) & 1))) {
+              (!first || cq.nu == 0 || mbar_test_wait(bar(kBarOEmpty), (cq.nu - 1) & 1))) {
             tc_fence_after();
             const uint32_t kvs = sKV + s * kKVBytes;
             const uint32_t ps = sP + s * C::kPBytes;
@@ -379,7 +389,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q, const Params p) {
               }
             }
             mma_commit(bar(kBarPVDone0 + s));
-            cp.next();
+            cq.next();
             did = true;
           }
         }
@@ -387,7 +397,6 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q, const Params p) {
           spins = 0;
           continue;
         }
-        __nanosleep(32);  // idle: leave issue slots to the softmax warp on this sub-partition
         if ((++spins & 63u) == 0) {
           if (*abort_flag) break;
           const uint64_t now = globaltimer_ns();
@@ -399,20 +408,28 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q, const Params p) {
           }
         }
       }
-      // drain the tensor pipe and the last q copy before TMEM and smem go away
-      mma_commit(bar(kBarDrain));
-      drain_bar(bar(kBarDrain), 0, p.hdr);
-      if (q_issued >= 1) drain_bar(bar(kBarQFull), (q_issued - 1) & 1, p.hdr);
+      // drain this thread's MMAs (and the last q copy) before TMEM and smem go away
+      const int drain = qk_role ? kBarDrain : kBarDrainPv;
+      mma_commit(bar(drain));
+      drain_bar(bar(drain), 0, p.hdr);
+      if (qk_role && q_issued >= 1) drain_bar(bar(kBarQFull), (q_issued - 1) & 1, p.hdr);
     }
     __syncwarp();
-  } else {
+  } else if (warp < kSoftmaxWarp0 + 4) {
     // ===================================================== softmax + epilogue
-    const int q4 = warp & 3;                  // TMEM lane quadrant of this warp
+    // S is read with the 16x256b TMEM shape: thread t of warp q4 holds heads
+    // hA = 16*q4 + t/4 and hB = hA + 8 (the M = 64 accumulator keeps row r in
+    // lane 32*(r/16) + r%16), each for the 16 slots 8*rep + 2*(t%4) + {0,1},
+    // rep = 0..7.  A head's 64 slots are spread over the 4 threads of a quad,
+    // so every lane works and row reductions are two quad shuffles.
+    const int q4 = warp & 3;                          // TMEM lane quadrant of this warp
     const int st = threadIdx.x - kSoftmaxWarp0 * 32;  // 0..127
-    // M = 64 accumulator layout: row r lives in lane 32*(r/16) + r%16.
-    const int head = (lane < 16) ? q4 * 16 + lane : -1;
-    const bool has_head = head >= 0 && head < NH;
+    const int tq = lane & 3;
+    const int hA = q4 * 16 + (lane >> 2), hB = hA + 8;
+    const bool vA = hA < NH, vB = hB < NH;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    const float sc = p.qk_scale_log2;
+    const bool pos_sc = sc >= 0.f;  // a negative scale makes the smallest score the largest logit
     // Control flow here is identical in the four warps (it depends only on
     // the unit list and on block-wide votes), so every named barrier is
     // reached by all 128 threads even after a wait timed out: a timed-out
@@ -430,63 +447,85 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q, const Params p) {
         continue;
       }
       const int ntiles = (len + kTileN - 1) / kTileN;
-      float m = -INFINITY, l = 0.f;
+      float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;  // l: this thread's share
       for (int i = 0; i < ntiles; ++i, ++g) {
         const int s = g & 1;
+        const int n = min(kTileN, len - i * kTileN);
         wait_bar(bar(kBarSFull0 + s), (g >> 1) & 1, abort_flag, p.hdr);
         tc_fence_after();
-        uint32_t sv[64];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tmem_ld16(tmem + lane_base + s * 64 + c * 16, *reinterpret_cast<uint32_t(*)[16]>(sv + 16 * c));
+        uint32_t sv[32];
+        tmem_ld_16x256b_x8(tmem + lane_base + s * 64, sv);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarSEmpty0 + s));
-        const int n = min(kTileN, len - i * kTileN);
-        float alpha = 1.f;
-        bool need_rescale = false;
-        uint32_t pk[32];
-        if (has_head) {
-          float y[64];
-          float tmax = -INFINITY;
+        if (lane == 0) mbar_arrive(bar(kBarSEmpty0 + s));  // S buffer s may be overwritten
+        // largest scaled logit per head over the tile's valid slots
+        float eA = pos_sc ? -INFINITY : INFINITY, eB = eA;
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            y[j] = j < n ? __uint_as_float(sv[j]) * p.qk_scale_log2 : -INFINITY;
-            tmax = fmaxf(tmax, y[j]);
-          }
-          if (tmax > m + kRescaleThreshold) {
-            alpha = ex2_approx(m - tmax);  // 0 on the first tile (m = -inf)
-            need_rescale = i > 0;
-            l *= alpha;
-            m = tmax;
-          }
-          float ls = 0.f;
+        for (int rep = 0; rep < 8; ++rep) {
 #pragma unroll
-          for (int j = 0; j < 64; j += 2) {
-            const float p0 = ex2_approx(y[j] - m), p1 = ex2_approx(y[j + 1] - m);
-            ls += p0 + p1;
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-            pk[j >> 1] = *reinterpret_cast<uint32_t*>(&b2);
+          for (int kk = 0; kk < 2; ++kk) {
+            if (8 * rep + 2 * tq + kk < n) {
+              const float a = __uint_as_float(sv[4 * rep + kk]), b = __uint_as_float(sv[4 * rep + 2 + kk]);
+              eA = pos_sc ? fmaxf(eA, a) : fminf(eA, a);
+              eB = pos_sc ? fmaxf(eB, b) : fminf(eB, b);
+            }
           }
-          l += ls;
+        }
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+          const float xa = __shfl_xor_sync(0xffffffffu, eA, o), xb = __shfl_xor_sync(0xffffffffu, eB, o);
+          eA = pos_sc ? fmaxf(eA, xa) : fminf(eA, xa);
+          eB = pos_sc ? fmaxf(eB, xb) : fminf(eB, xb);
+        }
+        const float tA = eA * sc, tB = eB * sc;
+        float alphaA = 1.f, alphaB = 1.f;
+        bool need = false;
+        if (vA && tA > mA + kRescaleThreshold) {
+          alphaA = ex2_approx(mA - tA);  // 0 on the first tile (m = -inf)
+          need = i > 0;
+          lA *= alphaA;
+          mA = tA;
+        }
+        if (vB && tB > mB + kRescaleThreshold) {
+          alphaB = ex2_approx(mB - tB);
+          need = need || i > 0;
+          lB *= alphaB;
+          mB = tB;
         }
         // P buffer s is free once the PV of tile g-2 is done
         if (g >= 2) {
           if (lane == 0) wait_bar(bar(kBarPVDone0 + s), ((g >> 1) - 1) & 1, abort_flag, p.hdr);
           __syncwarp();
         }
-        if (has_head) {
-          // row `head` of P (K-major, 128-byte swizzle): chunk c at (c ^ (head & 7)) * 16
-          uint8_t* prow = smem + C::kOffP + s * C::kPBytes + (head >> 3) * 1024 + (head & 7) * 128;
+        // p = 2^(s*scale - m) in bf16 into rows hA, hB of P (K-major, 128-byte
+        // swizzle: 16-byte chunk `rep` of 8 slots at (rep ^ (h & 7)) * 16,
+        // this thread's slot pair at byte 4*tq of the chunk)
+        uint8_t* pbase = smem + C::kOffP + s * C::kPBytes;
+        uint8_t* prowA = pbase + (hA >> 3) * 1024 + (hA & 7) * 128 + 4 * tq;
+        uint8_t* prowB = pbase + (hB >> 3) * 1024 + (hB & 7) * 128 + 4 * tq;
+        float sA = 0.f, sB = 0.f;
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(prow + ((c ^ (head & 7)) << 4)) =
-                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        for (int rep = 0; rep < 8; ++rep) {
+          const int j = 8 * rep + 2 * tq;
+          const float a0 = j < n ? ex2_approx(fmaf(__uint_as_float(sv[4 * rep + 0]), sc, -mA)) : 0.f;
+          const float a1 = j + 1 < n ? ex2_approx(fmaf(__uint_as_float(sv[4 * rep + 1]), sc, -mA)) : 0.f;
+          const float b0 = j < n ? ex2_approx(fmaf(__uint_as_float(sv[4 * rep + 2]), sc, -mB)) : 0.f;
+          const float b1 = j + 1 < n ? ex2_approx(fmaf(__uint_as_float(sv[4 * rep + 3]), sc, -mB)) : 0.f;
+          sA += a0 + a1;
+          sB += b0 + b1;
+          __nv_bfloat162 pa = __floats2bfloat162_rn(a0, a1), pb = __floats2bfloat162_rn(b0, b1);
+          if (vA) *reinterpret_cast<uint32_t*>(prowA + ((rep ^ (hA & 7)) << 4)) = *reinterpret_cast<uint32_t*>(&pa);
+          if (vB) *reinterpret_cast<uint32_t*>(prowB + ((rep ^ (hB & 7)) << 4)) = *reinterpret_cast<uint32_t*>(&pb);
         }
+        lA += sA;
+        lB += sB;
         fence_proxy_async_smem();
-        if (named_bar_or(1, kSoftmaxThreads, need_rescale)) {
-          if (has_head) s_alpha[head] = alpha;
+        if (named_bar_or(1, kSoftmaxThreads, need)) {
+          if (tq == 0) {
+            if (vA) s_alpha[hA] = alphaA;
+            if (vB) s_alpha[hB] = alphaB;
+          }
           named_bar_sync(1, kSoftmaxThreads);
           // O^T must be quiescent: wait for the PV of tile g-1
           if (lane == 0) wait_bar(bar(kBarPVDone0 + ((g - 1) & 1)), ((g - 1) >> 1) & 1, abort_flag, p.hdr);
@@ -513,55 +552,73 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q, const Params p) {
         if (lane == 0) mbar_arrive(bar(kBarPFull0 + s));
       }
       // ---------------------------------------------- epilogue of the unit
+      // denominators: sum the quad's shares
+      lA += __shfl_xor_sync(0xffffffffu, lA, 1);
+      lA += __shfl_xor_sync(0xffffffffu, lA, 2);
+      lB += __shfl_xor_sync(0xffffffffu, lB, 1);
+      lB += __shfl_xor_sync(0xffffffffu, lB, 2);
       const int gl = g - 1;
       if (lane == 0) wait_bar(bar(kBarPVDone0 + (gl & 1)), (gl >> 1) & 1, abort_flag, p.hdr);
       __syncwarp();
       tc_fence_after();
-      if (has_head) {
-        const int hh = hg * NH + head;
-        if (row < 0) {
-          const float ms = p.attn_sink[hh] * kLog2e;
-          const float M = fmaxf(m, ms);
-          float f = 0.f;
-          if (M != -INFINITY && ms != INFINITY) {
-            const float a = ex2_approx(m - M);
-            f = a / (l * a + ex2_approx(ms - M));
+      if (tq == 0) {
+#pragma unroll
+        for (int w2 = 0; w2 < 2; ++w2) {
+          const int hd = w2 ? hB : hA;
+          const float mh = w2 ? mB : mA, lh = w2 ? lB : lA;
+          if (hd >= NH) continue;
+          const int hh = hg * NH + hd;
+          if (row < 0) {
+            const float ms = p.attn_sink[hh] * kLog2e;
+            const float M = fmaxf(mh, ms);
+            float f = 0.f;
+            if (M != -INFINITY && ms != INFINITY) {
+              const float a = ex2_approx(mh - M);
+              f = a / (lh * a + ex2_approx(ms - M));
+            }
+            s_fac[hd] = f;
+          } else {
+            p.part_ml[(size_t)row * H + hh] = make_float2(mh, lh);
+            s_fac[hd] = 1.f;
           }
-          s_fac[head] = f;
-        } else {
-          p.part_ml[(size_t)row * H + hh] = make_float2(m, l);
-          s_fac[head] = 1.f;
         }
       }
       named_bar_sync(1, kSoftmaxThreads);
-      // The P buffers are idle here (the unit's last PV is done): each warp
-      // stages its 32 rows of D x 16 heads there, so that the bf16 output
-      // leaves as 16-byte stores (64 contiguous bytes per head).
-      __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + C::kOffP + q4 * 1024);
+      if (row < 0) {
+        // bf16 output, one 128-row block of D at a time: staged in the idle P
+        // buffers as [NH heads][128 d] (they hold exactly that) and written
+        // by one TMA store, so the warps never wait on global stores
+        __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + C::kOffP);
+        const int dl = q4 * 32 + lane;  // this thread's row of the block
+#pragma unroll 1
+        for (int b = 0; b < 4; ++b) {
+          uint32_t ov[NH];
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int d = b * 128 + q4 * 32 + lane;
-#pragma unroll
-        for (int c = 0; c < NH / 16; ++c) {
-          uint32_t ov[16];
-          tmem_ld16(tmem + lane_base + C::kOCol + b * NH + c * 16, ov);
+          for (int c = 0; c < NH / 16; ++c)
+            tmem_ld16(tmem + lane_base + C::kOCol + b * NH + c * 16, *reinterpret_cast<uint32_t(*)[16]>(ov + 16 * c));
           tmem_wait_ld();
-          if (row < 0) {
-            // "+ 0.f" turns -0 into +0 when the factor is 0 (sink = +inf)
+          // "+ 0.f" turns -0 into +0 when the factor is 0 (sink = +inf)
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              stage[e * 32 + lane] = __float2bfloat16_rn(__uint_as_float(ov[e]) * s_fac[c * 16 + e] + 0.f);
-            __syncwarp();
+          for (int e = 0; e < NH; ++e)
+            stage[e * 128 + dl] = __float2bfloat16_rn(__uint_as_float(ov[e]) * s_fac[e] + 0.f);
+          fence_proxy_async_smem();
+          named_bar_sync(1, kSoftmaxThreads);
+          if (st == 0) {
+            tma_store_2d(&tmap_out, b * 128, t * H + hg * NH, smem_addr(stage));
+            bulk_commit();
+            bulk_wait_read0();  // the staging area may be rewritten
+          }
+          named_bar_sync(1, kSoftmaxThreads);
+        }
+      } else {
+#pragma unroll 1
+        for (int b = 0; b < 4; ++b) {
+          const int d = b * 128 + q4 * 32 + lane;
 #pragma unroll
-            for (int k2 = 0; k2 < 2; ++k2) {
-              const int chunk = lane + 32 * k2;  // 16 heads x 4 chunks of 8 d
-              const int hh = chunk >> 2, part = chunk & 3;
-              const uint4 v = *reinterpret_cast<const uint4*>(stage + hh * 32 + part * 8);
-              *reinterpret_cast<uint4*>(p.out + ((size_t)t * H + hg * NH + c * 16 + hh) * kD + b * 128 +
-                                        q4 * 32 + part * 8) = v;
-            }
-            __syncwarp();
-          } else {
+          for (int c = 0; c < NH / 16; ++c) {
+            uint32_t ov[16];
+            tmem_ld16(tmem + lane_base + C::kOCol + b * NH + c * 16, ov);
+            tmem_wait_ld();
             float* o = p.part_o + ((size_t)row * H + hg * NH + c * 16) * kD + d;
 #pragma unroll
             for (int e = 0; e < 16; ++e) o[(size_t)e * kD] = __uint_as_float(ov[e]);
@@ -572,6 +629,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q, const Params p) {
       named_bar_sync(1, kSoftmaxThreads);  // s_fac is rewritten by the next unit
       if (lane == 0) mbar_arrive(bar(kBarOEmpty));
     }
+    if (st == 0) bulk_wait0();  // every output store has landed before the CTA exits
   }
 
   tc_fence_before();
@@ -600,7 +658,8 @@ EncodeTiledFn encode_fn() {
 }
 
 bool make_map_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-                 uint32_t box_rows, CUtensorMapL2promotion promo) {
+                 uint32_t box_rows, CUtensorMapL2promotion promo,
+                 CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -608,7 +667,7 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, promo,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -617,8 +676,10 @@ cudaError_t launch_nh(const void* q, const void* kv, int64_t total_pages, const 
                       const float* attn_sink, float scale, int N, int H, void* out, void* ws,
                       const WsLayout& L, const LaunchPlan& lp, cudaStream_t st) {
   (void)total_pages;
-  CUtensorMap tq;
-  if (!make_map_2d(&tq, q, kD, (uint64_t)N * H, 64, NH, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
+  CUtensorMap tq, tout;
+  if (!make_map_2d(&tq, q, kD, (uint64_t)N * H, 64, NH, CU_TENSOR_MAP_L2_PROMOTION_L2_128B) ||
+      !make_map_2d(&tout, out, kD, (uint64_t)N * H, 128, NH, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   char* base = static_cast<char*>(ws);
   Params p;
@@ -634,7 +695,7 @@ cudaError_t launch_nh(const void* q, const void* kv, int64_t total_pages, const 
   p.qk_scale_log2 = scale * kLog2e;
   p.H = H;
   return launch_pdl(decode_umma_kernel<NH>, dim3(lp.grid), dim3(kThreads), (size_t)Cfg<NH>::kSmem,
-                    st, tq, p);
+                    st, tq, tout, p);
 }
 
 }  // namespace

@@ -7,7 +7,7 @@
 
 #include <utility>
 
-#include "../../include/sda.h"
+#include "sda.h"  // include/sda.h (on the include path of the build)
 
 namespace sda {
 

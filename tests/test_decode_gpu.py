@@ -274,3 +274,12 @@ def test_timing_hook_records_around_the_kernel():
     torch.cuda.synchronize()
     assert a.elapsed_time(b) > 0.0
     parity.assert_parity(parity.compare(out, parity.run_oracle(w)), "timing hook")
+
+
+def test_negative_and_large_softmax_scale():
+    """The kernels must not assume softmax_scale > 0 (the running max of the
+    scaled logits comes from the smallest raw score when the scale is negative)."""
+    w = inputs.random_small(seed=20, N=3, H=64, D=512, P=20000, lengths=[700, 64, 1], device="cuda")
+    for scale in (-w.softmax_scale, 4.0 * w.softmax_scale):
+        out = parity.run_gpu(w, scale=scale)
+        parity.assert_parity(parity.compare(out, parity.run_oracle(w, scale=scale)), f"scale {scale}")
