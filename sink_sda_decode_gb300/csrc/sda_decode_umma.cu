@@ -30,8 +30,8 @@
 //    online softmax, write P (bf16) to shared memory, rescale O^T in TMEM
 //    only when a head's running max grows by more than 8 (2^8 headroom, so
 //    p <= 256), and finally normalise with the sink and write out through
-//    TMA stores (or, for a piece of a split token, write the unnormalised
-//    partial for the combine kernel).
+//    stmatrix + TMA stores (or, for a piece of a split token, write the
+//    unnormalised partial for the combine kernel).
 //  * Every mbarrier wait is bounded (2 s); on timeout the kernel raises the
 //    workspace error word, drains its own copies and returns.
 #include <cuda.h>
@@ -322,90 +322,84 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
   } else if (warp == kMmaWarp || warp == kPvWarp) {
     // ===================================================== MMA issuers
     // Two threads issue tcgen05 MMAs, so that one waiting for the tensor
-    // pipe to accept its instructions never delays the other's reaction:
-    //  - warp 12, lane 0: q of each unit (tiled TMA, once the previous unit's
-    //    last QK is done) and S = Q K^T of every tile, as soon as the tile
-    //    has landed and its S buffer is free;
+    // pipe to accept its instructions never delays the other:
+    //  - warp 12, lane 0: S = Q K^T of every tile, as soon as the tile has
+    //    landed and its S buffer is free, and q of the next unit (tiled TMA)
+    //    as soon as this unit's last QK has read q;
     //  - warp 13, lane 0: O^T += V^T P^T of every tile as soon as its P is
     //    written (its commit releases the KV stage and the P buffer).
     // Each thread's commits track only its own MMAs.
+    // Each has a single next event at any time, so it sleeps in the
+    // mbarrier wait (hardware suspend) instead of spinning, which leaves the
+    // issue slots of its sub-partition to the softmax and loader warps.
     if (lane == 0) {
       const bool qk_role = warp == kMmaWarp;
-      TileCursor cq, cql;
+      TileCursor cq;
       cq.init(p.units, n_units);
-      cql.init(p.units, n_units);
       int q_issued = 0;
-      uint64_t t_last = globaltimer_ns();
-      uint32_t spins = 0;
-      while (cq.valid) {
-        bool did = false;
+      bool ok = true;
+      if (qk_role && cq.valid) {  // q of the first unit
+        mbar_arrive_expect_tx(bar(kBarQFull), NH * 128 * kPanels);
+        const int qrow = cq.u.x * H + unit_head_group(cq.u.w) * NH;
+#pragma unroll
+        for (int c = 0; c < kPanels; ++c) tma_load_2d(sQ + c * kPanelQ, &tmap_q, c * 64, qrow, bar(kBarQFull));
+        q_issued = 1;
+      }
+      while (cq.valid && ok) {
         const int g = cq.g, s = g & 1;
         if (qk_role) {
-          if (cql.valid && (cql.nu == 0 || mbar_test_wait(bar(kBarQEmpty), (cql.nu - 1) & 1))) {
-            mbar_arrive_expect_tx(bar(kBarQFull), NH * 128 * kPanels);
-            const int qrow = cql.u.x * H + unit_head_group(cql.u.w) * NH;
+          ok = wait_bar(bar(kBarKVFull0 + s), (g >> 1) & 1, abort_flag, p.hdr);
+          if (ok && g >= 2) ok = wait_bar(bar(kBarSEmpty0 + s), ((g >> 1) - 1) & 1, abort_flag, p.hdr);
+          if (ok && cq.i == 0) ok = wait_bar(bar(kBarQFull), cq.nu & 1, abort_flag, p.hdr);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t kvs = sKV + s * kKVBytes;
 #pragma unroll
-            for (int c = 0; c < kPanels; ++c)
-              tma_load_2d(sQ + c * kPanelQ, &tmap_q, c * 64, qrow, bar(kBarQFull));
-            q_issued = cql.nu + 1;
-            cql.next_unit();
-            did = true;
-          } else if (mbar_test_wait(bar(kBarKVFull0 + s), (g >> 1) & 1) &&
-                     (g < 2 || mbar_test_wait(bar(kBarSEmpty0 + s), ((g >> 1) - 1) & 1)) &&
-                     (cq.i != 0 || mbar_test_wait(bar(kBarQFull), cq.nu & 1))) {
-            tc_fence_after();
-            const uint32_t kvs = sKV + s * kKVBytes;
+          for (int c = 0; c < kPanels; ++c) {
 #pragma unroll
-            for (int c = 0; c < kPanels; ++c) {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t a = sdesc_sw128(sQ + c * kPanelQ + kk * 32, 16, 1024);
-                const uint64_t bd = sdesc_sw128(kvs + c * kPanelKV + kk * 32, 16, 1024);
-                mma_bf16(tmem + s * 64, a, bd, C::kIdescQK, (c | kk) ? 1u : 0u);
-              }
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t a = sdesc_sw128(sQ + c * kPanelQ + kk * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(kvs + c * kPanelKV + kk * 32, 16, 1024);
+              mma_bf16(tmem + s * 64, a, bd, C::kIdescQK, (c | kk) ? 1u : 0u);
             }
-            mma_commit(bar(kBarSFull0 + s));
-            if (cq.i == cq.ntiles - 1) mma_commit(bar(kBarQEmpty));
-            cq.next();
-            did = true;
+          }
+          mma_commit(bar(kBarSFull0 + s));
+          const bool last = cq.i == cq.ntiles - 1;
+          const int nu = cq.nu;
+          if (last) mma_commit(bar(kBarQEmpty));
+          cq.next();
+          if (last && cq.valid) {
+            // q of the next unit once this unit's QKs have read q
+            ok = wait_bar(bar(kBarQEmpty), nu & 1, abort_flag, p.hdr);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bar(kBarQFull), NH * 128 * kPanels);
+            const int qrow = cq.u.x * H + unit_head_group(cq.u.w) * NH;
+#pragma unroll
+            for (int c = 0; c < kPanels; ++c) tma_load_2d(sQ + c * kPanelQ, &tmap_q, c * 64, qrow, bar(kBarQFull));
+            q_issued = cq.nu + 1;
           }
         } else {
           const bool first = cq.i == 0;
-          if (mbar_test_wait(bar(kBarPFull0 + s), (g >> 1) & 1) &&
-              (!first || cq.nu == 0 || mbar_test_wait(bar(kBarOEmpty), (cq.nu - 1) & 1))) {
-            tc_fence_after();
-            const uint32_t kvs = sKV + s * kKVBytes;
-            const uint32_t ps = sP + s * C::kPBytes;
+          ok = wait_bar(bar(kBarPFull0 + s), (g >> 1) & 1, abort_flag, p.hdr);
+          if (ok && first && cq.nu >= 1) ok = wait_bar(bar(kBarOEmpty), (cq.nu - 1) & 1, abort_flag, p.hdr);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t kvs = sKV + s * kKVBytes;
+          const uint32_t ps = sP + s * C::kPBytes;
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
+          for (int b = 0; b < 4; ++b) {
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                // A = V^T block b: rows d in [128b, 128b+128) = panels 2b, 2b+1 (MN-major);
-                //     K = slots [16kk, 16kk+16) = row groups 2kk, 2kk+1
-                const uint64_t a = sdesc_sw128(kvs + (2 * b) * kPanelKV + kk * 2048, kPanelKV, 1024);
-                // B = P^T: N = NH heads (rows), K = 16 slots at byte offset 32kk (K-major)
-                const uint64_t bd = sdesc_sw128(ps + kk * 32, 16, 1024);
-                mma_bf16(tmem + C::kOCol + b * NH, a, bd, C::kIdescPV, (first && kk == 0) ? 0u : 1u);
-              }
+            for (int kk = 0; kk < 4; ++kk) {
+              // A = V^T block b: rows d in [128b, 128b+128) = panels 2b, 2b+1 (MN-major);
+              //     K = slots [16kk, 16kk+16) = row groups 2kk, 2kk+1
+              const uint64_t a = sdesc_sw128(kvs + (2 * b) * kPanelKV + kk * 2048, kPanelKV, 1024);
+              // B = P^T: N = NH heads (rows), K = 16 slots at byte offset 32kk (K-major)
+              const uint64_t bd = sdesc_sw128(ps + kk * 32, 16, 1024);
+              mma_bf16(tmem + C::kOCol + b * NH, a, bd, C::kIdescPV, (first && kk == 0) ? 0u : 1u);
             }
-            mma_commit(bar(kBarPVDone0 + s));
-            cq.next();
-            did = true;
           }
-        }
-        if (did) {
-          spins = 0;
-          continue;
-        }
-        if ((++spins & 63u) == 0) {
-          if (*abort_flag) break;
-          const uint64_t now = globaltimer_ns();
-          if (spins == 64) t_last = now;  // first idle probe since the last issue
-          else if (now - t_last > kWaitTimeoutNs) {
-            *abort_flag = 1;
-            atomicExch(&p.hdr->error, 1);
-            break;
-          }
+          mma_commit(bar(kBarPVDone0 + s));
+          cq.next();
         }
       }
       // drain this thread's MMAs (and the last q copy) before TMEM and smem go away
@@ -585,26 +579,58 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
       }
       named_bar_sync(1, kSoftmaxThreads);
       if (row < 0) {
-        // bf16 output, one 128-row block of D at a time: staged in the idle P
-        // buffers as [NH heads][128 d] (they hold exactly that) and written
-        // by one TMA store, so the warps never wait on global stores
-        __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + C::kOffP);
-        const int dl = q4 * 32 + lane;  // this thread's row of the block
+        // bf16 output, one 128-row block of D at a time.  O^T is read with the
+        // 16x256b shape (thread t: rows d = t/4 and t/4 + 8 of a 16-row band,
+        // head pairs 8*rep + 2*(t%4), +1), scaled, packed to bf16 pairs and
+        // written transposed with stmatrix into the idle P buffers as two
+        // [NH heads][64 d] boxes in the 128-byte-swizzled layout (no bank
+        // conflicts), which two TMA stores copy to out.
+        uint8_t* stg = smem + C::kOffP;  // 2 boxes of NH x 128 B
+        float fac[NH / 4];               // this thread's heads 8*rep + 2*tq, +1
+#pragma unroll
+        for (int rep = 0; rep < NH / 8; ++rep) {
+          fac[2 * rep] = s_fac[8 * rep + 2 * tq];
+          fac[2 * rep + 1] = s_fac[8 * rep + 2 * tq + 1];
+        }
 #pragma unroll 1
         for (int b = 0; b < 4; ++b) {
-          uint32_t ov[NH];
 #pragma unroll
-          for (int c = 0; c < NH / 16; ++c)
-            tmem_ld16(tmem + lane_base + C::kOCol + b * NH + c * 16, *reinterpret_cast<uint32_t(*)[16]>(ov + 16 * c));
-          tmem_wait_ld();
-          // "+ 0.f" turns -0 into +0 when the factor is 0 (sink = +inf)
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t taddr = tmem + ((uint32_t)(q4 * 32 + 16 * half) << 16) + C::kOCol + b * NH;
+            uint32_t r[NH / 2];
+            if constexpr (NH == 64) tmem_ld_16x256b_x8(taddr, r);
+            else if constexpr (NH == 32) tmem_ld_16x256b_x4(taddr, r);
+            else tmem_ld_16x256b_x2(taddr, r);
+            tmem_wait_ld();
+            // "+ 0.f" turns -0 into +0 when the factor is 0 (sink = +inf)
+            uint32_t pk[NH / 4];  // [rep][row d or d+8]
 #pragma unroll
-          for (int e = 0; e < NH; ++e)
-            stage[e * 128 + dl] = __float2bfloat16_rn(__uint_as_float(ov[e]) * s_fac[e] + 0.f);
+            for (int rep = 0; rep < NH / 8; ++rep) {
+#pragma unroll
+              for (int dg = 0; dg < 2; ++dg) {
+                __nv_bfloat162 v2 = __floats2bfloat162_rn(
+                    __uint_as_float(r[4 * rep + 2 * dg]) * fac[2 * rep] + 0.f,
+                    __uint_as_float(r[4 * rep + 2 * dg + 1]) * fac[2 * rep + 1] + 0.f);
+                pk[2 * rep + dg] = *reinterpret_cast<uint32_t*>(&v2);
+              }
+            }
+            // matrix m of a stmatrix.x4 = (rep0 + m/2, d group m%2); lane
+            // 8m + j addresses row j (head 8*rep + j) of transposed matrix m
+            const int m = lane >> 3, j = lane & 7;
+            const int dl = q4 * 32 + 16 * half + 8 * (m & 1);  // block-local d of the 8 columns
+            const int box = dl >> 6, chunk = (dl & 63) >> 3;
+#pragma unroll
+            for (int rep0 = 0; rep0 < NH / 8; rep0 += 2) {
+              const int h = 8 * (rep0 + (m >> 1)) + j;
+              const uint32_t addr = smem_addr(stg) + box * (NH * 128) + h * 128 + ((chunk ^ (h & 7)) << 4);
+              stmatrix_x4_trans(addr, pk[2 * rep0], pk[2 * rep0 + 1], pk[2 * rep0 + 2], pk[2 * rep0 + 3]);
+            }
+          }
           fence_proxy_async_smem();
           named_bar_sync(1, kSoftmaxThreads);
           if (st == 0) {
-            tma_store_2d(&tmap_out, b * 128, t * H + hg * NH, smem_addr(stage));
+            tma_store_2d(&tmap_out, b * 128, t * H + hg * NH, smem_addr(stg));
+            tma_store_2d(&tmap_out, b * 128 + 64, t * H + hg * NH, smem_addr(stg) + NH * 128);
             bulk_commit();
             bulk_wait_read0();  // the staging area may be rewritten
           }
@@ -678,8 +704,7 @@ cudaError_t launch_nh(const void* q, const void* kv, int64_t total_pages, const 
   (void)total_pages;
   CUtensorMap tq, tout;
   if (!make_map_2d(&tq, q, kD, (uint64_t)N * H, 64, NH, CU_TENSOR_MAP_L2_PROMOTION_L2_128B) ||
-      !make_map_2d(&tout, out, kD, (uint64_t)N * H, 128, NH, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_NONE))
+      !make_map_2d(&tout, out, kD, (uint64_t)N * H, 64, NH, CU_TENSOR_MAP_L2_PROMOTION_NONE))
     return cudaErrorInvalidValue;
   char* base = static_cast<char*>(ws);
   Params p;
