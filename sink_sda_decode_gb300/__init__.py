@@ -21,6 +21,7 @@ import torch
 from . import _lib
 
 __all__ = ["decode", "workspace_size", "build_indices", "validate_indices", "decode_error_flag",
+           "decode_kernel",
            "decode_host", "set_timing_events", "decode_noalloc", "library_path"]
 
 library_path = _lib.LIB_PATH
@@ -127,6 +128,19 @@ def decode_noalloc(q: torch.Tensor, unified_kv: torch.Tensor, kv_indices: torch.
                                     _stream_ptr(stream))
     _lib.check(rc, "sda_decode_noalloc")
     return out
+
+
+KERNEL_NAMES = {0: "simt", 1: "one_cta", 2: "cluster"}
+
+
+def decode_kernel(H: int, D: int, device=None) -> str:
+    """Name of the attention kernel decode() launches for (H, D) on `device`
+    ("simt", "one_cta" or "cluster")."""
+    lib = _lib.load()
+    k = ctypes.c_int(-1)
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        _lib.check(lib.sda_decode_kernel(H, D, ctypes.byref(k)), "sda_decode_kernel")
+    return KERNEL_NAMES[k.value]
 
 
 def decode_error_flag(workspace: torch.Tensor, stream=None) -> int:

@@ -29,25 +29,30 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
   std::once_flag once;
-  int num_sms = 0;
+  DeviceCaps caps;
   cudaError_t err = cudaSuccess;
 };
 DeviceInfo g_dev[kMaxDevices];
 
-// SM count of the current device, queried once per device; also sets the
-// tensor-core kernels' shared-memory attribute on that device.
-cudaError_t device_sms(int* sms) {
+// SM count of the current device and how many CTA pairs of the cluster
+// kernel fit at once, queried once per device; also sets the tensor-core
+// kernels' shared-memory attributes on that device.
+cudaError_t device_caps(DeviceCaps* caps) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   DeviceInfo& d = g_dev[dev];
   std::call_once(d.once, [&]() {
-    d.err = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    d.err = cudaDeviceGetAttribute(&d.caps.num_sms, cudaDevAttrMultiProcessorCount, dev);
     for (int nh : {16, 32, 64})
       if (d.err == cudaSuccess) d.err = umma_prepare(nh);
+    for (int i = 0; i < 3 && d.err == cudaSuccess; ++i) {
+      const cudaError_t pe = pair_prepare(16 << i, &d.caps.pairs[i]);
+      if (pe != cudaSuccess) note_cuda_error(pe, "cluster kernel unavailable");
+    }
   });
-  *sms = d.num_sms;
+  *caps = d.caps;
   return d.err;
 }
 
@@ -55,33 +60,63 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) &
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Optional A/B switch for tests: SDA_FORCE_VARIANT=simt forces the CUDA-core kernel.
-bool force_simt() {
+// Optional A/B switch for tests: SDA_FORCE_VARIANT=simt|umma|pair forces a
+// decode kernel (pair and umma only where the shape allows them).
+int forced_variant() {
   const char* v = std::getenv("SDA_FORCE_VARIANT");
-  return v && std::strcmp(v, "simt") == 0;
+  if (!v) return -1;
+  if (std::strcmp(v, "simt") == 0) return kSimt;
+  if (std::strcmp(v, "umma") == 0) return kUmma;
+  if (std::strcmp(v, "pair") == 0) return kPair;
+  return -1;
 }
 
 }  // namespace
 
-bool choose_plan(int H, int D, int num_sms, LaunchPlan* lp) {
-  if (!(D == 64 || D == 128 || D == 256 || D == 512)) return false;
-  if (H < 1 || H > 256) return false;
-  lp->num_sms = num_sms;
-  const bool umma_shape = D == 512 && (H == 16 || H == 32 || H % 64 == 0);
-  if (umma_shape && !force_simt()) {
-    lp->variant = kUmma;
-    lp->nh = H < 64 ? H : 64;
+bool shape_supported(int H, int D) {
+  return (D == 64 || D == 128 || D == 256 || D == 512) && H >= 1 && H <= 256;
+}
+
+bool choose_plan(int H, int D, const DeviceCaps& caps, LaunchPlan* lp) {
+  if (!shape_supported(H, D)) return false;
+  lp->num_sms = caps.num_sms;
+  const bool tc_shape = D == 512 && (H == 16 || H == 32 || H % 64 == 0);
+  const int nh = H < 64 ? H : 64;
+  const int pairs = tc_shape ? caps.pairs[nh == 16 ? 0 : nh == 32 ? 1 : 2] : 0;
+  const int forced = forced_variant();
+  // The one-CTA kernel is the default: the cluster kernel's exchange of
+  // partial scores through distributed shared memory (~25 GB/s per SM
+  // measured) costs more per tile than the MMAs it saves.
+  Variant v = tc_shape ? kUmma : kSimt;
+  if (forced == kSimt || (forced == kUmma && tc_shape) || (forced == kPair && pairs > 0))
+    v = static_cast<Variant>(forced);
+  lp->variant = v;
+  if (v == kPair) {
+    // two CTAs (one cluster) per unit, each holding half of D; units are
+    // spread over the clusters that fit on the device at once
+    lp->nh = nh;
+    lp->hg = H / nh;
+    lp->grid = pairs;
+    lp->threads = 640;
+    lp->smem = pair_smem_bytes(nh);
+    lp->tile = kPairTileSlots;
+    lp->min_chunk = kPairTileSlots;
+  } else if (v == kUmma) {
+    lp->nh = nh;
     lp->hg = H / lp->nh;
-    lp->grid = num_sms;  // one CTA per SM (about 200 KB of shared memory each)
-    lp->threads = 192;
+    lp->grid = caps.num_sms;  // one CTA per SM (about 200 KB of shared memory each)
+    lp->threads = 448;
     lp->smem = umma_smem_bytes(lp->nh);
+    lp->tile = kTileSlots;
+    lp->min_chunk = kTileSlots;
   } else {
-    lp->variant = kSimt;
     lp->nh = H;
     lp->hg = 1;
-    lp->grid = num_sms * 4;
+    lp->grid = caps.num_sms * 4;
     lp->threads = 256;
     lp->smem = 0;
+    lp->tile = kTileSlots;
+    lp->min_chunk = kTileSlots;
   }
   return true;
 }
@@ -89,9 +124,9 @@ bool choose_plan(int H, int D, int num_sms, LaunchPlan* lp) {
 WsLayout workspace_layout(int N, int H, int D, int64_t total_indices, const LaunchPlan& lp) {
   WsLayout L;
   // Partial rows: fewer than 2 * grid / hg (pieces are >= T*hg/grid slots)
-  // and fewer than 2 * T / 64 + 1 (pieces are >= 64 slots); T <= total_indices.
+  // and fewer than 2 * T / min_chunk + 1 (chunk >= min_chunk slots); T <= total_indices.
   int64_t p1 = 2 * ((int64_t)(lp.grid + lp.hg - 1) / lp.hg) + 2;
-  int64_t p2 = 2 * ((total_indices + kMinChunk - 1) / kMinChunk) + 2;
+  int64_t p2 = 2 * ((total_indices + lp.min_chunk - 1) / lp.min_chunk) + 2;
   int64_t p_max = p1 < p2 ? p1 : p2;
   int64_t s_max = p_max / 2 + 1;
   if (s_max > N) s_max = N;
@@ -134,14 +169,15 @@ int sda_abi_version(void) { return 1; }
 
 sda_status sda_decode_workspace_size(int N, int H, int D, int64_t total_indices, size_t* bytes) {
   if (!bytes || N < 0 || total_indices < 0) return SDA_ERR_INVALID_ARG;
-  int sms = 0;
-  cudaError_t e = device_sms(&sms);
+  if (!shape_supported(H, D)) return SDA_ERR_UNSUPPORTED;
+  DeviceCaps caps;
+  cudaError_t e = device_caps(&caps);
   if (e != cudaSuccess) {
     note_cuda_error(e, "sda_decode_workspace_size");
     return SDA_ERR_CUDA;
   }
   LaunchPlan lp;
-  if (!choose_plan(H, D, sms, &lp)) return SDA_ERR_UNSUPPORTED;
+  if (!choose_plan(H, D, caps, &lp)) return SDA_ERR_UNSUPPORTED;
   *bytes = workspace_layout(N, H, D, total_indices, lp).total;
   return SDA_OK;
 }
@@ -153,8 +189,7 @@ sda_status sda_decode(const void* q, const void* unified_kv, int64_t total_pages
                       void* stream) {
   if (N < 0 || total_indices < 0 || total_indices > 0x7fffffffll) return SDA_ERR_INVALID_ARG;
   if (total_pages <= 0 || total_pages > 0x7fffffffll) return SDA_ERR_INVALID_ARG;
-  LaunchPlan lp;
-  if (!choose_plan(H, D, 1, &lp)) return SDA_ERR_UNSUPPORTED;
+  if (!shape_supported(H, D)) return SDA_ERR_UNSUPPORTED;
   if (N == 0) return SDA_OK;
   if (!q || !unified_kv || !kv_indptr || !attn_sink || !out || !workspace) return SDA_ERR_INVALID_ARG;
   if (total_indices > 0 && !kv_indices) return SDA_ERR_INVALID_ARG;
@@ -162,13 +197,14 @@ sda_status sda_decode(const void* q, const void* unified_kv, int64_t total_pages
       !aligned(attn_sink, 4) || (kv_indices && !aligned(kv_indices, 4)))
     return SDA_ERR_INVALID_ARG;
   if (!aligned(workspace, 256)) return SDA_ERR_WORKSPACE;
-  int sms = 0;
-  cudaError_t e = device_sms(&sms);
+  DeviceCaps caps;
+  cudaError_t e = device_caps(&caps);
   if (e != cudaSuccess) {
     note_cuda_error(e, "sda_decode");
     return SDA_ERR_CUDA;
   }
-  choose_plan(H, D, sms, &lp);
+  LaunchPlan lp;
+  choose_plan(H, D, caps, &lp);
   const WsLayout L = workspace_layout(N, H, D, total_indices, lp);
   if (workspace_bytes < L.total) return SDA_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -176,7 +212,10 @@ sda_status sda_decode(const void* q, const void* unified_kv, int64_t total_pages
   e = launch_plan(kv_indptr, N, total_indices, lp, workspace, L, st);
   if (e == cudaSuccess && g_ev_before && g_ev_after) e = cudaEventRecord(g_ev_before, st);
   if (e == cudaSuccess) {
-    if (lp.variant == kUmma)
+    if (lp.variant == kPair)
+      e = launch_decode_pair(q, unified_kv, kv_indices, attn_sink, softmax_scale, N, H, D, out,
+                             workspace, L, lp, st);
+    else if (lp.variant == kUmma)
       e = launch_decode_umma(q, unified_kv, total_pages, kv_indices, attn_sink, softmax_scale, N, H,
                              D, out, workspace, L, lp, st);
     else
@@ -184,11 +223,28 @@ sda_status sda_decode(const void* q, const void* unified_kv, int64_t total_pages
                              workspace, L, lp, st);
   }
   if (e == cudaSuccess && g_ev_before && g_ev_after) e = cudaEventRecord(g_ev_after, st);
-  if (e == cudaSuccess) e = launch_combine(attn_sink, N, H, D, out, workspace, L, sms, st);
+  if (e == cudaSuccess) e = launch_combine(attn_sink, N, H, D, out, workspace, L, caps.num_sms, st);
   if (e != cudaSuccess) {
     note_cuda_error(e, "sda_decode");
     return SDA_ERR_CUDA;
   }
+  return SDA_OK;
+}
+
+sda_status sda_decode_kernel(int H, int D, int* kernel) {
+  if (!kernel) return SDA_ERR_INVALID_ARG;
+  if (!shape_supported(H, D)) return SDA_ERR_UNSUPPORTED;
+  DeviceCaps caps;
+  cudaError_t e = device_caps(&caps);
+  if (e != cudaSuccess) {
+    note_cuda_error(e, "sda_decode_kernel");
+    return SDA_ERR_CUDA;
+  }
+  LaunchPlan lp;
+  choose_plan(H, D, caps, &lp);
+  static_assert(SDA_KERNEL_SIMT == kSimt && SDA_KERNEL_ONE_CTA == kUmma && SDA_KERNEL_CLUSTER == kPair,
+                "public kernel codes");
+  *kernel = lp.variant;
   return SDA_OK;
 }
 

@@ -506,9 +506,12 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
           const float a1 = j + 1 < n ? ex2_approx(fmaf(__uint_as_float(sv[4 * rep + 1]), sc, -mA)) : 0.f;
           const float b0 = j < n ? ex2_approx(fmaf(__uint_as_float(sv[4 * rep + 2]), sc, -mB)) : 0.f;
           const float b1 = j + 1 < n ? ex2_approx(fmaf(__uint_as_float(sv[4 * rep + 3]), sc, -mB)) : 0.f;
-          sA += a0 + a1;
-          sB += b0 + b1;
           __nv_bfloat162 pa = __floats2bfloat162_rn(a0, a1), pb = __floats2bfloat162_rn(b0, b1);
+          // the denominator sums the same bf16 weights the PV MMA multiplies,
+          // so rounding p perturbs the weights but biases nothing
+          const float2 fa = __bfloat1622float2(pa), fb = __bfloat1622float2(pb);
+          sA += fa.x + fa.y;
+          sB += fb.x + fb.y;
           if (vA) *reinterpret_cast<uint32_t*>(prowA + ((rep ^ (hA & 7)) << 4)) = *reinterpret_cast<uint32_t*>(&pa);
           if (vB) *reinterpret_cast<uint32_t*>(prowB + ((rep ^ (hB & 7)) << 4)) = *reinterpret_cast<uint32_t*>(&pb);
         }

@@ -53,19 +53,20 @@ struct TokenSplit {
   int len, pieces, piece_len;
 };
 
-__device__ __forceinline__ TokenSplit token_split(const int32_t* indptr, int t, int chunk) {
+__device__ __forceinline__ TokenSplit token_split(const int32_t* indptr, int t, int chunk, int tile) {
   TokenSplit s;
   int L = indptr[t + 1] - indptr[t];
   s.len = L > 0 ? L : 0;
   s.pieces = s.len == 0 ? 1 : (s.len + chunk - 1) / chunk;
   const int even = (s.len + s.pieces - 1) / s.pieces;
-  s.piece_len = s.pieces == 1 ? s.len : ((even + kTileSlots - 1) / kTileSlots) * kTileSlots;
+  s.piece_len = s.pieces == 1 ? s.len : ((even + tile - 1) / tile) * tile;
   return s;
 }
 
 __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(const int32_t* __restrict__ indptr, int N, long long total_indices, int hg, int grid,
-            WsHeader* __restrict__ hdr, int4* __restrict__ units, int4* __restrict__ splits) {
+            int tile, int min_chunk, WsHeader* __restrict__ hdr, int4* __restrict__ units,
+            int4* __restrict__ splits) {
   __shared__ int warp_sums[32];
   __shared__ int s_total[2];
   __shared__ int bucket_count[kBuckets];
@@ -97,8 +98,10 @@ plan_kernel(const int32_t* __restrict__ indptr, int N, long long total_indices, 
     long long T = N > 0 ? (long long)indptr[N] - (long long)indptr[0] : 0;
     if (T < 0) T = 0;
     long long target = (T * hg + grid - 1) / grid;
-    long long chunk = ((target + kTileSlots - 1) / kTileSlots) * kTileSlots;
-    if (chunk < kMinChunk) chunk = kMinChunk;
+    // a multiple of the tile, so that every piece but the last is whole
+    // tiles and no piece is empty
+    long long chunk = ((target + tile - 1) / tile) * tile;
+    if (chunk < min_chunk) chunk = min_chunk;
     if (chunk > (1ll << 30)) chunk = 1ll << 30;
     s_chunk = (int)chunk;
   }
@@ -109,7 +112,7 @@ plan_kernel(const int32_t* __restrict__ indptr, int N, long long total_indices, 
   for (int t0 = 0; t0 < N; t0 += kPlanThreads) {
     const int t = t0 + threadIdx.x;
     if (t < N) {
-      TokenSplit s = token_split(indptr, t, chunk);
+      TokenSplit s = token_split(indptr, t, chunk, tile);
       for (int k = 0; k < s.pieces; ++k) {
         int plen = s.pieces == 1 ? s.len : min(s.piece_len, s.len - k * s.piece_len);
         atomicAdd(&bucket_count[len_bucket(plen)], hg);
@@ -132,7 +135,7 @@ plan_kernel(const int32_t* __restrict__ indptr, int N, long long total_indices, 
   for (int t0 = 0; t0 < N; t0 += kPlanThreads) {
     const int t = t0 + threadIdx.x;
     TokenSplit s{0, 1, 0};
-    if (t < N) s = token_split(indptr, t, chunk);
+    if (t < N) s = token_split(indptr, t, chunk, tile);
     const bool split = t < N && s.pieces > 1;
     const int part_base = block_exclusive_scan(split ? s.pieces : 0, warp_sums, &s_total[0]) + part_carry;
     const int split_idx = block_exclusive_scan(split ? 1 : 0, warp_sums, &s_total[1]) + split_carry;
@@ -210,7 +213,8 @@ cudaError_t launch_plan(const int32_t* kv_indptr, int N, int64_t total_indices,
                         const LaunchPlan& lp, void* ws, const WsLayout& L, cudaStream_t st) {
   char* base = static_cast<char*>(ws);
   return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, kv_indptr, N,
-                    (long long)total_indices, lp.hg, lp.grid, reinterpret_cast<WsHeader*>(base),
+                    (long long)total_indices, lp.hg, lp.grid, lp.tile, lp.min_chunk,
+                    reinterpret_cast<WsHeader*>(base),
                     reinterpret_cast<int4*>(base + L.units_off),
                     reinterpret_cast<int4*>(base + L.split_off));
 }

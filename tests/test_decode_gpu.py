@@ -33,9 +33,21 @@ def sample_tokens(w, k, seed):
 
 
 # ----------------------------------------------------------------------------- workloads
+# "default" is the kernel the library picks (the one-CTA tensor-core kernel
+# for D = 512 and H in {16, 32, 64k}); "pair" forces the two-CTA cluster kernel.
+TC_VARIANTS = ["default", "pair"]
+
+
+def _force(monkeypatch, variant):
+    if variant != "default":
+        monkeypatch.setenv("SDA_FORCE_VARIANT", variant)
+
+
+@pytest.mark.parametrize("variant", TC_VARIANTS)
 @pytest.mark.parametrize("cfg,k", [(0, None), (1, None), (2, 40), (3, 24), (4, 24)],
                          ids=inputs.CONFIG_NAMES)
-def test_workload_parity(cfg, k):
+def test_workload_parity(monkeypatch, cfg, k, variant):
+    _force(monkeypatch, variant)
     w = inputs.config(cfg, device="cuda")
     out = parity.run_gpu(w)
     torch.cuda.synchronize()
@@ -43,8 +55,8 @@ def test_workload_parity(cfg, k):
     ref = parity.run_oracle(w, tokens=toks)
     got = out if toks is None else out[torch.tensor(toks, device=out.device)]
     st = parity.compare(got, ref)
-    print(f"\n{inputs.CONFIG_NAMES[cfg]}: {st}")
-    parity.assert_parity(st, inputs.CONFIG_NAMES[cfg])
+    print(f"\n{inputs.CONFIG_NAMES[cfg]} {variant}: {st}")
+    parity.assert_parity(st, f"{inputs.CONFIG_NAMES[cfg]} {variant}")
     # padded tokens: exactly +0.0 (bf16 bit pattern 0)
     zero = np.nonzero(w.lengths == 0)[0]
     if zero.size:
@@ -58,6 +70,25 @@ def _ws_and_flag(w):
     ws = torch.empty(n, dtype=torch.uint8, device="cuda")
     out = sda.decode(w.q, w.unified_kv, idx, ptr, w.attn_sink, w.softmax_scale, workspace=ws)
     return out, sda.decode_error_flag(ws)
+
+
+def test_kernel_choice():
+    """D = 512 with H in {16, 32, 64k} runs the one-CTA tensor-core kernel;
+    other shapes the CUDA-core kernel."""
+    for H in (16, 32, 64, 128):
+        assert sda.decode_kernel(H, 512) == "one_cta"
+    assert sda.decode_kernel(48, 512) == "simt"
+    assert sda.decode_kernel(16, 128) == "simt"
+
+
+def test_kernel_choice_forced(monkeypatch):
+    """The environment switch reaches the other kernels (the cluster kernel
+    must be runnable on this GPU)."""
+    monkeypatch.setenv("SDA_FORCE_VARIANT", "pair")
+    for H in (16, 32, 64, 128):
+        assert sda.decode_kernel(H, 512) == "cluster"
+    monkeypatch.setenv("SDA_FORCE_VARIANT", "simt")
+    assert sda.decode_kernel(64, 512) == "simt"
 
 
 def test_error_flag_clear_after_normal_call():
@@ -74,8 +105,21 @@ SHAPES = [  # (H, D) -- tensor-core path for D=512 and H in {16,32,64k}; CUDA co
 LENGTHS = [0, 1, 2, 31, 63, 64, 65, 127, 128, 129, 300, 640, 1000, 2500]
 
 
+TC_SHAPES = [(16, 512), (32, 512), (64, 512), (128, 512)]
+
+
 @pytest.mark.parametrize("H,D", SHAPES, ids=[f"H{h}_D{d}" for h, d in SHAPES])
 def test_shapes_and_ragged_lengths(H, D):
+    _check_shape(H, D)
+
+
+@pytest.mark.parametrize("H,D", TC_SHAPES, ids=[f"H{h}_D{d}" for h, d in TC_SHAPES])
+def test_cluster_kernel_shapes(monkeypatch, H, D):
+    monkeypatch.setenv("SDA_FORCE_VARIANT", "pair")
+    _check_shape(H, D)
+
+
+def _check_shape(H, D):
     w = inputs.random_small(seed=1000 + H + D, N=len(LENGTHS), H=H, D=D, P=20000, lengths=LENGTHS,
                             device="cuda")
     out = parity.run_gpu(w)
@@ -85,12 +129,11 @@ def test_shapes_and_ragged_lengths(H, D):
     assert torch.all(out[0].view(torch.int16) == 0)
 
 
-@pytest.mark.parametrize("variant", ["simt", "default"])
+@pytest.mark.parametrize("variant", ["simt", "pair", "default"])
 def test_split_long_lists(monkeypatch, variant):
     """Few tokens with long lists: the plan cuts every list into pieces and
     the combine kernel merges them (including the sink exactly once)."""
-    if variant == "simt":
-        monkeypatch.setenv("SDA_FORCE_VARIANT", "simt")
+    _force(monkeypatch, variant)
     w = inputs.random_small(seed=7, N=3, H=64, D=512, P=1 << 17, lengths=[30000, 5, 12345],
                             sink_sigma=2.0, device="cuda")
     out = parity.run_gpu(w)
@@ -98,17 +141,18 @@ def test_split_long_lists(monkeypatch, variant):
     parity.assert_parity(parity.compare(out, ref), f"split {variant}")
 
 
-def test_variants_agree():
-    """CUDA-core and tensor-core kernels on the same input."""
+def test_variants_agree(monkeypatch):
+    """CUDA-core, one-CTA and two-CTA tensor-core kernels on the same input."""
     w = inputs.random_small(seed=8, N=5, H=64, D=512, P=50000, lengths=[1, 64, 700, 0, 129],
                             device="cuda")
     a = parity.run_gpu(w).float()
-    os.environ["SDA_FORCE_VARIANT"] = "simt"
-    try:
-        b = parity.run_gpu(w).float()
-    finally:
-        del os.environ["SDA_FORCE_VARIANT"]
-    assert (a - b).abs().max().item() <= 2 * parity.MAX_ABS
+    outs = {}
+    for v in ("simt", "pair"):
+        monkeypatch.setenv("SDA_FORCE_VARIANT", v)
+        outs[v] = parity.run_gpu(w).float()
+    monkeypatch.delenv("SDA_FORCE_VARIANT")
+    for v, b in outs.items():
+        assert (a - b).abs().max().item() <= 2 * parity.MAX_ABS, v
 
 
 # ----------------------------------------------------------------------------- edge cases
