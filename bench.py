@@ -92,58 +92,133 @@ def ncu_traffic(config_name):
     return None
 
 
+class _Nvml:
+    """Read-only NVML through ctypes (libnvidia-ml ships with the driver):
+    current / maximum SM clock and the active clock-event reasons."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, cuda_index):
+        import ctypes
+        self.c = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        bus = None
+        try:
+            p = torch.cuda.get_device_properties(cuda_index)
+            bus = "%04x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        except Exception:
+            pass
+        ok = bus is not None and lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h)) == 0
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(cuda_index, ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle")
+        get = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.get_reasons = get or lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint(0)
+        lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))  # NVML_CLOCK_SM
+        self.max_mhz = float(mx.value)
+
+    def sample(self):
+        mhz = self.c.c_uint(0)
+        r = self.c.c_ulonglong(0)
+        self.lib.nvmlDeviceGetClockInfo(self.h, 1, self.c.byref(mhz))
+        self.get_reasons(self.h, self.c.byref(r))
+        return float(mhz.value), int(r.value)
+
+
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during timing."""
-    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event reasons sampled during the timed region:
+    NVML polled about every millisecond in a thread (nvidia-smi at 10 ms
+    intervals where NVML cannot be loaded)."""
 
     def __init__(self, index):
         self.index = index
-        self.proc = None
-        self.lines = []
+        self.samples = []  # (host time, mhz, set of reason names)
+        self.window = None
+        self.max_mhz = None
+        self.source = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._proc = None
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
-            self.t.start()
+            nv = _Nvml(self.index)
+            self.max_mhz, self.source = nv.max_mhz, "nvml"
+
+            def poll():
+                while not self._stop.is_set():
+                    mhz, bits = nv.sample()
+                    self.samples.append((time.perf_counter(), mhz,
+                                         {n for b, n in _Nvml.REASONS.items() if bits & b}))
+                    time.sleep(0.001)
+                nv.lib.nvmlShutdown()
+            self._thread = threading.Thread(target=poll, daemon=True)
+            self._thread.start()
         except Exception:
-            self.proc = None
+            self._start_smi()
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+    def _start_smi(self):
+        fields = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_power_cap")
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={fields}",
+                 "--format=csv,noheader,nounits", "-lms", "10"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi"
+
+            def read():
+                for ln in self._proc.stdout:
+                    parts = [x.strip() for x in ln.split(",")]
+                    if len(parts) != 6:
+                        continue
+                    try:
+                        mhz, self.max_mhz = float(parts[0]), float(parts[1])
+                    except ValueError:
+                        continue
+                    self.samples.append((time.perf_counter(), mhz,
+                                         {n for n, v in zip(names, parts[2:]) if v.lower() == "active"}))
+            self._thread = threading.Thread(target=read, daemon=True)
+            self._thread.start()
+        except Exception:
+            self._proc = None
 
     def __exit__(self, *a):
-        if self.proc is not None:
-            self.proc.terminate()
+        self._stop.set()
+        if self._proc is not None:
+            self._proc.terminate()
             try:
-                self.proc.wait(timeout=5)
+                self._proc.wait(timeout=5)
             except Exception:
-                self.proc.kill()
+                self._proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
+
+    def wait_first(self, timeout=5.0):
+        t0 = time.perf_counter()
+        while not self.samples and time.perf_counter() - t0 < timeout:
+            time.sleep(0.001)
+
+    def mark(self, t_start, t_end):
+        """Host-time window of the timed region (first launch .. final sync)."""
+        self.window = (t_start, t_end)
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [x.strip() for x in ln.split(",")]
-            if len(parts) != 6:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx = float(parts[1])
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[2:]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        sel = [x for x in self.samples
+               if self.window is None or self.window[0] <= x[0] <= self.window[1]]
+        sm = [m for _, m, _ in sel]
+        reasons = set()
+        for _, _, r in sel:
+            reasons |= r
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(sm), "source": self.source}
 
 
 def algorithmic_bytes(w):
@@ -217,8 +292,10 @@ def gpu_arm(args, w, device, ws, rank):
     # ---- timed region 1: K graph replays, L2 flushed before each step
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
-    barrier()
     with ClockSampler(torch.cuda.current_device() if device.index is None else device.index) as cs:
+        cs.wait_first()
+        barrier()
+        t_start = time.perf_counter()
         with torch.cuda.stream(s):
             for a, b in evs:
                 flush.zero_()
@@ -226,6 +303,7 @@ def gpu_arm(args, w, device, ws, rank):
                 g.replay()
                 b.record(s)
         barrier()
+        cs.mark(t_start, time.perf_counter())
     step_ms = [a.elapsed_time(b) for a, b in evs]
     ms_per_step = sum(step_ms) / len(step_ms)
 

@@ -167,43 +167,85 @@ plan_kernel(const int32_t* __restrict__ indptr, int N, long long total_indices, 
 //   out = sum_k 2^(m_k - M) acc_k / (2^(sink*log2e - M) + sum_k 2^(m_k - M) l_k)
 // m_k, l_k, acc_k are the log2-domain running max, denominator and
 // unnormalised output of piece k (without the sink).
-__global__ void __launch_bounds__(128)
-combine_kernel(const float* __restrict__ attn_sink, int H, int D,
-               __nv_bfloat16* __restrict__ out, const WsHeader* __restrict__ hdr,
-               const int4* __restrict__ splits, const float2* __restrict__ part_ml,
-               const float* __restrict__ part_o) {
+//
+// One warp per (split token, head): lane k loads (m_k, l_k) of piece k, the
+// maxima and denominator are warp reductions, then every lane accumulates
+// 16 values of D (D = 512; 4 x 16-byte loads per piece, independent across
+// pieces) and stores them as bf16.  Warps past the actual number of split
+// tokens exit at once (the grid is sized for the worst case so that it can
+// be captured in a CUDA graph).
+constexpr int kCombineWarps = 8;
+
+template <int D>
+__global__ void __launch_bounds__(kCombineWarps * 32)
+combine_kernel(const float* __restrict__ attn_sink, int H, __nv_bfloat16* __restrict__ out,
+               const WsHeader* __restrict__ hdr, const int4* __restrict__ splits,
+               const float2* __restrict__ part_ml, const float* __restrict__ part_o) {
+  // lane l owns the 4-value groups at d = 4l + 128g (16 values for D = 512;
+  // for D = 64 only lanes 0..15 hold a group)
+  constexpr int kGroups = D >= 128 ? D / 128 : 1;
+  constexpr int kPer = 4 * kGroups;
   pdl_wait();
-  const int n_items = hdr->n_split * H;
-  for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
-    const int si = w / H, h = w % H;
-    const int4 sp = splits[si];
-    const int t = sp.x, row0 = sp.y, np = sp.z;
-    const float ms = attn_sink[h] * kLog2e;
-    float M = ms;
-    for (int k = 0; k < np; ++k) M = fmaxf(M, part_ml[(size_t)(row0 + k) * H + h].x);
-    const bool dead = (ms == INFINITY) || (M == -INFINITY);
-    float den = dead ? 1.f : ex2_approx(ms - M);
-    for (int k = 0; k < np; ++k) {
-      const float2 ml = part_ml[(size_t)(row0 + k) * H + h];
-      den += dead ? 0.f : ml.y * ex2_approx(ml.x - M);
-    }
-    for (int d0 = threadIdx.x * 4; d0 < D; d0 += blockDim.x * 4) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (!dead) {
-        for (int k = 0; k < np; ++k) {
-          const float wk = ex2_approx(part_ml[(size_t)(row0 + k) * H + h].x - M);
-          const float4 o = *reinterpret_cast<const float4*>(part_o + ((size_t)(row0 + k) * H + h) * D + d0);
-          acc.x += wk * o.x; acc.y += wk * o.y; acc.z += wk * o.z; acc.w += wk * o.w;
+  const int lane = threadIdx.x & 31;
+  const int item = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+  if (item >= hdr->n_split * H) return;
+  const int si = item / H, h = item % H;
+  const int4 sp = splits[si];
+  const int t = sp.x, row0 = sp.y, np = sp.z;
+  const float ms = attn_sink[h] * kLog2e;
+  // maxima and denominator over the pieces (lanes stride over them)
+  float mk = -INFINITY;
+  for (int k = lane; k < np; k += 32) mk = fmaxf(mk, part_ml[(size_t)(row0 + k) * H + h].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, o));
+  const float M = fmaxf(ms, mk);
+  const bool dead = (ms == INFINITY) || (M == -INFINITY);
+  float den = 0.f;
+  for (int k = lane; k < np; k += 32) {
+    const float2 ml = part_ml[(size_t)(row0 + k) * H + h];
+    den += dead ? 0.f : ml.y * ex2_approx(ml.x - M);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  den += dead ? 1.f : ex2_approx(ms - M);
+  float acc[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+  if (!dead) {
+    const int d0 = lane * 4;  // this lane's 4-value groups at d0 + 128*j
+    for (int k0 = 0; k0 < np; k0 += 32) {
+      // weight of piece k0 + j lives in lane j
+      const int kk = k0 + lane;
+      const float wl = kk < np ? ex2_approx(part_ml[(size_t)(row0 + kk) * H + h].x - M) : 0.f;
+      const int nk = min(32, np - k0);
+#pragma unroll 4
+      for (int j = 0; j < nk; ++j) {
+        const float wk = __shfl_sync(0xffffffffu, wl, j);
+        const float* o = part_o + ((size_t)(row0 + k0 + j) * H + h) * D + d0;
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g) {
+          if (D < 128 && d0 >= D) break;
+          const float4 v = *reinterpret_cast<const float4*>(o + 128 * g);
+          acc[4 * g + 0] += wk * v.x;
+          acc[4 * g + 1] += wk * v.y;
+          acc[4 * g + 2] += wk * v.z;
+          acc[4 * g + 3] += wk * v.w;
         }
       }
-      const float inv = dead ? 0.f : 1.f / den;
-      __nv_bfloat162 a = __floats2bfloat162_rn(acc.x * inv + 0.f, acc.y * inv + 0.f);
-      __nv_bfloat162 b = __floats2bfloat162_rn(acc.z * inv + 0.f, acc.w * inv + 0.f);
-      uint2 pk;
-      pk.x = *reinterpret_cast<uint32_t*>(&a);
-      pk.y = *reinterpret_cast<uint32_t*>(&b);
-      *reinterpret_cast<uint2*>(out + ((size_t)t * H + h) * D + d0) = pk;
     }
+  }
+  const float inv = dead ? 0.f : 1.f / den;
+  __nv_bfloat16* orow = out + ((size_t)t * H + h) * D + lane * 4;
+#pragma unroll
+  for (int g = 0; g < kGroups; ++g) {
+    if (D < 128 && lane * 4 >= D) break;
+    // "+ 0.f" turns -0 into +0 (a factor of 0 when the sink is +inf)
+    __nv_bfloat162 a = __floats2bfloat162_rn(acc[4 * g] * inv + 0.f, acc[4 * g + 1] * inv + 0.f);
+    __nv_bfloat162 b = __floats2bfloat162_rn(acc[4 * g + 2] * inv + 0.f, acc[4 * g + 3] * inv + 0.f);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&a);
+    pk.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(orow + 128 * g) = pk;
   }
 }
 
@@ -221,16 +263,26 @@ cudaError_t launch_plan(const int32_t* kv_indptr, int N, int64_t total_indices,
 
 cudaError_t launch_combine(const float* attn_sink, int N, int H, int D, void* out, void* ws,
                            const WsLayout& L, int num_sms, cudaStream_t st) {
+  (void)N;
+  (void)num_sms;
   if (L.s_max == 0) return cudaSuccess;
   char* base = static_cast<char*>(ws);
-  int blocks = L.s_max * H;
-  if (blocks > num_sms * 2) blocks = num_sms * 2;
-  if (blocks < 1) blocks = 1;
-  return launch_pdl(combine_kernel, dim3(blocks), dim3(128), 0, st, attn_sink, H, D,
-                    static_cast<__nv_bfloat16*>(out), reinterpret_cast<const WsHeader*>(base),
-                    reinterpret_cast<const int4*>(base + L.split_off),
-                    reinterpret_cast<const float2*>(base + L.ml_off),
-                    reinterpret_cast<const float*>(base + L.o_off));
+  const long long items = (long long)L.s_max * H;
+  const int blocks = (int)((items + kCombineWarps - 1) / kCombineWarps);
+  auto args = [&](auto kernel) {
+    return launch_pdl(kernel, dim3(blocks), dim3(kCombineWarps * 32), 0, st, attn_sink, H,
+                      static_cast<__nv_bfloat16*>(out), reinterpret_cast<const WsHeader*>(base),
+                      reinterpret_cast<const int4*>(base + L.split_off),
+                      reinterpret_cast<const float2*>(base + L.ml_off),
+                      reinterpret_cast<const float*>(base + L.o_off));
+  };
+  switch (D) {
+    case 64: return args(combine_kernel<64>);
+    case 128: return args(combine_kernel<128>);
+    case 256: return args(combine_kernel<256>);
+    case 512: return args(combine_kernel<512>);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace sda
