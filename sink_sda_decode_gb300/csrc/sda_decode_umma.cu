@@ -91,7 +91,11 @@ struct Cfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kQBytes;
   static constexpr int kOffP = kOffKV + kStages * kKVBytes;
-  static constexpr int kOffBar = kOffP + kStages * kPBytes;
+  // second output staging area (the first is the two P buffers): the TMA
+  // stores of one 128-row block of D read one area while the next block is
+  // written into the other
+  static constexpr int kOffStage2 = kOffP + kStages * kPBytes;
+  static constexpr int kOffBar = kOffStage2 + NH * 256;
   static constexpr int kOffMisc = kOffBar + 128;
   // misc: tmem base (4), abort flag (4), pad, then per-head float arrays
   static constexpr int kOffAlpha = kOffMisc + 16;
@@ -442,6 +446,9 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
       }
       const int ntiles = (len + kTileN - 1) / kTileN;
       float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;  // l: this thread's share
+      // the sink logits are only needed in the epilogue: load them now
+      const float sinkA = (row < 0 && vA && tq == 0) ? __ldg(p.attn_sink + hg * NH + hA) : 0.f;
+      const float sinkB = (row < 0 && vB && tq == 0) ? __ldg(p.attn_sink + hg * NH + hB) : 0.f;
       for (int i = 0; i < ntiles; ++i, ++g) {
         const int s = g & 1;
         const int n = min(kTileN, len - i * kTileN);
@@ -566,7 +573,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
           if (hd >= NH) continue;
           const int hh = hg * NH + hd;
           if (row < 0) {
-            const float ms = p.attn_sink[hh] * kLog2e;
+            const float ms = (w2 ? sinkB : sinkA) * kLog2e;
             const float M = fmaxf(mh, ms);
             float f = 0.f;
             if (M != -INFINITY && ms != INFINITY) {
@@ -587,8 +594,9 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         // head pairs 8*rep + 2*(t%4), +1), scaled, packed to bf16 pairs and
         // written transposed with stmatrix into the idle P buffers as two
         // [NH heads][64 d] boxes in the 128-byte-swizzled layout (no bank
-        // conflicts), which two TMA stores copy to out.
-        uint8_t* stg = smem + C::kOffP;  // 2 boxes of NH x 128 B
+        // conflicts), which two TMA stores copy to out.  Blocks alternate
+        // between two staging areas, so a block's stores overlap the next
+        // block's TMEM reads.
         float fac[NH / 4];               // this thread's heads 8*rep + 2*tq, +1
 #pragma unroll
         for (int rep = 0; rep < NH / 8; ++rep) {
@@ -597,6 +605,12 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         }
 #pragma unroll 1
         for (int b = 0; b < 4; ++b) {
+          uint8_t* stg = smem + ((b & 1) ? C::kOffStage2 : C::kOffP);  // 2 boxes of NH x 128 B
+          if (b >= 2) {
+            // the stores of block b - 2 have read this area
+            if (st == 0) bulk_wait_read1();
+            named_bar_sync(1, kSoftmaxThreads);
+          }
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             const uint32_t taddr = tmem + ((uint32_t)(q4 * 32 + 16 * half) << 16) + C::kOCol + b * NH;
@@ -635,10 +649,11 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
             tma_store_2d(&tmap_out, b * 128, t * H + hg * NH, smem_addr(stg));
             tma_store_2d(&tmap_out, b * 128 + 64, t * H + hg * NH, smem_addr(stg) + NH * 128);
             bulk_commit();
-            bulk_wait_read0();  // the staging area may be rewritten
           }
-          named_bar_sync(1, kSoftmaxThreads);
         }
+        // both areas (one is the P buffers) are free again before this
+        // unit's epilogue ends
+        if (st == 0) bulk_wait_read0();
       } else {
 #pragma unroll 1
         for (int b = 0; b < 4; ++b) {
