@@ -17,9 +17,12 @@
 //  * Warps 4..11 load KV tiles of 64 slots: each 1 KB row is read by a whole
 //    warp as two contiguous 512-byte loads (16 x 16 B in flight per thread,
 //    64 KB per SM), then stored 128-byte-swizzled into one of two
-//    shared-memory stages.  Whole-row loads keep DRAM accesses contiguous;
-//    TMA tile::gather4, which fetches 128 bytes of four rows per
-//    instruction, topped out near a third of HBM bandwidth on this GPU.
+//    shared-memory stages, one half of D at a time: a half is refilled as
+//    soon as the PV MMAs that read it (blocks 0-1 or 2-3) are done, and the
+//    next QK starts on the first half while the second is still stored.
+//    Whole-row loads keep DRAM accesses contiguous; TMA tile::gather4, which
+//    fetches 128 bytes of four rows per instruction, topped out near a third
+//    of HBM bandwidth on this GPU.
 //  * Warps 12 and 13 issue tcgen05 MMAs, event driven and apart, so that one
 //    waiting for the tensor pipe never delays the other:  S = Q K^T  (M = 64
 //    padded heads, N = 64 slots, K = 512) into TMEM by warp 12, which also
@@ -69,11 +72,9 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 enum Bar : int {
   kBarQFull = 0,
   kBarQEmpty,
-  kBarKVFull0,
-  kBarKVFull1,
-  kBarPVDone0,
-  kBarPVDone1,
-  kBarSFull0,
+  kBarKVFull0,                   // + 2 * stage + half (columns [256 half, +256) of the rows)
+  kBarPVDone0 = kBarKVFull0 + 4,  // + 2 * stage + half (PV blocks 2 half, 2 half + 1 done)
+  kBarSFull0 = kBarPVDone0 + 4,
   kBarSFull1,
   kBarSEmpty0,
   kBarSEmpty1,
@@ -84,6 +85,9 @@ enum Bar : int {
   kBarDrainPv,
   kNumBars
 };
+
+__host__ __device__ constexpr int kv_full(int s, int h) { return kBarKVFull0 + 2 * s + h; }
+__host__ __device__ constexpr int pv_done(int s, int h) { return kBarPVDone0 + 2 * s + h; }
 
 template <int NH>
 struct Cfg {
@@ -96,7 +100,7 @@ struct Cfg {
   // written into the other
   static constexpr int kOffStage2 = kOffP + kStages * kPBytes;
   static constexpr int kOffBar = kOffStage2 + NH * 256;
-  static constexpr int kOffMisc = kOffBar + 128;
+  static constexpr int kOffMisc = kOffBar + 192;
   // misc: tmem base (4), abort flag (4), pad, then per-head float arrays
   static constexpr int kOffAlpha = kOffMisc + 16;
   static constexpr int kOffFac = kOffAlpha + 4 * 64;
@@ -234,10 +238,10 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQFull), 1);
     mbar_init(bar(kBarQEmpty), 1);
-    mbar_init(bar(kBarKVFull0), kLoaderWarps);
-    mbar_init(bar(kBarKVFull1), kLoaderWarps);
-    mbar_init(bar(kBarPVDone0), 1);
-    mbar_init(bar(kBarPVDone1), 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar(kBarKVFull0 + i), kLoaderWarps);
+      mbar_init(bar(kBarPVDone0 + i), 1);
+    }
     mbar_init(bar(kBarSFull0), 1);
     mbar_init(bar(kBarSFull1), 1);
     mbar_init(bar(kBarSEmpty0), 4);
@@ -302,26 +306,29 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
       }
       cur.next();
       if (cur.valid) fetch_slots();  // next tile's slots, while this tile's rows are in flight
-      if (g >= 2) {
-        if (lane == 0) ok = wait_bar(bar(kBarPVDone0 + s), ((g >> 1) - 1) & 1, abort_flag, p.hdr);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-      }
+      // store the tile in two halves of D (each row's loads v[2r] and
+      // v[2r + 1]), each as soon as the PV MMAs that read that half of the
+      // tile last in this stage are done
       uint8_t* stage = smem + C::kOffKV + s * kKVBytes;
 #pragma unroll
-      for (int r = 0; r < kRowsPerLoader; ++r) {
-        const int row = lw * kRowsPerLoader + r;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int q = h * 32 + lane;  // 16-byte chunk of the row, 0..63
-          const int c = q >> 3, k = q & 7;
-          *reinterpret_cast<uint4*>(stage + c * kPanelKV + (row >> 3) * 1024 + (row & 7) * 128 +
-                                    ((k ^ (row & 7)) << 4)) = v[2 * r + h];
+      for (int hh = 0; hh < 2; ++hh) {
+        if (g >= 2) {
+          if (lane == 0) ok = wait_bar(bar(pv_done(s, hh)), ((g >> 1) - 1) & 1, abort_flag, p.hdr);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
         }
+        const int q = hh * 32 + lane;  // 16-byte chunk of the row, 0..63
+        const int c = q >> 3, k = q & 7;
+#pragma unroll
+        for (int r = 0; r < kRowsPerLoader; ++r) {
+          const int row = lw * kRowsPerLoader + r;
+          *reinterpret_cast<uint4*>(stage + c * kPanelKV + (row >> 3) * 1024 + (row & 7) * 128 +
+                                    ((k ^ (row & 7)) << 4)) = v[2 * r + hh];
+        }
+        fence_proxy_async_smem();  // generic-proxy stores -> read by the tensor cores
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kv_full(s, hh)));
       }
-      fence_proxy_async_smem();  // generic-proxy stores -> read by the tensor cores
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarKVFull0 + s));
     }
   } else if (warp == kMmaWarp || warp == kPvWarp) {
     // ===================================================== MMA issuers
@@ -331,7 +338,8 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
     //    landed and its S buffer is free, and q of the next unit (tiled TMA)
     //    as soon as this unit's last QK has read q;
     //  - warp 13, lane 0: O^T += V^T P^T of every tile as soon as its P is
-    //    written (its commit releases the KV stage and the P buffer).
+    //    written (a commit after blocks 1 and 3 releases each half of the KV
+    //    stage; the second also frees the P buffer).
     // Each thread's commits track only its own MMAs.
     // Each has a single next event at any time, so it sleeps in the
     // mbarrier wait (hardware suspend) instead of spinning, which leaves the
@@ -352,14 +360,17 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
       while (cq.valid && ok) {
         const int g = cq.g, s = g & 1;
         if (qk_role) {
-          ok = wait_bar(bar(kBarKVFull0 + s), (g >> 1) & 1, abort_flag, p.hdr);
-          if (ok && g >= 2) ok = wait_bar(bar(kBarSEmpty0 + s), ((g >> 1) - 1) & 1, abort_flag, p.hdr);
+          if (g >= 2) ok = wait_bar(bar(kBarSEmpty0 + s), ((g >> 1) - 1) & 1, abort_flag, p.hdr);
           if (ok && cq.i == 0) ok = wait_bar(bar(kBarQFull), cq.nu & 1, abort_flag, p.hdr);
           if (!ok) break;
-          tc_fence_after();
           const uint32_t kvs = sKV + s * kKVBytes;
 #pragma unroll
           for (int c = 0; c < kPanels; ++c) {
+            if ((c & 3) == 0) {  // panels 4h..4h+3 = half h of the stage
+              ok = wait_bar(bar(kv_full(s, c >> 2)), (g >> 1) & 1, abort_flag, p.hdr);
+              if (!ok) break;
+              tc_fence_after();
+            }
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t a = sdesc_sw128(sQ + c * kPanelQ + kk * 32, 16, 1024);
@@ -367,6 +378,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
               mma_bf16(tmem + s * 64, a, bd, C::kIdescQK, (c | kk) ? 1u : 0u);
             }
           }
+          if (!ok) break;
           mma_commit(bar(kBarSFull0 + s));
           const bool last = cq.i == cq.ntiles - 1;
           const int nu = cq.nu;
@@ -401,8 +413,8 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
               const uint64_t bd = sdesc_sw128(ps + kk * 32, 16, 1024);
               mma_bf16(tmem + C::kOCol + b * NH, a, bd, C::kIdescPV, (first && kk == 0) ? 0u : 1u);
             }
+            if (b & 1) mma_commit(bar(pv_done(s, b >> 1)));  // half b/2 of the stage may be refilled
           }
-          mma_commit(bar(kBarPVDone0 + s));
           cq.next();
         }
       }
@@ -496,7 +508,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         }
         // P buffer s is free once the PV of tile g-2 is done
         if (g >= 2) {
-          if (lane == 0) wait_bar(bar(kBarPVDone0 + s), ((g >> 1) - 1) & 1, abort_flag, p.hdr);
+          if (lane == 0) wait_bar(bar(pv_done(s, 1)), ((g >> 1) - 1) & 1, abort_flag, p.hdr);
           __syncwarp();
         }
         // p = 2^(s*scale - m) in bf16 into rows hA, hB of P (K-major, 128-byte
@@ -532,7 +544,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
           }
           named_bar_sync(1, kSoftmaxThreads);
           // O^T must be quiescent: wait for the PV of tile g-1
-          if (lane == 0) wait_bar(bar(kBarPVDone0 + ((g - 1) & 1)), ((g - 1) >> 1) & 1, abort_flag, p.hdr);
+          if (lane == 0) wait_bar(bar(pv_done((g - 1) & 1, 1)), ((g - 1) >> 1) & 1, abort_flag, p.hdr);
           __syncwarp();
           tc_fence_after();
 #pragma unroll
@@ -562,7 +574,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
       lB += __shfl_xor_sync(0xffffffffu, lB, 1);
       lB += __shfl_xor_sync(0xffffffffu, lB, 2);
       const int gl = g - 1;
-      if (lane == 0) wait_bar(bar(kBarPVDone0 + (gl & 1)), (gl >> 1) & 1, abort_flag, p.hdr);
+      if (lane == 0) wait_bar(bar(pv_done(gl & 1, 1)), (gl >> 1) & 1, abort_flag, p.hdr);
       __syncwarp();
       tc_fence_after();
       if (tq == 0) {
