@@ -53,11 +53,9 @@ constexpr int kD = 512;
 constexpr int kPanels = kD / 64;           // 128-byte column panels per row
 constexpr int kTileN = kTileSlots;         // 64 slots per KV tile
 constexpr int kQRows = 64;                 // QK MMA M (heads padded to 64)
-constexpr int kPanelQ = kQRows * 128;      // bytes of one Q panel
 constexpr int kPanelKV = kTileN * 128;     // bytes of one KV panel
-constexpr int kQBytes = kPanels * kPanelQ;     // 64 KB
 constexpr int kKVBytes = kPanels * kPanelKV;   // 64 KB per stage
-constexpr int kStages = 2;
+constexpr int kMaxStages = 3;
 constexpr int kSoftmaxWarp0 = 0;           // warps 0..3: softmax / epilogue (TMEM quadrants 0..3)
 constexpr int kLoaderWarp0 = 4;            // warps 4..11: KV row loaders
 constexpr int kLoaderWarps = 8;
@@ -72,9 +70,9 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 enum Bar : int {
   kBarQFull = 0,
   kBarQEmpty,
-  kBarKVFull0,                   // + 2 * stage + half (columns [256 half, +256) of the rows)
-  kBarPVDone0 = kBarKVFull0 + 4,  // + 2 * stage + half (PV blocks 2 half, 2 half + 1 done)
-  kBarSFull0 = kBarPVDone0 + 4,
+  kBarKVFull0,                                // + 2 * stage + half (columns [256 half, +256))
+  kBarPVDone0 = kBarKVFull0 + 2 * kMaxStages,  // + 2 * stage + half (PV blocks 2 half, 2 half + 1 done)
+  kBarSFull0 = kBarPVDone0 + 2 * kMaxStages,
   kBarSFull1,
   kBarSEmpty0,
   kBarSEmpty1,
@@ -91,6 +89,14 @@ __host__ __device__ constexpr int pv_done(int s, int h) { return kBarPVDone0 + 2
 
 template <int NH>
 struct Cfg {
+  // q panels are packed NH rows apart; the QK MMA reads 64 rows per panel,
+  // so for NH < 64 rows NH..63 of a panel are whatever follows (the next
+  // panels, then the first KV stage): valid shared memory whose products
+  // land in TMEM lanes that nothing reads.  The space this saves at NH = 16
+  // buys a third KV stage.
+  static constexpr int kStages = NH <= 16 ? 3 : 2;
+  static constexpr int kPanelQ = NH * 128;
+  static constexpr int kQBytes = kPanels * kPanelQ;
   static constexpr int kPBytes = NH * 128;  // P: NH rows x 64 slots bf16
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kQBytes;
@@ -100,7 +106,7 @@ struct Cfg {
   // written into the other
   static constexpr int kOffStage2 = kOffP + kStages * kPBytes;
   static constexpr int kOffBar = kOffStage2 + NH * 256;
-  static constexpr int kOffMisc = kOffBar + 192;
+  static constexpr int kOffMisc = kOffBar + 192;  // kNumBars <= 24
   // misc: tmem base (4), abort flag (4), pad, then per-head float arrays
   static constexpr int kOffAlpha = kOffMisc + 16;
   static constexpr int kOffFac = kOffAlpha + 4 * 64;
@@ -111,6 +117,9 @@ struct Cfg {
   static constexpr uint32_t kIdescQK = idesc_bf16_f32(64, 64, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, NH, true, false);
   static_assert(kOffP % 1024 == 0 && kPBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
+  static_assert(kOffKV % 1024 == 0 && kPanelQ % 1024 == 0, "swizzle atoms need 1 KB alignment");
+  static_assert((kPanels - 1) * kPanelQ + kQRows * 128 <= kOffBar, "padded QK A operand inside smem");
+  static_assert(kStages <= kMaxStages, "barrier rings");
   static_assert(kNumBars * 8 <= kOffMisc - kOffBar, "mbarrier area");
   static_assert(kSmem <= 232448, "shared memory budget");
 };
@@ -220,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_out, const Params p) {
   using C = Cfg<NH>;
+  constexpr int KS = C::kStages;  // KV stages: tile g lives in stage g % KS
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_addr(smem);
@@ -238,7 +248,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQFull), 1);
     mbar_init(bar(kBarQEmpty), 1);
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 2 * C::kStages; ++i) {
       mbar_init(bar(kBarKVFull0 + i), kLoaderWarps);
       mbar_init(bar(kBarPVDone0 + i), 1);
     }
@@ -290,7 +300,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
     if (cur.valid) fetch_slots();
     bool ok = true;
     while (cur.valid && ok) {
-      const int g = cur.g, s = g & 1;
+      const int g = cur.g, s = g % KS;  // KV stage
       uint4 v[2 * kRowsPerLoader];
 #pragma unroll
       for (int r = 0; r < kRowsPerLoader; ++r) {
@@ -312,8 +322,8 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
       uint8_t* stage = smem + C::kOffKV + s * kKVBytes;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        if (g >= 2) {
-          if (lane == 0) ok = wait_bar(bar(pv_done(s, hh)), ((g >> 1) - 1) & 1, abort_flag, p.hdr);
+        if (g >= KS) {  // the tile KS back in this stage
+          if (lane == 0) ok = wait_bar(bar(pv_done(s, hh)), ((g / KS) - 1) & 1, abort_flag, p.hdr);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
         }
@@ -354,26 +364,26 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         mbar_arrive_expect_tx(bar(kBarQFull), NH * 128 * kPanels);
         const int qrow = cq.u.x * H + unit_head_group(cq.u.w) * NH;
 #pragma unroll
-        for (int c = 0; c < kPanels; ++c) tma_load_2d(sQ + c * kPanelQ, &tmap_q, c * 64, qrow, bar(kBarQFull));
+        for (int c = 0; c < kPanels; ++c) tma_load_2d(sQ + c * C::kPanelQ, &tmap_q, c * 64, qrow, bar(kBarQFull));
         q_issued = 1;
       }
       while (cq.valid && ok) {
-        const int g = cq.g, s = g & 1;
+        const int g = cq.g, s = g & 1, ks = g % KS;  // S / P buffer, KV stage
         if (qk_role) {
           if (g >= 2) ok = wait_bar(bar(kBarSEmpty0 + s), ((g >> 1) - 1) & 1, abort_flag, p.hdr);
           if (ok && cq.i == 0) ok = wait_bar(bar(kBarQFull), cq.nu & 1, abort_flag, p.hdr);
           if (!ok) break;
-          const uint32_t kvs = sKV + s * kKVBytes;
+          const uint32_t kvs = sKV + ks * kKVBytes;
 #pragma unroll
           for (int c = 0; c < kPanels; ++c) {
             if ((c & 3) == 0) {  // panels 4h..4h+3 = half h of the stage
-              ok = wait_bar(bar(kv_full(s, c >> 2)), (g >> 1) & 1, abort_flag, p.hdr);
+              ok = wait_bar(bar(kv_full(ks, c >> 2)), (g / KS) & 1, abort_flag, p.hdr);
               if (!ok) break;
               tc_fence_after();
             }
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t a = sdesc_sw128(sQ + c * kPanelQ + kk * 32, 16, 1024);
+              const uint64_t a = sdesc_sw128(sQ + c * C::kPanelQ + kk * 32, 16, 1024);
               const uint64_t bd = sdesc_sw128(kvs + c * kPanelKV + kk * 32, 16, 1024);
               mma_bf16(tmem + s * 64, a, bd, C::kIdescQK, (c | kk) ? 1u : 0u);
             }
@@ -391,7 +401,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
             mbar_arrive_expect_tx(bar(kBarQFull), NH * 128 * kPanels);
             const int qrow = cq.u.x * H + unit_head_group(cq.u.w) * NH;
 #pragma unroll
-            for (int c = 0; c < kPanels; ++c) tma_load_2d(sQ + c * kPanelQ, &tmap_q, c * 64, qrow, bar(kBarQFull));
+            for (int c = 0; c < kPanels; ++c) tma_load_2d(sQ + c * C::kPanelQ, &tmap_q, c * 64, qrow, bar(kBarQFull));
             q_issued = cq.nu + 1;
           }
         } else {
@@ -400,7 +410,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
           if (ok && first && cq.nu >= 1) ok = wait_bar(bar(kBarOEmpty), (cq.nu - 1) & 1, abort_flag, p.hdr);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t kvs = sKV + s * kKVBytes;
+          const uint32_t kvs = sKV + ks * kKVBytes;
           const uint32_t ps = sP + s * C::kPBytes;
 #pragma unroll
           for (int b = 0; b < 4; ++b) {
@@ -413,7 +423,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
               const uint64_t bd = sdesc_sw128(ps + kk * 32, 16, 1024);
               mma_bf16(tmem + C::kOCol + b * NH, a, bd, C::kIdescPV, (first && kk == 0) ? 0u : 1u);
             }
-            if (b & 1) mma_commit(bar(pv_done(s, b >> 1)));  // half b/2 of the stage may be refilled
+            if (b & 1) mma_commit(bar(pv_done(ks, b >> 1)));  // half b/2 of the stage may be refilled
           }
           cq.next();
         }
@@ -508,7 +518,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         }
         // P buffer s is free once the PV of tile g-2 is done
         if (g >= 2) {
-          if (lane == 0) wait_bar(bar(pv_done(s, 1)), ((g >> 1) - 1) & 1, abort_flag, p.hdr);
+          if (lane == 0) wait_bar(bar(pv_done((g - 2) % KS, 1)), ((g - 2) / KS) & 1, abort_flag, p.hdr);
           __syncwarp();
         }
         // p = 2^(s*scale - m) in bf16 into rows hA, hB of P (K-major, 128-byte
@@ -544,7 +554,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
           }
           named_bar_sync(1, kSoftmaxThreads);
           // O^T must be quiescent: wait for the PV of tile g-1
-          if (lane == 0) wait_bar(bar(pv_done((g - 1) & 1, 1)), ((g - 1) >> 1) & 1, abort_flag, p.hdr);
+          if (lane == 0) wait_bar(bar(pv_done((g - 1) % KS, 1)), ((g - 1) / KS) & 1, abort_flag, p.hdr);
           __syncwarp();
           tc_fence_after();
 #pragma unroll
@@ -574,7 +584,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
       lB += __shfl_xor_sync(0xffffffffu, lB, 1);
       lB += __shfl_xor_sync(0xffffffffu, lB, 2);
       const int gl = g - 1;
-      if (lane == 0) wait_bar(bar(pv_done(gl & 1, 1)), (gl >> 1) & 1, abort_flag, p.hdr);
+      if (lane == 0) wait_bar(bar(pv_done(gl % KS, 1)), (gl / KS) & 1, abort_flag, p.hdr);
       __syncwarp();
       tc_fence_after();
       if (tq == 0) {
