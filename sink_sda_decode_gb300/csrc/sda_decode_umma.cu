@@ -327,14 +327,14 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
         }
-        const int q = hh * 32 + lane;  // 16-byte chunk of the row, 0..63
-        const int c = q >> 3, k = q & 7;
+        // 16-byte chunk q = 32*hh + lane of each row: panel q/8, chunk q%8;
+        // the warp's 8 rows are one 8-row swizzle atom of every panel
+        const int q = hh * 32 + lane, k = q & 7;
+        uint8_t* atom = stage + (q >> 3) * kPanelKV + lw * 1024;
+        static_assert(kRowsPerLoader == 8, "one swizzle atom per loader warp");
 #pragma unroll
-        for (int r = 0; r < kRowsPerLoader; ++r) {
-          const int row = lw * kRowsPerLoader + r;
-          *reinterpret_cast<uint4*>(stage + c * kPanelKV + (row >> 3) * 1024 + (row & 7) * 128 +
-                                    ((k ^ (row & 7)) << 4)) = v[2 * r + hh];
-        }
+        for (int r = 0; r < kRowsPerLoader; ++r)
+          *reinterpret_cast<uint4*>(atom + r * 128 + ((k ^ r) << 4)) = v[2 * r + hh];
         fence_proxy_async_smem();  // generic-proxy stores -> read by the tensor cores
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kv_full(s, hh)));
@@ -374,6 +374,8 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
           if (ok && cq.i == 0) ok = wait_bar(bar(kBarQFull), cq.nu & 1, abort_flag, p.hdr);
           if (!ok) break;
           const uint32_t kvs = sKV + ks * kKVBytes;
+          // descriptors of the first K step; the others only move the start address
+          const uint64_t a0 = sdesc_sw128(sQ, 16, 1024), b0 = sdesc_sw128(kvs, 16, 1024);
 #pragma unroll
           for (int c = 0; c < kPanels; ++c) {
             if ((c & 3) == 0) {  // panels 4h..4h+3 = half h of the stage
@@ -383,8 +385,8 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
             }
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t a = sdesc_sw128(sQ + c * C::kPanelQ + kk * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(kvs + c * kPanelKV + kk * 32, 16, 1024);
+              const uint64_t a = sdesc_advance(a0, c * C::kPanelQ + kk * 32);
+              const uint64_t bd = sdesc_advance(b0, c * kPanelKV + kk * 32);
               mma_bf16(tmem + s * 64, a, bd, C::kIdescQK, (c | kk) ? 1u : 0u);
             }
           }
@@ -412,15 +414,16 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
           tc_fence_after();
           const uint32_t kvs = sKV + ks * kKVBytes;
           const uint32_t ps = sP + s * C::kPBytes;
+          const uint64_t a0 = sdesc_sw128(kvs, kPanelKV, 1024), b0 = sdesc_sw128(ps, 16, 1024);
 #pragma unroll
           for (int b = 0; b < 4; ++b) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               // A = V^T block b: rows d in [128b, 128b+128) = panels 2b, 2b+1 (MN-major);
               //     K = slots [16kk, 16kk+16) = row groups 2kk, 2kk+1
-              const uint64_t a = sdesc_sw128(kvs + (2 * b) * kPanelKV + kk * 2048, kPanelKV, 1024);
+              const uint64_t a = sdesc_advance(a0, (2 * b) * kPanelKV + kk * 2048);
               // B = P^T: N = NH heads (rows), K = 16 slots at byte offset 32kk (K-major)
-              const uint64_t bd = sdesc_sw128(ps + kk * 32, 16, 1024);
+              const uint64_t bd = sdesc_advance(b0, kk * 32);
               mma_bf16(tmem + C::kOCol + b * NH, a, bd, C::kIdescPV, (first && kk == 0) ? 0u : 1u);
             }
             if (b & 1) mma_commit(bar(pv_done(ks, b >> 1)));  // half b/2 of the stage may be refilled

@@ -277,6 +277,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The same descriptor for a start address `byte_off` bytes further on: the
+// start-address field is the low 14 bits of (address >> 4), and shared
+// memory addresses stay below 2^18, so the addition cannot carry out of it.
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t byte_off) {
+  return desc + (uint64_t)(byte_off >> 4);
+}
+
 // Instruction descriptor of kind::f16 with bf16 A/B and fp32 D.
 // a_mn / b_mn: operand stored MN-major (transposed) instead of K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
