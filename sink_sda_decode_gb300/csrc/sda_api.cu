@@ -105,7 +105,7 @@ bool choose_plan(int H, int D, const DeviceCaps& caps, LaunchPlan* lp) {
     lp->nh = nh;
     lp->hg = H / lp->nh;
     lp->grid = caps.num_sms;  // one CTA per SM (about 200 KB of shared memory each)
-    lp->threads = 448;
+    lp->threads = 640;
     lp->smem = umma_smem_bytes(lp->nh);
     lp->tile = kTileSlots;
     lp->min_chunk = kTileSlots;

@@ -14,27 +14,30 @@
 //    token's slot list for NH <= 64 heads (H = 128 uses two CTAs per token).
 //    All heads of a token share each gathered KV row, so a row is read from
 //    HBM once per CTA.
-//  * Warps 4..11 load KV tiles of 64 slots: each 1 KB row is read by a whole
+//  * Warps 8..15 load KV tiles of 64 slots: each 1 KB row is read by a whole
 //    warp as two contiguous 512-byte loads (16 x 16 B in flight per thread,
-//    64 KB per SM), then stored 128-byte-swizzled into one of two
-//    shared-memory stages, one half of D at a time: a half is refilled as
-//    soon as the PV MMAs that read it (blocks 0-1 or 2-3) are done, and the
-//    next QK starts on the first half while the second is still stored.
+//    64 KB per SM), then stored 128-byte-swizzled into a shared-memory stage
+//    (2 stages, 3 for NH = 16), one half of D at a time: a half is refilled
+//    as soon as the PV MMAs that read it (blocks 0-1 or 2-3) are done, and
+//    the next QK starts on the first half while the second is still stored.
 //    Whole-row loads keep DRAM accesses contiguous; TMA tile::gather4, which
 //    fetches 128 bytes of four rows per instruction, topped out near a third
 //    of HBM bandwidth on this GPU.
-//  * Warps 12 and 13 issue tcgen05 MMAs, event driven and apart, so that one
+//  * Warps 16 and 17 issue tcgen05 MMAs, event driven and apart, so that one
 //    waiting for the tensor pipe never delays the other:  S = Q K^T  (M = 64
-//    padded heads, N = 64 slots, K = 512) into TMEM by warp 12, which also
+//    padded heads, N = 64 slots, K = 512) into TMEM by warp 16, which also
 //    loads q[t] with tiled TMA, and  O^T += V^T P^T  (M = 128 rows of D,
-//    N = NH heads, K = 64 slots) into a TMEM accumulator by warp 13; the
+//    N = NH heads, K = 64 slots) into a TMEM accumulator by warp 17; the
 //    same shared tile is K (K-major operand) and V (MN-major operand).
-//  * Warps 0..3 read S from TMEM (two heads per quad of threads), run the
-//    online softmax, write P (bf16) to shared memory, rescale O^T in TMEM
-//    only when a head's running max grows by more than 8 (2^8 headroom, so
-//    p <= 256), and finally normalise with the sink and write out through
-//    stmatrix + TMA stores (or, for a piece of a split token, write the
-//    unnormalised partial for the combine kernel).
+//    (Warps 18 and 19 only fill out the register split: 20 warps on four
+//    sub-partitions of 16 K registers leave 96 registers per thread.)
+//  * Warps 0..7 read S from TMEM (warps q and q + 4 share lane quadrant q
+//    and take slots 0..31 and 32..63; two heads per quad of threads), run
+//    the online softmax, write P (bf16) to shared memory, rescale O^T in
+//    TMEM only when a head's running max grows by more than 8 (2^8
+//    headroom, so p <= 256), and finally normalise with the sink and write
+//    out through stmatrix + TMA stores (or, for a piece of a split token,
+//    write the unnormalised partial for the combine kernel).
 //  * Every mbarrier wait is bounded (2 s); on timeout the kernel raises the
 //    workspace error word, drains its own copies and returns.
 #include <cuda.h>
@@ -56,14 +59,16 @@ constexpr int kQRows = 64;                 // QK MMA M (heads padded to 64)
 constexpr int kPanelKV = kTileN * 128;     // bytes of one KV panel
 constexpr int kKVBytes = kPanels * kPanelKV;   // 64 KB per stage
 constexpr int kMaxStages = 3;
-constexpr int kSoftmaxWarp0 = 0;           // warps 0..3: softmax / epilogue (TMEM quadrants 0..3)
-constexpr int kLoaderWarp0 = 4;            // warps 4..11: KV row loaders
+constexpr int kSmWarps = 8;                // warps 0..7: softmax / epilogue (warps q, q+4 share TMEM quadrant q)
+constexpr int kLoaderWarp0 = 8;            // warps 8..15: KV row loaders
 constexpr int kLoaderWarps = 8;
-constexpr int kMmaWarp = 12;               // warp 12: QK issuer + q loads
-constexpr int kPvWarp = 13;                // warp 13: PV issuer
-constexpr int kThreads = 448;              // 14 warps (<= 128 registers per thread)
+constexpr int kMmaWarp = 16;               // warp 16: QK issuer + q loads
+constexpr int kPvWarp = 17;                // warp 17: PV issuer
+// 20 warps (18, 19 idle): warps are spread over the SM's four sub-partitions,
+// each with 16 K registers, so 18 or 20 warps (5 on some) allow 96 registers
+constexpr int kThreads = 640;
 constexpr int kRowsPerLoader = kTileSlots / kLoaderWarps;  // 8 rows of a tile per loader warp
-constexpr int kSoftmaxThreads = 128;
+constexpr int kSoftmaxThreads = kSmWarps * 32;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
@@ -107,10 +112,15 @@ struct Cfg {
   static constexpr int kOffStage2 = kOffP + kStages * kPBytes;
   static constexpr int kOffBar = kOffStage2 + NH * 256;
   static constexpr int kOffMisc = kOffBar + 192;  // kNumBars <= 24
-  // misc: tmem base (4), abort flag (4), pad, then per-head float arrays
-  static constexpr int kOffAlpha = kOffMisc + 16;
-  static constexpr int kOffFac = kOffAlpha + 4 * 64;
-  static constexpr int kSmemUsed = kOffFac + 4 * 64;
+  // misc: tmem base (4), abort flag (4), pad, then per-head float arrays:
+  // l-sum [2 halves][64]; alpha aliases its first half (used only inside a
+  // unit's tiles) and fac its second (each thread reads its head's l-sums
+  // before it writes that head's fac); half-tile maxima [2 tiles][2][64]
+  static constexpr int kOffLSum = kOffMisc + 16;
+  static constexpr int kOffAlpha = kOffLSum;
+  static constexpr int kOffFac = kOffLSum + 4 * 64;
+  static constexpr int kOffHMax = kOffLSum + 4 * 128;
+  static constexpr int kSmemUsed = kOffHMax + 4 * 256;
   static constexpr int kSmem = kSmemUsed + 1024;  // slack for 1024-byte alignment
   static constexpr int kTmemCols = (128 + 4 * NH) <= 256 ? 256 : 512;
   static constexpr int kOCol = 128;  // O^T block b at columns [128 + b*NH, +NH)
@@ -241,6 +251,8 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   float* s_alpha = reinterpret_cast<float*>(smem + C::kOffAlpha);
   float* s_fac = reinterpret_cast<float*>(smem + C::kOffFac);
+  float* s_lsum = reinterpret_cast<float*>(smem + C::kOffLSum);
+  float* s_hmax = reinterpret_cast<float*>(smem + C::kOffHMax);
   auto bar = [&](int i) { return sBar + 8u * (uint32_t)i; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -254,11 +266,11 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
     }
     mbar_init(bar(kBarSFull0), 1);
     mbar_init(bar(kBarSFull1), 1);
-    mbar_init(bar(kBarSEmpty0), 4);
-    mbar_init(bar(kBarSEmpty1), 4);
-    mbar_init(bar(kBarPFull0), 4);
-    mbar_init(bar(kBarPFull1), 4);
-    mbar_init(bar(kBarOEmpty), 4);
+    mbar_init(bar(kBarSEmpty0), kSmWarps);
+    mbar_init(bar(kBarSEmpty1), kSmWarps);
+    mbar_init(bar(kBarPFull0), kSmWarps);
+    mbar_init(bar(kBarPFull1), kSmWarps);
+    mbar_init(bar(kBarOEmpty), kSmWarps);
     mbar_init(bar(kBarDrain), 1);
     mbar_init(bar(kBarDrainPv), 1);
     *abort_flag = 0;
@@ -344,10 +356,10 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
     // ===================================================== MMA issuers
     // Two threads issue tcgen05 MMAs, so that one waiting for the tensor
     // pipe to accept its instructions never delays the other:
-    //  - warp 12, lane 0: S = Q K^T of every tile, as soon as the tile has
+    //  - warp 16, lane 0: S = Q K^T of every tile, as soon as the tile has
     //    landed and its S buffer is free, and q of the next unit (tiled TMA)
     //    as soon as this unit's last QK has read q;
-    //  - warp 13, lane 0: O^T += V^T P^T of every tile as soon as its P is
+    //  - warp 17, lane 0: O^T += V^T P^T of every tile as soon as its P is
     //    written (a commit after blocks 1 and 3 releases each half of the KV
     //    stage; the second also frees the P buffer).
     // Each thread's commits track only its own MMAs.
@@ -438,25 +450,26 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
       if (qk_role && q_issued >= 1) drain_bar(bar(kBarQFull), (q_issued - 1) & 1, p.hdr);
     }
     __syncwarp();
-  } else if (warp < kSoftmaxWarp0 + 4) {
+  } else if (warp < kSmWarps) {
     // ===================================================== softmax + epilogue
-    // S is read with the 16x256b TMEM shape: thread t of warp q4 holds heads
-    // hA = 16*q4 + t/4 and hB = hA + 8 (the M = 64 accumulator keeps row r in
-    // lane 32*(r/16) + r%16), each for the 16 slots 8*rep + 2*(t%4) + {0,1},
-    // rep = 0..7.  A head's 64 slots are spread over the 4 threads of a quad,
-    // so every lane works and row reductions are two quad shuffles.
-    const int q4 = warp & 3;                          // TMEM lane quadrant of this warp
-    const int st = threadIdx.x - kSoftmaxWarp0 * 32;  // 0..127
+    // Warp w reads TMEM lane quadrant q = w % 4 and slots [32hc, 32hc + 32) of
+    // each tile, hc = w / 4, with the 16x256b shape: thread t holds heads
+    // hA = 16q + t/4 and hB = hA + 8 (the M = 64 accumulator keeps row r in
+    // lane 32*(r/16) + r%16) for the 8 slots 32hc + 8rep + 2(t%4) + {0,1},
+    // rep = 0..3.  A head's row max over the tile is two quad shuffles and
+    // one exchange with warp w ^ 4 through shared memory.
+    const int q4 = warp & 3, hc = warp >> 2;
+    const int st = threadIdx.x;  // 0..255
     const int tq = lane & 3;
     const int hA = q4 * 16 + (lane >> 2), hB = hA + 8;
     const bool vA = hA < NH, vB = hB < NH;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const float sc = p.qk_scale_log2;
     const bool pos_sc = sc >= 0.f;  // a negative scale makes the smallest score the largest logit
-    // Control flow here is identical in the four warps (it depends only on
+    // Control flow here is identical in the eight warps (it depends only on
     // the unit list and on block-wide votes), so every named barrier is
-    // reached by all 128 threads even after a wait timed out: a timed-out
-    // wait only leaves garbage in the outputs and the error word raised.
+    // reached by all of them even after a wait timed out: a timed-out wait
+    // only leaves garbage in the outputs and the error word raised.
     int g = 0;
     for (int k = 0;; ++k) {
       const int pos = unit_position(k, blockIdx.x, gridDim.x);
@@ -472,26 +485,26 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
       const int ntiles = (len + kTileN - 1) / kTileN;
       float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;  // l: this thread's share
       // the sink logits are only needed in the epilogue: load them now
-      const float sinkA = (row < 0 && vA && tq == 0) ? __ldg(p.attn_sink + hg * NH + hA) : 0.f;
-      const float sinkB = (row < 0 && vB && tq == 0) ? __ldg(p.attn_sink + hg * NH + hB) : 0.f;
+      const float sinkA = (row < 0 && vA && tq == 0 && hc == 0) ? __ldg(p.attn_sink + hg * NH + hA) : 0.f;
+      const float sinkB = (row < 0 && vB && tq == 0 && hc == 0) ? __ldg(p.attn_sink + hg * NH + hB) : 0.f;
       for (int i = 0; i < ntiles; ++i, ++g) {
         const int s = g & 1;
         const int n = min(kTileN, len - i * kTileN);
         wait_bar(bar(kBarSFull0 + s), (g >> 1) & 1, abort_flag, p.hdr);
         tc_fence_after();
-        uint32_t sv[32];
-        tmem_ld_16x256b_x8(tmem + lane_base + s * 64, sv);
+        uint32_t sv[16];
+        tmem_ld_16x256b_x4(tmem + lane_base + s * 64 + 32 * hc, sv);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarSEmpty0 + s));  // S buffer s may be overwritten
-        // largest scaled logit per head over the tile's valid slots
+        // largest scaled logit per head over this warp's valid slots
         float eA = pos_sc ? -INFINITY : INFINITY, eB = eA;
 #pragma unroll
-        for (int rep = 0; rep < 8; ++rep) {
+        for (int rep = 0; rep < 4; ++rep) {
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk) {
-            if (8 * rep + 2 * tq + kk < n) {
+            if (32 * hc + 8 * rep + 2 * tq + kk < n) {
               const float a = __uint_as_float(sv[4 * rep + kk]), b = __uint_as_float(sv[4 * rep + 2 + kk]);
               eA = pos_sc ? fmaxf(eA, a) : fminf(eA, a);
               eB = pos_sc ? fmaxf(eB, b) : fminf(eB, b);
@@ -503,6 +516,17 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
           const float xa = __shfl_xor_sync(0xffffffffu, eA, o), xb = __shfl_xor_sync(0xffffffffu, eB, o);
           eA = pos_sc ? fmaxf(eA, xa) : fminf(eA, xa);
           eB = pos_sc ? fmaxf(eB, xb) : fminf(eB, xb);
+        }
+        {  // combine with the other half of the tile (warp w ^ 4)
+          float* hm = s_hmax + (g & 1) * 128;
+          if (tq == 0) {
+            hm[hc * 64 + hA] = eA;
+            hm[hc * 64 + hB] = eB;
+          }
+          named_bar_sync(2 + q4, 64);
+          const float oA = hm[(hc ^ 1) * 64 + hA], oB = hm[(hc ^ 1) * 64 + hB];
+          eA = pos_sc ? fmaxf(eA, oA) : fminf(eA, oA);
+          eB = pos_sc ? fmaxf(eB, oB) : fminf(eB, oB);
         }
         const float tA = eA * sc, tB = eB * sc;
         float alphaA = 1.f, alphaB = 1.f;
@@ -525,15 +549,16 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
           __syncwarp();
         }
         // p = 2^(s*scale - m) in bf16 into rows hA, hB of P (K-major, 128-byte
-        // swizzle: 16-byte chunk `rep` of 8 slots at (rep ^ (h & 7)) * 16,
-        // this thread's slot pair at byte 4*tq of the chunk)
+        // swizzle: 16-byte chunk c of 8 slots at (c ^ (h & 7)) * 16, this
+        // thread's slot pair at byte 4*tq of the chunk)
         uint8_t* pbase = smem + C::kOffP + s * C::kPBytes;
         uint8_t* prowA = pbase + (hA >> 3) * 1024 + (hA & 7) * 128 + 4 * tq;
         uint8_t* prowB = pbase + (hB >> 3) * 1024 + (hB & 7) * 128 + 4 * tq;
         float sA = 0.f, sB = 0.f;
 #pragma unroll
-        for (int rep = 0; rep < 8; ++rep) {
-          const int j = 8 * rep + 2 * tq;
+        for (int rep = 0; rep < 4; ++rep) {
+          const int c = 4 * hc + rep;  // chunk of 8 slots within the tile
+          const int j = 8 * c + 2 * tq;
           const float a0 = j < n ? ex2_approx(fmaf(__uint_as_float(sv[4 * rep + 0]), sc, -mA)) : 0.f;
           const float a1 = j + 1 < n ? ex2_approx(fmaf(__uint_as_float(sv[4 * rep + 1]), sc, -mA)) : 0.f;
           const float b0 = j < n ? ex2_approx(fmaf(__uint_as_float(sv[4 * rep + 2]), sc, -mB)) : 0.f;
@@ -544,14 +569,14 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
           const float2 fa = __bfloat1622float2(pa), fb = __bfloat1622float2(pb);
           sA += fa.x + fa.y;
           sB += fb.x + fb.y;
-          if (vA) *reinterpret_cast<uint32_t*>(prowA + ((rep ^ (hA & 7)) << 4)) = *reinterpret_cast<uint32_t*>(&pa);
-          if (vB) *reinterpret_cast<uint32_t*>(prowB + ((rep ^ (hB & 7)) << 4)) = *reinterpret_cast<uint32_t*>(&pb);
+          if (vA) *reinterpret_cast<uint32_t*>(prowA + ((c ^ (hA & 7)) << 4)) = *reinterpret_cast<uint32_t*>(&pa);
+          if (vB) *reinterpret_cast<uint32_t*>(prowB + ((c ^ (hB & 7)) << 4)) = *reinterpret_cast<uint32_t*>(&pb);
         }
         lA += sA;
         lB += sB;
         fence_proxy_async_smem();
         if (named_bar_or(1, kSoftmaxThreads, need)) {
-          if (tq == 0) {
+          if (tq == 0 && hc == 0) {
             if (vA) s_alpha[hA] = alphaA;
             if (vB) s_alpha[hB] = alphaB;
           }
@@ -560,8 +585,9 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
           if (lane == 0) wait_bar(bar(pv_done((g - 1) % KS, 1)), ((g - 1) / KS) & 1, abort_flag, p.hdr);
           __syncwarp();
           tc_fence_after();
+          // this warp's lanes of O^T blocks 2hc, 2hc + 1
 #pragma unroll
-          for (int b = 0; b < 4; ++b) {
+          for (int b = 2 * hc; b < 2 * hc + 2; ++b) {
 #pragma unroll
             for (int c = 0; c < NH / 16; ++c) {
               uint32_t ov[16];
@@ -581,107 +607,115 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         if (lane == 0) mbar_arrive(bar(kBarPFull0 + s));
       }
       // ---------------------------------------------- epilogue of the unit
-      // denominators: sum the quad's shares
+      // denominators: the quad's shares, then the two halves of the tile
       lA += __shfl_xor_sync(0xffffffffu, lA, 1);
       lA += __shfl_xor_sync(0xffffffffu, lA, 2);
       lB += __shfl_xor_sync(0xffffffffu, lB, 1);
       lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+      if (tq == 0) {
+        s_lsum[hc * 64 + hA] = lA;
+        s_lsum[hc * 64 + hB] = lB;
+      }
       const int gl = g - 1;
       if (lane == 0) wait_bar(bar(pv_done(gl % KS, 1)), (gl / KS) & 1, abort_flag, p.hdr);
       __syncwarp();
       tc_fence_after();
-      if (tq == 0) {
+      named_bar_sync(1, kSoftmaxThreads);
+      if (tq == 0 && hc == 0) {
 #pragma unroll
         for (int w2 = 0; w2 < 2; ++w2) {
           const int hd = w2 ? hB : hA;
-          const float mh = w2 ? mB : mA, lh = w2 ? lB : lA;
+          const float mh = w2 ? mB : mA;
           if (hd >= NH) continue;
+          const float lh = s_lsum[hd] + s_lsum[64 + hd];  // read before fac[hd] overwrites s_lsum[64 + hd]
           const int hh = hg * NH + hd;
+          float f = 1.f;
           if (row < 0) {
             const float ms = (w2 ? sinkB : sinkA) * kLog2e;
             const float M = fmaxf(mh, ms);
-            float f = 0.f;
+            f = 0.f;
             if (M != -INFINITY && ms != INFINITY) {
               const float a = ex2_approx(mh - M);
               f = a / (lh * a + ex2_approx(ms - M));
             }
-            s_fac[hd] = f;
           } else {
             p.part_ml[(size_t)row * H + hh] = make_float2(mh, lh);
-            s_fac[hd] = 1.f;
           }
+          s_fac[hd] = f;
         }
       }
       named_bar_sync(1, kSoftmaxThreads);
       if (row < 0) {
-        // bf16 output, one 128-row block of D at a time.  O^T is read with the
-        // 16x256b shape (thread t: rows d = t/4 and t/4 + 8 of a 16-row band,
-        // head pairs 8*rep + 2*(t%4), +1), scaled, packed to bf16 pairs and
-        // written transposed with stmatrix into the idle P buffers as two
-        // [NH heads][64 d] boxes in the 128-byte-swizzled layout (no bank
-        // conflicts), which two TMA stores copy to out.  Blocks alternate
-        // between two staging areas, so a block's stores overlap the next
-        // block's TMEM reads.
-        float fac[NH / 4];               // this thread's heads 8*rep + 2*tq, +1
-#pragma unroll
-        for (int rep = 0; rep < NH / 8; ++rep) {
-          fac[2 * rep] = s_fac[8 * rep + 2 * tq];
-          fac[2 * rep + 1] = s_fac[8 * rep + 2 * tq + 1];
-        }
+        // bf16 output: warps 4hc..4hc+3 write O^T blocks 2hc and 2hc + 1
+        // (rows 256hc..256hc+255 of D) through staging area hc.  O^T is read
+        // with the 16x256b shape (thread t: rows d = t/4 and t/4 + 8 of a
+        // 16-row band, head pairs 8*rep + 2*(t%4), +1) in chunks of 32 heads,
+        // scaled, packed to bf16 pairs and written transposed with stmatrix as
+        // two [NH heads][64 d] boxes in the 128-byte-swizzled layout (no bank
+        // conflicts), which two TMA stores copy to out.
+        uint8_t* stg = smem + (hc ? C::kOffStage2 : C::kOffP);  // 2 boxes of NH x 128 B
+        constexpr int kCH = NH < 32 ? NH : 32;  // heads per chunk
 #pragma unroll 1
-        for (int b = 0; b < 4; ++b) {
-          uint8_t* stg = smem + ((b & 1) ? C::kOffStage2 : C::kOffP);  // 2 boxes of NH x 128 B
-          if (b >= 2) {
-            // the stores of block b - 2 have read this area
-            if (st == 0) bulk_wait_read1();
-            named_bar_sync(1, kSoftmaxThreads);
+        for (int b = 2 * hc; b < 2 * hc + 2; ++b) {
+          if (b & 1) {
+            // the stores of block b - 1 have read the staging area
+            if (q4 == 0 && lane == 0) bulk_wait_read0();
+            named_bar_sync(6 + hc, 128);
           }
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const uint32_t taddr = tmem + ((uint32_t)(q4 * 32 + 16 * half) << 16) + C::kOCol + b * NH;
-            uint32_t r[NH / 2];
-            if constexpr (NH == 64) tmem_ld_16x256b_x8(taddr, r);
-            else if constexpr (NH == 32) tmem_ld_16x256b_x4(taddr, r);
-            else tmem_ld_16x256b_x2(taddr, r);
-            tmem_wait_ld();
-            // "+ 0.f" turns -0 into +0 when the factor is 0 (sink = +inf)
-            uint32_t pk[NH / 4];  // [rep][row d or d+8]
+          for (int h0 = 0; h0 < NH; h0 += kCH) {
+            float fac[kCH / 4];  // this thread's heads h0 + 8*rep + 2*tq, +1
 #pragma unroll
-            for (int rep = 0; rep < NH / 8; ++rep) {
-#pragma unroll
-              for (int dg = 0; dg < 2; ++dg) {
-                __nv_bfloat162 v2 = __floats2bfloat162_rn(
-                    __uint_as_float(r[4 * rep + 2 * dg]) * fac[2 * rep] + 0.f,
-                    __uint_as_float(r[4 * rep + 2 * dg + 1]) * fac[2 * rep + 1] + 0.f);
-                pk[2 * rep + dg] = *reinterpret_cast<uint32_t*>(&v2);
-              }
+            for (int rep = 0; rep < kCH / 8; ++rep) {
+              fac[2 * rep] = s_fac[h0 + 8 * rep + 2 * tq];
+              fac[2 * rep + 1] = s_fac[h0 + 8 * rep + 2 * tq + 1];
             }
-            // matrix m of a stmatrix.x4 = (rep0 + m/2, d group m%2); lane
-            // 8m + j addresses row j (head 8*rep + j) of transposed matrix m
-            const int m = lane >> 3, j = lane & 7;
-            const int dl = q4 * 32 + 16 * half + 8 * (m & 1);  // block-local d of the 8 columns
-            const int box = dl >> 6, chunk = (dl & 63) >> 3;
 #pragma unroll
-            for (int rep0 = 0; rep0 < NH / 8; rep0 += 2) {
-              const int h = 8 * (rep0 + (m >> 1)) + j;
-              const uint32_t addr = smem_addr(stg) + box * (NH * 128) + h * 128 + ((chunk ^ (h & 7)) << 4);
-              stmatrix_x4_trans(addr, pk[2 * rep0], pk[2 * rep0 + 1], pk[2 * rep0 + 2], pk[2 * rep0 + 3]);
+            for (int half = 0; half < 2; ++half) {
+              const uint32_t taddr = tmem + ((uint32_t)(q4 * 32 + 16 * half) << 16) + C::kOCol + b * NH + h0;
+              uint32_t r[kCH / 2];
+              if constexpr (kCH == 32) tmem_ld_16x256b_x4(taddr, r);
+              else tmem_ld_16x256b_x2(taddr, r);
+              tmem_wait_ld();
+              // "+ 0.f" turns -0 into +0 when the factor is 0 (sink = +inf)
+              uint32_t pk[kCH / 4];  // [rep][row d or d+8]
+#pragma unroll
+              for (int rep = 0; rep < kCH / 8; ++rep) {
+#pragma unroll
+                for (int dg = 0; dg < 2; ++dg) {
+                  __nv_bfloat162 v2 = __floats2bfloat162_rn(
+                      __uint_as_float(r[4 * rep + 2 * dg]) * fac[2 * rep] + 0.f,
+                      __uint_as_float(r[4 * rep + 2 * dg + 1]) * fac[2 * rep + 1] + 0.f);
+                  pk[2 * rep + dg] = *reinterpret_cast<uint32_t*>(&v2);
+                }
+              }
+              // matrix m of a stmatrix.x4 = (rep0 + m/2, d group m%2); lane
+              // 8m + j addresses row j (head h0 + 8*rep + j) of matrix m
+              const int m = lane >> 3, j = lane & 7;
+              const int dl = q4 * 32 + 16 * half + 8 * (m & 1);  // block-local d of the 8 columns
+              const int box = dl >> 6, chunk = (dl & 63) >> 3;
+#pragma unroll
+              for (int rep0 = 0; rep0 < kCH / 8; rep0 += 2) {
+                const int h = h0 + 8 * (rep0 + (m >> 1)) + j;
+                const uint32_t addr = smem_addr(stg) + box * (NH * 128) + h * 128 + ((chunk ^ (h & 7)) << 4);
+                stmatrix_x4_trans(addr, pk[2 * rep0], pk[2 * rep0 + 1], pk[2 * rep0 + 2], pk[2 * rep0 + 3]);
+              }
             }
           }
           fence_proxy_async_smem();
-          named_bar_sync(1, kSoftmaxThreads);
-          if (st == 0) {
+          named_bar_sync(6 + hc, 128);
+          if (q4 == 0 && lane == 0) {
             tma_store_2d(&tmap_out, b * 128, t * H + hg * NH, smem_addr(stg));
             tma_store_2d(&tmap_out, b * 128 + 64, t * H + hg * NH, smem_addr(stg) + NH * 128);
             bulk_commit();
           }
         }
-        // both areas (one is the P buffers) are free again before this
-        // unit's epilogue ends
-        if (st == 0) bulk_wait_read0();
+        // the staging areas (one is the P buffers) are free again before
+        // this unit's epilogue ends
+        if (q4 == 0 && lane == 0) bulk_wait_read0();
       } else {
 #pragma unroll 1
-        for (int b = 0; b < 4; ++b) {
+        for (int b = 2 * hc; b < 2 * hc + 2; ++b) {
           const int d = b * 128 + q4 * 32 + lane;
 #pragma unroll
           for (int c = 0; c < NH / 16; ++c) {
@@ -695,10 +729,10 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         }
       }
       tc_fence_before();
-      named_bar_sync(1, kSoftmaxThreads);  // s_fac is rewritten by the next unit
+      named_bar_sync(1, kSoftmaxThreads);  // s_fac / s_lsum are rewritten by the next unit
       if (lane == 0) mbar_arrive(bar(kBarOEmpty));
     }
-    if (st == 0) bulk_wait0();  // every output store has landed before the CTA exits
+    if (q4 == 0 && lane == 0) bulk_wait0();  // every output store has landed before the CTA exits
   }
 
   tc_fence_before();
