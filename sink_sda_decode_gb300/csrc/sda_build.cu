@@ -19,7 +19,10 @@ namespace {
 
 constexpr int kScanThreads = 1024;
 
-constexpr int kTokThreads = 512;  // one CTA per token in the length and scatter passes
+// One CTA per token in the length and scatter passes; 1024 threads and loops
+// unrolled 8 deep keep a long list (e.g. 64 K compressed entries) to a few
+// dependent memory round trips.
+constexpr int kTokThreads = 1024;
 
 // One CTA per token: check every field, write the length to kv_indptr[t + 1]
 // (rewritten in place by the scan), or -(status bits) if the token is bad.
@@ -44,7 +47,7 @@ build_len_kernel(const int32_t* __restrict__ state_slot, const int32_t* __restri
       if (c0 < 0 || c1 < c0 || (int64_t)c1 > comp_total) {
         bad |= 4;
       } else {
-#pragma unroll 4
+#pragma unroll 8
         for (int32_t e = c0 + threadIdx.x; e < c1; e += kTokThreads) {
           const int32_t b = comp_block[e], s = comp_slot[e];
           if (b < 0 || s < 0 || s >= k_per_block) bad |= 8;
@@ -146,7 +149,7 @@ build_scatter_kernel(const int32_t* __restrict__ state_slot, const int32_t* __re
       kv_indices[o0 + j] = (int32_t)((int64_t)ss * win + ring);
     }
     const int32_t c0 = comp_indptr[t], c1 = comp_indptr[t + 1];
-#pragma unroll 4
+#pragma unroll 8
     for (int32_t e = c0 + threadIdx.x; e < c1; e += kTokThreads)
       kv_indices[o0 + n_swa + (e - c0)] =
           (int32_t)(swa_pages + (int64_t)comp_block[e] * k_per_block + comp_slot[e]);
