@@ -1,0 +1,59 @@
+"""Host-side arithmetic of bench.py (CPU only): the algorithmic bytes and
+FLOPs the roofline fraction divides by, and the clock sampler's restriction
+to the timed region."""
+import time
+
+import numpy as np
+import pytest
+
+import bench
+from sink_sda_decode_gb300 import inputs
+
+
+class _W:
+    """Just the fields the formulas read."""
+
+    def __init__(self, N, H, D, total_len):
+        self.N, self.H, self.D, self.total_len = N, H, D, total_len
+
+
+def test_algorithmic_bytes_and_flops_match_the_published_config_figures():
+    # N=64, H=16, D=512, 640 slots per token: 44.20 MB and 1.342 GFLOP
+    w = _W(64, 16, 512, 64 * 640)
+    b = bench.algorithmic_bytes(w)
+    assert b == 40960 * 1024 + 2 * 64 * 16 * 512 * 2 + 40960 * 4 + 65 * 4
+    assert abs(b / 1e6 - 44.20) < 0.01
+    assert bench.algorithmic_flops(w) == 4 * 16 * 512 * 40960
+    assert abs(bench.algorithmic_flops(w) / 1e9 - 1.342) < 0.001
+    # N=1024, H=128, L=640: 942.15 MB and 171.8 GFLOP
+    w = _W(1024, 128, 512, 1024 * 640)
+    assert abs(bench.algorithmic_bytes(w) / 1e6 - 942.15) < 0.01
+    assert abs(bench.algorithmic_flops(w) / 1e9 - 171.8) < 0.05
+
+
+def test_bytes_follow_the_generated_workload():
+    w = inputs.config(0)  # the tiny case: lengths {0, 1, 17, 64}
+    assert int(w.total_len) == 82
+    assert bench.algorithmic_bytes(w) == 82 * w.D * 2 + 2 * w.N * w.H * w.D * 2 + 82 * 4 + (w.N + 1) * 4
+
+
+def test_clock_summary_keeps_only_samples_inside_the_timed_region():
+    cs = bench.ClockSampler(0)
+    cs.max_mhz, cs.source = 2070.0, "test"
+    t = time.perf_counter()
+    cs.samples = [(t - 1.0, 345.0, {"hw_slowdown"}),      # before: idle clock, must not count
+                  (t + 0.1, 2070.0, set()),
+                  (t + 0.2, 2040.0, {"sw_power_cap"}),
+                  (t + 5.0, 900.0, {"sw_thermal_slowdown"})]  # after
+    cs.mark(t, t + 1.0)
+    s = cs.summary()
+    assert s["samples"] == 2
+    assert s["sm_mhz"] == pytest.approx(2055.0)
+    assert s["reasons"] == ["sw_power_cap"]
+    assert s["sm_max_mhz"] == 2070.0
+
+
+def test_kernel_source_hash_is_stable_and_short():
+    h = bench.kernel_source_hash()
+    assert h == bench.kernel_source_hash() and len(h) == 16
+    int(h, 16)
