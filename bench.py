@@ -18,8 +18,10 @@ pool.  `--config` picks another of the five workloads.
   cpu_baseline  the fp64 CPU oracle on the host cores (bounded sample)
 
 --impl reference times the fp64 CPU oracle instead (same config and metric).
-Under torchrun (N>1 GPUs) every rank runs its own copy of the workload
-(tokens are independent: weak scaling, no collective on the data path).
+Under torchrun (N>1 GPUs) every rank decodes its own batch of the same
+recipe (seeded per rank; tokens are independent: weak scaling, no collective
+on the data path); rank 0 prints all ranks' tokens over the slowest rank's
+time.  The reference arm runs on rank 0 alone.
 """
 from __future__ import annotations
 
@@ -344,6 +346,62 @@ def gpu_arm(args, w, device, ws, rank):
                 h2d=h2d, d2h=d2h, step=step)
 
 
+# ----------------------------------------------------------------------------- job-wide report
+def reduce_over_ranks(times_ms, units, ws, device):
+    """Job-wide timings and units of a data-parallel run.
+
+    Each per-rank time becomes its MAX over ranks (the slowest rank bounds
+    the job); the units (decoded tokens) are SUMMED, since every rank decodes
+    its own batch.  Two all_reduce calls on the default process group, on
+    tensors placed on `device` (the GPU for NCCL, the CPU for gloo); a single
+    process returns its own numbers."""
+    t = torch.tensor([float(x) for x in times_ms], dtype=torch.float64, device=device)
+    u = torch.tensor([float(units)], dtype=torch.float64, device=device)
+    if ws > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.all_reduce(u, op=torch.distributed.ReduceOp.SUM)
+    return [float(x) for x in t.cpu()], float(u.cpu().item())
+
+
+def report_line(args, w, ws, ms_step, ms_kernel, ms_e2e, tokens_total, r):
+    """The JSON line of the GPU arm from job-wide numbers (rank 0 prints it).
+
+    `value` and `e2e.value` are all ranks' tokens over the slowest rank's step
+    time; the roofline is the attention kernel of this rank's workload, whose
+    shape every rank shares."""
+    hbm, bf16, peak_src = peaks()
+    nbytes = algorithmic_bytes(w)
+    flops = algorithmic_flops(w)
+    value = tokens_total / (ms_step * 1e-3)
+    achieved = nbytes / (ms_kernel * 1e-3) / 1e9
+    t_hbm = nbytes / (hbm * 1e9)
+    t_tc = flops / (bf16 * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    return {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "N": w.N, "H": w.H, "D": w.D,
+                   "total_slots": int(w.total_len), "pool_slots": w.total_pages,
+                   "step": "index build + decode (plan, attention, combine) as one CUDA graph",
+                   "l2": "flushed before every timed step (256 MiB write)",
+                   "parallelism": f"dp{ws} (independent token batches)"},
+        "gathered_kv_gbs": int(w.total_len) * w.D * 2 / (ms_step * 1e-3) / 1e9,
+        "roofline": {"bound": bound, "achieved": achieved,
+                     "peak": hbm if bound == "hbm" else bf16,
+                     "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+                     "frac": achieved / (hbm if bound == "hbm" else bf16),
+                     "traffic": ncu_traffic(args.config), "peak_source": peak_src,
+                     "kernel": "sda decode attention kernel", "kernel_ms": ms_kernel,
+                     "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+                     "step_frac_of_roofline": max(t_hbm, t_tc) / (ms_step * 1e-3)},
+        "e2e": {"value": tokens_total / (ms_e2e * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": Step.launches_per_step * args.steps,
+        "clocks": r["clocks"],
+    }
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 def oracle_inputs(w, tokens):
     kv_bits, sub_idx, sub_ptr = w.kv_rows_for(tokens)
@@ -422,49 +480,16 @@ def main():
         torch.distributed.init_process_group("nccl")
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    w = inputs.config(cfg_idx, device=device)
+    w = inputs.config(cfg_idx, device=device, shard=rank)
     r = gpu_arm(args, w, device, ws, rank)
 
-    ms = torch.tensor([r["ms_per_step"], r["kernel_ms"], r["e2e_ms"]], device=device)
-    if ws > 1:
-        torch.distributed.all_reduce(ms, op=torch.distributed.ReduceOp.MAX)
-    ms_step, ms_kernel, ms_e2e = (float(x) for x in ms.cpu())
+    (ms_step, ms_kernel, ms_e2e), tokens_total = reduce_over_ranks(
+        [r["ms_per_step"], r["kernel_ms"], r["e2e_ms"]], w.N, ws, device)
     if rank != 0:
         torch.distributed.destroy_process_group()
         return
 
-    hbm, bf16, peak_src = peaks()
-    nbytes = algorithmic_bytes(w)
-    flops = algorithmic_flops(w)
-    tokens_total = w.N * ws
-    value = tokens_total / (ms_step * 1e-3)
-    achieved = nbytes / (ms_kernel * 1e-3) / 1e9
-    t_hbm = nbytes / (hbm * 1e9)
-    t_tc = flops / (bf16 * 1e12)
-    bound = "hbm" if t_hbm >= t_tc else "tensor"
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "N": w.N, "H": w.H, "D": w.D,
-                   "total_slots": int(w.total_len), "pool_slots": w.total_pages,
-                   "step": "index build + decode (plan, attention, combine) as one CUDA graph",
-                   "l2": "flushed before every timed step (256 MiB write)",
-                   "parallelism": f"dp{ws} (independent token batches)"},
-        "gathered_kv_gbs": int(w.total_len) * w.D * 2 / (ms_step * 1e-3) / 1e9,
-        "roofline": {"bound": bound, "achieved": achieved,
-                     "peak": hbm if bound == "hbm" else bf16,
-                     "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
-                     "frac": achieved / (hbm if bound == "hbm" else bf16),
-                     "traffic": ncu_traffic(args.config), "peak_source": peak_src,
-                     "kernel": "sda decode attention kernel", "kernel_ms": ms_kernel,
-                     "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
-                     "step_frac_of_roofline": max(t_hbm, t_tc) / (ms_step * 1e-3)},
-        "e2e": {"value": tokens_total / (ms_e2e * 1e-3), "unit": "tokens/s",
-                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
-        "gpu_launches": Step.launches_per_step * args.steps,
-        "clocks": r["clocks"],
-    }
+    line = report_line(args, w, ws, ms_step, ms_kernel, ms_e2e, tokens_total, r)
     if not args.no_cpu_baseline and ws == 1:
         tps, cores, toks, passes, el = time_oracle(w, args.cpu_seconds,
                                                    16 if w.total_len > 200000 else w.N)

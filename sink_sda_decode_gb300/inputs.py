@@ -265,9 +265,18 @@ GENERATORS = [tiny, h16, ragged_h64, h128, longtail_h64]
 CONFIG_NAMES = ["tiny", "h16", "ragged_h64", "h128", "longtail_h64"]
 
 
-def config(i: int, device="cpu") -> Workload:
-    """Workload i (0..4) with its fixed seed SEED_BASE + i."""
-    return GENERATORS[i](device=device, seed=SEED_BASE + i)
+SHARD_SEED_STRIDE = 1000
+
+
+def config(i: int, device="cpu", shard: int = 0) -> Workload:
+    """Workload i (0..4) with its fixed seed SEED_BASE + i.
+
+    `shard` > 0 draws another batch of the same recipe (seed offset by
+    SHARD_SEED_STRIDE per shard): under data parallelism each process decodes
+    its own independent token batch; shard 0 is the workload itself."""
+    if shard < 0:
+        raise ValueError("shard must be >= 0")
+    return GENERATORS[i](device=device, seed=SEED_BASE + i + SHARD_SEED_STRIDE * shard)
 
 
 def random_small(seed: int, N: int, H: int, D: int, P: int, lengths, sink_sigma=1.0,
