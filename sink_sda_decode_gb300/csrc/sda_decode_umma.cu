@@ -68,6 +68,7 @@ constexpr int kPvWarp = 17;                // warp 17: PV issuer
 // each with 16 K registers, so 18 or 20 warps (5 on some) allow 96 registers
 constexpr int kThreads = 640;
 constexpr int kRowsPerLoader = kTileSlots / kLoaderWarps;  // 8 rows of a tile per loader warp
+constexpr int kPrefetchTiles = 2;          // L2 prefetch distance of the loaders, in tiles
 constexpr int kSoftmaxThreads = kSmWarps * 32;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
@@ -299,24 +300,36 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
     // thread keeps 16 x 16 B in flight and an SM 64 KB; the loads of a tile
     // are issued before the warp waits for the tile's shared-memory stage,
     // then stored into the 128-byte-swizzled K-major layout the MMAs read.
+    // The rows of the tile kPrefetchTiles ahead are brought into L2 with one
+    // bulk prefetch per row, so that their loads wait on L2, not on DRAM.
     const int lw = warp - kLoaderWarp0;
     const uint4* kv4 = reinterpret_cast<const uint4*>(p.kv);
-    TileCursor cur;
-    cur.init(p.units, n_units);
-    int my_slot = -1;  // lanes 0..7: slot of row 8w + lane of the current tile
-    auto fetch_slots = [&]() {
-      const int n = min(kTileN, cur.len() - cur.i * kTileN);
+    TileCursor c;  // the next tile whose slots are read
+    c.init(p.units, n_units);
+    auto tile_slot = [&]() {  // lanes 0..7: slot of row 8w + lane of tile c, else -1
+      const int n = min(kTileN, c.len() - c.i * kTileN);
       const int r = lw * kRowsPerLoader + lane;
-      my_slot = (lane < kRowsPerLoader && r < n) ? __ldg(p.kv_indices + cur.u.y + cur.i * kTileN + r) : -1;
+      return (lane < kRowsPerLoader && r < n) ? __ldg(p.kv_indices + c.u.y + c.i * kTileN + r) : -1;
     };
-    if (cur.valid) fetch_slots();
+    auto prefetch_rows = [&](int slot_of_lane) {
+      if (slot_of_lane >= 0) bulk_prefetch_l2(kv4 + (size_t)slot_of_lane * (kD / 8), kD * 2);
+    };
+    constexpr int PF = kPrefetchTiles;
+    int sl[PF];    // slots of tiles g .. g + PF - 1
+    bool hv[PF];   // whether those tiles exist
+#pragma unroll
+    for (int j = 0; j < PF; ++j) {
+      hv[j] = c.valid;
+      sl[j] = c.valid ? tile_slot() : -1;
+      if (c.valid) c.next();
+    }
     bool ok = true;
-    while (cur.valid && ok) {
-      const int g = cur.g, s = g % KS;  // KV stage
+    for (int g = 0; hv[0] && ok; ++g) {
+      const int s = g % KS;  // KV stage
       uint4 v[2 * kRowsPerLoader];
 #pragma unroll
       for (int r = 0; r < kRowsPerLoader; ++r) {
-        const int slot = __shfl_sync(0xffffffffu, my_slot, r);
+        const int slot = __shfl_sync(0xffffffffu, sl[0], r);
         if (slot >= 0) {
           const uint4* src = kv4 + (size_t)slot * (kD / 8);
           v[2 * r] = __ldcg(src + lane);
@@ -326,8 +339,13 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
           v[2 * r + 1] = make_uint4(0, 0, 0, 0);
         }
       }
-      cur.next();
-      if (cur.valid) fetch_slots();  // next tile's slots, while this tile's rows are in flight
+      if (g == 0) {
+#pragma unroll
+        for (int j = 1; j < PF; ++j) prefetch_rows(sl[j]);
+      }
+      const bool hpf = c.valid;  // tile g + PF
+      const int spf = hpf ? tile_slot() : -1;
+      if (hpf) c.next();
       // store the tile in two halves of D (each row's loads v[2r] and
       // v[2r + 1]), each as soon as the PV MMAs that read that half of the
       // tile last in this stage are done
@@ -351,6 +369,14 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kv_full(s, hh)));
       }
+      prefetch_rows(spf);
+#pragma unroll
+      for (int j = 0; j + 1 < PF; ++j) {
+        sl[j] = sl[j + 1];
+        hv[j] = hv[j + 1];
+      }
+      sl[PF - 1] = spf;
+      hv[PF - 1] = hpf;
     }
   } else if (warp == kMmaWarp || warp == kPvWarp) {
     // ===================================================== MMA issuers
