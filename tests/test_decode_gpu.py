@@ -141,6 +141,25 @@ def test_split_long_lists(monkeypatch, variant):
     parity.assert_parity(parity.compare(out, ref), f"split {variant}")
 
 
+def test_split_merge_repeats_on_one_workspace(monkeypatch):
+    """Split tokens over two head groups with +-inf and finite sinks, three
+    calls on one workspace: identical outputs, each within the oracle bound."""
+    w = inputs.random_small(seed=17, N=4, H=128, D=512, P=1 << 16, lengths=[9000, 3, 0, 4000],
+                            sink_sigma=1.5, device="cuda")
+    sink = w.attn_sink.clone()
+    sink[0], sink[70], sink[127] = -math.inf, math.inf, 30.0
+    idx, ptr = parity.to_dev(w)
+    total = int(w.kv_indptr[-1])
+    ws = torch.empty(sda.workspace_size(w.N, w.H, w.D, total), dtype=torch.uint8, device="cuda")
+    ref = parity.run_oracle(w, sink=sink)
+    outs = [sda.decode(w.q, w.unified_kv, idx, ptr, sink, w.softmax_scale, workspace=ws)
+            for _ in range(3)]
+    for k, out in enumerate(outs):
+        parity.assert_parity(parity.compare(out, ref), f"split merge call {k}")
+        assert torch.equal(out, outs[0])
+    assert sda.decode_error_flag(ws) == 0
+
+
 def test_variants_agree(monkeypatch):
     """CUDA-core, one-CTA and two-CTA tensor-core kernels on the same input."""
     w = inputs.random_small(seed=8, N=5, H=64, D=512, P=50000, lengths=[1, 64, 700, 0, 129],
