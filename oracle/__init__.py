@@ -9,6 +9,10 @@ The arithmetic lives in ``sda_oracle.c`` (plain C, double precision, one
 OpenMP loop over (token, head)); this module only compiles it with gcc on
 first use and marshals NumPy arrays through ctypes.
 
+``sda_decode_fp8`` is the same attention over a pool stored as FP8 E4M3
+codes with one fp32 scale per row (a format the pages do not fix; it serves
+the FP8-pool variant of the path).
+
 What it computes follows the docstring of ``paged_decode.py`` quoted on the
 sglang PR 28392 summary page ("为 AMD V4 内核添加 ATOM 来源注释", section
 "关键源码片段": caller convention, returns, numerics):
@@ -38,6 +42,7 @@ _ERRORS = {1: "bad shape", 2: "bad kv_indptr", 3: "slot out of range", 4: "out o
 
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _u16p = ctypes.POINTER(ctypes.c_uint16)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
 _f32p = ctypes.POINTER(ctypes.c_float)
 _f64p = ctypes.POINTER(ctypes.c_double)
 
@@ -58,6 +63,12 @@ def _bind(lib):
     lib.oracle_sda_decode.argtypes = [
         _u16p, _u16p, ctypes.c_int64, _i32p, ctypes.c_int64, _i32p, _f32p, ctypes.c_float,
         ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int, _f64p]
+    lib.oracle_sda_decode_fp8.restype = ctypes.c_int
+    lib.oracle_sda_decode_fp8.argtypes = [
+        _u16p, _u8p, _f32p, ctypes.c_int64, _i32p, ctypes.c_int64, _i32p, _f32p, ctypes.c_float,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int, _f64p]
+    lib.oracle_e4m3_to_double.restype = ctypes.c_double
+    lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
     lib.oracle_build_indices.restype = ctypes.c_int
     lib.oracle_build_indices.argtypes = [
         _i32p, _i32p, _i32p, _i32p, _i32p, _i32p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
@@ -135,6 +146,59 @@ def sda_decode(q_bits, kv_bits, kv_indices, kv_indptr, attn_sink, softmax_scale,
                                _ptr(out, ctypes.c_double))
     if rc != 0:
         raise ValueError(f"oracle_sda_decode: {_ERRORS.get(rc, rc)}")
+    return out
+
+
+def e4m3_values(lib=None) -> np.ndarray:
+    """The 256 FP8 E4M3 codes decoded to float64 by the oracle (index = code)."""
+    lib = lib or load()
+    return np.array([lib.oracle_e4m3_to_double(c) for c in range(256)], dtype=np.float64)
+
+
+def fp8_codes(x) -> np.ndarray:
+    """View an FP8 array (uint8 codes or a torch float8_e4m3fn / uint8 tensor) as uint8."""
+    if hasattr(x, "detach"):  # torch tensor
+        import torch
+
+        x = x.detach().cpu().contiguous().view(torch.uint8).numpy()
+    return _as(np.asarray(x).view(np.uint8), np.uint8)
+
+
+def sda_decode_fp8(q_bits, kv_codes, kv_scale, kv_indices, kv_indptr, attn_sink, softmax_scale,
+                   tokens=None, lib=None) -> np.ndarray:
+    """fp64 sparse sink decode attention over an FP8 pool.
+
+    Row s, element d of the pool is e4m3(kv_codes[s, d]) * kv_scale[s];
+    otherwise as sda_decode.  q_bits [N,H,D] bf16 bits, kv_codes [P,D] uint8
+    E4M3 codes, kv_scale [P] fp32.
+    """
+    lib = lib or load()
+    q = _as(q_bits, np.uint16)
+    kv = _as(kv_codes, np.uint8)
+    sc = _as(kv_scale, np.float32)
+    N, H, D = q.shape
+    assert kv.ndim == 2 and kv.shape[1] == D and sc.shape == (kv.shape[0],)
+    idx = _as(kv_indices, np.int32)
+    ptr = _as(kv_indptr, np.int32)
+    sink = _as(attn_sink, np.float32)
+    assert ptr.shape == (N + 1,) and sink.shape == (H,)
+    if tokens is None:
+        tok = None
+        n_tok = N
+    else:
+        tok = _as(tokens, np.int32)
+        n_tok = int(tok.size)
+    out = np.zeros((n_tok, H, D), dtype=np.float64)
+    idx_arg = idx if idx.size else np.zeros(1, np.int32)
+    rc = lib.oracle_sda_decode_fp8(_ptr(q, ctypes.c_uint16), _ptr(kv, ctypes.c_uint8),
+                                   _ptr(sc, ctypes.c_float), kv.shape[0],
+                                   _ptr(idx_arg, ctypes.c_int32), idx.size,
+                                   _ptr(ptr, ctypes.c_int32), _ptr(sink, ctypes.c_float),
+                                   float(np.float32(softmax_scale)), N, H, D,
+                                   None if tok is None else _ptr(tok, ctypes.c_int32), n_tok,
+                                   _ptr(out, ctypes.c_double))
+    if rc != 0:
+        raise ValueError(f"oracle_sda_decode_fp8: {_ERRORS.get(rc, rc)}")
     return out
 
 

@@ -49,6 +49,23 @@ static double bf16_bits_to_double(uint16_t b) {
   return (double)f;
 }
 
+/*
+ * FP8 E4M3 code -> double, exactly, from the format's definition (sign bit,
+ * 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0 encodes
+ * subnormals m/8 * 2^-6; no infinities; S.1111.111 is NaN; largest finite
+ * magnitude 1.75 * 2^8 = 448).  The pool format that stores one code per
+ * element and one fp32 dequantisation scale per row is not on the pages (see
+ * the header of oracle_sda_decode_fp8).
+ */
+double oracle_e4m3_to_double(uint8_t c) {
+  const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) v = ldexp((double)m / 8.0, -6);
+  else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();
@@ -84,10 +101,22 @@ int oracle_num_threads(void) {
  *   out = sum_j e^(x_j - M) * kv[S_j, :] / Z
  * The whole input is validated first; nothing out of range is ever read.
  */
-int oracle_sda_decode(const uint16_t* q, const uint16_t* unified_kv, int64_t total_pages,
-                      const int32_t* kv_indices, int64_t total_indices,
-                      const int32_t* kv_indptr, const float* attn_sink, float softmax_scale,
-                      int N, int H, int D, const int32_t* tokens, int n_tokens, double* out) {
+/* Row value of the pool: bf16 bits, or an E4M3 code times the row's scale. */
+typedef struct {
+  const uint16_t* bf16;  /* [total_pages, D] bf16 bits, or NULL */
+  const uint8_t* fp8;    /* [total_pages, D] E4M3 codes, or NULL */
+  const float* scale;    /* [total_pages] fp32 dequantisation scale (fp8 only) */
+} Pool;
+
+static double pool_value(const Pool* p, int64_t s, int d, int D) {
+  if (p->bf16) return bf16_bits_to_double(p->bf16[(size_t)s * D + d]);
+  return oracle_e4m3_to_double(p->fp8[(size_t)s * D + d]) * (double)p->scale[s];
+}
+
+static int decode_core(const uint16_t* q, const Pool* pool, int64_t total_pages,
+                       const int32_t* kv_indices, int64_t total_indices,
+                       const int32_t* kv_indptr, const float* attn_sink, float softmax_scale,
+                       int N, int H, int D, const int32_t* tokens, int n_tokens, double* out) {
   if (N < 0 || H <= 0 || D <= 0 || total_pages <= 0 || total_indices < 0 || n_tokens < 0)
     return ORACLE_BAD_SHAPE;
   if (tokens == NULL && n_tokens != N) return ORACLE_BAD_SHAPE;
@@ -124,9 +153,9 @@ int oracle_sda_decode(const uint16_t* q, const uint16_t* unified_kv, int64_t tot
       /* logits */
       double M = sink;
       for (int32_t j = 0; j < len; ++j) {
-        const uint16_t* row = unified_kv + (size_t)kv_indices[begin + j] * D;
+        const int64_t s = kv_indices[begin + j];
         double dot = 0.0;
-        for (int d = 0; d < D; ++d) dot += bf16_bits_to_double(qh[d]) * bf16_bits_to_double(row[d]);
+        for (int d = 0; d < D; ++d) dot += bf16_bits_to_double(qh[d]) * pool_value(pool, s, d, D);
         x[j] = scale * dot;
         if (x[j] > M) M = x[j];
       }
@@ -140,13 +169,38 @@ int oracle_sda_decode(const uint16_t* q, const uint16_t* unified_kv, int64_t tot
       /* numerator: probability-weighted sum of the value rows (the same rows) */
       for (int32_t j = 0; j < len; ++j) {
         const double w = exp(x[j] - M) / Z;
-        const uint16_t* row = unified_kv + (size_t)kv_indices[begin + j] * D;
-        for (int d = 0; d < D; ++d) o[d] += w * bf16_bits_to_double(row[d]);
+        const int64_t s = kv_indices[begin + j];
+        for (int d = 0; d < D; ++d) o[d] += w * pool_value(pool, s, d, D);
       }
       free(x);
     }
   }
   return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
+}
+
+int oracle_sda_decode(const uint16_t* q, const uint16_t* unified_kv, int64_t total_pages,
+                      const int32_t* kv_indices, int64_t total_indices,
+                      const int32_t* kv_indptr, const float* attn_sink, float softmax_scale,
+                      int N, int H, int D, const int32_t* tokens, int n_tokens, double* out) {
+  const Pool pool = {unified_kv, NULL, NULL};
+  return decode_core(q, &pool, total_pages, kv_indices, total_indices, kv_indptr, attn_sink,
+                     softmax_scale, N, H, D, tokens, n_tokens, out);
+}
+
+/*
+ * The same attention over a pool stored in FP8: row s, element d has the value
+ * e4m3(kv_fp8[s, d]) * kv_scale[s] (exact in double).  Everything else --
+ * logits, sink, softmax, weighted sum -- is oracle_sda_decode's definition.
+ * The pages keep unified_kv in bf16; this format (one E4M3 code per element,
+ * one fp32 scale per row) is a reading, for the FP8-pool variant of the path.
+ */
+int oracle_sda_decode_fp8(const uint16_t* q, const uint8_t* kv_fp8, const float* kv_scale,
+                          int64_t total_pages, const int32_t* kv_indices, int64_t total_indices,
+                          const int32_t* kv_indptr, const float* attn_sink, float softmax_scale,
+                          int N, int H, int D, const int32_t* tokens, int n_tokens, double* out) {
+  const Pool pool = {NULL, kv_fp8, kv_scale};
+  return decode_core(q, &pool, total_pages, kv_indices, total_indices, kv_indptr, attn_sink,
+                     softmax_scale, N, H, D, tokens, n_tokens, out);
 }
 
 /*

@@ -276,12 +276,64 @@ def pin_validate(lib):
     assert oracle.validate_indices([2, 3], [0, 2], 3, lib=lib) == (4, 1)  # slot == total_pages
 
 
+# ----------------------------------------------------------------------------- FP8 pool
+def pin_e4m3_table(lib):
+    """All 256 E4M3 codes decode as torch's float8_e4m3fn conversion does (a
+    library routine of the same format): the finite values exactly, NaN at
+    S.1111.111."""
+    got = oracle.e4m3_values(lib)
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+
+
+def fp8_case(rng, N, H, D, P, lens):
+    """Random finite E4M3 codes, power-of-two row scales, and the bf16 bits of
+    the exactly dequantised pool (computed with torch, not with the oracle)."""
+    codes = rng.integers(0, 256, (P, D)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3C  # no NaN codes
+    scale = np.ldexp(1.0, rng.integers(-6, 4, P)).astype(np.float32)
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float32) * torch.from_numpy(scale)[:, None]
+    kv_bits = vals.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert torch.equal(vals.to(torch.bfloat16).to(torch.float32), vals)  # exact in bf16
+    q, _, idx, ptr, sink = random_case(rng, N, H, D, P, lens)
+    return q, codes, scale, kv_bits, idx, ptr, sink
+
+
+def pin_fp8_equals_bf16_pool(lib):
+    """On a pool whose dequantised values are exact in bf16, the FP8 entry
+    point equals the bf16 one (whose own pins tie it to the definition)."""
+    rng = np.random.default_rng(41)
+    q, codes, scale, kv_bits, idx, ptr, sink = fp8_case(rng, 4, 3, 16, 40, [0, 1, 7, 20])
+    a = oracle.sda_decode_fp8(q, codes, scale, idx, ptr, sink, 0.25, lib=lib)
+    b = oracle.sda_decode(q, kv_bits, idx, ptr, sink, 0.25, lib=lib)
+    assert np.max(np.abs(a - b)) <= 1e-12 * max(1.0, np.max(np.abs(b)))
+
+
+def pin_fp8_zero_scale_row(lib):
+    """A row with scale 0 is an all-zero key and value: its logit is 0, it
+    adds e^0 to the denominator and nothing to the output (closed form with
+    one ordinary slot beside it)."""
+    D = 8
+    codes = np.full((2, D), 0x38, np.uint8)  # e4m3 1.0 everywhere
+    scale = np.array([0.5, 0.0], np.float32)
+    q = bf16_bits(np.full((1, 1, D), 0.25))
+    out = oracle.sda_decode_fp8(q, codes, scale, [0, 1], [0, 2], [0.375], 1.0, lib=lib)
+    x = 0.25 * 0.5 * D
+    want = math.exp(x) * 0.5 / (math.exp(0.375) + math.exp(x) + 1.0)
+    assert np.allclose(out[0, 0], want, rtol=0, atol=1e-14)
+
+
+FP8_PINS = [pin_e4m3_table, pin_fp8_equals_bf16_pool, pin_fp8_zero_scale_row]
+
 DECODE_PINS = [pin_sdpa, pin_sink_minus_inf_is_softmax, pin_single_slot, pin_duplicate_adds_ln2,
                pin_zero_length, pin_permutation, pin_sink_factor, pin_scale_zero, pin_convexity,
                pin_hard_attention_limit, pin_sink_plus_inf, pin_token_subset]
 BUILDER_PINS = [pin_builder_golden, pin_builder_ring_closed_form, pin_builder_capacity]
 VALIDATE_PINS = [pin_validate]
-ALL_PINS = DECODE_PINS + BUILDER_PINS + VALIDATE_PINS
+ALL_PINS = DECODE_PINS + BUILDER_PINS + VALIDATE_PINS + FP8_PINS
 
 
 def failing_pins(lib, pins=ALL_PINS):

@@ -24,8 +24,8 @@ MUTANTS = {
     "missing_scale": ("x[j] = scale * dot;", "x[j] = dot;", pins.DECODE_PINS),
     "wrong_exp_sign": ("const double w = exp(x[j] - M) / Z;", "const double w = exp(M - x[j]) / Z;",
                        pins.DECODE_PINS),
-    "reversed_value_row": ("o[d] += w * bf16_bits_to_double(row[d]);",
-                           "o[d] += w * bf16_bits_to_double(row[D - 1 - d]);", pins.DECODE_PINS),
+    "reversed_value_row": ("o[d] += w * pool_value(pool, s, d, D);",
+                           "o[d] += w * pool_value(pool, s, D - 1 - d, D);", pins.DECODE_PINS),
     "wrong_head_of_q": ("const uint16_t* qh = q + ((size_t)t * H + h) * D;",
                         "const uint16_t* qh = q + ((size_t)t * H + (H - 1 - h)) * D;",
                         pins.DECODE_PINS),
@@ -33,6 +33,18 @@ MUTANTS = {
                          "const int32_t len = kv_indptr[t + 1] - begin - (kv_indptr[t + 1] > begin + 1);",
                          pins.DECODE_PINS),
     "max_ignores_logits": ("if (x[j] > M) M = x[j];", "(void)0;", pins.DECODE_PINS),
+    # FP8 pool
+    "e4m3_bias_8": ("else v = ldexp(1.0 + (double)m / 8.0, e - 7);",
+                    "else v = ldexp(1.0 + (double)m / 8.0, e - 8);", pins.FP8_PINS),
+    "e4m3_subnormal_scale": ("if (e == 0) v = ldexp((double)m / 8.0, -6);",
+                             "if (e == 0) v = ldexp((double)m / 8.0, -7);", pins.FP8_PINS),
+    "e4m3_mantissa_quarters": ("else v = ldexp(1.0 + (double)m / 8.0, e - 7);",
+                               "else v = ldexp(1.0 + (double)m / 4.0, e - 7);", pins.FP8_PINS),
+    "fp8_scale_ignored": ("return oracle_e4m3_to_double(p->fp8[(size_t)s * D + d]) * (double)p->scale[s];",
+                          "return oracle_e4m3_to_double(p->fp8[(size_t)s * D + d]);", pins.FP8_PINS),
+    "fp8_scale_of_wrong_row": ("return oracle_e4m3_to_double(p->fp8[(size_t)s * D + d]) * (double)p->scale[s];",
+                               "return oracle_e4m3_to_double(p->fp8[(size_t)s * D + d]) * (double)p->scale[0];",
+                               pins.FP8_PINS),
     # builder
     "ring_newest_first": ("(int64_t)swa_head[t] - n_swa + 1 + j", "(int64_t)swa_head[t] - j",
                           pins.BUILDER_PINS),
