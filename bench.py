@@ -223,11 +223,13 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm), "source": self.source}
 
 
-def algorithmic_bytes(w):
+def algorithmic_bytes(w, kv="bf16"):
     """Bytes the method must move per decode: gathered KV rows + q + out +
-    kv_indices + kv_indptr."""
+    kv_indices + kv_indptr.  An FP8 pool row is D one-byte codes plus its
+    4-byte scale."""
     L = int(w.total_len)
-    return L * w.D * 2 + 2 * w.N * w.H * w.D * 2 + L * 4 + (w.N + 1) * 4
+    row = w.D * 2 if kv == "bf16" else w.D + 4
+    return L * row + 2 * w.N * w.H * w.D * 2 + L * 4 + (w.N + 1) * 4
 
 
 def algorithmic_flops(w):
@@ -238,10 +240,11 @@ def algorithmic_flops(w):
 class Step:
     """Device-resident inputs and buffers of one hot-path step."""
 
-    def __init__(self, w, device):
+    def __init__(self, w, device, pool=None):
         import sink_sda_decode_gb300 as sda
         self.sda = sda
         self.w = w
+        self.pool = pool  # an FP8 pool (inputs.Fp8Pool) replaces the bf16 one
         self.dev = device
         self.bi = w.builder_inputs(device)
         self.capacity = w.N * w.win + int(w.comp_block.size)
@@ -249,8 +252,9 @@ class Step:
         self.kv_indptr = torch.empty(w.N + 1, dtype=torch.int32, device=device)
         self.status = torch.empty(1, dtype=torch.int32, device=device)
         self.out = torch.empty_like(w.q)
-        self.ws = torch.empty(sda.workspace_size(w.N, w.H, w.D, self.capacity), dtype=torch.uint8,
-                              device=device)
+        size = (sda.workspace_size if pool is None else sda.workspace_size_fp8)(
+            w.N, w.H, w.D, self.capacity)
+        self.ws = torch.empty(size, dtype=torch.uint8, device=device)
 
     def run(self, q=None, bi=None, out=None, stream=None):
         w = self.w
@@ -259,16 +263,22 @@ class Step:
                                total_pages=w.total_pages, capacity=self.capacity,
                                kv_indices=self.kv_indices, kv_indptr=self.kv_indptr,
                                status=self.status, stream=stream)
-        self.sda.decode(q if q is not None else w.q, w.unified_kv, self.kv_indices, self.kv_indptr,
-                        w.attn_sink, w.softmax_scale, out=self.out if out is None else out,
-                        workspace=self.ws, stream=stream)
+        if self.pool is None:
+            self.sda.decode(q if q is not None else w.q, w.unified_kv, self.kv_indices,
+                            self.kv_indptr, w.attn_sink, w.softmax_scale,
+                            out=self.out if out is None else out, workspace=self.ws, stream=stream)
+        else:
+            self.sda.decode_fp8(q if q is not None else w.q, self.pool.codes, self.pool.scale,
+                                self.kv_indices, self.kv_indptr, w.attn_sink, w.softmax_scale,
+                                out=self.out if out is None else out, workspace=self.ws,
+                                stream=stream)
 
     # kernels of this library launched per step: 3 (index build) + plan + attention + combine
     launches_per_step = 6
 
 
-def gpu_arm(args, w, device, ws, rank):
-    step = Step(w, device)
+def gpu_arm(args, w, device, ws, rank, pool=None):
+    step = Step(w, device, pool)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     s = torch.cuda.Stream(device)
     s.wait_stream(torch.cuda.current_stream(device))
@@ -370,28 +380,34 @@ def report_line(args, w, ws, ms_step, ms_kernel, ms_e2e, tokens_total, r):
     time; the roofline is the attention kernel of this rank's workload, whose
     shape every rank shares."""
     hbm, bf16, peak_src = peaks()
-    nbytes = algorithmic_bytes(w)
+    kv = getattr(args, "kv", "bf16")
+    nbytes = algorithmic_bytes(w, kv)
     flops = algorithmic_flops(w)
     value = tokens_total / (ms_step * 1e-3)
-    achieved = nbytes / (ms_kernel * 1e-3) / 1e9
     t_hbm = nbytes / (hbm * 1e9)
     t_tc = flops / (bf16 * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
+    # achieved rate of the binding resource: GB/s of algorithmic bytes, or
+    # TFLOP/s of algorithmic FLOPs
+    achieved = (nbytes / 1e9 if bound == "hbm" else flops / 1e12) / (ms_kernel * 1e-3)
     return {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "N": w.N, "H": w.H, "D": w.D,
                    "total_slots": int(w.total_len), "pool_slots": w.total_pages,
+                   "kv": "bf16" if kv == "bf16" else "fp8 e4m3, fp32 scale per row",
                    "step": "index build + decode (plan, attention, combine) as one CUDA graph",
                    "l2": "flushed before every timed step (256 MiB write)",
                    "parallelism": f"dp{ws} (independent token batches)"},
-        "gathered_kv_gbs": int(w.total_len) * w.D * 2 / (ms_step * 1e-3) / 1e9,
+        "gathered_kv_gbs": int(w.total_len) * (w.D * 2 if kv == "bf16" else w.D + 4)
+                           / (ms_step * 1e-3) / 1e9,
         "roofline": {"bound": bound, "achieved": achieved,
                      "peak": hbm if bound == "hbm" else bf16,
                      "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
                      "frac": achieved / (hbm if bound == "hbm" else bf16),
-                     "traffic": ncu_traffic(args.config), "peak_source": peak_src,
+                     "traffic": ncu_traffic(args.config if kv == "bf16" else args.config + "_fp8"),
+                     "peak_source": peak_src,
                      "kernel": "sda decode attention kernel", "kernel_ms": ms_kernel,
                      "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
                      "step_frac_of_roofline": max(t_hbm, t_tc) / (ms_step * 1e-3)},
@@ -403,10 +419,20 @@ def report_line(args, w, ws, ms_step, ms_kernel, ms_e2e, tokens_total, r):
 
 
 # ----------------------------------------------------------------------------- CPU oracle
-def oracle_inputs(w, tokens):
-    kv_bits, sub_idx, sub_ptr = w.kv_rows_for(tokens)
+def oracle_inputs(w, tokens, pool=None):
+    """Arguments of the oracle call for `tokens` (bf16 pool, or an FP8 pool)."""
     q_bits = w.q_bits()[np.asarray(tokens)]
-    return q_bits, kv_bits, sub_idx, sub_ptr, w.attn_sink.cpu().numpy()
+    if pool is None:
+        kv_bits, sub_idx, sub_ptr = w.kv_rows_for(tokens)
+        return q_bits, kv_bits, sub_idx, sub_ptr, w.attn_sink.cpu().numpy()
+    codes, scale, sub_idx, sub_ptr = inputs.fp8_rows_for(w, pool, tokens)
+    return q_bits, codes, scale, sub_idx, sub_ptr, w.attn_sink.cpu().numpy()
+
+
+def oracle_decode(oargs, w):
+    import oracle
+    fn = oracle.sda_decode if len(oargs) == 5 else oracle.sda_decode_fp8
+    return fn(*oargs, w.softmax_scale)
 
 
 def oracle_sample(w, budget_tokens):
@@ -416,14 +442,14 @@ def oracle_sample(w, budget_tokens):
     return np.sort(rng.choice(w.N, k, replace=False))
 
 
-def time_oracle(w, seconds, max_tokens):
+def time_oracle(w, seconds, max_tokens, pool=None):
     import oracle
     toks = oracle_sample(w, max_tokens)
-    args = oracle_inputs(w, toks)
+    args = oracle_inputs(w, toks, pool)
     done_tokens, t0 = 0, time.perf_counter()
     passes = 0
     while True:
-        oracle.sda_decode(*args, w.softmax_scale)
+        oracle_decode(args, w)
         done_tokens += len(toks)
         passes += 1
         el = time.perf_counter() - t0
@@ -441,6 +467,9 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--config", default=inputs.CONFIG_NAMES[DEFAULT_CONFIG],
                     choices=inputs.CONFIG_NAMES)
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                    help="pool format: bf16 rows, or FP8 E4M3 codes with one fp32 scale per row "
+                         "(the workload's pool quantised row by row)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -453,13 +482,14 @@ def main():
             return
         w = inputs.config(cfg_idx, device="cuda" if torch.cuda.is_available() else "cpu")
         import oracle
+        pool = inputs.fp8_pool(w) if args.kv == "fp8" else None
         toks = oracle_sample(w, 16 if w.total_len > 200000 else w.N)
-        oargs = oracle_inputs(w, toks)
+        oargs = oracle_inputs(w, toks, pool)
         for _ in range(args.warmup):
-            oracle.sda_decode(*oargs, w.softmax_scale)
+            oracle_decode(oargs, w)
         t0 = time.perf_counter()
         for _ in range(args.steps):
-            oracle.sda_decode(*oargs, w.softmax_scale)
+            oracle_decode(oargs, w)
         el = time.perf_counter() - t0
         tps = len(toks) * args.steps / el
         sample = f"{len(toks)} of {w.N} tokens per step"
@@ -468,7 +498,7 @@ def main():
                 "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": w.name, "N": w.N, "H": w.H, "D": w.D,
-                           "total_slots": w.total_len},
+                           "total_slots": w.total_len, "kv": args.kv},
                 "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": oracle.num_threads(),
                                  "kind": "oracle", "sample": sample},
                 "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -481,7 +511,8 @@ def main():
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     w = inputs.config(cfg_idx, device=device, shard=rank)
-    r = gpu_arm(args, w, device, ws, rank)
+    pool = inputs.fp8_pool(w) if args.kv == "fp8" else None
+    r = gpu_arm(args, w, device, ws, rank, pool)
 
     (ms_step, ms_kernel, ms_e2e), tokens_total = reduce_over_ranks(
         [r["ms_per_step"], r["kernel_ms"], r["e2e_ms"]], w.N, ws, device)
@@ -492,7 +523,7 @@ def main():
     line = report_line(args, w, ws, ms_step, ms_kernel, ms_e2e, tokens_total, r)
     if not args.no_cpu_baseline and ws == 1:
         tps, cores, toks, passes, el = time_oracle(w, args.cpu_seconds,
-                                                   16 if w.total_len > 200000 else w.N)
+                                                   16 if w.total_len > 200000 else w.N, pool)
         line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": f"{len(toks)} of {w.N} tokens x {passes} passes, "
                                           f"{el:.1f} s"}

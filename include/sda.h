@@ -96,6 +96,46 @@ sda_status sda_decode(const void* q, const void* unified_kv, int64_t total_pages
                       void* stream);
 
 /*
+ * Workspace bytes sda_decode_fp8 needs for these sizes (as
+ * sda_decode_workspace_size, for the FP8-pool kernel).  SDA_ERR_UNSUPPORTED
+ * for an (H, D) that sda_decode_fp8 rejects.
+ */
+sda_status sda_decode_fp8_workspace_size(int N, int H, int D, int64_t total_indices,
+                                         size_t* bytes);
+
+/*
+ * sda_decode over a pool stored in FP8: the same attention (paged_decode.py
+ * docstring: caller convention, returns, numerics) with row s, element d of
+ * the pool worth e4m3(kv_fp8[s, d]) * kv_scale[s].  The pages keep unified_kv
+ * in bf16 and quantise to FP8 only on the cache-store side (the fused
+ * RMSNorm + RoPE + FP8 quantisation + paged SWA store kernel of the sglang
+ * PR 25898 summary page, "关键文件"); this entry point is the pool format
+ * that halves the gathered bytes: one FP8 E4M3 code per element (sign, 4
+ * exponent bits with bias 7, 3 mantissa bits, no infinities, S.1111.111 =
+ * NaN) and one fp32 dequantisation scale per row.
+ *
+ *   kv_fp8       [total_pages, D] E4M3 codes (one byte each), contiguous,
+ *                16-byte aligned.
+ *   kv_scale     [total_pages] fp32, 4-byte aligned; any finite value
+ *                (0 makes the row an all-zero key and value).
+ *   other arguments, results, contract and errors as sda_decode; workspace
+ *   of at least sda_decode_fp8_workspace_size() bytes.
+ *
+ * Numerics: each gathered element is dequantised to bf16 (code * scale,
+ * rounded to nearest even) in shared memory, then the tensor-core path
+ * computes exactly as for a bf16 pool.  With power-of-two scales (as 8-bit
+ * exponent block scales are) that product is exact, so the result is as
+ * accurate as sda_decode's on the dequantised pool; any other scale rounds
+ * each element once more (relative 2^-9).  Supported: D = 512 with H in {16, 32,
+ * 64, 128, 192, 256}; other shapes return SDA_ERR_UNSUPPORTED.
+ */
+sda_status sda_decode_fp8(const void* q, const void* kv_fp8, const float* kv_scale,
+                          int64_t total_pages, const int32_t* kv_indices, int64_t total_indices,
+                          const int32_t* kv_indptr, const float* attn_sink, float softmax_scale,
+                          int N, int H, int D, void* out, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/*
  * sda_decode without a workspace argument, for callers that cannot allocate
  * device memory: hosts that give an operator only its input and output
  * buffers and forbid it to allocate (e.g. an inference engine that owns all

@@ -21,7 +21,7 @@ import torch
 from . import _lib
 
 __all__ = ["decode", "workspace_size", "build_indices", "validate_indices", "decode_error_flag",
-           "decode_kernel",
+           "decode_kernel", "decode_fp8", "workspace_size_fp8",
            "decode_host", "set_timing_events", "decode_noalloc", "library_path"]
 
 library_path = _lib.LIB_PATH
@@ -99,6 +99,64 @@ def decode(q: torch.Tensor, unified_kv: torch.Tensor, kv_indices: torch.Tensor,
                             float(softmax_scale), N, H, D, out.data_ptr(), workspace.data_ptr(),
                             workspace.numel(), _stream_ptr(stream))
     _lib.check(rc, "sda_decode")
+    return out
+
+
+def workspace_size_fp8(N: int, H: int, D: int, total_indices: int) -> int:
+    """Bytes of workspace decode_fp8() needs on the current CUDA device."""
+    lib = _lib.load()
+    n = ctypes.c_size_t(0)
+    _lib.check(lib.sda_decode_fp8_workspace_size(int(N), int(H), int(D), int(total_indices),
+                                                 ctypes.byref(n)), "sda_decode_fp8_workspace_size")
+    return int(n.value)
+
+
+def decode_fp8(q: torch.Tensor, kv_fp8: torch.Tensor, kv_scale: torch.Tensor,
+               kv_indices: torch.Tensor, kv_indptr: torch.Tensor, attn_sink: torch.Tensor,
+               softmax_scale: float, out: torch.Tensor | None = None,
+               workspace: torch.Tensor | None = None,
+               stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """decode() over a pool stored in FP8: row s of the pool is
+    e4m3(kv_fp8[s]) * kv_scale[s].
+
+    kv_fp8 [P, D] float8_e4m3fn (or uint8 holding E4M3 codes); kv_scale [P]
+    fp32; the other arguments and the result as decode().  D = 512 with
+    H in {16, 32} or a multiple of 64 up to 256.
+    """
+    lib = _lib.load()
+    _req(q, "q", torch.bfloat16, 3)
+    dev = q.device
+    if kv_fp8.dtype == torch.float8_e4m3fn:
+        kv_fp8 = kv_fp8.view(torch.uint8)
+    _req(kv_fp8, "kv_fp8", torch.uint8, 2, dev)
+    _req(kv_scale, "kv_scale", torch.float32, 1, dev)
+    _req(kv_indices, "kv_indices", torch.int32, 1, dev)
+    _req(kv_indptr, "kv_indptr", torch.int32, 1, dev)
+    _req(attn_sink, "attn_sink", torch.float32, 1, dev)
+    N, H, D = q.shape
+    if kv_fp8.shape[1] != D or kv_scale.numel() != kv_fp8.shape[0]:
+        raise ValueError("kv_fp8 rows must have q's head dim and kv_scale one entry per row")
+    if kv_indptr.numel() != N + 1 or attn_sink.numel() != H:
+        raise ValueError("kv_indptr must have N+1 entries and attn_sink H entries")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _req(out, "out", torch.bfloat16, 3, dev)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    with torch.cuda.device(dev):
+        need = workspace_size_fp8(N, H, D, kv_indices.numel())
+        if workspace is None:
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        else:
+            _req(workspace, "workspace", torch.uint8, 1, dev)
+        rc = lib.sda_decode_fp8(q.data_ptr(), kv_fp8.data_ptr(), kv_scale.data_ptr(),
+                                kv_fp8.shape[0],
+                                kv_indices.data_ptr() if kv_indices.numel() else None,
+                                kv_indices.numel(), kv_indptr.data_ptr(), attn_sink.data_ptr(),
+                                float(softmax_scale), N, H, D, out.data_ptr(), workspace.data_ptr(),
+                                workspace.numel(), _stream_ptr(stream))
+    _lib.check(rc, "sda_decode_fp8")
     return out
 
 

@@ -32,6 +32,10 @@ SIGNATURES = {
     "sda_decode_workspace_size": (_i32, [_i32, _i32, _i32, _i64, ctypes.POINTER(ctypes.c_size_t)]),
     "sda_decode": (_i32, [_vp, _vp, _i64, _vp, _i64, _vp, _vp, _f32, _i32, _i32, _i32, _vp, _vp,
                           ctypes.c_size_t, _vp]),
+    "sda_decode_fp8_workspace_size": (_i32, [_i32, _i32, _i32, _i64,
+                                             ctypes.POINTER(ctypes.c_size_t)]),
+    "sda_decode_fp8": (_i32, [_vp, _vp, _vp, _i64, _vp, _i64, _vp, _vp, _f32, _i32, _i32, _i32, _vp,
+                              _vp, ctypes.c_size_t, _vp]),
     "sda_decode_noalloc": (_i32, [_vp, _vp, _i64, _vp, _i64, _vp, _vp, _f32, _i32, _i32, _i32, _vp,
                                   _vp]),
     "sda_decode_error_flag": (_i32, [_vp, _vp, _vp]),

@@ -77,10 +77,14 @@ bool shape_supported(int H, int D) {
   return (D == 64 || D == 128 || D == 256 || D == 512) && H >= 1 && H <= 256;
 }
 
+bool tc_shape_supported(int H, int D) {
+  return D == 512 && (H == 16 || H == 32 || (H % 64 == 0 && H <= 256));
+}
+
 bool choose_plan(int H, int D, const DeviceCaps& caps, LaunchPlan* lp) {
   if (!shape_supported(H, D)) return false;
   lp->num_sms = caps.num_sms;
-  const bool tc_shape = D == 512 && (H == 16 || H == 32 || H % 64 == 0);
+  const bool tc_shape = tc_shape_supported(H, D);
   const int nh = H < 64 ? H : 64;
   const int pairs = tc_shape ? caps.pairs[nh == 16 ? 0 : nh == 32 ? 1 : 2] : 0;
   const int forced = forced_variant();
@@ -216,8 +220,8 @@ sda_status sda_decode(const void* q, const void* unified_kv, int64_t total_pages
       e = launch_decode_pair(q, unified_kv, kv_indices, attn_sink, softmax_scale, N, H, D, out,
                              workspace, L, lp, st);
     else if (lp.variant == kUmma)
-      e = launch_decode_umma(q, unified_kv, total_pages, kv_indices, attn_sink, softmax_scale, N, H,
-                             D, out, workspace, L, lp, st);
+      e = launch_decode_umma(q, unified_kv, nullptr, total_pages, kv_indices, attn_sink,
+                             softmax_scale, N, H, D, out, workspace, L, lp, st);
     else
       e = launch_decode_simt(q, unified_kv, kv_indices, attn_sink, softmax_scale, N, H, D, out,
                              workspace, L, lp, st);
@@ -226,6 +230,78 @@ sda_status sda_decode(const void* q, const void* unified_kv, int64_t total_pages
   if (e == cudaSuccess) e = launch_combine(attn_sink, N, H, D, out, workspace, L, caps.num_sms, st);
   if (e != cudaSuccess) {
     note_cuda_error(e, "sda_decode");
+    return SDA_ERR_CUDA;
+  }
+  return SDA_OK;
+}
+
+// The FP8-pool entry points run the one-CTA tensor-core kernel only.
+static bool fp8_plan(int H, int D, const DeviceCaps& caps, LaunchPlan* lp) {
+  if (!tc_shape_supported(H, D) || !choose_plan(H, D, caps, lp)) return false;
+  if (lp->variant != kUmma) {  // a forced variant does not apply to the FP8 pool
+    lp->variant = kUmma;
+    lp->nh = H < 64 ? H : 64;
+    lp->hg = H / lp->nh;
+    lp->grid = caps.num_sms;
+    lp->threads = 640;
+    lp->smem = umma_smem_bytes(lp->nh);
+    lp->tile = kTileSlots;
+    lp->min_chunk = kTileSlots;
+  }
+  return true;
+}
+
+sda_status sda_decode_fp8_workspace_size(int N, int H, int D, int64_t total_indices, size_t* bytes) {
+  if (!bytes || N < 0 || total_indices < 0) return SDA_ERR_INVALID_ARG;
+  if (!tc_shape_supported(H, D)) return SDA_ERR_UNSUPPORTED;
+  DeviceCaps caps;
+  cudaError_t e = device_caps(&caps);
+  if (e != cudaSuccess) {
+    note_cuda_error(e, "sda_decode_fp8_workspace_size");
+    return SDA_ERR_CUDA;
+  }
+  LaunchPlan lp;
+  if (!fp8_plan(H, D, caps, &lp)) return SDA_ERR_UNSUPPORTED;
+  *bytes = workspace_layout(N, H, D, total_indices, lp).total;
+  return SDA_OK;
+}
+
+sda_status sda_decode_fp8(const void* q, const void* kv_fp8, const float* kv_scale,
+                          int64_t total_pages, const int32_t* kv_indices, int64_t total_indices,
+                          const int32_t* kv_indptr, const float* attn_sink, float softmax_scale,
+                          int N, int H, int D, void* out, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  if (N < 0 || total_indices < 0 || total_indices > 0x7fffffffll) return SDA_ERR_INVALID_ARG;
+  if (total_pages <= 0 || total_pages > 0x7fffffffll) return SDA_ERR_INVALID_ARG;
+  if (!tc_shape_supported(H, D)) return SDA_ERR_UNSUPPORTED;
+  if (N == 0) return SDA_OK;
+  if (!q || !kv_fp8 || !kv_scale || !kv_indptr || !attn_sink || !out || !workspace)
+    return SDA_ERR_INVALID_ARG;
+  if (total_indices > 0 && !kv_indices) return SDA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv_fp8, 16) || !aligned(out, 16) || !aligned(kv_scale, 4) ||
+      !aligned(kv_indptr, 4) || !aligned(attn_sink, 4) || (kv_indices && !aligned(kv_indices, 4)))
+    return SDA_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return SDA_ERR_WORKSPACE;
+  DeviceCaps caps;
+  cudaError_t e = device_caps(&caps);
+  if (e != cudaSuccess) {
+    note_cuda_error(e, "sda_decode_fp8");
+    return SDA_ERR_CUDA;
+  }
+  LaunchPlan lp;
+  fp8_plan(H, D, caps, &lp);
+  const WsLayout L = workspace_layout(N, H, D, total_indices, lp);
+  if (workspace_bytes < L.total) return SDA_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  e = launch_plan(kv_indptr, N, total_indices, lp, workspace, L, st);
+  if (e == cudaSuccess && g_ev_before && g_ev_after) e = cudaEventRecord(g_ev_before, st);
+  if (e == cudaSuccess)
+    e = launch_decode_umma(q, kv_fp8, kv_scale, total_pages, kv_indices, attn_sink, softmax_scale,
+                           N, H, D, out, workspace, L, lp, st);
+  if (e == cudaSuccess && g_ev_before && g_ev_after) e = cudaEventRecord(g_ev_after, st);
+  if (e == cudaSuccess) e = launch_combine(attn_sink, N, H, D, out, workspace, L, caps.num_sms, st);
+  if (e != cudaSuccess) {
+    note_cuda_error(e, "sda_decode_fp8");
     return SDA_ERR_CUDA;
   }
   return SDA_OK;

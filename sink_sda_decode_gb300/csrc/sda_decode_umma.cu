@@ -69,6 +69,7 @@ constexpr int kPvWarp = 17;                // warp 17: PV issuer
 constexpr int kThreads = 640;
 constexpr int kRowsPerLoader = kTileSlots / kLoaderWarps;  // 8 rows of a tile per loader warp
 constexpr int kPrefetchTiles = 2;          // L2 prefetch distance of the loaders, in tiles
+static_assert(kPrefetchTiles >= 2, "the loaders read the next tile's slots one tile early");
 constexpr int kSoftmaxThreads = kSmWarps * 32;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
@@ -137,7 +138,8 @@ struct Cfg {
 
 struct Params {
   const __nv_bfloat16* q;
-  const __nv_bfloat16* kv;
+  const __nv_bfloat16* kv;  // bf16 pool, or (FP8 kernels) the E4M3 codes [P, D] as bytes
+  const float* kv_scale;    // FP8 kernels: per-row dequantisation scale [P]
   const int32_t* kv_indices;
   const float* attn_sink;
   __nv_bfloat16* out;
@@ -235,7 +237,7 @@ struct TileCursor {
   }
 };
 
-template <int NH>
+template <int NH, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_out, const Params p) {
@@ -312,7 +314,11 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
       return (lane < kRowsPerLoader && r < n) ? __ldg(p.kv_indices + c.u.y + c.i * kTileN + r) : -1;
     };
     auto prefetch_rows = [&](int slot_of_lane) {
-      if (slot_of_lane >= 0) bulk_prefetch_l2(kv4 + (size_t)slot_of_lane * (kD / 8), kD * 2);
+      constexpr uint32_t kRowBytes = FP8 ? kD : kD * 2;
+      if (slot_of_lane >= 0) {
+        bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(p.kv) + (size_t)slot_of_lane * kRowBytes, kRowBytes);
+        if constexpr (FP8) bulk_prefetch_l2(p.kv_scale + (slot_of_lane & ~3), 16);  // the row's scale
+      }
     };
     constexpr int PF = kPrefetchTiles;
     int sl[PF];    // slots of tiles g .. g + PF - 1
@@ -324,6 +330,83 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
       if (c.valid) c.next();
     }
     bool ok = true;
+    if constexpr (FP8) {
+      // E4M3 pool: each row is 512 bytes of codes; lane l reads bytes
+      // [8l, 8l+8) of each half (one 8-byte load per row and half, 256 bytes
+      // per warp instruction), lanes 0..7 also read the row's scale; the
+      // codes are dequantised (code * scale, rounded to bf16) into the same
+      // swizzled bf16 tile as the bf16 pool's rows.
+      const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
+      // lanes 0..7: scale of their row of the current tile, read one tile early
+      float scl = (lane < kRowsPerLoader && hv[0] && sl[0] >= 0) ? __ldg(p.kv_scale + sl[0]) : 0.f;
+      for (int g = 0; hv[0] && ok; ++g) {
+        const int s = g % KS;  // KV stage
+        uint2 w[2 * kRowsPerLoader];
+#pragma unroll
+        for (int r = 0; r < kRowsPerLoader; ++r) {
+          const int slot = __shfl_sync(0xffffffffu, sl[0], r);
+          if (slot >= 0) {
+            const uint2* src = reinterpret_cast<const uint2*>(kv8 + (size_t)slot * kD);
+            w[2 * r] = __ldcg(src + lane);
+            w[2 * r + 1] = __ldcg(src + 32 + lane);
+          } else {  // tail row of a partial tile: zeros (its p is forced to 0)
+            w[2 * r] = make_uint2(0, 0);
+            w[2 * r + 1] = make_uint2(0, 0);
+          }
+        }
+        const float scl_next =
+            (lane < kRowsPerLoader && hv[1] && sl[1] >= 0) ? __ldg(p.kv_scale + sl[1]) : 0.f;
+        if (g == 0) {
+#pragma unroll
+          for (int j = 1; j < PF; ++j) prefetch_rows(sl[j]);
+        }
+        const bool hpf = c.valid;  // tile g + PF
+        const int spf = hpf ? tile_slot() : -1;
+        if (hpf) c.next();
+        // dequantise both halves now, while the stage may still be busy, so
+        // that the conversion stays off the path from "stage free" to "stored"
+        uint4 v[2 * kRowsPerLoader];
+#pragma unroll
+        for (int r = 0; r < kRowsPerLoader; ++r) {
+          const float sr = __shfl_sync(0xffffffffu, scl, r);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint2 c8 = w[2 * r + hh];
+            v[2 * r + hh] = make_uint4(e4m3x2_to_bf16x2_scaled(c8.x & 0xffffu, sr),
+                                       e4m3x2_to_bf16x2_scaled(c8.x >> 16, sr),
+                                       e4m3x2_to_bf16x2_scaled(c8.y & 0xffffu, sr),
+                                       e4m3x2_to_bf16x2_scaled(c8.y >> 16, sr));
+          }
+        }
+        uint8_t* stage = smem + C::kOffKV + s * kKVBytes;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          if (g >= KS) {  // the tile KS back in this stage
+            if (lane == 0) ok = wait_bar(bar(pv_done(s, hh)), ((g / KS) - 1) & 1, abort_flag, p.hdr);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+          }
+          // 16-byte chunk q = 32*hh + lane (8 bf16) of each row: panel q/8, chunk q%8
+          const int q = hh * 32 + lane, k = q & 7;
+          uint8_t* atom = stage + (q >> 3) * kPanelKV + lw * 1024;
+#pragma unroll
+          for (int r = 0; r < kRowsPerLoader; ++r)
+            *reinterpret_cast<uint4*>(atom + r * 128 + ((k ^ r) << 4)) = v[2 * r + hh];
+          fence_proxy_async_smem();  // generic-proxy stores -> read by the tensor cores
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kv_full(s, hh)));
+        }
+        prefetch_rows(spf);
+        scl = scl_next;
+#pragma unroll
+        for (int j = 0; j + 1 < PF; ++j) {
+          sl[j] = sl[j + 1];
+          hv[j] = hv[j + 1];
+        }
+        sl[PF - 1] = spf;
+        hv[PF - 1] = hpf;
+      }
+    } else {
     for (int g = 0; hv[0] && ok; ++g) {
       const int s = g % KS;  // KV stage
       uint4 v[2 * kRowsPerLoader];
@@ -377,6 +460,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
       }
       sl[PF - 1] = spf;
       hv[PF - 1] = hpf;
+    }
     }
   } else if (warp == kMmaWarp || warp == kPvWarp) {
     // ===================================================== MMA issuers
@@ -800,10 +884,10 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NH>
-cudaError_t launch_nh(const void* q, const void* kv, int64_t total_pages, const int32_t* kv_indices,
-                      const float* attn_sink, float scale, int N, int H, void* out, void* ws,
-                      const WsLayout& L, const LaunchPlan& lp, cudaStream_t st) {
+template <int NH, bool FP8>
+cudaError_t launch_nh(const void* q, const void* kv, const float* kv_scale, int64_t total_pages,
+                      const int32_t* kv_indices, const float* attn_sink, float scale, int N, int H,
+                      void* out, void* ws, const WsLayout& L, const LaunchPlan& lp, cudaStream_t st) {
   (void)total_pages;
   CUtensorMap tq, tout;
   if (!make_map_2d(&tq, q, kD, (uint64_t)N * H, 64, NH, CU_TENSOR_MAP_L2_PROMOTION_L2_128B) ||
@@ -813,6 +897,7 @@ cudaError_t launch_nh(const void* q, const void* kv, int64_t total_pages, const 
   Params p;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.kv = static_cast<const __nv_bfloat16*>(kv);
+  p.kv_scale = kv_scale;
   p.kv_indices = kv_indices;
   p.attn_sink = attn_sink;
   p.out = static_cast<__nv_bfloat16*>(out);
@@ -822,7 +907,7 @@ cudaError_t launch_nh(const void* q, const void* kv, int64_t total_pages, const 
   p.part_o = reinterpret_cast<float*>(base + L.o_off);
   p.qk_scale_log2 = scale * kLog2e;
   p.H = H;
-  return launch_pdl(decode_umma_kernel<NH>, dim3(lp.grid), dim3(kThreads), (size_t)Cfg<NH>::kSmem,
+  return launch_pdl(decode_umma_kernel<NH, FP8>, dim3(lp.grid), dim3(kThreads), (size_t)Cfg<NH>::kSmem,
                     st, tq, tout, p);
 }
 
@@ -837,26 +922,44 @@ size_t umma_smem_bytes(int nh) {
   }
 }
 
+template <int NH>
+cudaError_t prepare_nh() {
+  cudaError_t e = cudaFuncSetAttribute(decode_umma_kernel<NH, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<NH>::kSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_umma_kernel<NH, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<NH>::kSmem);
+  return e;
+}
+
 cudaError_t umma_prepare(int nh) {
   switch (nh) {
-    case 16: return cudaFuncSetAttribute(decode_umma_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<16>::kSmem);
-    case 32: return cudaFuncSetAttribute(decode_umma_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<32>::kSmem);
-    case 64: return cudaFuncSetAttribute(decode_umma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<64>::kSmem);
+    case 16: return prepare_nh<16>();
+    case 32: return prepare_nh<32>();
+    case 64: return prepare_nh<64>();
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_decode_umma(const void* q, const void* kv, int64_t total_pages,
-                               const int32_t* kv_indices, const float* attn_sink,
-                               float softmax_scale, int N, int H, int D, void* out, void* ws,
-                               const WsLayout& L, const LaunchPlan& lp, cudaStream_t st) {
+cudaError_t launch_decode_umma(const void* q, const void* kv, const float* kv_scale,
+                               int64_t total_pages, const int32_t* kv_indices,
+                               const float* attn_sink, float softmax_scale, int N, int H, int D,
+                               void* out, void* ws, const WsLayout& L, const LaunchPlan& lp,
+                               cudaStream_t st) {
   if (D != kD) return cudaErrorInvalidValue;
+  const bool fp8 = kv_scale != nullptr;
+#define SDA_LAUNCH(NHV)                                                                          \
+  return fp8 ? launch_nh<NHV, true>(q, kv, kv_scale, total_pages, kv_indices, attn_sink,          \
+                                    softmax_scale, N, H, out, ws, L, lp, st)                      \
+             : launch_nh<NHV, false>(q, kv, nullptr, total_pages, kv_indices, attn_sink,         \
+                                     softmax_scale, N, H, out, ws, L, lp, st)
   switch (lp.nh) {
-    case 16: return launch_nh<16>(q, kv, total_pages, kv_indices, attn_sink, softmax_scale, N, H, out, ws, L, lp, st);
-    case 32: return launch_nh<32>(q, kv, total_pages, kv_indices, attn_sink, softmax_scale, N, H, out, ws, L, lp, st);
-    case 64: return launch_nh<64>(q, kv, total_pages, kv_indices, attn_sink, softmax_scale, N, H, out, ws, L, lp, st);
+    case 16: SDA_LAUNCH(16);
+    case 32: SDA_LAUNCH(32);
+    case 64: SDA_LAUNCH(64);
     default: return cudaErrorInvalidValue;
   }
+#undef SDA_LAUNCH
 }
 
 }  // namespace sda

@@ -91,10 +91,13 @@ cudaError_t launch_decode_simt(const void* q, const void* kv, const int32_t* kv_
                                const float* attn_sink, float softmax_scale, int N, int H, int D,
                                void* out, void* ws, const WsLayout& L, const LaunchPlan& lp,
                                cudaStream_t st);
-cudaError_t launch_decode_umma(const void* q, const void* kv, int64_t total_pages,
-                               const int32_t* kv_indices, const float* attn_sink,
-                               float softmax_scale, int N, int H, int D, void* out, void* ws,
-                               const WsLayout& L, const LaunchPlan& lp, cudaStream_t st);
+// kv_scale == nullptr: kv is the bf16 pool; otherwise kv holds E4M3 codes
+// [total_pages, D] and kv_scale [total_pages] the rows' dequantisation scales.
+cudaError_t launch_decode_umma(const void* q, const void* kv, const float* kv_scale,
+                               int64_t total_pages, const int32_t* kv_indices,
+                               const float* attn_sink, float softmax_scale, int N, int H, int D,
+                               void* out, void* ws, const WsLayout& L, const LaunchPlan& lp,
+                               cudaStream_t st);
 size_t umma_smem_bytes(int nh);
 cudaError_t umma_prepare(int nh);  // one-time kernel attribute set-up
 cudaError_t launch_decode_pair(const void* q, const void* kv, const int32_t* kv_indices,

@@ -3,6 +3,8 @@
 // tcgen05 MMA / TMEM, and the descriptors they take.  sm_100a / sm_103a only.
 #pragma once
 
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace sda {
@@ -121,6 +123,18 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t threads, bool
       : "r"((uint32_t)pred), "r"(id), "r"(threads)
       : "memory");
   return r != 0;
+}
+
+// Two FP8 E4M3 codes (low byte first) -> two bf16 of code * scale, packed
+// low half first.  E4M3 -> f16 is exact (hardware conversion); the product
+// is rounded to bf16 (round to nearest even).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_scaled(uint32_t two_codes, float scale) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)two_codes));
+  const float lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
+  const float hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+  const __nv_bfloat162 b = __floats2bfloat162_rn(lo * scale, hi * scale);
+  return *reinterpret_cast<const uint32_t*>(&b);
 }
 
 // ------------------------------------------------------------------ TMA

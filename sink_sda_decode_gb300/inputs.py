@@ -119,6 +119,60 @@ def random_pool(total_pages: int, D: int, seed: int, device, chunk_rows: int = 1
     return out
 
 
+E4M3_MAX = 448.0  # largest finite FP8 E4M3 magnitude
+
+
+@dataclasses.dataclass
+class Fp8Pool:
+    """A pool stored as FP8: row s is e4m3(codes[s]) * scale[s]."""
+    codes: torch.Tensor  # [P, D] uint8 E4M3 codes (device of the workload)
+    scale: torch.Tensor  # [P] fp32
+
+
+def fp8_pool(w: "Workload", pow2: bool = True, chunk_rows: int = 1 << 19) -> Fp8Pool:
+    """The workload's bf16 pool quantised row by row the way an FP8 cache store
+    fills one: code = E4M3 of row / scale rounded to nearest even (torch's
+    float8_e4m3fn conversion, clamped to the finite range first) with
+    scale = max|row| / 448 (1 for an all-zero row), or with `pow2` that value
+    rounded up to a power of two (as block-scaled FP8 formats with 8-bit
+    exponent scales store it), which makes code * scale exact in bf16."""
+    P, D = w.unified_kv.shape
+    dev = w.unified_kv.device
+    codes = torch.empty((P, D), dtype=torch.uint8, device=dev)
+    scale = torch.empty(P, dtype=torch.float32, device=dev)
+    for r0 in range(0, P, chunk_rows):
+        r1 = min(P, r0 + chunk_rows)
+        rows = w.unified_kv[r0:r1].float()
+        amax = rows.abs().amax(dim=1)
+        sc = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+        if pow2:
+            sc = torch.exp2(torch.ceil(torch.log2(sc)))
+        x = (rows / sc[:, None]).clamp_(-E4M3_MAX, E4M3_MAX)
+        codes[r0:r1] = x.to(torch.float8_e4m3fn).view(torch.uint8)
+        scale[r0:r1] = sc
+    return Fp8Pool(codes=codes, scale=scale)
+
+
+def fp8_rows_for(w: "Workload", pool: Fp8Pool, tokens=None):
+    """Host copy of an FP8 pool restricted to the rows the given tokens read:
+    (codes [R, D] uint8, scale [R] fp32, kv_indices remapped into [0, R),
+    kv_indptr rebased), as Workload.kv_rows_for."""
+    ptr = w.kv_indptr.astype(np.int64)
+    if tokens is None:
+        tokens = np.arange(w.N)
+    tokens = np.asarray(tokens, dtype=np.int64)
+    pieces = [w.kv_indices[ptr[t]:ptr[t + 1]] for t in tokens]
+    lens = np.array([len(p) for p in pieces], dtype=np.int64)
+    sub_idx = np.concatenate(pieces) if len(pieces) else np.zeros(0, np.int32)
+    sub_ptr = np.zeros(len(tokens) + 1, dtype=np.int32)
+    sub_ptr[1:] = np.cumsum(lens)
+    uniq, inv = np.unique(sub_idx, return_inverse=True)
+    sel = torch.from_numpy(uniq.astype(np.int64)).to(pool.codes.device)
+    codes = pool.codes.index_select(0, sel).cpu().numpy() if uniq.size else np.zeros((0, w.D), np.uint8)
+    scale = pool.scale.index_select(0, sel).cpu().numpy() if uniq.size else np.zeros(0, np.float32)
+    return codes, scale, inv.astype(np.int32), sub_ptr
+
+
 def _descriptors(lists, swa_parts, swa_pages, win, kpb):
     """Builder descriptors that reproduce `lists` (SWA part first, then compressed)."""
     N = len(lists)

@@ -31,6 +31,13 @@ def test_algorithmic_bytes_and_flops_match_the_published_config_figures():
     assert abs(bench.algorithmic_flops(w) / 1e9 - 171.8) < 0.05
 
 
+def test_fp8_pool_bytes():
+    # an FP8 row is D one-byte codes plus a 4-byte scale
+    w = _W(64, 16, 512, 64 * 640)
+    assert bench.algorithmic_bytes(w, "fp8") == 40960 * (512 + 4) + 2 * 64 * 16 * 512 * 2 + 40960 * 4 + 65 * 4
+    assert bench.algorithmic_bytes(w, "fp8") < bench.algorithmic_bytes(w)
+
+
 def test_bytes_follow_the_generated_workload():
     w = inputs.config(0)  # the tiny case: lengths {0, 1, 17, 64}
     assert int(w.total_len) == 82
