@@ -46,13 +46,13 @@ def test_workload_lists_bit_exact(cfg):
     assert np.array_equal(idx, o_idx) and np.array_equal(ptr, o_ptr) and st == o_st
 
 
-def random_descriptors(rng, N, win, kpb, n_states, n_blocks, bad=True):
+def random_descriptors(rng, N, win, kpb, n_states, n_blocks, bad=True, max_comp=40):
     swa_pages = n_states * win
     total_pages = swa_pages + n_blocks * kpb
     ss = rng.integers(-1, n_states, N)
     sl = rng.integers(0, win + 1, N)
     sh = rng.integers(0, win, N)
-    cl = rng.integers(0, 40, N)
+    cl = rng.integers(0, max_comp, N)
     cp = np.zeros(N + 1, np.int64)
     cp[1:] = np.cumsum(cl)
     cb = rng.integers(0, n_blocks, cp[-1])
@@ -74,6 +74,27 @@ def random_descriptors(rng, N, win, kpb, n_states, n_blocks, bad=True):
 def test_random_descriptors_bit_exact(seed, N):
     rng = np.random.default_rng(seed * 7919 + N)
     args = random_descriptors(rng, N, win=16, kpb=8, n_states=max(N // 2, 1), n_blocks=300)
+    idx, ptr, st = gpu_build(*args)
+    o_idx, o_ptr, o_st = oracle.build_indices(*args)
+    assert st == o_st
+    assert np.array_equal(ptr, o_ptr)
+    assert np.array_equal(idx, o_idx)
+
+
+@pytest.mark.parametrize("seed", [1, 2])
+@pytest.mark.parametrize("N", [1, 9, 300])
+def test_long_lists_bit_exact(seed, N):
+    """Thousands of compressed entries per token (each token's entries take
+    several passes of its CTA's threads); bad entries sit at the ends of long
+    lists."""
+    rng = np.random.default_rng(seed * 104729 + N)
+    ss, sl, sh, cp, cb, cs, win, kpb, swa_pages, total_pages = random_descriptors(
+        rng, N, win=16, kpb=8, n_states=max(N // 2, 1), n_blocks=5000, max_comp=6000)
+    for t in rng.integers(0, N, 3):
+        if cp[t + 1] - cp[t] > 10:
+            cs[cp[t + 1] - 1] = kpb if rng.random() < 0.5 else cs[cp[t + 1] - 1]
+            cb[cp[t + 1] - 2] = 5000 if rng.random() < 0.5 else cb[cp[t + 1] - 2]
+    args = (ss, sl, sh, cp, cb, cs, win, kpb, swa_pages, total_pages)
     idx, ptr, st = gpu_build(*args)
     o_idx, o_ptr, o_st = oracle.build_indices(*args)
     assert st == o_st
