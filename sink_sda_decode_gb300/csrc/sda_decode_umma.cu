@@ -229,12 +229,6 @@ struct TileCursor {
       seek();
     }
   }
-  __device__ __forceinline__ void next_unit() {
-    g += ntiles - i;
-    ++nu;
-    ++k;
-    seek();
-  }
 };
 
 template <int NH, bool FP8>
