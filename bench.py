@@ -12,7 +12,8 @@ pool.  `--config` picks another of the five workloads.
   value     decode tokens/s with inputs resident in HBM (graph replays,
             CUDA events, L2 flushed between steps)
   e2e       the same metric through the public API from pinned host
-            buffers: H2D of q + index descriptors, build + decode, D2H of out
+            memory: one packed H2D copy of q + the index descriptors, build +
+            decode, D2H of out, replayed as one CUDA graph
   roofline  the attention kernel alone (events recorded around it by the
             library's timing hook): algorithmic bytes / time vs measured HBM
   cpu_baseline  the fp64 CPU oracle on the host cores (bounded sample)
@@ -332,12 +333,41 @@ def gpu_arm(args, w, device, ws, rank, pool=None):
     barrier()
     kernel_ms = sum(a.elapsed_time(b) for a, b in kev) / len(kev)
 
-    # ---- timed region 3: end to end from pinned host buffers
-    q_h = w.q.cpu().pin_memory()
-    bi_h = {k: v.cpu().pin_memory() for k, v in step.bi.items()}
+    # ---- timed region 3: end to end from pinned host memory.  The step's
+    # inputs (q and the builder's descriptors) sit packed in one pinned host
+    # buffer: one H2D copy, the public build_indices + decode calls on views
+    # of the device copy, one D2H copy of out -- replayed as one CUDA graph,
+    # as a serving loop replays its decode step.
+    parts = [w.q.reshape(-1).view(torch.uint8)] + [v.reshape(-1).view(torch.uint8)
+                                                    for v in step.bi.values()]
+    offs, total = [], 0
+    for t_ in parts:
+        offs.append(total)
+        total += (t_.numel() + 255) // 256 * 256
+    h_in = torch.zeros(max(total, 256), dtype=torch.uint8, pin_memory=True)
+    for o, t_ in zip(offs, parts):
+        h_in[o:o + t_.numel()].copy_(t_.cpu())
+    d_in = torch.empty_like(h_in, device=device)
+    q_v = d_in[offs[0]:offs[0] + parts[0].numel()].view(w.q.dtype).view(w.q.shape)
+    bi_v = {k: d_in[o:o + v.numel() * 4].view(torch.int32)
+            for (k, v), o in zip(step.bi.items(), offs[1:])}
     out_h = torch.empty(w.q.shape, dtype=w.q.dtype, pin_memory=True)
-    h2d = q_h.numel() * q_h.element_size() + sum(v.numel() * v.element_size() for v in bi_h.values())
+    h2d = sum(t_.numel() for t_ in parts)
     d2h = out_h.numel() * out_h.element_size()
+
+    def e2e_step():
+        d_in.copy_(h_in, non_blocking=True)
+        step.run(q=q_v, bi=bi_v, stream=s)
+        out_h.copy_(step.out, non_blocking=True)
+
+    with torch.cuda.stream(s):
+        for _ in range(max(args.warmup, 3)):
+            e2e_step()
+    torch.cuda.synchronize(device)
+    ge = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(ge, stream=s):
+        e2e_step()
+    torch.cuda.synchronize(device)
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
     barrier()
@@ -345,10 +375,7 @@ def gpu_arm(args, w, device, ws, rank, pool=None):
         for a, b in e2e_ev:
             flush.zero_()
             a.record(s)
-            q_d = q_h.to(device, non_blocking=True)
-            bi_d = {k: v.to(device, non_blocking=True) for k, v in bi_h.items()}
-            step.run(q=q_d, bi=bi_d, stream=s)
-            out_h.copy_(step.out, non_blocking=True)
+            ge.replay()
             b.record(s)
     barrier()
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / len(e2e_ev)
