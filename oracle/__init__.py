@@ -13,6 +13,12 @@ first use and marshals NumPy arrays through ctypes.
 codes with one fp32 scale per row (a format the pages do not fix; it serves
 the FP8-pool variant of the path).
 
+``qk_norm_rope_store`` is the step that fills the pool before decode: the
+per-head RMSNorm of q, the RMSNorm of the step's new KV row, GPT-J RoPE on
+the last R dims and the store of the KV row into its SWA ring slot (sglang PR
+25898 summary page, sections "关键文件" and "关键符号"); ``bf16_rne`` and
+``fp8_quantise_rows`` give the rounded forms it stores.
+
 What it computes follows the docstring of ``paged_decode.py`` quoted on the
 sglang PR 28392 summary page ("为 AMD V4 内核添加 ATOM 来源注释", section
 "关键源码片段": caller convention, returns, numerics):
@@ -41,6 +47,7 @@ _lib = None
 _ERRORS = {1: "bad shape", 2: "bad kv_indptr", 3: "slot out of range", 4: "out of memory"}
 
 _i32p = ctypes.POINTER(ctypes.c_int32)
+_i64p = ctypes.POINTER(ctypes.c_int64)
 _u16p = ctypes.POINTER(ctypes.c_uint16)
 _u8p = ctypes.POINTER(ctypes.c_uint8)
 _f32p = ctypes.POINTER(ctypes.c_float)
@@ -78,6 +85,19 @@ def _bind(lib):
         _i32p, ctypes.c_int64, _i32p, ctypes.c_int, ctypes.c_int64, _i32p]
     lib.oracle_num_threads.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
+    lib.oracle_qk_norm_rope_store.restype = ctypes.c_int
+    lib.oracle_qk_norm_rope_store.argtypes = [
+        _u16p, _u16p, _u16p, _u16p, _f32p, _f32p, ctypes.c_int, _i32p, _i32p, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int64,
+        _f64p, _f64p, _i64p, _i32p]
+    lib.oracle_bf16_rne_array.restype = None
+    lib.oracle_bf16_rne_array.argtypes = [_f64p, ctypes.c_int64, _u16p]
+    lib.oracle_fp8_quantise_rows.restype = None
+    lib.oracle_fp8_quantise_rows.argtypes = [_f64p, ctypes.c_int64, ctypes.c_int, _u8p, _f32p]
+    lib.oracle_e4m3_rne.restype = ctypes.c_uint8
+    lib.oracle_e4m3_rne.argtypes = [ctypes.c_double]
+    lib.oracle_fp8_scale_exponent.restype = ctypes.c_int
+    lib.oracle_fp8_scale_exponent.argtypes = [ctypes.c_double]
     return lib
 
 
@@ -245,3 +265,81 @@ def validate_indices(kv_indices, kv_indptr, total_pages, lib=None):
     if rc != 0:
         raise ValueError(f"oracle_validate_indices: {_ERRORS.get(rc, rc)}")
     return int(st[0]), int(st[1])
+
+
+def qk_norm_rope_store(q_bits, kv_bits, q_norm_w_bits, kv_norm_w_bits, cos_cache, sin_cache,
+                       positions, state_slot, eps, win, swa_pages, lib=None) -> dict:
+    """fp64 fused q/kv RMSNorm + GPT-J RoPE (last R dims) + SWA ring slot.
+
+    q_bits [N,H,D], kv_bits [N,D], weights [D]: bf16 bits; cos_cache and
+    sin_cache [max_pos, R/2] fp32; positions, state_slot [N] int32.  Returns
+    ``q_val`` [N,H,D] and ``kv_val`` [N,D] (exact results, float64), ``slot``
+    [N] int64 (pool row of the KV store, -1 if none) and ``status``.
+    """
+    lib = lib or load()
+    q = _as(q_bits, np.uint16)
+    kv = _as(kv_bits, np.uint16)
+    N, H, D = q.shape
+    assert kv.shape == (N, D)
+    qw = _as(q_norm_w_bits, np.uint16)
+    kw = _as(kv_norm_w_bits, np.uint16)
+    assert qw.shape == (D,) and kw.shape == (D,)
+    cs = _as(cos_cache, np.float32)
+    sn = _as(sin_cache, np.float32)
+    assert cs.ndim == 2 and cs.shape == sn.shape
+    max_pos, half = cs.shape
+    pos = _as(positions, np.int32)
+    ss = _as(state_slot, np.int32)
+    assert pos.shape == (N,) and ss.shape == (N,)
+    q_val = np.zeros((N, H, D), np.float64)
+    kv_val = np.zeros((N, D), np.float64)
+    slot = np.full(max(N, 1), -1, np.int64)
+    st = np.zeros(1, np.int32)
+    one16 = np.zeros(1, np.uint16)
+    one32 = np.zeros(1, np.int32)
+    onef = np.zeros(1, np.float32)
+    rc = lib.oracle_qk_norm_rope_store(
+        _ptr(q if N else one16, ctypes.c_uint16), _ptr(kv if N else one16, ctypes.c_uint16),
+        _ptr(qw, ctypes.c_uint16), _ptr(kw, ctypes.c_uint16),
+        _ptr(cs if cs.size else onef, ctypes.c_float), _ptr(sn if sn.size else onef, ctypes.c_float),
+        max_pos, _ptr(pos if N else one32, ctypes.c_int32), _ptr(ss if N else one32, ctypes.c_int32),
+        N, H, D, 2 * half, float(np.float32(eps)), int(win), int(swa_pages),
+        _ptr(q_val if N else np.zeros(1), ctypes.c_double),
+        _ptr(kv_val if N else np.zeros(1), ctypes.c_double), _ptr(slot, ctypes.c_int64),
+        _ptr(st, ctypes.c_int32))
+    if rc != 0:
+        raise ValueError(f"oracle_qk_norm_rope_store: {_ERRORS.get(rc, rc)}")
+    return {"q_val": q_val, "kv_val": kv_val, "slot": slot[:N].copy(), "status": int(st[0])}
+
+
+def bf16_rne(values, lib=None) -> np.ndarray:
+    """bf16 bit patterns of float64 values rounded to nearest even."""
+    lib = lib or load()
+    v = _as(values, np.float64)
+    out = np.zeros(v.shape, np.uint16)
+    if v.size:
+        lib.oracle_bf16_rne_array(_ptr(v, ctypes.c_double), v.size, _ptr(out, ctypes.c_uint16))
+    return out
+
+
+def e4m3_rne(value, lib=None) -> int:
+    """E4M3 code of one float64 value rounded to nearest even (saturating)."""
+    return int((lib or load()).oracle_e4m3_rne(float(value)))
+
+
+def fp8_scale_exponent(amax, lib=None) -> int:
+    """e of the power-of-two row scale 2^e: the smallest e with 448 * 2^e >= amax."""
+    return int((lib or load()).oracle_fp8_scale_exponent(float(amax)))
+
+
+def fp8_quantise_rows(values, lib=None):
+    """(codes [rows, D] uint8, scale [rows] fp32) of float64 rows [rows, D]."""
+    lib = lib or load()
+    v = _as(values, np.float64)
+    rows, D = v.shape
+    codes = np.zeros((rows, D), np.uint8)
+    scale = np.zeros(rows, np.float32)
+    if rows:
+        lib.oracle_fp8_quantise_rows(_ptr(v, ctypes.c_double), rows, D,
+                                     _ptr(codes, ctypes.c_uint8), _ptr(scale, ctypes.c_float))
+    return codes, scale

@@ -1,6 +1,8 @@
 /*
  * sda_oracle.c -- plain, slow, fp64 CPU oracle for sparse sink decode attention
- * over a unified KV pool, and for the ragged index builder in front of it.
+ * over a unified KV pool, for the ragged index builder in front of it, and for
+ * the fused q/kv RMSNorm + RoPE + SWA ring store that fills the pool (end of
+ * this file, with its own sources).
  *
  * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
  * benchmark's CPU-baseline leg may load this code.  It shares nothing with the
@@ -306,4 +308,162 @@ int oracle_validate_indices(const int32_t* kv_indices, int64_t total_indices,
   status[0] = flags;
   status[1] = (int32_t)(n_bad > INT32_MAX ? INT32_MAX : n_bad);
   return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/*
+ * Fused q / kv RMSNorm + RoPE + SWA ring store, fp64.
+ *
+ * Source: the sglang PR 25898 summary page ("修复 DSV4 在 AMD GPU 上的运行时
+ * 崩溃与 JIT 不兼容"), section "关键文件": fused_qk_norm_rope_store.py is one
+ * kernel that does the per-head RMSNorm of Q, the RMSNorm of the new KV, RoPE,
+ * FP8 quantisation and the paged SWA store; section "关键符号" names its parts
+ * (_batched_rmsnorm, _gptj_rotate, _batched_rope, fused_qk_norm_rope_swa_store);
+ * section "实现拆解" item 2 names the cos_cache / sin_cache it reads.  The SWA
+ * slot of an entry is state_slot * win + ring (the paged_decode.py docstring
+ * on the PR 28392 page).
+ *
+ * Readings where the pages are silent (each also in the design notes):
+ *   - RMSNorm of a row x of length D with weight w:
+ *       y_d = x_d / sqrt(mean_d x_d^2 + eps) * w_d      (one weight [D] per
+ *     tensor, shared by all heads of q);
+ *   - RoPE acts on the last R dims of each row; "GPT-J" rotation pairs
+ *     adjacent elements: for i < R/2, d = D - R + 2i,
+ *       (y_d, y_{d+1}) <- (y_d c - y_{d+1} s,  y_{d+1} c + y_d s),
+ *     c = cos_cache[pos, i], s = sin_cache[pos, i] (caches [max_pos, R/2]);
+ *   - norm and rotation happen in full precision and the result is rounded
+ *     once: to bf16 (nearest even) for q and for a bf16 pool, or quantised for
+ *     an FP8 pool;
+ *   - the new KV row goes to ring position pos mod win of its state:
+ *     slot = state_slot * win + pos mod win, which must be < swa_pages;
+ *   - state_slot < 0 marks a padded token: its q row is 0 and nothing is
+ *     stored; a real token whose position is outside [0, max_pos) is treated
+ *     the same way and raises status bit 1; a slot outside [0, swa_pages)
+ *     raises bit 2 and is not stored (q is still produced).
+ *
+ * q [N,H,D], kv [N,D], q_norm_w [D], kv_norm_w [D]: bf16 bits.
+ * Outputs: q_val [N,H,D] and kv_val [N,D] the exact (unrounded) results,
+ * slot [N] the pool row written (-1 if none), *status the bits above.
+ */
+int oracle_qk_norm_rope_store(const uint16_t* q, const uint16_t* kv, const uint16_t* q_norm_w,
+                              const uint16_t* kv_norm_w, const float* cos_cache,
+                              const float* sin_cache, int max_pos, const int32_t* positions,
+                              const int32_t* state_slot, int N, int H, int D, int R, float eps,
+                              int win, int64_t swa_pages, double* q_val, double* kv_val,
+                              int64_t* slot, int32_t* status) {
+  if (N < 0 || H <= 0 || D <= 0 || R < 0 || R > D || (R & 1) || win <= 0 || swa_pages < 0 ||
+      max_pos < 0)
+    return ORACLE_BAD_SHAPE;
+  int32_t flags = 0;
+  for (int t = 0; t < N; ++t) {
+    const int pos = positions[t];
+    int live = state_slot[t] >= 0;
+    if (live && (pos < 0 || pos >= max_pos)) {
+      flags |= 1;
+      live = 0;
+    }
+    slot[t] = -1;
+    for (int r = 0; r <= H; ++r) {            /* rows 0..H-1: q heads; row H: the KV row */
+      const uint16_t* x = r < H ? q + ((size_t)t * H + r) * D : kv + (size_t)t * D;
+      const uint16_t* w = r < H ? q_norm_w : kv_norm_w;
+      double* y = r < H ? q_val + ((size_t)t * H + r) * D : kv_val + (size_t)t * D;
+      if (!live) {
+        for (int d = 0; d < D; ++d) y[d] = 0.0;
+        continue;
+      }
+      double ss = 0.0;
+      for (int d = 0; d < D; ++d) ss += bf16_bits_to_double(x[d]) * bf16_bits_to_double(x[d]);
+      const double inv_rms = 1.0 / sqrt(ss / D + (double)eps);
+      for (int d = 0; d < D; ++d)
+        y[d] = bf16_bits_to_double(x[d]) * inv_rms * bf16_bits_to_double(w[d]);
+      for (int i = 0; i < R / 2; ++i) {
+        const int d = D - R + 2 * i;
+        const double c = cos_cache[(size_t)pos * (R / 2) + i];
+        const double s = sin_cache[(size_t)pos * (R / 2) + i];
+        const double a = y[d], b = y[d + 1];
+        y[d] = a * c - b * s;
+        y[d + 1] = b * c + a * s;
+      }
+    }
+    if (live) {
+      const int64_t sl = (int64_t)state_slot[t] * win + pos % win;
+      if (sl >= swa_pages) flags |= 2;
+      else slot[t] = sl;
+    }
+  }
+  *status = flags;
+  return ORACLE_OK;
+}
+
+/* Round to the nearest bf16, ties to even, from the format's definition
+ * (8 significant bits, exponent range of fp32): returns the bit pattern. */
+uint16_t oracle_bf16_rne(double v) {
+  if (isnan(v)) return 0x7FC0;
+  const uint16_t sign = signbit(v) ? 0x8000 : 0;
+  const double a = fabs(v);
+  if (a == 0.0) return sign;
+  int e2;
+  frexp(a, &e2);                      /* a = m * 2^e2, m in [0.5, 1) */
+  int E = e2 - 1;                     /* floor(log2 a) */
+  if (E < -126) E = -126;             /* subnormal range: fixed quantum 2^-133 */
+  const double quantum = ldexp(1.0, E - 7);
+  const double r = rint(a / quantum) * quantum;   /* rint: nearest, ties to even */
+  if (r >= ldexp(1.0, 128)) return sign | 0x7F80;  /* rounds past the largest finite */
+  const float f = (float)r;           /* exact: r has at most 8 significant bits */
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return (uint16_t)(sign | (u >> 16));
+}
+
+/* Round to the nearest FP8 E4M3 value, ties to even, saturating at +-448
+ * (format: bias 7, 3 mantissa bits, subnormal quantum 2^-9): returns the code. */
+uint8_t oracle_e4m3_rne(double v) {
+  if (isnan(v)) return 0x7F;
+  const uint8_t sign = signbit(v) ? 0x80 : 0;
+  const double a = fabs(v);
+  if (a == 0.0) return sign;
+  int e2;
+  frexp(a, &e2);
+  int E = e2 - 1;
+  if (E < -6) E = -6;                 /* subnormals share the quantum of binade -6 */
+  const double quantum = ldexp(1.0, E - 3);
+  double r = rint(a / quantum) * quantum;
+  if (r > 448.0) r = 448.0;
+  if (r < ldexp(1.0, -6)) return (uint8_t)(sign | (uint8_t)(r / ldexp(1.0, -9)));  /* 0..7 */
+  frexp(r, &e2);
+  const int Er = e2 - 1;              /* 2^Er <= r < 2^(Er+1) */
+  const int mant = (int)(r / ldexp(1.0, Er) * 8.0) - 8;
+  return (uint8_t)(sign | ((Er + 7) << 3) | mant);
+}
+
+/* Power-of-two row scale of the FP8 store: 2^e with e the smallest integer
+ * such that 448 * 2^e >= amax (so every element divided by it fits in E4M3),
+ * e >= -126; amax = 0 gives 1.  Returns e. */
+int oracle_fp8_scale_exponent(double amax) {
+  if (!(amax > 0.0)) return 0;
+  int e = (int)ceil(log2(amax / 448.0));
+  while (ldexp(448.0, e) < amax) ++e;
+  while (ldexp(448.0, e - 1) >= amax) --e;
+  return e < -126 ? -126 : e;
+}
+
+/* bf16 bits of n values, each rounded to nearest even. */
+void oracle_bf16_rne_array(const double* v, int64_t n, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_rne(v[i]);
+}
+
+/* FP8 quantisation of `rows` rows of D values (the FP8 pool's format: one
+ * E4M3 code per element and one fp32 scale per row, element = code * scale):
+ * scale = 2^oracle_fp8_scale_exponent(max_d |y_d|), code = E4M3 of y / scale
+ * rounded to nearest even.  Dividing by a power of two is exact. */
+void oracle_fp8_quantise_rows(const double* y, int64_t rows, int D, uint8_t* codes, float* scale) {
+  for (int64_t r = 0; r < rows; ++r) {
+    const double* yr = y + (size_t)r * D;
+    double amax = 0.0;
+    for (int d = 0; d < D; ++d)
+      if (fabs(yr[d]) > amax) amax = fabs(yr[d]);
+    const int e = oracle_fp8_scale_exponent(amax);
+    scale[r] = (float)ldexp(1.0, e);
+    for (int d = 0; d < D; ++d) codes[(size_t)r * D + d] = oracle_e4m3_rne(ldexp(yr[d], -e));
+  }
 }

@@ -328,12 +328,193 @@ def pin_fp8_zero_scale_row(lib):
 
 FP8_PINS = [pin_e4m3_table, pin_fp8_equals_bf16_pool, pin_fp8_zero_scale_row]
 
+
+# ----------------------------------------------------------------------------- q/kv norm + RoPE + store
+# Source: the sglang PR 25898 summary page ("修复 DSV4 在 AMD GPU 上的运行时崩溃与
+# JIT 不兼容"), sections "关键文件" / "关键符号" (fused_qk_norm_rope_store.py:
+# Q per-head RMSNorm, KV RMSNorm, GPT-J RoPE, FP8 quantisation, paged SWA store;
+# cos_cache / sin_cache in "实现拆解" item 2) and the SWA slot formula
+# state_slot * win + ring of the paged_decode.py docstring (PR 28392 page).
+def store_case(rng, N, H, D, R, max_pos=64, sigma=1.0):
+    q = bf16_bits(rng.standard_normal((N, H, D)) * sigma)
+    kv = bf16_bits(rng.standard_normal((N, D)) * sigma)
+    qw = bf16_bits(rng.uniform(0.5, 1.5, D))
+    kw = bf16_bits(rng.uniform(0.5, 1.5, D))
+    ang = rng.uniform(-math.pi, math.pi, (max_pos, R // 2))
+    cos = np.cos(ang).astype(np.float32)
+    sin = np.sin(ang).astype(np.float32)
+    pos = rng.integers(0, max_pos, N).astype(np.int32)
+    return q, kv, qw, kw, cos, sin, pos
+
+
+def pin_store_matches_torch(lib):
+    """torch's RMSNorm (F.rms_norm, float64) followed by RoPE written as the
+    complex product (y_d + i y_{d+1}) * (cos + i sin) of each adjacent pair of
+    the last R dims: a library routine and a different formulation of the
+    same rotation."""
+    rng = np.random.default_rng(81)
+    N, H, D, R = 5, 3, 32, 8
+    q, kv, qw, kw, cos, sin, pos = store_case(rng, N, H, D, R)
+    eps = 0.75  # large, so that a dropped eps shows
+    ss = np.arange(N, dtype=np.int32)
+    res = oracle.qk_norm_rope_store(q, kv, qw, kw, cos, sin, pos, ss, eps, 16, 1 << 20, lib=lib)
+    assert res["status"] == 0
+
+    def torch_ref(x_bits, w_bits):
+        x = torch.from_numpy(bits_to_f64(x_bits))
+        w = torch.from_numpy(bits_to_f64(w_bits))
+        y = F.rms_norm(x, (D,), w, eps)
+        rot = torch.view_as_complex(y[..., D - R:].reshape(*y.shape[:-1], R // 2, 2).contiguous())
+        p = torch.from_numpy(pos.astype(np.int64))
+        c = torch.from_numpy(cos.astype(np.float64))[p]
+        s = torch.from_numpy(sin.astype(np.float64))[p]
+        if y.dim() == 3:
+            c, s = c[:, None, :], s[:, None, :]
+        rot = torch.view_as_real(rot * torch.complex(c, s)).reshape(*y.shape[:-1], R)
+        return torch.cat([y[..., :D - R], rot], -1).numpy()
+
+    assert np.allclose(res["q_val"], torch_ref(q, qw), rtol=0, atol=1e-13)
+    assert np.allclose(res["kv_val"], torch_ref(kv, kw), rtol=0, atol=1e-13)
+
+
+def pin_store_closed_forms(lib):
+    """eps = 0: a constant row c normalises to sign(c) * w; a row with one
+    non-zero element x_0 to sqrt(D) * sign(x_0) * w_0 there; a quarter turn
+    (cos 0, sin 1) maps the pair (a, b) to (-b, a); R = 0 leaves the norm."""
+    D, R = 16, 4
+    w = bf16_bits(np.linspace(0.5, 2.0, D))
+    wf = bits_to_f64(w)
+    q = bf16_bits(np.stack([np.full(D, -3.0), np.eye(D)[0] * 5.0])[None])      # N=1, H=2
+    kv = bf16_bits(np.full((1, D), 0.125))
+    cos = np.zeros((1, R // 2), np.float32)
+    sin = np.ones((1, R // 2), np.float32)
+    res = oracle.qk_norm_rope_store(q, kv, w, w, cos, sin, [0], [0], 0.0, 4, 4, lib=lib)
+    quarter = lambda y: np.concatenate([y[:D - R], np.stack([-y[D - R + 1::2], y[D - R::2]], 1).ravel()])
+    assert np.array_equal(res["q_val"][0, 0], quarter(-wf))
+    one_hot = np.zeros(D)
+    one_hot[0] = math.sqrt(D) * wf[0]
+    assert np.allclose(res["q_val"][0, 1], quarter(one_hot), rtol=1e-15, atol=0)
+    assert np.array_equal(res["kv_val"][0], quarter(wf))
+    res0 = oracle.qk_norm_rope_store(q, kv, w, w, np.zeros((1, 0), np.float32),
+                                     np.zeros((1, 0), np.float32), [0], [0], 0.0, 4, 4, lib=lib)
+    assert np.array_equal(res0["kv_val"][0], wf)
+
+
+def pin_store_rotation_invariants(lib):
+    """Rotating by an angle and then by its negative restores the row; each
+    pair's length is kept; rotation at position p uses row p of the caches."""
+    rng = np.random.default_rng(82)
+    N, H, D, R = 4, 2, 16, 8
+    q, kv, qw, kw, cos, sin, pos = store_case(rng, N, H, D, R, max_pos=8)
+    plain = oracle.qk_norm_rope_store(q, kv, qw, kw, np.ones_like(cos), np.zeros_like(sin),
+                                      pos, np.arange(N), 1e-6, 8, 64, lib=lib)
+    rot = oracle.qk_norm_rope_store(q, kv, qw, kw, cos, sin, pos, np.arange(N), 1e-6, 8, 64, lib=lib)
+    y0, y1 = plain["q_val"][..., D - R:], rot["q_val"][..., D - R:]
+    n0 = y0[..., 0::2] ** 2 + y0[..., 1::2] ** 2
+    n1 = y1[..., 0::2] ** 2 + y1[..., 1::2] ** 2
+    c = cos[pos].astype(np.float64)[:, None, :]
+    s = sin[pos].astype(np.float64)[:, None, :]
+    assert np.allclose(n1, n0 * (c * c + s * s), rtol=1e-12, atol=0)  # fp32 caches: c^2+s^2 ~ 1
+    assert np.array_equal(plain["q_val"][..., :D - R], rot["q_val"][..., :D - R])
+    back_a = y1[..., 0::2] * c + y1[..., 1::2] * s
+    back_b = y1[..., 1::2] * c - y1[..., 0::2] * s
+    assert np.allclose(back_a, y0[..., 0::2] * (c * c + s * s), rtol=1e-12, atol=1e-12)
+    assert np.allclose(back_b, y0[..., 1::2] * (c * c + s * s), rtol=1e-12, atol=1e-12)
+
+
+def pin_store_slots(lib):
+    """Ring slot = state_slot * win + pos mod win (worked by hand); padded
+    tokens store nothing and give q = 0; a position outside the caches or a
+    slot outside the SWA region raises its status bit."""
+    D, R = 8, 2
+    rng = np.random.default_rng(83)
+    q, kv, qw, kw, cos, sin, _ = store_case(rng, 6, 1, D, R, max_pos=300)
+    pos = [0, 129, 255, 7, 300, 1]
+    ss = [0, 2, 1, -1, 0, 5]
+    res = oracle.qk_norm_rope_store(q, kv, qw, kw, cos, sin, pos, ss, 1e-6, 128, 5 * 128, lib=lib)
+    # token 0: 0*128 + 0; token 1: 2*128 + 1; token 2: 128 + 127; 3 padded; 4 pos out of range;
+    # token 5: 5*128 + 1 = 641 >= 640 -> not stored
+    assert res["slot"].tolist() == [0, 257, 255, -1, -1, -1]
+    assert res["status"] == 3
+    assert not res["q_val"][3].any() and not res["q_val"][4].any() and not res["kv_val"][4].any()
+    assert res["q_val"][5].any() and res["kv_val"][5].any()
+
+
+def pin_bf16_rne(lib):
+    """Round to nearest even bf16: equal to torch's float32 -> bfloat16
+    conversion on values exact in fp32 (no double rounding possible there),
+    and correct on hand cases where rounding through fp32 would not be."""
+    rng = np.random.default_rng(84)
+    v = np.concatenate([rng.standard_normal(4000) * 10.0 ** rng.integers(-40, 38, 4000),
+                        np.float32(1.0) + np.arange(-64, 64) * np.float32(2.0 ** -9)]).astype(np.float32)
+    v = v[np.isfinite(v)]
+    want = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.bf16_rne(v.astype(np.float64), lib=lib), want)
+    hand = [(1.0 + 2.0 ** -8, 0x3F80), (1.0 + 3 * 2.0 ** -8, 0x3F82),
+            (1.0 + 2.0 ** -8 + 2.0 ** -30, 0x3F81), (-(1.0 + 2.0 ** -8 + 2.0 ** -40), 0xBF81),
+            (2.0 ** -133, 0x0001), (2.0 ** -134, 0x0000), (3.0 * 2.0 ** -134, 0x0002),
+            (0.0, 0x0000), (-0.0, 0x8000), (1e39, 0x7F80), (-3.0, 0xC040)]
+    got = oracle.bf16_rne([v for v, _ in hand], lib=lib)
+    assert got.tolist() == [b for _, b in hand]
+
+
+def pin_e4m3_rne(lib):
+    """E4M3 rounding: every code's value maps back to that code, and a dense
+    sweep of fp32 values (midpoints included) equals torch's float8_e4m3fn
+    conversion after clamping to +-448; hand cases for ties and saturation."""
+    vals = oracle.e4m3_values(lib)
+    for c in range(256):
+        if not np.isnan(vals[c]) and c != 0x80:
+            assert oracle.e4m3_rne(vals[c], lib=lib) == c
+    fin = np.sort(np.unique(vals[~np.isnan(vals)]))
+    mids = (fin[1:] + fin[:-1]) / 2
+    rng = np.random.default_rng(85)
+    sweep = np.concatenate([fin, mids, np.nextafter(mids, np.inf), np.nextafter(mids, -np.inf),
+                            rng.uniform(-500, 500, 3000), rng.standard_normal(3000) * 1e-2]).astype(np.float32)
+    want = torch.from_numpy(sweep).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_rne(float(x), lib=lib) for x in sweep], np.uint8)
+    zero = sweep == 0  # the sign of a zero is kept by both; compare magnitudes there
+    assert np.array_equal(got[~zero], want[~zero]) and np.all((got[zero] & 0x7F) == 0)
+    # 17 = 1.0625 * 2^4: exponent field 11, mantissa tie 0.5 -> even 0: 0x58
+    hand = [(2.0 ** -10, 0x00), (3 * 2.0 ** -10, 0x02), (470.0, 0x7E), (-1e9, 0xFE), (1.0, 0x38),
+            (1.0625, 0x38), (1.1875, 0x3A), (17.0, 0x58), (2.0 ** -9, 0x01), (-0.0, 0x80)]
+    assert [oracle.e4m3_rne(v, lib=lib) for v, _ in hand] == [c for _, c in hand]
+
+
+def pin_fp8_scale(lib):
+    """Row scale 2^e, e the least integer with 448 * 2^e >= amax (hand cases at
+    and around the powers of two), and quantised rows that dequantise to
+    within half a code step of every value, with the largest at |code| > 224."""
+    hand = {0.0: 0, 448.0: 0, 448.0 * (1 + 2.0 ** -40): 1, 1.0: -8, 1.75: -8, 1.7500001: -7,
+            224.0: -1, 3.5: -7, 448.0 * 2.0 ** -130: -126}
+    assert [oracle.fp8_scale_exponent(a, lib=lib) for a in hand] == list(hand.values())
+    rng = np.random.default_rng(86)
+    y = rng.standard_normal((64, 32)) * 10.0 ** rng.integers(-3, 4, (64, 1))
+    y[3] = 0.0
+    codes, scale = oracle.fp8_quantise_rows(y, lib=lib)
+    assert scale[3] == 1.0 and not (codes[3] & 0x7F).any()
+    table = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    deq = table[codes] * scale[:, None]
+    for r in range(64):
+        if r == 3:
+            continue
+        amax = np.abs(y[r]).max()
+        assert 448.0 * scale[r] >= amax > 224.0 * scale[r]
+        x = y[r] / scale[r]
+        step = np.where(np.abs(x) < 2.0 ** -6, 2.0 ** -9, 2.0 ** (np.floor(np.log2(np.maximum(np.abs(x), 1e-300))) - 3))
+        assert np.all(np.abs(deq[r] - y[r]) <= 0.5 * step * scale[r] * (1 + 1e-12))
+
+
+STORE_PINS = [pin_store_matches_torch, pin_store_closed_forms, pin_store_rotation_invariants,
+              pin_store_slots]
+ROUNDING_PINS = [pin_bf16_rne, pin_e4m3_rne, pin_fp8_scale]
+
 DECODE_PINS = [pin_sdpa, pin_sink_minus_inf_is_softmax, pin_single_slot, pin_duplicate_adds_ln2,
                pin_zero_length, pin_permutation, pin_sink_factor, pin_scale_zero, pin_convexity,
                pin_hard_attention_limit, pin_sink_plus_inf, pin_token_subset]
 BUILDER_PINS = [pin_builder_golden, pin_builder_ring_closed_form, pin_builder_capacity]
 VALIDATE_PINS = [pin_validate]
-ALL_PINS = DECODE_PINS + BUILDER_PINS + VALIDATE_PINS + FP8_PINS
+ALL_PINS = DECODE_PINS + BUILDER_PINS + VALIDATE_PINS + FP8_PINS + STORE_PINS + ROUNDING_PINS
 
 
 def failing_pins(lib, pins=ALL_PINS):

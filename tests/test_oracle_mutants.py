@@ -45,6 +45,34 @@ MUTANTS = {
     "fp8_scale_of_wrong_row": ("return oracle_e4m3_to_double(p->fp8[(size_t)s * D + d]) * (double)p->scale[s];",
                                "return oracle_e4m3_to_double(p->fp8[(size_t)s * D + d]) * (double)p->scale[0];",
                                pins.FP8_PINS),
+    # q/kv norm + RoPE + store
+    "rms_drops_eps": ("sqrt(ss / D + (double)eps)", "sqrt(ss / D)", pins.STORE_PINS),
+    "rms_sum_not_mean": ("sqrt(ss / D + (double)eps)", "sqrt(ss + (double)eps)", pins.STORE_PINS),
+    "rms_wrong_weight": ("const uint16_t* w = r < H ? q_norm_w : kv_norm_w;",
+                         "const uint16_t* w = q_norm_w;", pins.STORE_PINS),
+    "rope_sign": ("y[d] = a * c - b * s;", "y[d] = a * c + b * s;", pins.STORE_PINS),
+    "rope_leading_dims": ("const int d = D - R + 2 * i;", "const int d = 2 * i;", pins.STORE_PINS),
+    "rope_neox_pairs": ("const double a = y[d], b = y[d + 1];\n        y[d] = a * c - b * s;\n        y[d + 1] = b * c + a * s;",
+                        "const double a = y[D - R + i], b = y[D - R / 2 + i];\n        y[D - R + i] = a * c - b * s;\n        y[D - R / 2 + i] = b * c + a * s;",
+                        pins.STORE_PINS),
+    "rope_cos_sin_swapped": ("const double c = cos_cache[", "const double c = sin_cache[", pins.STORE_PINS),
+    "rope_wrong_position": ("cos_cache[(size_t)pos * (R / 2) + i]", "cos_cache[(size_t)0 * (R / 2) + i]",
+                            pins.STORE_PINS),
+    "ring_without_mod": ("state_slot[t] * win + pos % win;", "state_slot[t] * win + pos;",
+                         pins.STORE_PINS),
+    "bf16_truncates": ("const double r = rint(a / quantum) * quantum;",
+                       "const double r = trunc(a / quantum) * quantum;", pins.ROUNDING_PINS),
+    "bf16_ties_away": ("const double r = rint(a / quantum) * quantum;",
+                       "const double r = round(a / quantum) * quantum;", pins.ROUNDING_PINS),
+    "e4m3_ties_away": ("double r = rint(a / quantum) * quantum;\n  if (r > 448.0)",
+                       "double r = round(a / quantum) * quantum;\n  if (r > 448.0)", pins.ROUNDING_PINS),
+    "e4m3_no_saturation": ("if (r > 448.0) r = 448.0;", "(void)0;", pins.ROUNDING_PINS),
+    "e4m3_subnormal_binade": ("if (E < -6) E = -6;", "if (E < -7) E = -7;", pins.ROUNDING_PINS),
+    "fp8_scale_floor": ("int e = (int)ceil(log2(amax / 448.0));\n  while (ldexp(448.0, e) < amax) ++e;",
+                        "int e = (int)floor(log2(amax / 448.0));", pins.ROUNDING_PINS),
+    "fp8_scale_one_too_big": ("while (ldexp(448.0, e - 1) >= amax) --e;\n  return e",
+                              "while (ldexp(448.0, e - 1) >= amax) --e;\n  ++e;\n  return e",
+                              pins.ROUNDING_PINS),
     # builder
     "ring_newest_first": ("(int64_t)swa_head[t] - n_swa + 1 + j", "(int64_t)swa_head[t] - j",
                           pins.BUILDER_PINS),
