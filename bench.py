@@ -18,6 +18,11 @@ pool.  `--config` picks another of the five workloads.
             library's timing hook): algorithmic bytes / time vs measured HBM
   cpu_baseline  the fp64 CPU oracle on the host cores (bounded sample)
 
+--path store times the step that fills the pool instead (per-head RMSNorm of
+q, RMSNorm of the new KV row, GPT-J RoPE, store into the SWA ring slot: one
+kernel); --path layer times the three calls of a decode layer's attention
+together (store, index build, decode) as one CUDA graph.
+
 --impl reference times the fp64 CPU oracle instead (same config and metric).
 Under torchrun (N>1 GPUs) every rank decodes its own batch of the same
 recipe (seeded per rank; tokens are independent: weak scaling, no collective
@@ -46,6 +51,8 @@ if ROOT not in sys.path:
 from sink_sda_decode_gb300 import inputs  # noqa: E402
 
 METRIC = "decode tokens/s and gathered-KV GB/s; % of binding roofline (HBM vs bf16)"
+STORE_METRIC = "q/kv RMSNorm + RoPE + SWA store tokens/s; % of HBM roofline"
+BUILDER_KEYS = ("state_slot", "swa_len", "swa_head", "comp_indptr", "comp_block", "comp_slot")
 DEFAULT_CONFIG = 1
 L2_FLUSH_BYTES = 256 << 20
 HBM_FALLBACK_GBS = 6800.0
@@ -233,53 +240,106 @@ def algorithmic_bytes(w, kv="bf16"):
     return L * row + 2 * w.N * w.H * w.D * 2 + L * 4 + (w.N + 1) * 4
 
 
+def store_algorithmic_bytes(w, rope_dim, kv="bf16"):
+    """Bytes the store step must move: q read and written (bf16), the new KV
+    row read (bf16) and written to the pool (bf16, or D codes + a 4-byte
+    scale), each token's position and state slot, its RoPE cache rows (R/2
+    cos + R/2 sin, fp32) and the two norm weights once."""
+    row_out = w.D * 2 if kv == "bf16" else w.D + 4
+    per_token = 2 * w.H * w.D * 2 + w.D * 2 + row_out + 4 + 4 + rope_dim * 4
+    return w.N * per_token + 2 * w.D * 2
+
+
 def algorithmic_flops(w):
     return 4 * w.H * w.D * int(w.total_len)
 
 
 # ----------------------------------------------------------------------------- GPU arm
 class Step:
-    """Device-resident inputs and buffers of one hot-path step."""
+    """Device-resident inputs and buffers of one step of the chosen path:
+    "decode" (index build + decode), "store" (q/kv norm + RoPE + SWA store)
+    or "layer" (store, then build + decode on the stored pool and the rotated
+    q).  `ins` holds the per-step inputs, the tensors the end-to-end run
+    copies from the host."""
 
-    def __init__(self, w, device, pool=None):
+    def __init__(self, w, device, pool=None, path="decode"):
         import sink_sda_decode_gb300 as sda
         self.sda = sda
         self.w = w
+        self.path = path
         self.pool = pool  # an FP8 pool (inputs.Fp8Pool) replaces the bf16 one
         self.dev = device
-        self.bi = w.builder_inputs(device)
-        self.capacity = w.N * w.win + int(w.comp_block.size)
-        self.kv_indices = torch.empty(max(self.capacity, 1), dtype=torch.int32, device=device)
-        self.kv_indptr = torch.empty(w.N + 1, dtype=torch.int32, device=device)
-        self.status = torch.empty(1, dtype=torch.int32, device=device)
-        self.out = torch.empty_like(w.q)
-        size = (sda.workspace_size if pool is None else sda.workspace_size_fp8)(
-            w.N, w.H, w.D, self.capacity)
-        self.ws = torch.empty(size, dtype=torch.uint8, device=device)
+        self.ins = {"q": w.q}
+        if path != "store":
+            self.ins.update(w.builder_inputs(device))
+            self.capacity = w.N * w.win + int(w.comp_block.size)
+            self.kv_indices = torch.empty(max(self.capacity, 1), dtype=torch.int32, device=device)
+            self.kv_indptr = torch.empty(w.N + 1, dtype=torch.int32, device=device)
+            self.status = torch.empty(1, dtype=torch.int32, device=device)
+            self.out = torch.empty_like(w.q)
+            size = (sda.workspace_size if pool is None else sda.workspace_size_fp8)(
+                w.N, w.H, w.D, self.capacity)
+            self.ws = torch.empty(size, dtype=torch.uint8, device=device)
+        if path != "decode":
+            self.si = inputs.store_inputs(w)
+            self.ins["kv_new"] = self.si.kv_new
+            self.ins["positions"] = self.si.positions
+            self.ins.setdefault("state_slot", self.si.state_slot)
+            self.q_rot = torch.empty_like(w.q)
+            self.store_status = torch.empty(1, dtype=torch.int32, device=device)
+        self.result = self.q_rot if path == "store" else self.out
+        self.launches_per_step = {"decode": 6, "store": 1, "layer": 7}[path]
 
-    def run(self, q=None, bi=None, out=None, stream=None):
+    @property
+    def rope_dim(self):
+        return self.si.cos_cache.shape[1] * 2
+
+    def run(self, ins=None, stream=None, timing=None):
+        """One step.  `timing` = (before, after) events: recorded around the
+        store kernel on the store path, around the attention kernel otherwise."""
         w = self.w
-        bi = bi or self.bi
-        self.sda.build_indices(**bi, win=w.win, k_per_block=w.k_per_block, swa_pages=w.swa_pages,
+        ins = ins or self.ins
+        q = ins["q"]
+        if self.path != "decode":
+            si = self.si
+            if timing and self.path == "store":
+                self.sda.set_timing_events(*timing)
+            self.sda.qk_norm_rope_swa_store(
+                q, ins["kv_new"], si.q_norm_w, si.kv_norm_w, si.cos_cache, si.sin_cache,
+                ins["positions"], ins["state_slot"], eps=si.eps, win=w.win,
+                swa_pages=w.swa_pages, unified_kv=w.unified_kv if self.pool is None else None,
+                kv_fp8=None if self.pool is None else self.pool.codes,
+                kv_scale=None if self.pool is None else self.pool.scale, q_out=self.q_rot,
+                status=self.store_status, stream=stream)
+            self.sda.set_timing_events(None, None)
+            q = self.q_rot
+        if self.path == "store":
+            return
+        self.sda.build_indices(**{k: ins[k] for k in BUILDER_KEYS}, win=w.win,
+                               k_per_block=w.k_per_block, swa_pages=w.swa_pages,
                                total_pages=w.total_pages, capacity=self.capacity,
                                kv_indices=self.kv_indices, kv_indptr=self.kv_indptr,
                                status=self.status, stream=stream)
+        if timing:
+            self.sda.set_timing_events(*timing)
         if self.pool is None:
-            self.sda.decode(q if q is not None else w.q, w.unified_kv, self.kv_indices,
-                            self.kv_indptr, w.attn_sink, w.softmax_scale,
-                            out=self.out if out is None else out, workspace=self.ws, stream=stream)
+            self.sda.decode(q, w.unified_kv, self.kv_indices, self.kv_indptr, w.attn_sink,
+                            w.softmax_scale, out=self.out, workspace=self.ws, stream=stream)
         else:
-            self.sda.decode_fp8(q if q is not None else w.q, self.pool.codes, self.pool.scale,
-                                self.kv_indices, self.kv_indptr, w.attn_sink, w.softmax_scale,
-                                out=self.out if out is None else out, workspace=self.ws,
-                                stream=stream)
+            self.sda.decode_fp8(q, self.pool.codes, self.pool.scale, self.kv_indices,
+                                self.kv_indptr, w.attn_sink, w.softmax_scale, out=self.out,
+                                workspace=self.ws, stream=stream)
+        self.sda.set_timing_events(None, None)
 
-    # kernels of this library launched per step: 3 (index build) + plan + attention + combine
-    launches_per_step = 6
+    def check_status(self):
+        if self.path != "store" and int(self.status.item()) != 0:
+            raise RuntimeError(f"index builder status {int(self.status.item())}")
+        if self.path != "decode" and int(self.store_status.item()) != 0:
+            raise RuntimeError(f"store status {int(self.store_status.item())}")
 
 
 def gpu_arm(args, w, device, ws, rank, pool=None):
-    step = Step(w, device, pool)
+    step = Step(w, device, pool, getattr(args, "path", "decode"))
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     s = torch.cuda.Stream(device)
     s.wait_stream(torch.cuda.current_stream(device))
@@ -288,9 +348,7 @@ def gpu_arm(args, w, device, ws, rank, pool=None):
             step.run(stream=s)
     torch.cuda.current_stream(device).wait_stream(s)
     torch.cuda.synchronize(device)
-    st = int(step.status.item())
-    if st != 0:
-        raise RuntimeError(f"index builder status {st}")
+    step.check_status()
     # whole step as one CUDA graph
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
@@ -320,26 +378,25 @@ def gpu_arm(args, w, device, ws, rank, pool=None):
     step_ms = [a.elapsed_time(b) for a, b in evs]
     ms_per_step = sum(step_ms) / len(step_ms)
 
-    # ---- timed region 2: the attention kernel alone (library timing hook)
+    # ---- timed region 2: the dominant kernel alone (library timing hook)
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     barrier()
     with torch.cuda.stream(s):
         for a, b in kev:
             flush.zero_()
-            step.sda.set_timing_events(a, b)
-            step.run(stream=s)
-        step.sda.set_timing_events(None, None)
+            step.run(stream=s, timing=(a, b))
     barrier()
     kernel_ms = sum(a.elapsed_time(b) for a, b in kev) / len(kev)
 
     # ---- timed region 3: end to end from pinned host memory.  The step's
-    # inputs (q and the builder's descriptors) sit packed in one pinned host
-    # buffer: one H2D copy, the public build_indices + decode calls on views
-    # of the device copy, one D2H copy of out -- replayed as one CUDA graph,
-    # as a serving loop replays its decode step.
-    parts = [w.q.reshape(-1).view(torch.uint8)] + [v.reshape(-1).view(torch.uint8)
-                                                    for v in step.bi.values()]
+    # inputs (q, the builder's descriptors, the new KV rows and positions)
+    # sit packed in one pinned host buffer: one H2D copy, the public calls on
+    # views of the device copy, one D2H copy of the result (out, or the
+    # rotated q of the store path) -- replayed as one CUDA graph, as a
+    # serving loop replays its decode step.
+    names = list(step.ins)
+    parts = [step.ins[k].reshape(-1).view(torch.uint8) for k in names]
     offs, total = [], 0
     for t_ in parts:
         offs.append(total)
@@ -348,17 +405,16 @@ def gpu_arm(args, w, device, ws, rank, pool=None):
     for o, t_ in zip(offs, parts):
         h_in[o:o + t_.numel()].copy_(t_.cpu())
     d_in = torch.empty_like(h_in, device=device)
-    q_v = d_in[offs[0]:offs[0] + parts[0].numel()].view(w.q.dtype).view(w.q.shape)
-    bi_v = {k: d_in[o:o + v.numel() * 4].view(torch.int32)
-            for (k, v), o in zip(step.bi.items(), offs[1:])}
-    out_h = torch.empty(w.q.shape, dtype=w.q.dtype, pin_memory=True)
+    views = {k: d_in[o:o + p.numel()].view(step.ins[k].dtype).view(step.ins[k].shape)
+             for k, o, p in zip(names, offs, parts)}
+    out_h = torch.empty(step.result.shape, dtype=step.result.dtype, pin_memory=True)
     h2d = sum(t_.numel() for t_ in parts)
     d2h = out_h.numel() * out_h.element_size()
 
     def e2e_step():
         d_in.copy_(h_in, non_blocking=True)
-        step.run(q=q_v, bi=bi_v, stream=s)
-        out_h.copy_(step.out, non_blocking=True)
+        step.run(ins=views, stream=s)
+        out_h.copy_(step.result, non_blocking=True)
 
     with torch.cuda.stream(s):
         for _ in range(max(args.warmup, 3)):
@@ -380,7 +436,8 @@ def gpu_arm(args, w, device, ws, rank, pool=None):
     barrier()
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / len(e2e_ev)
     return dict(ms_per_step=ms_per_step, kernel_ms=kernel_ms, e2e_ms=e2e_ms, clocks=cs.summary(),
-                h2d=h2d, d2h=d2h, step=step)
+                h2d=h2d, d2h=d2h, launches_per_step=step.launches_per_step,
+                rope_dim=step.rope_dim if step.path != "decode" else None)
 
 
 # ----------------------------------------------------------------------------- job-wide report
@@ -400,49 +457,73 @@ def reduce_over_ranks(times_ms, units, ws, device):
     return [float(x) for x in t.cpu()], float(u.cpu().item())
 
 
+STEP_TEXT = {
+    "decode": "index build + decode (plan, attention, combine) as one CUDA graph",
+    "store": "q/kv RMSNorm + GPT-J RoPE + SWA ring store (one kernel) as one CUDA graph",
+    "layer": "q/kv norm + RoPE + SWA store, index build, decode as one CUDA graph",
+}
+
+
 def report_line(args, w, ws, ms_step, ms_kernel, ms_e2e, tokens_total, r):
     """The JSON line of the GPU arm from job-wide numbers (rank 0 prints it).
 
     `value` and `e2e.value` are all ranks' tokens over the slowest rank's step
-    time; the roofline is the attention kernel of this rank's workload, whose
-    shape every rank shares."""
+    time; the roofline is the dominant kernel of this rank's workload (the
+    attention kernel, or the store kernel on the store path), whose shape
+    every rank shares."""
     hbm, bf16, peak_src = peaks()
     kv = getattr(args, "kv", "bf16")
-    nbytes = algorithmic_bytes(w, kv)
-    flops = algorithmic_flops(w)
+    path = getattr(args, "path", "decode")
     value = tokens_total / (ms_step * 1e-3)
-    t_hbm = nbytes / (hbm * 1e9)
-    t_tc = flops / (bf16 * 1e12)
-    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    if path == "store":
+        nbytes = store_algorithmic_bytes(w, r["rope_dim"], kv)
+        flops = 0
+        bound = "hbm"
+        kernel = "q/kv norm + RoPE + SWA store kernel"
+        traffic_key = "store_" + args.config
+    else:
+        nbytes = algorithmic_bytes(w, kv)
+        flops = algorithmic_flops(w)
+        bound = "hbm" if nbytes / (hbm * 1e9) >= flops / (bf16 * 1e12) else "tensor"
+        kernel = "sda decode attention kernel"
+        traffic_key = args.config
+    if kv != "bf16":
+        traffic_key += "_fp8"
+    t_bound = nbytes / (hbm * 1e9) if bound == "hbm" else flops / (bf16 * 1e12)
     # achieved rate of the binding resource: GB/s of algorithmic bytes, or
     # TFLOP/s of algorithmic FLOPs
     achieved = (nbytes / 1e9 if bound == "hbm" else flops / 1e12) / (ms_kernel * 1e-3)
-    return {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+    line = {
+        "metric": STORE_METRIC if path == "store" else METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
         "config": {"workload": w.name, "N": w.N, "H": w.H, "D": w.D,
                    "total_slots": int(w.total_len), "pool_slots": w.total_pages,
                    "kv": "bf16" if kv == "bf16" else "fp8 e4m3, fp32 scale per row",
-                   "step": "index build + decode (plan, attention, combine) as one CUDA graph",
+                   "path": path, "step": STEP_TEXT[path],
                    "l2": "flushed before every timed step (256 MiB write)",
                    "parallelism": f"dp{ws} (independent token batches)"},
-        "gathered_kv_gbs": int(w.total_len) * (w.D * 2 if kv == "bf16" else w.D + 4)
-                           / (ms_step * 1e-3) / 1e9,
         "roofline": {"bound": bound, "achieved": achieved,
                      "peak": hbm if bound == "hbm" else bf16,
                      "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
                      "frac": achieved / (hbm if bound == "hbm" else bf16),
-                     "traffic": ncu_traffic(args.config if kv == "bf16" else args.config + "_fp8"),
+                     "traffic": ncu_traffic(traffic_key),
                      "peak_source": peak_src,
-                     "kernel": "sda decode attention kernel", "kernel_ms": ms_kernel,
+                     "kernel": kernel, "kernel_ms": ms_kernel,
                      "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
-                     "step_frac_of_roofline": max(t_hbm, t_tc) / (ms_step * 1e-3)},
+                     "step_frac_of_roofline": t_bound / (ms_step * 1e-3)},
         "e2e": {"value": tokens_total / (ms_e2e * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
-        "gpu_launches": Step.launches_per_step * args.steps,
+        "gpu_launches": r["launches_per_step"] * args.steps,
         "clocks": r["clocks"],
     }
+    if path == "store":
+        line["config"]["rope_dim"] = r["rope_dim"]
+    else:
+        line["gathered_kv_gbs"] = (int(w.total_len) * (w.D * 2 if kv == "bf16" else w.D + 4)
+                                   / (ms_step * 1e-3) / 1e9)
+    return line
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -469,14 +550,47 @@ def oracle_sample(w, budget_tokens):
     return np.sort(rng.choice(w.N, k, replace=False))
 
 
-def time_oracle(w, seconds, max_tokens, pool=None):
+def oracle_job(w, toks, pool=None, path="decode"):
+    """The oracle's share of one step on the token sample `toks`, as a
+    callable: the store (exact values, then the rounding the pool stores)
+    and / or the decode."""
+    import oracle
+    calls = []
+    if path != "decode":
+        si = inputs.store_inputs(w)
+        bits = inputs.bf16_to_bits
+        sargs = (w.q_bits()[toks], bits(si.kv_new)[toks], bits(si.q_norm_w), bits(si.kv_norm_w),
+                 si.cos_cache.cpu().numpy(), si.sin_cache.cpu().numpy(),
+                 si.positions.cpu().numpy()[toks], si.state_slot.cpu().numpy()[toks], si.eps,
+                 w.win, w.swa_pages)
+
+        def store():
+            res = oracle.qk_norm_rope_store(*sargs)
+            oracle.bf16_rne(res["q_val"])
+            if pool is None:
+                oracle.bf16_rne(res["kv_val"])
+            else:
+                oracle.fp8_quantise_rows(res["kv_val"])
+        calls.append(store)
+    if path != "store":
+        oargs = oracle_inputs(w, toks, pool)
+        calls.append(lambda: oracle_decode(oargs, w))
+    return lambda: [c() for c in calls]
+
+
+def oracle_budget(w, path):
+    """Tokens per oracle pass: all of them where a pass is cheap."""
+    return w.N if path == "store" or w.total_len <= 200000 else 16
+
+
+def time_oracle(w, seconds, max_tokens, pool=None, path="decode"):
     import oracle
     toks = oracle_sample(w, max_tokens)
-    args = oracle_inputs(w, toks, pool)
+    job = oracle_job(w, toks, pool, path)
     done_tokens, t0 = 0, time.perf_counter()
     passes = 0
     while True:
-        oracle_decode(args, w)
+        job()
         done_tokens += len(toks)
         passes += 1
         el = time.perf_counter() - t0
@@ -497,6 +611,9 @@ def main():
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="pool format: bf16 rows, or FP8 E4M3 codes with one fp32 scale per row "
                          "(the workload's pool quantised row by row)")
+    ap.add_argument("--path", choices=["decode", "store", "layer"], default="decode",
+                    help="decode: index build + decode; store: q/kv norm + RoPE + SWA store; "
+                         "layer: all three")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -510,22 +627,23 @@ def main():
         w = inputs.config(cfg_idx, device="cuda" if torch.cuda.is_available() else "cpu")
         import oracle
         pool = inputs.fp8_pool(w) if args.kv == "fp8" else None
-        toks = oracle_sample(w, 16 if w.total_len > 200000 else w.N)
-        oargs = oracle_inputs(w, toks, pool)
+        toks = oracle_sample(w, oracle_budget(w, args.path))
+        job = oracle_job(w, toks, pool, args.path)
         for _ in range(args.warmup):
-            oracle_decode(oargs, w)
+            job()
         t0 = time.perf_counter()
         for _ in range(args.steps):
-            oracle_decode(oargs, w)
+            job()
         el = time.perf_counter() - t0
         tps = len(toks) * args.steps / el
         sample = f"{len(toks)} of {w.N} tokens per step"
-        line = {"metric": METRIC, "value": tps, "unit": "tokens/s", "impl": "reference",
+        line = {"metric": STORE_METRIC if args.path == "store" else METRIC, "value": tps,
+                "unit": "tokens/s", "impl": "reference",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": w.name, "N": w.N, "H": w.H, "D": w.D,
-                           "total_slots": w.total_len, "kv": args.kv},
+                           "total_slots": w.total_len, "kv": args.kv, "path": args.path},
                 "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": oracle.num_threads(),
                                  "kind": "oracle", "sample": sample},
                 "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -550,7 +668,7 @@ def main():
     line = report_line(args, w, ws, ms_step, ms_kernel, ms_e2e, tokens_total, r)
     if not args.no_cpu_baseline and ws == 1:
         tps, cores, toks, passes, el = time_oracle(w, args.cpu_seconds,
-                                                   16 if w.total_len > 200000 else w.N, pool)
+                                                   oracle_budget(w, args.path), pool, args.path)
         line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": f"{len(toks)} of {w.N} tokens x {passes} passes, "
                                           f"{el:.1f} s"}

@@ -191,10 +191,12 @@ sda_status sda_decode_kernel(int H, int D, int* kernel);
 sda_status sda_decode_error_flag(const void* workspace, int32_t* device_flag, void* stream);
 
 /*
- * Timing hook.  When both events are non-NULL, every later sda_decode made
- * from the calling host thread records `before` on its stream immediately
- * before its attention kernel and `after` immediately after it, so that the
- * caller can time that kernel alone (cudaEventElapsedTime).  The events are
+ * Timing hook.  When both events are non-NULL, every later sda_decode /
+ * sda_decode_fp8 made from the calling host thread records `before` on its
+ * stream immediately before its attention kernel and `after` immediately
+ * after it, and every later sda_qk_norm_rope_swa_store(_fp8) does the same
+ * around its kernel, so that the caller can time that kernel alone
+ * (cudaEventElapsedTime).  The events are
  * cudaEvent_t handles created and owned by the caller.  NULL, NULL turns the
  * hook off.  No effect on results.
  */
@@ -245,6 +247,67 @@ sda_status sda_build_indices(const int32_t* state_slot, const int32_t* swa_len,
 sda_status sda_validate_indices(const int32_t* kv_indices, int64_t total_indices,
                                 const int32_t* kv_indptr, int N, int64_t total_pages,
                                 int32_t* status, void* stream);
+
+/*
+ * Fused q / kv RMSNorm + RoPE + SWA ring store: the step of a decode layer
+ * that fills the pool sda_decode reads.  Source: the sglang PR 25898 summary
+ * page ("修复 DSV4 在 AMD GPU 上的运行时崩溃与 JIT 不兼容"), section "关键文件"
+ * (fused_qk_norm_rope_store.py: Q per-head RMSNorm, KV RMSNorm, RoPE, FP8
+ * quantisation and the paged SWA store in one kernel), section "关键符号"
+ * (_batched_rmsnorm, _gptj_rotate, fused_qk_norm_rope_swa_store) and
+ * "实现拆解" item 2 (cos_cache / sin_cache); the ring slot state_slot * win +
+ * ring is the paged_decode.py docstring's (PR 28392 page).
+ *
+ * Arguments (device pointers unless noted; all 16-byte aligned except
+ * positions, state_slot, status):
+ *   q          [N, H, D] bf16, the step's query heads (read)
+ *   kv         [N, D] bf16, the step's new latent row per token (key = value)
+ *   q_norm_w, kv_norm_w  [D] bf16 RMSNorm weights (q's shared by all heads)
+ *   cos_cache, sin_cache [max_pos, rope_dim / 2] fp32, row = position
+ *   positions  [N] int32, state_slot [N] int32 (< 0: padded token)
+ *   D % 8 == 0, 8 <= D <= 2048; rope_dim % 8 == 0, 0 <= rope_dim <= D;
+ *   eps >= 0 finite; win > 0; 0 <= swa_pages <= total_pages.
+ *   q_out      [N, H, D] bf16; may be q itself, must not partly overlap it.
+ * Per token t with state_slot[t] >= 0 and 0 <= pos = positions[t] < max_pos,
+ * for every row x (the H rows of q[t] with q_norm_w, and kv[t] with kv_norm_w),
+ * in fp32:
+ *   y_d = x_d / sqrt(mean_d x_d^2 + eps) * w_d
+ *   for i < rope_dim/2, d = D - rope_dim + 2i ("GPT-J": adjacent pairs):
+ *     (y_d, y_{d+1}) <- (y_d c - y_{d+1} s, y_{d+1} c + y_d s),
+ *     c = cos_cache[pos][i], s = sin_cache[pos][i]
+ *   q_out[t] = y rounded to nearest even bf16;
+ *   the KV row goes to slot = state_slot[t] * win + pos mod win.
+ * Padded tokens (and real tokens whose position is outside [0, max_pos)) get
+ * q_out = 0 and store nothing.  *status (device int32, overwritten): bit 1 =
+ * a real token had a position outside [0, max_pos); bit 2 = a slot fell
+ * outside [0, swa_pages) (that row is not stored).  Two tokens with the same
+ * slot in one call race (the caller's contract: one new entry per ring slot).
+ */
+sda_status sda_qk_norm_rope_swa_store(const void* q, const void* kv, const void* q_norm_w,
+                                      const void* kv_norm_w, const float* cos_cache,
+                                      const float* sin_cache, int max_pos,
+                                      const int32_t* positions, const int32_t* state_slot, int N,
+                                      int H, int D, int rope_dim, float eps, int win,
+                                      int64_t swa_pages, int64_t total_pages, void* q_out,
+                                      void* unified_kv, int32_t* status, void* stream);
+
+/*
+ * As sda_qk_norm_rope_swa_store, into the FP8 pool of sda_decode_fp8
+ * (kv_fp8 [total_pages, D] E4M3 codes, 16-byte aligned; kv_scale
+ * [total_pages] fp32): the row's scale is 2^e, e the least integer with
+ * 448 * 2^e >= max_d |y_d| (e >= -126; 1 for an all-zero row) -- a power of
+ * two, like the UE8M0 scales of block-scaled FP8 -- and code_d = y_d / 2^e
+ * rounded to the nearest E4M3 value (ties to even).  The quantised value is
+ * computed from the fp32 y, not from its bf16 rounding.
+ */
+sda_status sda_qk_norm_rope_swa_store_fp8(const void* q, const void* kv, const void* q_norm_w,
+                                          const void* kv_norm_w, const float* cos_cache,
+                                          const float* sin_cache, int max_pos,
+                                          const int32_t* positions, const int32_t* state_slot,
+                                          int N, int H, int D, int rope_dim, float eps, int win,
+                                          int64_t swa_pages, int64_t total_pages, void* q_out,
+                                          void* kv_fp8, float* kv_scale, int32_t* status,
+                                          void* stream);
 
 #ifdef __cplusplus
 }

@@ -94,6 +94,8 @@ def _bind(lib):
     lib.oracle_bf16_rne_array.argtypes = [_f64p, ctypes.c_int64, _u16p]
     lib.oracle_fp8_quantise_rows.restype = None
     lib.oracle_fp8_quantise_rows.argtypes = [_f64p, ctypes.c_int64, ctypes.c_int, _u8p, _f32p]
+    lib.oracle_e4m3_rne_array.restype = None
+    lib.oracle_e4m3_rne_array.argtypes = [_f64p, ctypes.c_int64, _u8p]
     lib.oracle_e4m3_rne.restype = ctypes.c_uint8
     lib.oracle_e4m3_rne.argtypes = [ctypes.c_double]
     lib.oracle_fp8_scale_exponent.restype = ctypes.c_int
@@ -325,6 +327,16 @@ def bf16_rne(values, lib=None) -> np.ndarray:
 def e4m3_rne(value, lib=None) -> int:
     """E4M3 code of one float64 value rounded to nearest even (saturating)."""
     return int((lib or load()).oracle_e4m3_rne(float(value)))
+
+
+def e4m3_rne_array(values, lib=None) -> np.ndarray:
+    """E4M3 codes of float64 values rounded to nearest even (saturating)."""
+    lib = lib or load()
+    v = _as(values, np.float64)
+    out = np.zeros(v.shape, np.uint8)
+    if v.size:
+        lib.oracle_e4m3_rne_array(_ptr(v, ctypes.c_double), v.size, _ptr(out, ctypes.c_uint8))
+    return out
 
 
 def fp8_scale_exponent(amax, lib=None) -> int:

@@ -467,3 +467,8 @@ void oracle_fp8_quantise_rows(const double* y, int64_t rows, int D, uint8_t* cod
     for (int d = 0; d < D; ++d) codes[(size_t)r * D + d] = oracle_e4m3_rne(ldexp(yr[d], -e));
   }
 }
+
+/* E4M3 codes of n values, each rounded to nearest even (saturating). */
+void oracle_e4m3_rne_array(const double* v, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_rne(v[i]);
+}

@@ -21,7 +21,7 @@ import torch
 from . import _lib
 
 __all__ = ["decode", "workspace_size", "build_indices", "validate_indices", "decode_error_flag",
-           "decode_kernel", "decode_fp8", "workspace_size_fp8",
+           "decode_kernel", "decode_fp8", "workspace_size_fp8", "qk_norm_rope_swa_store",
            "decode_host", "set_timing_events", "decode_noalloc", "library_path"]
 
 library_path = _lib.LIB_PATH
@@ -216,8 +216,9 @@ def decode_error_flag(workspace: torch.Tensor, stream=None) -> int:
 
 def set_timing_events(before: torch.cuda.Event | None, after: torch.cuda.Event | None) -> None:
     """Record `before` / `after` around the attention kernel of every later
-    decode() on this thread (None, None turns it off).  Events must be
-    created with enable_timing=True."""
+    decode() / decode_fp8() and around the kernel of every later
+    qk_norm_rope_swa_store() on this thread (None, None turns it off).
+    Events must be created with enable_timing=True."""
     lib = _lib.load()
     handles = []
     for ev in (before, after):
@@ -280,6 +281,71 @@ def validate_indices(kv_indices, kv_indptr, total_pages, status=None, stream=Non
                                       _stream_ptr(stream))
     _lib.check(rc, "sda_validate_indices")
     return status
+
+
+def qk_norm_rope_swa_store(q, kv, q_norm_w, kv_norm_w, cos_cache, sin_cache, positions,
+                           state_slot, *, eps, win, swa_pages, unified_kv=None, kv_fp8=None,
+                           kv_scale=None, q_out=None, status=None, stream=None):
+    """Per-head RMSNorm of q and RMSNorm of the new KV rows, GPT-J RoPE on the
+    last cos_cache.shape[1] * 2 dims, and the store of each token's KV row into
+    its ring slot state_slot * win + position mod win of the pool: bf16
+    (`unified_kv`) or E4M3 codes + power-of-two row scales (`kv_fp8`,
+    `kv_scale`).  Returns (q_out [N, H, D] bf16, status [1] int32); the status
+    bits are documented in include/sda.h.  `q_out` may be `q` (in place)."""
+    lib = _lib.load()
+    _req(q, "q", torch.bfloat16, 3)
+    dev = q.device
+    N, H, D = q.shape
+    _req(kv, "kv", torch.bfloat16, 2, dev)
+    _req(q_norm_w, "q_norm_w", torch.bfloat16, 1, dev)
+    _req(kv_norm_w, "kv_norm_w", torch.bfloat16, 1, dev)
+    _req(cos_cache, "cos_cache", torch.float32, 2, dev)
+    _req(sin_cache, "sin_cache", torch.float32, 2, dev)
+    _req(positions, "positions", torch.int32, 1, dev)
+    _req(state_slot, "state_slot", torch.int32, 1, dev)
+    if kv.shape != (N, D) or q_norm_w.numel() != D or kv_norm_w.numel() != D:
+        raise ValueError("kv must be [N, D] and the norm weights [D]")
+    if cos_cache.shape != sin_cache.shape or positions.numel() != N or state_slot.numel() != N:
+        raise ValueError("cos_cache / sin_cache must match; positions, state_slot must be [N]")
+    max_pos, half = cos_cache.shape
+    if (unified_kv is None) == (kv_fp8 is None):
+        raise ValueError("pass exactly one of unified_kv (bf16 pool) or kv_fp8 + kv_scale")
+    if unified_kv is not None:
+        _req(unified_kv, "unified_kv", torch.bfloat16, 2, dev)
+        total_pages = unified_kv.shape[0]
+        if unified_kv.shape[1] != D:
+            raise ValueError("unified_kv must be [total_pages, D]")
+    else:
+        if kv_fp8.dtype == torch.float8_e4m3fn:
+            kv_fp8 = kv_fp8.view(torch.uint8)
+        _req(kv_fp8, "kv_fp8", torch.uint8, 2, dev)
+        _req(kv_scale, "kv_scale", torch.float32, 1, dev)
+        total_pages = kv_fp8.shape[0]
+        if kv_fp8.shape[1] != D or kv_scale.numel() != total_pages:
+            raise ValueError("kv_fp8 must be [total_pages, D] and kv_scale [total_pages]")
+    if q_out is None:
+        q_out = torch.empty_like(q)
+    else:
+        _req(q_out, "q_out", torch.bfloat16, 3, dev)
+        if q_out.shape != q.shape:
+            raise ValueError("q_out must have q's shape")
+    if status is None:
+        status = torch.empty(1, dtype=torch.int32, device=dev)
+    common = (q.data_ptr(), kv.data_ptr(), q_norm_w.data_ptr(), kv_norm_w.data_ptr(),
+              cos_cache.data_ptr() if cos_cache.numel() else None,
+              sin_cache.data_ptr() if sin_cache.numel() else None, int(max_pos),
+              positions.data_ptr(), state_slot.data_ptr(), N, H, D, 2 * int(half),
+              float(eps), int(win), int(swa_pages), int(total_pages), q_out.data_ptr())
+    with torch.cuda.device(dev):
+        if unified_kv is not None:
+            rc = lib.sda_qk_norm_rope_swa_store(*common, unified_kv.data_ptr(), status.data_ptr(),
+                                                _stream_ptr(stream))
+        else:
+            rc = lib.sda_qk_norm_rope_swa_store_fp8(*common, kv_fp8.data_ptr(),
+                                                    kv_scale.data_ptr(), status.data_ptr(),
+                                                    _stream_ptr(stream))
+    _lib.check(rc, "sda_qk_norm_rope_swa_store")
+    return q_out, status
 
 
 def decode_host(q_host: torch.Tensor, unified_kv: torch.Tensor, kv_indices_host: torch.Tensor,

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -382,6 +383,76 @@ sda_status sda_validate_indices(const int32_t* kv_indices, int64_t total_indices
     return SDA_ERR_CUDA;
   }
   return SDA_OK;
+}
+
+static sda_status store_common(const void* q, const void* kv, const void* q_norm_w,
+                               const void* kv_norm_w, const float* cos_cache,
+                               const float* sin_cache, int max_pos, const int32_t* positions,
+                               const int32_t* state_slot, int N, int H, int D, int rope_dim,
+                               float eps, int win, int64_t swa_pages, int64_t total_pages,
+                               void* q_out, void* pool, uint8_t* pool_fp8, float* pool_scale,
+                               int32_t* status, void* stream, const char* who) {
+  using namespace sda;
+  if (N < 0 || H < 1 || D < 8 || D > 2048 || D % 8 || rope_dim < 0 || rope_dim > D ||
+      rope_dim % 8 || max_pos < 0 || win <= 0 || swa_pages < 0 || total_pages <= 0 ||
+      swa_pages > total_pages || !(eps >= 0.f) || !std::isfinite(eps))
+    return SDA_ERR_INVALID_ARG;
+  if (!status || !q_norm_w || !kv_norm_w) return SDA_ERR_INVALID_ARG;
+  if (N > 0 && (!q || !kv || !positions || !state_slot || !q_out)) return SDA_ERR_INVALID_ARG;
+  if (N > 0 && rope_dim > 0 && max_pos > 0 && (!cos_cache || !sin_cache)) return SDA_ERR_INVALID_ARG;
+  if (N > 0 && !pool && !pool_fp8) return SDA_ERR_INVALID_ARG;
+  if (pool_fp8 && !pool_scale) return SDA_ERR_INVALID_ARG;
+  const void* vec16[] = {q, kv, q_norm_w, kv_norm_w, q_out, pool, pool_fp8, cos_cache, sin_cache};
+  for (const void* ptr : vec16)
+    if (ptr && !aligned(ptr, 16)) return SDA_ERR_INVALID_ARG;
+  if (pool_scale && !aligned(pool_scale, 4)) return SDA_ERR_INVALID_ARG;
+  // q_out is either q itself (in place) or a disjoint buffer.
+  const size_t qbytes = (size_t)N * H * D * 2;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(q), b = reinterpret_cast<uintptr_t>(q_out);
+  if (N > 0 && a != b && a < b + qbytes && b < a + qbytes) return SDA_ERR_INVALID_ARG;
+  DeviceCaps caps;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = device_caps(&caps);
+  if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+  if (e == cudaSuccess && g_ev_before && g_ev_after) e = cudaEventRecord(g_ev_before, st);
+  if (e == cudaSuccess)
+    e = launch_qk_norm_rope_store(q, kv, q_norm_w, kv_norm_w, cos_cache, sin_cache, max_pos,
+                                  positions, state_slot, N, H, D, rope_dim, eps, win, swa_pages,
+                                  q_out, pool, pool_fp8, pool_scale, status, caps.num_sms, st);
+  if (e == cudaSuccess && g_ev_before && g_ev_after) e = cudaEventRecord(g_ev_after, st);
+  if (e != cudaSuccess) {
+    note_cuda_error(e, who);
+    return SDA_ERR_CUDA;
+  }
+  return SDA_OK;
+}
+
+sda_status sda_qk_norm_rope_swa_store(const void* q, const void* kv, const void* q_norm_w,
+                                      const void* kv_norm_w, const float* cos_cache,
+                                      const float* sin_cache, int max_pos,
+                                      const int32_t* positions, const int32_t* state_slot, int N,
+                                      int H, int D, int rope_dim, float eps, int win,
+                                      int64_t swa_pages, int64_t total_pages, void* q_out,
+                                      void* unified_kv, int32_t* status, void* stream) {
+  if (N > 0 && !unified_kv) return SDA_ERR_INVALID_ARG;
+  return store_common(q, kv, q_norm_w, kv_norm_w, cos_cache, sin_cache, max_pos, positions,
+                      state_slot, N, H, D, rope_dim, eps, win, swa_pages, total_pages, q_out,
+                      unified_kv, nullptr, nullptr, status, stream, "sda_qk_norm_rope_swa_store");
+}
+
+sda_status sda_qk_norm_rope_swa_store_fp8(const void* q, const void* kv, const void* q_norm_w,
+                                          const void* kv_norm_w, const float* cos_cache,
+                                          const float* sin_cache, int max_pos,
+                                          const int32_t* positions, const int32_t* state_slot,
+                                          int N, int H, int D, int rope_dim, float eps, int win,
+                                          int64_t swa_pages, int64_t total_pages, void* q_out,
+                                          void* kv_fp8, float* kv_scale, int32_t* status,
+                                          void* stream) {
+  if (N > 0 && (!kv_fp8 || !kv_scale)) return SDA_ERR_INVALID_ARG;
+  return store_common(q, kv, q_norm_w, kv_norm_w, cos_cache, sin_cache, max_pos, positions,
+                      state_slot, N, H, D, rope_dim, eps, win, swa_pages, total_pages, q_out,
+                      nullptr, static_cast<uint8_t*>(kv_fp8), kv_scale, status, stream,
+                      "sda_qk_norm_rope_swa_store_fp8");
 }
 
 }  // extern "C"

@@ -120,6 +120,16 @@ cudaError_t launch_build_indices(const int32_t* state_slot, const int32_t* swa_l
 cudaError_t launch_validate(const int32_t* kv_indices, int64_t total_indices,
                             const int32_t* kv_indptr, int N, int64_t total_pages,
                             int32_t* status, cudaStream_t st);
+// q/kv RMSNorm + RoPE + SWA ring store; bf16 pool when pool_fp8 == nullptr,
+// else E4M3 codes + row scales.  The caller zeroes *status beforehand.
+cudaError_t launch_qk_norm_rope_store(const void* q, const void* kv, const void* q_norm_w,
+                                      const void* kv_norm_w, const float* cos_cache,
+                                      const float* sin_cache, int max_pos,
+                                      const int32_t* positions, const int32_t* state_slot, int N,
+                                      int H, int D, int R, float eps, int win, int64_t swa_pages,
+                                      void* q_out, void* pool, uint8_t* pool_fp8,
+                                      float* pool_scale, int32_t* status, int num_sms,
+                                      cudaStream_t st);
 
 // Launch with programmatic dependent launch (PDL): the kernel may start while
 // the previous kernel on the stream is still running (once that kernel has

@@ -153,6 +153,59 @@ def fp8_pool(w: "Workload", pow2: bool = True, chunk_rows: int = 1 << 19) -> Fp8
     return Fp8Pool(codes=codes, scale=scale)
 
 
+ROPE_DIM = 64        # rotated trailing dims of each 512-wide row
+ROPE_BASE = 10000.0
+MAX_POS = 1 << 16
+
+
+@dataclasses.dataclass
+class StoreInputs:
+    """Inputs of the q/kv norm + RoPE + SWA store step of one decode step."""
+    kv_new: torch.Tensor      # [N, D] bf16, the step's new latent row per token
+    q_norm_w: torch.Tensor    # [D] bf16
+    kv_norm_w: torch.Tensor   # [D] bf16
+    cos_cache: torch.Tensor   # [max_pos, R/2] fp32
+    sin_cache: torch.Tensor   # [max_pos, R/2] fp32
+    positions: torch.Tensor   # [N] int32
+    state_slot: torch.Tensor  # [N] int32 (< 0: padded)
+    eps: float
+    recipe: str = ""
+
+
+def rope_caches(max_pos: int, rope_dim: int, base: float = ROPE_BASE, device="cpu"):
+    """cos / sin tables [max_pos, rope_dim/2] of the angles pos * base^(-2i/R),
+    evaluated in float64 and stored as fp32 (the usual RoPE frequency ladder)."""
+    inv = base ** (-np.arange(0, rope_dim, 2, dtype=np.float64) / max(rope_dim, 1))
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+    cos = torch.from_numpy(np.cos(ang).astype(np.float32)).to(device)
+    sin = torch.from_numpy(np.sin(ang).astype(np.float32)).to(device)
+    return cos, sin
+
+
+def store_inputs(w: "Workload", rope_dim: int = ROPE_DIM, max_pos: int = MAX_POS,
+                 seed: int | None = None, eps: float = 1e-6) -> StoreInputs:
+    """Store-step inputs matching a decode workload: each live token's position
+    is congruent to its ring head modulo win (so its new row lands on the
+    newest SWA entry of its own list) and at least win; new KV rows ~ N(0,1)
+    bf16; norm weights ~ U[0.5, 1.5) bf16; RoPE tables of base 10000 on the
+    last `rope_dim` dims.  Padded tokens keep state_slot < 0."""
+    rng = np.random.default_rng(SEED_BASE + 700 + (w.N * 7919 + w.H) % 1000 if seed is None else seed)
+    dev = w.q.device
+    N, D, win = w.N, w.D, w.win
+    kv_new = _to_bf16(rng.standard_normal((N, D)), dev)
+    qw = _to_bf16(rng.uniform(0.5, 1.5, D), dev)
+    kw = _to_bf16(rng.uniform(0.5, 1.5, D), dev)
+    laps = rng.integers(1, max(2, max_pos // win), N)
+    pos = (w.swa_head.astype(np.int64) + laps * win).astype(np.int64)
+    pos = np.minimum(pos, max_pos - win + w.swa_head.astype(np.int64)).astype(np.int32)
+    cos, sin = rope_caches(max_pos, rope_dim, device=dev)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+    return StoreInputs(kv_new=kv_new, q_norm_w=qw, kv_norm_w=kw, cos_cache=cos, sin_cache=sin,
+                       positions=t(pos), state_slot=t(w.state_slot), eps=eps,
+                       recipe=f"new KV N(0,1) bf16, weights U[0.5,1.5), RoPE base 1e4 on the last "
+                              f"{rope_dim} dims, positions = ring head + win * U{{1..{max_pos // win - 1}}}")
+
+
 def fp8_rows_for(w: "Workload", pool: Fp8Pool, tokens=None):
     """Host copy of an FP8 pool restricted to the rows the given tokens read:
     (codes [R, D] uint8, scale [R] fp32, kv_indices remapped into [0, R),

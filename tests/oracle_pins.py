@@ -473,6 +473,7 @@ def pin_e4m3_rne(lib):
                             rng.uniform(-500, 500, 3000), rng.standard_normal(3000) * 1e-2]).astype(np.float32)
     want = torch.from_numpy(sweep).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     got = np.array([oracle.e4m3_rne(float(x), lib=lib) for x in sweep], np.uint8)
+    assert np.array_equal(oracle.e4m3_rne_array(sweep.astype(np.float64), lib=lib), got)
     zero = sweep == 0  # the sign of a zero is kept by both; compare magnitudes there
     assert np.array_equal(got[~zero], want[~zero]) and np.all((got[zero] & 0x7F) == 0)
     # 17 = 1.0625 * 2^4: exponent field 11, mantissa tie 0.5 -> even 0: 0x58
