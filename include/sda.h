@@ -266,6 +266,7 @@ sda_status sda_validate_indices(const int32_t* kv_indices, int64_t total_indices
  *   cos_cache, sin_cache [max_pos, rope_dim / 2] fp32, row = position
  *   positions  [N] int32, state_slot [N] int32 (< 0: padded token)
  *   D % 8 == 0, 8 <= D <= 2048; rope_dim % 8 == 0, 0 <= rope_dim <= D;
+ *   N * (H + 1) <= 2^30;
  *   eps >= 0 finite; win > 0; 0 <= swa_pages <= total_pages.
  *   q_out      [N, H, D] bf16; may be q itself, must not partly overlap it.
  * Per token t with state_slot[t] >= 0 and 0 <= pos = positions[t] < max_pos,

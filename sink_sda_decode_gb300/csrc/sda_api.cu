@@ -397,6 +397,7 @@ static sda_status store_common(const void* q, const void* kv, const void* q_norm
       rope_dim % 8 || max_pos < 0 || win <= 0 || swa_pages < 0 || total_pages <= 0 ||
       swa_pages > total_pages || !(eps >= 0.f) || !std::isfinite(eps))
     return SDA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(N) * (H + 1) > (int64_t{1} << 30)) return SDA_ERR_INVALID_ARG;
   if (!status || !q_norm_w || !kv_norm_w) return SDA_ERR_INVALID_ARG;
   if (N > 0 && (!q || !kv || !positions || !state_slot || !q_out)) return SDA_ERR_INVALID_ARG;
   if (N > 0 && rope_dim > 0 && max_pos > 0 && (!cos_cache || !sin_cache)) return SDA_ERR_INVALID_ARG;

@@ -99,152 +99,205 @@ __device__ __forceinline__ int fp8_scale_exponent(float amax) {
   return e < -126 ? -126 : e;
 }
 
-// CPL: 16-byte chunks per lane (D <= 256 * CPL); RPW: rows a warp keeps in
-// flight (2 for D <= 512, 1 above, which already has >= 2 KB per warp).
-template <int CPL>
-constexpr int store_ctas_per_sm() { return CPL <= 2 ? 4 : 2; }  // 64 / 128 registers a thread
-
-template <int CPL, int RPW, bool FP8>
-__global__ void __launch_bounds__(kStoreThreads, store_ctas_per_sm<CPL>())
-    qk_norm_rope_store_kernel(StoreParams p) {
-  constexpr int kRowsPerWarp = RPW;
-  pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const int chunks = p.D >> 3;           // 16-byte chunks per row
+// Norm, rotation, rounding and store of one loaded row x of token t (row
+// `head` of it; head == H is the KV row).  With LASTJ the caller has already
+// loaded this lane's RoPE factors of chunk CPL-1 (cs, sn): the rotated dims
+// then all lie in that chunk (D a multiple of 256, R <= 256).  Otherwise they
+// are loaded here.
+template <int CPL, bool FP8, bool LASTJ>
+__device__ __forceinline__ void process_row(const StoreParams& p, int lane, const uint4 (&x)[CPL],
+                                            int t, int head, int st, int pos, float4 cs_last,
+                                            float4 sn_last) {
+  const int chunks = p.D >> 3;  // 16-byte chunks per row
   const int rope_chunk0 = (p.D - p.R) >> 3;
   const int half = p.R >> 1;
-
-  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kStoreThreads + threadIdx.x) >> 5;
-  const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * kStoreThreads) >> 5;
-  const int rows_per_token = p.H + 1;
-
-  for (int64_t base = warp * kRowsPerWarp; base < p.rows; base += n_warps * kRowsPerWarp) {
-    // Issue both rows' loads before any arithmetic.
-    uint4 x[kRowsPerWarp][CPL];
-    int tok[kRowsPerWarp], head[kRowsPerWarp];
+  const bool is_kv = head == p.H;
+  const bool live = st >= 0 && pos >= 0 && pos < p.max_pos;
+  if (!live) {
+    if (!is_kv) {
+      uint4* dst = reinterpret_cast<uint4*>(p.q_out + (static_cast<size_t>(t) * p.H + head) * p.D);
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
-      const int64_t row = base + r;
-      const bool valid = row < p.rows;
-      tok[r] = valid ? static_cast<int>(row / rows_per_token) : 0;
-      head[r] = valid ? static_cast<int>(row - static_cast<int64_t>(tok[r]) * rows_per_token) : -1;
-      const uint16_t* src =
-          !valid        ? p.q
-          : head[r] < p.H ? p.q + (static_cast<size_t>(tok[r]) * p.H + head[r]) * p.D
-                          : p.kv + static_cast<size_t>(tok[r]) * p.D;
+      for (int j = 0; j < CPL; ++j)
+        if (lane + 32 * j < chunks) __stcs(dst + lane + 32 * j, make_uint4(0, 0, 0, 0));
+    } else if (st >= 0 && lane == 0) {
+      atomicOr(p.status, 1);  // a real token whose position has no cache row
+    }
+    return;
+  }
+  // RMSNorm: one sum of squares over the row (lane partials, then the warp).
+  float f[CPL][8];
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < CPL; ++j) {
+    unpack8(x[j], f[j]);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) ss = fmaf(f[j][k], f[j][k], ss);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float inv_rms = 1.0f / sqrtf(ss / static_cast<float>(p.D) + p.eps);
+  float amax = 0.f;
+  const uint4* wrow = reinterpret_cast<const uint4*>(is_kv ? p.kv_norm_w : p.q_norm_w);
+#pragma unroll
+  for (int j = 0; j < CPL; ++j) {
+    const int c = lane + 32 * j;
+    float w[8];
+    unpack8(c < chunks ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0), w);  // L1-resident
+#pragma unroll
+    for (int k = 0; k < 8; ++k) f[j][k] = f[j][k] * inv_rms * w[k];
+    if (c >= rope_chunk0 && c < chunks && (!LASTJ || j == CPL - 1)) {
+      // GPT-J rotation of the pairs (2i, 2i+1), i = 4 (c - rope_chunk0) + 0..3.
+      float4 cs = cs_last, sn = sn_last;
+      if (!LASTJ) {
+        const size_t off = static_cast<size_t>(pos) * half + 4 * (c - rope_chunk0);
+        cs = __ldg(reinterpret_cast<const float4*>(p.cos_cache + off));
+        sn = __ldg(reinterpret_cast<const float4*>(p.sin_cache + off));
+      }
+      const float cv[4] = {cs.x, cs.y, cs.z, cs.w}, sv[4] = {sn.x, sn.y, sn.z, sn.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a = f[j][2 * i], b = f[j][2 * i + 1];
+        f[j][2 * i] = a * cv[i] - b * sv[i];
+        f[j][2 * i + 1] = b * cv[i] + a * sv[i];
+      }
+    }
+    if (FP8 && is_kv && c < chunks) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[j][k]));
+    }
+  }
+  if (!is_kv) {
+    uint4* dst = reinterpret_cast<uint4*>(p.q_out + (static_cast<size_t>(t) * p.H + head) * p.D);
+#pragma unroll
+    for (int j = 0; j < CPL; ++j)
+      if (lane + 32 * j < chunks) __stcs(dst + lane + 32 * j, pack8_bf16(f[j]));
+    return;
+  }
+  const int64_t slot = static_cast<int64_t>(st) * p.win + pos % p.win;
+  if (slot >= p.swa_pages) {
+    if (lane == 0) atomicOr(p.status, 2);
+    return;
+  }
+  if constexpr (FP8) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const int e = fp8_scale_exponent(amax);
+    const float inv_scale = __int_as_float((127 - e) << 23);  // 2^-e, exact (e in [-126, 127])
+    uint2* dst = reinterpret_cast<uint2*>(p.pool_fp8 + static_cast<size_t>(slot) * p.D);
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+      if (lane + 32 * j < chunks) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f[j][k] *= inv_scale;
+        dst[lane + 32 * j] = pack8_e4m3(f[j]);
+      }
+    }
+    if (lane == 0) p.pool_scale[slot] = __int_as_float((127 + e) << 23);
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(p.pool + static_cast<size_t>(slot) * p.D);
+#pragma unroll
+    for (int j = 0; j < CPL; ++j)
+      if (lane + 32 * j < chunks) dst[lane + 32 * j] = pack8_bf16(f[j]);
+  }
+}
+
+// State slot and position of the tokens of rows base .. base+RPW-1 (-1 past
+// the last row).  Row counts fit in 32 bits (checked on the host).
+template <int RPW>
+__device__ __forceinline__ void load_meta(const StoreParams& p, int base, int (&st)[RPW],
+                                          int (&pos)[RPW]) {
+#pragma unroll
+  for (int r = 0; r < RPW; ++r) {
+    const int row = base + r;
+    const bool valid = row < static_cast<int>(p.rows);
+    const int t = valid ? static_cast<int>(static_cast<unsigned>(row) / (p.H + 1)) : 0;
+    st[r] = valid ? __ldg(p.state_slot + t) : -1;
+    pos[r] = valid ? __ldg(p.positions + t) : -1;
+  }
+}
+
+// CPL: 16-byte chunks per lane (D <= 256 * CPL); RPW: rows a warp loads at
+// once (1: measured best with 5 CTAs = 40 warps per SM).  A warp walks its row batches grid-stride.  The state slots and
+// positions of the next batch are requested one batch ahead, so that a
+// batch's row loads and (LASTJ) its RoPE factor loads go out together: one
+// memory latency per batch rather than a position load followed by a
+// dependent cache load.
+template <int CPL>
+constexpr int store_ctas_per_sm() { return CPL <= 2 ? 5 : 2; }  // 48 / 128 registers a thread
+
+template <int CPL, int RPW, bool FP8, bool LASTJ>
+__global__ void __launch_bounds__(kStoreThreads, store_ctas_per_sm<CPL>())
+    qk_norm_rope_store_kernel(StoreParams p) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int chunks = p.D >> 3;
+  const int rope_chunk0 = (p.D - p.R) >> 3;
+  const int half = p.R >> 1;
+  const int rows = static_cast<int>(p.rows);
+  const int rows_per_token = p.H + 1;
+  const int warp = static_cast<int>((blockIdx.x * kStoreThreads + threadIdx.x) >> 5);
+  const int stride = static_cast<int>((gridDim.x * kStoreThreads) >> 5) * RPW;
+  int base = warp * RPW;
+  int nst[RPW], npos[RPW];
+  load_meta<RPW>(p, base, nst, npos);
+  for (; base < rows; base += stride) {
+    int st[RPW], pos[RPW], tok[RPW], head[RPW];
+    uint4 x[RPW][CPL];
+    float4 cs[RPW], sn[RPW];
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) {
+      st[r] = nst[r];
+      pos[r] = npos[r];
+      const int row = base + r;
+      const bool valid = row < rows;
+      const int t = valid ? static_cast<int>(static_cast<unsigned>(row) / rows_per_token) : 0;
+      tok[r] = t;
+      head[r] = valid ? row - t * rows_per_token : -1;
+      const uint16_t* src = !valid            ? p.q
+                            : head[r] < p.H ? p.q + (static_cast<size_t>(t) * p.H + head[r]) * p.D
+                                            : p.kv + static_cast<size_t>(t) * p.D;
 #pragma unroll
       for (int j = 0; j < CPL; ++j) {
         const int c = lane + 32 * j;
         x[r][j] = (valid && c < chunks) ? __ldcs(reinterpret_cast<const uint4*>(src) + c)
                                         : make_uint4(0, 0, 0, 0);
       }
-    }
-#pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
-      if (head[r] < 0) continue;  // past the last row (warp-uniform)
-      const int t = tok[r];
-      const bool is_kv = head[r] == p.H;
-      const int st = __ldg(p.state_slot + t);
-      const int pos = __ldg(p.positions + t);
-      const bool pos_ok = pos >= 0 && pos < p.max_pos;
-      const bool live = st >= 0 && pos_ok;
-      if (!live) {
-        if (!is_kv) {
-          uint4* dst = reinterpret_cast<uint4*>(p.q_out + (static_cast<size_t>(t) * p.H + head[r]) * p.D);
-#pragma unroll
-          for (int j = 0; j < CPL; ++j)
-            if (lane + 32 * j < chunks) __stcs(dst + lane + 32 * j, make_uint4(0, 0, 0, 0));
-        } else if (st >= 0 && lane == 0) {
-          atomicOr(p.status, 1);  // a real token whose position has no cache row
+      cs[r] = sn[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (LASTJ) {
+        const int c = lane + 32 * (CPL - 1);
+        if (valid && st[r] >= 0 && pos[r] >= 0 && pos[r] < p.max_pos && c >= rope_chunk0 &&
+            c < chunks) {
+          const size_t off = static_cast<size_t>(pos[r]) * half + 4 * (c - rope_chunk0);
+          cs[r] = __ldg(reinterpret_cast<const float4*>(p.cos_cache + off));
+          sn[r] = __ldg(reinterpret_cast<const float4*>(p.sin_cache + off));
         }
-        continue;
-      }
-      // RMSNorm: one sum of squares over the row (lane partials, then the warp).
-      float f[CPL][8];
-      float ss = 0.f;
-#pragma unroll
-      for (int j = 0; j < CPL; ++j) {
-        unpack8(x[r][j], f[j]);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) ss = fmaf(f[j][k], f[j][k], ss);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      const float inv_rms = 1.0f / sqrtf(ss / static_cast<float>(p.D) + p.eps);
-      float amax = 0.f;
-      const uint4* wrow = reinterpret_cast<const uint4*>(is_kv ? p.kv_norm_w : p.q_norm_w);
-#pragma unroll
-      for (int j = 0; j < CPL; ++j) {
-        const int c = lane + 32 * j;
-        float w[8];
-        unpack8(c < chunks ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0), w);  // L1-resident
-#pragma unroll
-        for (int k = 0; k < 8; ++k) f[j][k] = f[j][k] * inv_rms * w[k];
-        if (c >= rope_chunk0 && c < chunks) {
-          // GPT-J rotation of the pairs (2i, 2i+1), i = 4 (c - rope_chunk0) + 0..3.
-          const size_t off = static_cast<size_t>(pos) * half + 4 * (c - rope_chunk0);
-          const float4 cs = __ldg(reinterpret_cast<const float4*>(p.cos_cache + off));
-          const float4 sn = __ldg(reinterpret_cast<const float4*>(p.sin_cache + off));
-          const float cv[4] = {cs.x, cs.y, cs.z, cs.w}, sv[4] = {sn.x, sn.y, sn.z, sn.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float a = f[j][2 * i], b = f[j][2 * i + 1];
-            f[j][2 * i] = a * cv[i] - b * sv[i];
-            f[j][2 * i + 1] = b * cv[i] + a * sv[i];
-          }
-        }
-        if (FP8 && is_kv && c < chunks) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[j][k]));
-        }
-      }
-      if (!is_kv) {
-        uint4* dst = reinterpret_cast<uint4*>(p.q_out + (static_cast<size_t>(t) * p.H + head[r]) * p.D);
-#pragma unroll
-        for (int j = 0; j < CPL; ++j)
-          if (lane + 32 * j < chunks) __stcs(dst + lane + 32 * j, pack8_bf16(f[j]));
-        continue;
-      }
-      const int64_t slot = static_cast<int64_t>(st) * p.win + pos % p.win;
-      if (slot >= p.swa_pages) {
-        if (lane == 0) atomicOr(p.status, 2);
-        continue;
-      }
-      if constexpr (FP8) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const int e = fp8_scale_exponent(amax);
-        const float inv_scale = __int_as_float((127 - e) << 23);  // 2^-e, exact (e in [-126, 127])
-        uint2* dst = reinterpret_cast<uint2*>(p.pool_fp8 + static_cast<size_t>(slot) * p.D);
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-          if (lane + 32 * j < chunks) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) f[j][k] *= inv_scale;
-            dst[lane + 32 * j] = pack8_e4m3(f[j]);
-          }
-        }
-        if (lane == 0) p.pool_scale[slot] = __int_as_float((127 + e) << 23);
-      } else {
-        uint4* dst = reinterpret_cast<uint4*>(p.pool + static_cast<size_t>(slot) * p.D);
-#pragma unroll
-        for (int j = 0; j < CPL; ++j)
-          if (lane + 32 * j < chunks) dst[lane + 32 * j] = pack8_bf16(f[j]);
       }
     }
+    load_meta<RPW>(p, base + stride, nst, npos);
+#pragma unroll
+    for (int r = 0; r < RPW; ++r)
+      if (head[r] >= 0)
+        process_row<CPL, FP8, LASTJ>(p, lane, x[r], tok[r], head[r], st[r], pos[r], cs[r], sn[r]);
   }
   pdl_trigger();
 }
 
-template <int CPL, bool FP8>
-cudaError_t launch_cpl(const StoreParams& p, int num_sms, cudaStream_t st) {
-  constexpr int kRowsPerWarp = CPL <= 2 ? 2 : 1;
+template <int CPL, bool FP8, bool LASTJ>
+cudaError_t launch_variant(const StoreParams& p, int num_sms, cudaStream_t st) {
+  constexpr int kRowsPerWarp = 1;  // more rows per warp measured slower (fewer warps per SM)
   const int64_t warps = (p.rows + kRowsPerWarp - 1) / kRowsPerWarp;
   const int64_t want = (warps * 32 + kStoreThreads - 1) / kStoreThreads;
   const int64_t cap = static_cast<int64_t>(num_sms) * store_ctas_per_sm<CPL>();
   const int grid = static_cast<int>(want < cap ? want : cap);
-  return launch_pdl(qk_norm_rope_store_kernel<CPL, kRowsPerWarp, FP8>, dim3(grid),
+  return launch_pdl(qk_norm_rope_store_kernel<CPL, kRowsPerWarp, FP8, LASTJ>, dim3(grid),
                     dim3(kStoreThreads), 0, st, p);
+}
+
+template <int CPL, bool FP8>
+cudaError_t launch_cpl(const StoreParams& p, int num_sms, cudaStream_t st) {
+  const bool lastj = p.D % 256 == 0 && p.R <= 256;  // rotated dims all in chunk CPL-1
+  return lastj ? launch_variant<CPL, FP8, true>(p, num_sms, st)
+               : launch_variant<CPL, FP8, false>(p, num_sms, st);
 }
 
 }  // namespace
