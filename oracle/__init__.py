@@ -19,6 +19,12 @@ the last R dims and the store of the KV row into its SWA ring slot (sglang PR
 25898 summary page, sections "关键文件" and "关键符号"); ``bf16_rne`` and
 ``fp8_quantise_rows`` give the rounded forms it stores.
 
+``topk_slots`` is the step before the index builder: per token, the k
+best-scored compressed-cache positions (NaN padding ranks below -inf, ties in
+position order), emitted in position order and mapped through the token's
+block table to (block, slot in block) pairs (sglang attention tag page,
+entry "DSV4.1 新增索引器内核，重做 Top-K v2 分派").
+
 What it computes follows the docstring of ``paged_decode.py`` quoted on the
 sglang PR 28392 summary page ("为 AMD V4 内核添加 ATOM 来源注释", section
 "关键源码片段": caller convention, returns, numerics):
@@ -94,6 +100,10 @@ def _bind(lib):
     lib.oracle_bf16_rne_array.argtypes = [_f64p, ctypes.c_int64, _u16p]
     lib.oracle_fp8_quantise_rows.restype = None
     lib.oracle_fp8_quantise_rows.argtypes = [_f64p, ctypes.c_int64, ctypes.c_int, _u8p, _f32p]
+    lib.oracle_topk_slots.restype = ctypes.c_int
+    lib.oracle_topk_slots.argtypes = [
+        _f32p, ctypes.c_int64, _i32p, _i32p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, _i32p, _i32p, _i32p, _i32p]
     lib.oracle_e4m3_rne_array.restype = None
     lib.oracle_e4m3_rne_array.argtypes = [_f64p, ctypes.c_int64, _u8p]
     lib.oracle_e4m3_rne.restype = ctypes.c_uint8
@@ -355,3 +365,32 @@ def fp8_quantise_rows(values, lib=None):
         lib.oracle_fp8_quantise_rows(_ptr(v, ctypes.c_double), rows, D,
                                      _ptr(codes, ctypes.c_uint8), _ptr(scale, ctypes.c_float))
     return codes, scale
+
+
+def topk_slots(scores, lengths, block_table, k, k_per_block, lib=None):
+    """Reference top-k -> (comp_indptr [N+1], comp_block, comp_slot, status).
+
+    scores [N, S] fp32 (token t's candidates are scores[t, :lengths[t]]),
+    lengths [N] int32, block_table [N, B] int32 with B * k_per_block >= S."""
+    lib = lib or load()
+    sc = _as(scores, np.float32)
+    N, S = sc.shape
+    ln = _as(lengths, np.int32)
+    bt = _as(block_table, np.int32)
+    assert ln.shape == (N,) and bt.ndim == 2 and bt.shape[0] == N
+    cap = max(1, int(np.minimum(np.clip(ln, 0, S), k).sum()))
+    ptr = np.zeros(N + 1, np.int32)
+    blk = np.zeros(cap, np.int32)
+    slot = np.zeros(cap, np.int32)
+    st = np.zeros(1, np.int32)
+    one_f = np.zeros(1, np.float32)
+    one_i = np.zeros(1, np.int32)
+    rc = lib.oracle_topk_slots(_ptr(sc if sc.size else one_f, ctypes.c_float), S,
+                               _ptr(ln if N else one_i, ctypes.c_int32),
+                               _ptr(bt if bt.size else one_i, ctypes.c_int32), bt.shape[1], N,
+                               int(k), int(k_per_block), _ptr(ptr, ctypes.c_int32),
+                               _ptr(blk, ctypes.c_int32), _ptr(slot, ctypes.c_int32),
+                               _ptr(st, ctypes.c_int32))
+    if rc != 0:
+        raise ValueError(f"oracle_topk_slots: {_ERRORS.get(rc, rc)}")
+    return ptr, blk[: ptr[N]].copy(), slot[: ptr[N]].copy(), int(st[0])

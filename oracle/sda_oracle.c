@@ -472,3 +472,103 @@ void oracle_fp8_quantise_rows(const double* y, int64_t rows, int D, uint8_t* cod
 void oracle_e4m3_rne_array(const double* v, int64_t n, uint8_t* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_rne(v[i]);
 }
+
+/* ------------------------------------------------------------------------ */
+/*
+ * Top-k selection of compressed-cache entries -> slot lists (the input of the
+ * index builder), fp32 scores.
+ *
+ * Source: the sglang attention tag page, entry "DSV4.1 新增索引器内核，重做
+ * Top-K v2 分派": the selection pads with NaN rather than a very small value so
+ * that a legitimate -inf score stays selectable, and a separate page-table
+ * transform ("PageTransform") turns selected positions into cache locations.
+ * The positions map to pool entries by the compressed-slot formula of the
+ * paged_decode.py docstring (PR 28392 page): block_id * K_PER_BLOCK +
+ * slot_in_block, the block being the token's block_table entry.
+ *
+ * Readings where the page is silent (each also in the design notes):
+ *   - token t's candidates are positions p in [0, n_t), n_t = lengths[t], with
+ *     scores[t * score_stride + p]; positions at or past n_t are padding and
+ *     are never read or selected; lengths outside [0, score_stride] count as
+ *     0 and raise status bit 1;
+ *   - ranking: larger score first; -0 equals +0; a NaN inside [0, n_t) ranks
+ *     below -inf (as padding does) but is still a candidate (status bit 8);
+ *     equal scores are taken in increasing position;
+ *   - the token keeps min(k, n_t) positions, emitted in increasing position;
+ *   - position p -> (block_table[t * bt_stride + p / k_per_block],
+ *     p % k_per_block); a negative block id raises bit 4 and is emitted as is
+ *     (the index builder rejects it);
+ *   - comp_indptr[0] = 0, comp_indptr[t + 1] = comp_indptr[t] + min(k, n_t).
+ */
+typedef struct {
+  uint32_t key;  /* order-preserving image of the score: larger score, larger key */
+  int32_t pos;
+} KeyPos;
+
+static uint32_t score_key(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if (isnan(f)) return 0;                         /* below every number, -inf included */
+  if (u == 0x80000000u) u = 0;                    /* -0 ranks as +0 */
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+static int keypos_order(const void* a, const void* b) {
+  const KeyPos* x = (const KeyPos*)a;
+  const KeyPos* y = (const KeyPos*)b;
+  if (x->key != y->key) return x->key > y->key ? -1 : 1;  /* larger score first */
+  return (x->pos > y->pos) - (x->pos < y->pos);            /* then smaller position */
+}
+
+static int int_order(const void* a, const void* b) {
+  const int32_t x = *(const int32_t*)a, y = *(const int32_t*)b;
+  return (x > y) - (x < y);
+}
+
+int oracle_topk_slots(const float* scores, int64_t score_stride, const int32_t* lengths,
+                      const int32_t* block_table, int64_t bt_stride, int N, int k,
+                      int k_per_block, int32_t* comp_indptr, int32_t* comp_block,
+                      int32_t* comp_slot, int32_t* status) {
+  if (N < 0 || k < 0 || k_per_block <= 0 || score_stride < 0 || bt_stride < 0 ||
+      bt_stride * (int64_t)k_per_block < score_stride)
+    return ORACLE_BAD_SHAPE;
+  int32_t flags = 0;
+  comp_indptr[0] = 0;
+  for (int t = 0; t < N; ++t) {
+    int64_t n = lengths[t];
+    if (n < 0 || n > score_stride) {
+      flags |= 1;
+      n = 0;
+    }
+    const int64_t kk = n < k ? n : k;
+    comp_indptr[t + 1] = (int32_t)(comp_indptr[t] + kk);
+    if (kk == 0) continue;
+    KeyPos* c = (KeyPos*)malloc(sizeof(KeyPos) * (size_t)n);
+    int32_t* sel = (int32_t*)malloc(sizeof(int32_t) * (size_t)kk);
+    if (!c || !sel) {
+      free(c);
+      free(sel);
+      return ORACLE_NO_MEMORY;
+    }
+    for (int64_t p = 0; p < n; ++p) {
+      const float f = scores[(size_t)t * score_stride + p];
+      if (isnan(f)) flags |= 8;
+      c[p].key = score_key(f);
+      c[p].pos = (int32_t)p;
+    }
+    qsort(c, (size_t)n, sizeof(KeyPos), keypos_order);
+    for (int64_t i = 0; i < kk; ++i) sel[i] = c[i].pos;
+    qsort(sel, (size_t)kk, sizeof(int32_t), int_order);
+    for (int64_t i = 0; i < kk; ++i) {
+      const int32_t p = sel[i];
+      const int32_t blk = block_table[(size_t)t * bt_stride + p / k_per_block];
+      if (blk < 0) flags |= 4;
+      comp_block[comp_indptr[t] + i] = blk;
+      comp_slot[comp_indptr[t] + i] = p % k_per_block;
+    }
+    free(c);
+    free(sel);
+  }
+  *status = flags;
+  return ORACLE_OK;
+}

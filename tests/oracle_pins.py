@@ -506,6 +506,83 @@ def pin_fp8_scale(lib):
         assert np.all(np.abs(deq[r] - y[r]) <= 0.5 * step * scale[r] * (1 + 1e-12))
 
 
+# ----------------------------------------------------------------------------- top-k -> slot lists
+# Source: the sglang attention tag page, entry "DSV4.1 新增索引器内核，重做 Top-K v2
+# 分派" (NaN padding below a legitimate -inf; a separate page-table transform),
+# and the compressed-slot formula block_id * K_PER_BLOCK + slot_in_block of the
+# paged_decode.py docstring (PR 28392 page).
+def topk_numpy(scores, lengths, block_table, k, kpb):
+    """The same selection with numpy's lexsort: non-NaN before NaN, then
+    larger score (so -0 == +0), then smaller position; kept positions in
+    increasing order, mapped through the block table."""
+    ptr, blks, slots = [0], [], []
+    S = scores.shape[1]
+    for t in range(scores.shape[0]):
+        n = int(lengths[t]) if 0 <= lengths[t] <= S else 0
+        s = scores[t, :n].astype(np.float64)
+        nan = np.isnan(s)
+        order = np.lexsort((np.arange(n), -np.where(nan, 0.0, s), nan))
+        keep = np.sort(order[:min(k, n)])
+        blks += [int(block_table[t, p // kpb]) for p in keep]
+        slots += [int(p % kpb) for p in keep]
+        ptr.append(ptr[-1] + len(keep))
+    return np.array(ptr), np.array(blks, np.int64), np.array(slots, np.int64)
+
+
+def topk_case(rng, N, S, lens, kpb, tie_values=None):
+    if tie_values is None:
+        scores = rng.standard_normal((N, S)).astype(np.float32)
+    else:
+        scores = rng.choice(np.asarray(tie_values, np.float32), (N, S))
+    B = -(-S // kpb)
+    bt = rng.integers(0, 1000, (N, B)).astype(np.int32)
+    return scores, np.asarray(lens, np.int32), bt
+
+
+def pin_topk_matches_lexsort(lib):
+    """Random scores, heavy ties (+-0, -inf, NaN among few values), ragged
+    lengths around k: equal to numpy's lexsort formulation."""
+    rng = np.random.default_rng(87)
+    for ties in (None, [1.0, 0.0, -0.0, -np.inf, np.nan, 2.5, -1.0]):
+        for k in (1, 5, 16):
+            scores, lens, bt = topk_case(rng, 7, 40, [0, 1, 5, 16, 17, 40, 33], 8, ties)
+            ptr, blk, slot, st = oracle.topk_slots(scores, lens, bt, k, 8, lib=lib)
+            want = topk_numpy(scores, lens, bt, k, 8)
+            assert np.array_equal(ptr, want[0]) and np.array_equal(blk, want[1])
+            assert np.array_equal(slot, want[2])
+            assert st == (8 if ties is not None and np.isnan(scores).any() and
+                          any(np.isnan(scores[t, :lens[t]]).any() for t in range(7)) else 0)
+
+
+def pin_topk_closed_forms(lib):
+    """k >= n keeps every position; constant scores keep the first k; rising
+    scores keep the last k; a worked example with ties, -0, -inf and NaN; bad
+    lengths and negative block ids raise their status bits."""
+    bt = np.array([[7, 9, 11]], np.int32)
+    s = np.arange(12, dtype=np.float32)[None]
+    assert oracle.topk_slots(s, [12], bt, 20, 4, lib=lib)[2].tolist() == [0, 1, 2, 3] * 3
+    const = np.full((1, 12), 0.5, np.float32)
+    ptr, blk, slot, _ = oracle.topk_slots(const, [12], bt, 5, 4, lib=lib)
+    assert ptr.tolist() == [0, 5] and blk.tolist() == [7, 7, 7, 7, 9] and slot.tolist() == [0, 1, 2, 3, 0]
+    ptr, blk, slot, _ = oracle.topk_slots(s, [12], bt, 3, 4, lib=lib)
+    assert blk.tolist() == [11, 11, 11] and slot.tolist() == [1, 2, 3]
+    # scores 0.5, 2, -inf, 2, NaN, 1, 0, -0 (block size 4, blocks 7 and 9): the
+    # best five are p1, p3 (2.0), p5 (1.0), p0 (0.5) and p6 (0 ties -0, p6 first)
+    ex = np.array([[0.5, 2.0, -np.inf, 2.0, np.nan, 1.0, 0.0, -0.0]], np.float32)
+    bt2 = np.array([[7, 9]], np.int32)
+    ptr, blk, slot, st = oracle.topk_slots(ex, [8], bt2, 5, 4, lib=lib)
+    assert blk.tolist() == [7, 7, 7, 9, 9] and slot.tolist() == [0, 1, 3, 1, 2] and st == 8
+    # seven: -0 (p7) and then -inf (p2) join; the NaN (p4) is last
+    ptr, blk, slot, _ = oracle.topk_slots(ex, [8], bt2, 7, 4, lib=lib)
+    assert slot.tolist() == [0, 1, 2, 3, 1, 2, 3]
+    # length 0 and a length past the row (bit 1) keep nothing; a negative block id (bit 4)
+    two = np.zeros((3, 8), np.float32)
+    btn = np.array([[1, 2], [3, 4], [-5, 6]], np.int32)
+    ptr, blk, slot, st = oracle.topk_slots(two, [0, 9, 2], btn, 4, 4, lib=lib)
+    assert ptr.tolist() == [0, 0, 0, 2] and blk.tolist() == [-5, -5] and st == 1 | 4
+
+
+TOPK_PINS = [pin_topk_matches_lexsort, pin_topk_closed_forms]
 STORE_PINS = [pin_store_matches_torch, pin_store_closed_forms, pin_store_rotation_invariants,
               pin_store_slots]
 ROUNDING_PINS = [pin_bf16_rne, pin_e4m3_rne, pin_fp8_scale]
@@ -515,7 +592,8 @@ DECODE_PINS = [pin_sdpa, pin_sink_minus_inf_is_softmax, pin_single_slot, pin_dup
                pin_hard_attention_limit, pin_sink_plus_inf, pin_token_subset]
 BUILDER_PINS = [pin_builder_golden, pin_builder_ring_closed_form, pin_builder_capacity]
 VALIDATE_PINS = [pin_validate]
-ALL_PINS = DECODE_PINS + BUILDER_PINS + VALIDATE_PINS + FP8_PINS + STORE_PINS + ROUNDING_PINS
+ALL_PINS = (DECODE_PINS + BUILDER_PINS + VALIDATE_PINS + FP8_PINS + STORE_PINS + ROUNDING_PINS
+            + TOPK_PINS)
 
 
 def failing_pins(lib, pins=ALL_PINS):

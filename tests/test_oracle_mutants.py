@@ -73,6 +73,22 @@ MUTANTS = {
     "fp8_scale_one_too_big": ("while (ldexp(448.0, e - 1) >= amax) --e;\n  return e",
                               "while (ldexp(448.0, e - 1) >= amax) --e;\n  ++e;\n  return e",
                               pins.ROUNDING_PINS),
+    # top-k -> slot lists
+    "topk_ties_larger_position_first": ("return (x->pos > y->pos) - (x->pos < y->pos);",
+                                        "return (x->pos < y->pos) - (x->pos > y->pos);",
+                                        pins.TOPK_PINS),
+    "topk_nan_ranks_first": ("if (isnan(f)) return 0;", "if (isnan(f)) return 0xFFFFFFFFu;",
+                             pins.TOPK_PINS),
+    "topk_minus_zero_below_zero": ("if (u == 0x80000000u) u = 0;", "(void)0;", pins.TOPK_PINS),
+    "topk_smallest_scores": ("return x->key > y->key ? -1 : 1;", "return x->key > y->key ? 1 : -1;",
+                             pins.TOPK_PINS),
+    "topk_not_in_position_order": ("qsort(sel, (size_t)kk, sizeof(int32_t), int_order);", "(void)0;",
+                                   pins.TOPK_PINS),
+    "topk_block_slot_swapped": ("block_table[(size_t)t * bt_stride + p / k_per_block];",
+                                "block_table[(size_t)t * bt_stride + p % k_per_block];",
+                                pins.TOPK_PINS),
+    "topk_reads_padding": ("int64_t n = lengths[t];", "int64_t n = score_stride;", pins.TOPK_PINS),
+    "topk_bad_length_unflagged": ("flags |= 1;\n      n = 0;", "n = 0;", pins.TOPK_PINS),
     # builder
     "ring_newest_first": ("(int64_t)swa_head[t] - n_swa + 1 + j", "(int64_t)swa_head[t] - j",
                           pins.BUILDER_PINS),
