@@ -20,6 +20,8 @@ pool.  `--config` picks another of the five workloads.
             library's timing hook): algorithmic bytes / time vs measured HBM
   cpu_baseline  the fp64 CPU oracle on the host cores (bounded sample)
 
+--path topk times the step in front of the index build: per token, the k
+best-scored of its compressed-cache positions, as (block, slot) lists.
 --path store times the step that fills the pool instead (per-head RMSNorm of
 q, RMSNorm of the new KV row, GPT-J RoPE, store into the SWA ring slot: one
 kernel); --path layer times the three calls of a decode layer's attention
@@ -54,6 +56,7 @@ from sink_sda_decode_gb300 import inputs  # noqa: E402
 
 METRIC = "decode tokens/s and gathered-KV GB/s; % of binding roofline (HBM vs bf16)"
 STORE_METRIC = "q/kv RMSNorm + RoPE + SWA store tokens/s; % of HBM roofline"
+TOPK_METRIC = "top-k -> slot list tokens/s; % of HBM roofline"
 BUILDER_KEYS = ("state_slot", "swa_len", "swa_head", "comp_indptr", "comp_block", "comp_slot")
 DEFAULT_CONFIG = 1
 L2_FLUSH_BYTES = 256 << 20
@@ -252,6 +255,16 @@ def store_algorithmic_bytes(w, rope_dim, kv="bf16"):
     return w.N * per_token + 2 * w.D * 2
 
 
+def topk_algorithmic_bytes(lengths, k, kpb):
+    """Bytes the top-k step must move: every candidate score (fp32) once, the
+    lengths, the block-table rows of the candidates, and the output lists
+    (indptr + a block id and a slot per kept position)."""
+    n = np.asarray(lengths, np.int64)
+    kept = np.minimum(n, k)
+    return int((n * 4).sum() + n.size * 4 + (-(-n // kpb) * 4).sum() + (n.size + 1) * 4
+               + (kept * 8).sum())
+
+
 def algorithmic_flops(w):
     return 4 * w.H * w.D * int(w.total_len)
 
@@ -288,6 +301,18 @@ class Step:
         self.path = path
         self.pool = pool  # an FP8 pool (inputs.Fp8Pool) replaces the bf16 one
         self.dev = device
+        if path == "topk":
+            self.ti = inputs.topk_inputs(w)
+            self.ins = {"scores": self.ti.scores, "lengths": self.ti.lengths,
+                        "block_table": self.ti.block_table}
+            cap = w.N * self.ti.k
+            self.comp = [torch.empty(w.N + 1, dtype=torch.int32, device=device),
+                         torch.empty(cap, dtype=torch.int32, device=device),
+                         torch.empty(cap, dtype=torch.int32, device=device)]
+            self.topk_status = torch.empty(1, dtype=torch.int32, device=device)
+            self.results = list(self.comp)
+            self.launches_per_step = 2
+            return
         self.ins = {"q": w.q}
         if path != "store":
             self.ins.update(w.builder_inputs(device))
@@ -306,7 +331,7 @@ class Step:
             self.ins.setdefault("state_slot", self.si.state_slot)
             self.q_rot = torch.empty_like(w.q)
             self.store_status = torch.empty(1, dtype=torch.int32, device=device)
-        self.result = self.q_rot if path == "store" else self.out
+        self.results = [self.q_rot if path == "store" else self.out]
         self.launches_per_step = {"decode": 6, "store": 1, "layer": 7}[path]
 
     @property
@@ -318,6 +343,15 @@ class Step:
         store kernel on the store path, around the attention kernel otherwise."""
         w = self.w
         ins = ins or self.ins
+        if self.path == "topk":
+            if timing:
+                self.sda.set_timing_events(*timing)
+            self.sda.topk_slots(ins["scores"], ins["lengths"], ins["block_table"], k=self.ti.k,
+                                k_per_block=w.k_per_block, comp_indptr=self.comp[0],
+                                comp_block=self.comp[1], comp_slot=self.comp[2],
+                                status=self.topk_status, stream=stream)
+            self.sda.set_timing_events(None, None)
+            return
         q = ins["q"]
         if self.path != "decode":
             si = self.si
@@ -351,6 +385,10 @@ class Step:
         self.sda.set_timing_events(None, None)
 
     def check_status(self):
+        if self.path == "topk":
+            if int(self.topk_status.item()) != 0:
+                raise RuntimeError(f"top-k status {int(self.topk_status.item())}")
+            return
         if self.path != "store" and int(self.status.item()) != 0:
             raise RuntimeError(f"index builder status {int(self.status.item())}")
         if self.path != "decode" and int(self.store_status.item()) != 0:
@@ -426,14 +464,15 @@ def gpu_arm(args, w, device, ws, rank, pool=None):
     d_in = torch.empty_like(h_in, device=device)
     views = {k: d_in[o:o + p.numel()].view(step.ins[k].dtype).view(step.ins[k].shape)
              for k, o, p in zip(names, offs, parts)}
-    out_h = torch.empty(step.result.shape, dtype=step.result.dtype, pin_memory=True)
+    outs_h = [torch.empty(t_.shape, dtype=t_.dtype, pin_memory=True) for t_ in step.results]
     h2d = sum(t_.numel() for t_ in parts)
-    d2h = out_h.numel() * out_h.element_size()
+    d2h = sum(o.numel() * o.element_size() for o in outs_h)
 
     def e2e_step():
         d_in.copy_(h_in, non_blocking=True)
         step.run(ins=views, stream=s)
-        out_h.copy_(step.result, non_blocking=True)
+        for o, t_ in zip(outs_h, step.results):
+            o.copy_(t_, non_blocking=True)
 
     with torch.cuda.stream(s):
         for _ in range(max(args.warmup, 3)):
@@ -456,7 +495,9 @@ def gpu_arm(args, w, device, ws, rank, pool=None):
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / len(e2e_ev)
     return dict(ms_per_step=ms_per_step, kernel_ms=kernel_ms, e2e_ms=e2e_ms, clocks=cs.summary(),
                 h2d=h2d, d2h=d2h, launches_per_step=step.launches_per_step,
-                rope_dim=step.rope_dim if step.path != "decode" else None)
+                rope_dim=step.rope_dim if step.path in ("store", "layer") else None,
+                topk_bytes=(topk_algorithmic_bytes(step.ti.lengths.cpu().numpy(), step.ti.k,
+                                                   w.k_per_block) if step.path == "topk" else None))
 
 
 # ----------------------------------------------------------------------------- job-wide report
@@ -477,6 +518,8 @@ def reduce_over_ranks(times_ms, units, ws, device):
 
 
 STEP_TEXT = {
+    "topk": "top-k of each token's scores -> compressed (block, slot) lists (2 kernels) as one "
+            "CUDA graph",
     "decode": "index build + decode (plan, attention, combine) as one CUDA graph",
     "store": "q/kv RMSNorm + GPT-J RoPE + SWA ring store (one kernel) as one CUDA graph",
     "layer": "q/kv norm + RoPE + SWA store, index build, decode as one CUDA graph",
@@ -500,6 +543,12 @@ def report_line(args, w, ws, ms_step, ms_kernel, ms_e2e, tokens_total, r):
         bound = "hbm"
         kernel = "q/kv norm + RoPE + SWA store kernel"
         traffic_key = "store_" + args.config
+    elif path == "topk":
+        nbytes = r["topk_bytes"]
+        flops = 0
+        bound = "hbm"
+        kernel = "top-k slot-list kernels (indptr scan + per-token radix select)"
+        traffic_key = "topk_" + args.config
     else:
         nbytes = algorithmic_bytes(w, kv)
         flops = algorithmic_flops(w)
@@ -513,10 +562,11 @@ def report_line(args, w, ws, ms_step, ms_kernel, ms_e2e, tokens_total, r):
     # TFLOP/s of algorithmic FLOPs
     achieved = (nbytes / 1e9 if bound == "hbm" else flops / 1e12) / (ms_kernel * 1e-3)
     line = {
-        "metric": STORE_METRIC if path == "store" else METRIC, "value": value, "unit": "tokens/s",
+        "metric": {"store": STORE_METRIC, "topk": TOPK_METRIC}.get(path, METRIC), "value": value,
+        "unit": "tokens/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if path == "topk" else "bf16", "data": "synthetic",
         "config": {"workload": w.name, "N": w.N, "H": w.H, "D": w.D,
                    "total_slots": int(w.total_len), "pool_slots": w.total_pages,
                    "kv": "bf16" if kv == "bf16" else "fp8 e4m3, fp32 scale per row",
@@ -539,6 +589,8 @@ def report_line(args, w, ws, ms_step, ms_kernel, ms_e2e, tokens_total, r):
     }
     if path == "store":
         line["config"]["rope_dim"] = r["rope_dim"]
+    elif path == "topk":
+        line["config"]["topk"] = {"k": inputs.TOPK_K, "candidates": inputs.TOPK_CANDIDATES}
     else:
         line["gathered_kv_gbs"] = (int(w.total_len) * (w.D * 2 if kv == "bf16" else w.D + 4)
                                    / (ms_step * 1e-3) / 1e9)
@@ -575,6 +627,11 @@ def oracle_job(w, toks, pool=None, path="decode"):
     and / or the decode."""
     import oracle
     calls = []
+    if path == "topk":
+        ti = inputs.topk_inputs(w)
+        targs = (ti.scores.cpu().numpy()[toks], ti.lengths.cpu().numpy()[toks],
+                 ti.block_table.cpu().numpy()[toks], ti.k, w.k_per_block)
+        return lambda: oracle.topk_slots(*targs)
     if path != "decode":
         si = inputs.store_inputs(w)
         bits = inputs.bf16_to_bits
@@ -599,7 +656,7 @@ def oracle_job(w, toks, pool=None, path="decode"):
 
 def oracle_budget(w, path):
     """Tokens per oracle pass: all of them where a pass is cheap."""
-    return w.N if path == "store" or w.total_len <= 200000 else 16
+    return w.N if path in ("store", "topk") or w.total_len <= 200000 else 16
 
 
 def time_oracle(w, seconds, max_tokens, pool=None, path="decode"):
@@ -630,9 +687,9 @@ def main():
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="pool format: bf16 rows, or FP8 E4M3 codes with one fp32 scale per row "
                          "(the workload's pool quantised row by row)")
-    ap.add_argument("--path", choices=["decode", "store", "layer"], default="decode",
+    ap.add_argument("--path", choices=["decode", "store", "layer", "topk"], default="decode",
                     help="decode: index build + decode; store: q/kv norm + RoPE + SWA store; "
-                         "layer: all three")
+                         "layer: store + build + decode; topk: top-k -> slot lists")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -656,11 +713,13 @@ def main():
         el = time.perf_counter() - t0
         tps = len(toks) * args.steps / el
         sample = f"{len(toks)} of {w.N} tokens per step"
-        line = {"metric": STORE_METRIC if args.path == "store" else METRIC, "value": tps,
+        line = {"metric": {"store": STORE_METRIC, "topk": TOPK_METRIC}.get(args.path, METRIC),
+                "value": tps,
                 "unit": "tokens/s", "impl": "reference",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "vs_baseline": None, "dtype": "f32" if args.path == "topk" else "f64",
+                "data": "synthetic",
                 "config": {"workload": w.name, "N": w.N, "H": w.H, "D": w.D,
                            "total_slots": w.total_len, "kv": args.kv, "path": args.path},
                 "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": oracle.num_threads(),

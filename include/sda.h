@@ -194,8 +194,8 @@ sda_status sda_decode_error_flag(const void* workspace, int32_t* device_flag, vo
  * Timing hook.  When both events are non-NULL, every later sda_decode /
  * sda_decode_fp8 made from the calling host thread records `before` on its
  * stream immediately before its attention kernel and `after` immediately
- * after it, and every later sda_qk_norm_rope_swa_store(_fp8) does the same
- * around its kernel, so that the caller can time that kernel alone
+ * after it, and every later sda_qk_norm_rope_swa_store(_fp8) / sda_topk_slots
+ * does the same around its kernel(s), so that the caller can time them alone
  * (cudaEventElapsedTime).  The events are
  * cudaEvent_t handles created and owned by the caller.  NULL, NULL turns the
  * hook off.  No effect on results.
@@ -247,6 +247,38 @@ sda_status sda_build_indices(const int32_t* state_slot, const int32_t* swa_len,
 sda_status sda_validate_indices(const int32_t* kv_indices, int64_t total_indices,
                                 const int32_t* kv_indptr, int N, int64_t total_pages,
                                 int32_t* status, void* stream);
+
+/*
+ * Top-k selection straight into the compressed slot lists of
+ * sda_build_indices.  Source: the sglang attention tag page, entry "DSV4.1
+ * 新增索引器内核，重做 Top-K v2 分派" (NaN padding ranks below a legitimate
+ * -inf; the page-table transform is a separate step from the selection); the
+ * compressed pool entry block_id * K_PER_BLOCK + slot_in_block is the
+ * paged_decode.py docstring's (PR 28392 page).
+ *
+ * Arguments (device pointers):
+ *   scores      [N, score_stride] fp32; token t's candidates are positions
+ *               p < n_t = lengths[t] (later positions are padding: never read)
+ *   lengths     [N] int32; outside [0, score_stride] counts as 0 (bit 1)
+ *   block_table [N, bt_stride] int32: position p of token t lies in block
+ *               block_table[t][p / k_per_block] at slot p % k_per_block;
+ *               bt_stride * k_per_block >= score_stride
+ *   k >= 0, k_per_block > 0; comp_block / comp_slot hold `capacity` entries.
+ * Per token: the min(k, n_t) best candidates -- larger score first, -0 equal
+ * to +0, NaN below -inf (bit 8 if any NaN is a candidate), equal scores by
+ * increasing position -- emitted in increasing position as
+ * (comp_block, comp_slot) = (block_table[t][p / k_per_block], p % k_per_block);
+ * comp_indptr [N + 1] is the prefix sum of min(k, n_t), comp_indptr[0] = 0.
+ * *status (device int32, overwritten): bits 1 (bad length), 4 (a kept
+ * position has a negative block id, emitted as is), 8 (NaN candidate), 32
+ * (the total exceeds capacity: every list is empty).  The outputs are exactly
+ * sda_build_indices' comp_indptr / comp_block / comp_slot inputs.  Two
+ * launches; graph-capturable; the timing hook brackets both.
+ */
+sda_status sda_topk_slots(const float* scores, int64_t score_stride, const int32_t* lengths,
+                          const int32_t* block_table, int64_t bt_stride, int N, int k,
+                          int k_per_block, int32_t* comp_indptr, int32_t* comp_block,
+                          int32_t* comp_slot, int64_t capacity, int32_t* status, void* stream);
 
 /*
  * Fused q / kv RMSNorm + RoPE + SWA ring store: the step of a decode layer

@@ -21,7 +21,7 @@ import torch
 from . import _lib
 
 __all__ = ["decode", "workspace_size", "build_indices", "validate_indices", "decode_error_flag",
-           "decode_kernel", "decode_fp8", "workspace_size_fp8", "qk_norm_rope_swa_store",
+           "decode_kernel", "decode_fp8", "workspace_size_fp8", "qk_norm_rope_swa_store", "topk_slots",
            "decode_host", "set_timing_events", "decode_noalloc", "library_path"]
 
 library_path = _lib.LIB_PATH
@@ -217,7 +217,8 @@ def decode_error_flag(workspace: torch.Tensor, stream=None) -> int:
 def set_timing_events(before: torch.cuda.Event | None, after: torch.cuda.Event | None) -> None:
     """Record `before` / `after` around the attention kernel of every later
     decode() / decode_fp8() and around the kernel of every later
-    qk_norm_rope_swa_store() on this thread (None, None turns it off).
+    qk_norm_rope_swa_store() / topk_slots() on this thread (None, None turns
+    it off).
     Events must be created with enable_timing=True."""
     lib = _lib.load()
     handles = []
@@ -281,6 +282,43 @@ def validate_indices(kv_indices, kv_indptr, total_pages, status=None, stream=Non
                                       _stream_ptr(stream))
     _lib.check(rc, "sda_validate_indices")
     return status
+
+
+def topk_slots(scores, lengths, block_table, *, k, k_per_block, capacity=None, comp_indptr=None,
+               comp_block=None, comp_slot=None, status=None, stream=None):
+    """Per token, the k best of scores[t, :lengths[t]] (NaN below -inf, ties by
+    position), in increasing position, as (block, slot in block) pairs through
+    block_table [N, B]: the comp_indptr / comp_block / comp_slot inputs of
+    build_indices.  Returns (comp_indptr [N+1], comp_block [capacity],
+    comp_slot [capacity], status [1]) int32 device tensors."""
+    lib = _lib.load()
+    _req(scores, "scores", torch.float32, 2)
+    dev = scores.device
+    _req(lengths, "lengths", torch.int32, 1, dev)
+    _req(block_table, "block_table", torch.int32, 2, dev)
+    N, S = scores.shape
+    if lengths.numel() != N or block_table.shape[0] != N:
+        raise ValueError("lengths must be [N] and block_table [N, B]")
+    if capacity is None:
+        capacity = N * int(k)
+    if comp_indptr is None:
+        comp_indptr = torch.empty(N + 1, dtype=torch.int32, device=dev)
+    if comp_block is None:
+        comp_block = torch.empty(max(int(capacity), 1), dtype=torch.int32, device=dev)
+    if comp_slot is None:
+        comp_slot = torch.empty(max(int(capacity), 1), dtype=torch.int32, device=dev)
+    if status is None:
+        status = torch.empty(1, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        rc = lib.sda_topk_slots(scores.data_ptr() if scores.numel() else None, S,
+                                lengths.data_ptr() if N else None,
+                                block_table.data_ptr() if block_table.numel() else None,
+                                block_table.shape[1], N, int(k), int(k_per_block),
+                                comp_indptr.data_ptr(), comp_block.data_ptr(),
+                                comp_slot.data_ptr(), int(capacity), status.data_ptr(),
+                                _stream_ptr(stream))
+    _lib.check(rc, "sda_topk_slots")
+    return comp_indptr, comp_block, comp_slot, status
 
 
 def qk_norm_rope_swa_store(q, kv, q_norm_w, kv_norm_w, cos_cache, sin_cache, positions,

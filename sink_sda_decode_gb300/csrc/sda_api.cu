@@ -385,6 +385,32 @@ sda_status sda_validate_indices(const int32_t* kv_indices, int64_t total_indices
   return SDA_OK;
 }
 
+sda_status sda_topk_slots(const float* scores, int64_t score_stride, const int32_t* lengths,
+                          const int32_t* block_table, int64_t bt_stride, int N, int k,
+                          int k_per_block, int32_t* comp_indptr, int32_t* comp_block,
+                          int32_t* comp_slot, int64_t capacity, int32_t* status, void* stream) {
+  if (N < 0 || k < 0 || k_per_block <= 0 || score_stride < 0 || score_stride > 0x7fffffffll ||
+      bt_stride < 0 || bt_stride * static_cast<int64_t>(k_per_block) < score_stride ||
+      capacity < 0 || capacity > 0x7fffffffll)
+    return SDA_ERR_INVALID_ARG;
+  if (!comp_indptr || !status) return SDA_ERR_INVALID_ARG;
+  if (N > 0 && !lengths) return SDA_ERR_INVALID_ARG;
+  if (N > 0 && k > 0 && score_stride > 0 && (!scores || !block_table)) return SDA_ERR_INVALID_ARG;
+  if (capacity > 0 && (!comp_block || !comp_slot)) return SDA_ERR_INVALID_ARG;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+  if (e == cudaSuccess && g_ev_before && g_ev_after) e = cudaEventRecord(g_ev_before, st);
+  if (e == cudaSuccess)
+    e = launch_topk_slots(scores, score_stride, lengths, block_table, bt_stride, N, k,
+                          k_per_block, comp_indptr, comp_block, comp_slot, capacity, status, st);
+  if (e == cudaSuccess && g_ev_before && g_ev_after) e = cudaEventRecord(g_ev_after, st);
+  if (e != cudaSuccess) {
+    note_cuda_error(e, "sda_topk_slots");
+    return SDA_ERR_CUDA;
+  }
+  return SDA_OK;
+}
+
 static sda_status store_common(const void* q, const void* kv, const void* q_norm_w,
                                const void* kv_norm_w, const float* cos_cache,
                                const float* sin_cache, int max_pos, const int32_t* positions,

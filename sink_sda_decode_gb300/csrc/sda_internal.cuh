@@ -120,6 +120,13 @@ cudaError_t launch_build_indices(const int32_t* state_slot, const int32_t* swa_l
 cudaError_t launch_validate(const int32_t* kv_indices, int64_t total_indices,
                             const int32_t* kv_indptr, int N, int64_t total_pages,
                             int32_t* status, cudaStream_t st);
+// Top-k of each token's scores -> (comp_indptr, comp_block, comp_slot); the
+// caller zeroes *status beforehand.
+cudaError_t launch_topk_slots(const float* scores, int64_t score_stride, const int32_t* lengths,
+                              const int32_t* block_table, int64_t bt_stride, int N, int k,
+                              int k_per_block, int32_t* comp_indptr, int32_t* comp_block,
+                              int32_t* comp_slot, int64_t capacity, int32_t* status,
+                              cudaStream_t st);
 // q/kv RMSNorm + RoPE + SWA ring store; bf16 pool when pool_fp8 == nullptr,
 // else E4M3 codes + row scales.  The caller zeroes *status beforehand.
 cudaError_t launch_qk_norm_rope_store(const void* q, const void* kv, const void* q_norm_w,

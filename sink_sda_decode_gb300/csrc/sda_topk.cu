@@ -1,0 +1,244 @@
+// sda_topk.cu -- top-k selection of compressed-cache entries straight into the
+// slot lists the index builder consumes: for every token, the k best-scored
+// of its candidate positions, emitted in position order as (block id, slot in
+// block) pairs through the token's block table.
+//
+// Source: the sglang attention tag page, entry "DSV4.1 新增索引器内核，重做 Top-K
+// v2 分派": padding is NaN, not a very small number, so that a legitimate -inf
+// stays selectable; the page-table transform is a separate step from the
+// selection.  The pool entry of a compressed position is block_id *
+// K_PER_BLOCK + slot_in_block (the paged_decode.py docstring on the PR 28392
+// page), which sda_build_indices then offsets by swa_pages.
+//
+// Order used (plainest reading, identical on both sides of the parity tests):
+// larger score first, -0 equal to +0, NaN below -inf, equal scores by
+// increasing position.  Scores map to 32-bit keys that preserve that order,
+// so the selection is an exact radix select on integers:
+//   1. topk_indptr_kernel (one CTA): comp_indptr = prefix sums of min(k, n_t);
+//   2. topk_select_kernel (one CTA per token): four 8-bit digit passes (MSB
+//      first) find the key T of the k-th best candidate and how many
+//      candidates equal to T to keep; one ordered pass then keeps every key
+//      above T and the first `need` keys equal to T, writing each kept
+//      position at its rank among kept positions (a block scan per chunk), so
+//      the output is in increasing position with no sort.
+// A token's keys are staged once in shared memory when its row fits
+// (<= kSmemKeys candidates); longer rows are re-read from global memory (L2)
+// by each pass.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "sda_internal.cuh"
+
+namespace sda {
+
+namespace {
+
+constexpr int kTopkThreads = 512;
+constexpr int kSmemKeys = 11264;  // 44 KB of staged keys (static shared memory <= 48 KB)
+
+__device__ __forceinline__ uint32_t score_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return 0u;  // NaN: below every number
+  if (u == 0x80000000u) u = 0u;                     // -0 ranks as +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ int valid_length(const int32_t* lengths, int t, int64_t stride) {
+  const int n = lengths[t];
+  return (n < 0 || n > stride) ? 0 : n;
+}
+
+// Exclusive block scan of one 32-bit value per thread (blockDim.x == kTopkThreads);
+// *total receives the block sum.  `warp_sums` holds kTopkThreads / 32 words.
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_sums,
+                                                         uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    constexpr int kWarps = kTopkThreads / 32;
+    uint32_t w = lane < kWarps ? warp_sums[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kWarps) warp_sums[lane] = w;  // inclusive prefix of the warp totals
+  }
+  __syncthreads();
+  const uint32_t before = warp == 0 ? 0u : warp_sums[warp - 1];
+  *total = warp_sums[kTopkThreads / 32 - 1];
+  __syncthreads();  // warp_sums is reused by the next call
+  return before + x - v;
+}
+
+// comp_indptr[0..N] = prefix sums of min(k, n_t); bit 1 for a bad length, bit 32
+// (and every list empty) if the total exceeds capacity.
+__global__ void __launch_bounds__(kTopkThreads) topk_indptr_kernel(
+    const int32_t* __restrict__ lengths, int64_t score_stride, int N, int k, int64_t capacity,
+    int32_t* __restrict__ comp_indptr, int32_t* __restrict__ status) {
+  pdl_wait();
+  __shared__ uint32_t warp_sums[kTopkThreads / 32];
+  __shared__ int s_flags;
+  if (threadIdx.x == 0) s_flags = 0;
+  __syncthreads();
+  // First pass: the total (to check capacity); second pass: the prefix sums.
+  uint64_t total = 0;
+  for (int base = 0; base < N; base += kTopkThreads) {
+    const int t = base + threadIdx.x;
+    uint32_t c = 0;
+    if (t < N) {
+      const int n = lengths[t];
+      if (n < 0 || n > score_stride) atomicOr(&s_flags, 1);
+      const int vn = valid_length(lengths, t, score_stride);
+      c = static_cast<uint32_t>(vn < k ? vn : k);
+    }
+    uint32_t chunk;
+    block_exclusive_scan(c, warp_sums, &chunk);
+    total += chunk;
+  }
+  const bool over = total > static_cast<uint64_t>(capacity);
+  uint32_t run = 0;
+  if (threadIdx.x == 0) comp_indptr[0] = 0;
+  for (int base = 0; base < N; base += kTopkThreads) {
+    const int t = base + threadIdx.x;
+    uint32_t c = 0;
+    if (t < N && !over) {
+      const int vn = valid_length(lengths, t, score_stride);
+      c = static_cast<uint32_t>(vn < k ? vn : k);
+    }
+    uint32_t chunk;
+    const uint32_t ex = block_exclusive_scan(c, warp_sums, &chunk);
+    if (t < N) comp_indptr[t + 1] = static_cast<int32_t>(run + ex + c);
+    run += chunk;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int f = s_flags | (over ? 32 : 0);
+    if (f) atomicOr(status, f);
+  }
+  pdl_trigger();
+}
+
+template <bool STAGED>
+__global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(
+    const float* __restrict__ scores, int64_t score_stride, const int32_t* __restrict__ lengths,
+    const int32_t* __restrict__ block_table, int64_t bt_stride, int k, int k_per_block,
+    const int32_t* __restrict__ comp_indptr, int32_t* __restrict__ comp_block,
+    int32_t* __restrict__ comp_slot, int32_t* __restrict__ status) {
+  pdl_wait();
+  __shared__ uint32_t s_keys[STAGED ? kSmemKeys : 1];
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t warp_sums[kTopkThreads / 32];
+  __shared__ uint32_t s_digit, s_above;
+  const int t = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int n = valid_length(lengths, t, score_stride);
+  const int kk = n < k ? n : k;
+  const int32_t out0 = comp_indptr[t];
+  // kk == 0, or the lists were emptied for lack of capacity
+  if (kk == 0 || comp_indptr[t + 1] - out0 != kk) return;
+  const float* row = scores + static_cast<size_t>(t) * score_stride;
+  const int32_t* bt = block_table + static_cast<size_t>(t) * bt_stride;
+  int flags = 0;
+
+  auto emit = [&](int idx, int p) {
+    const int32_t blk = bt[p / k_per_block];
+    if (blk < 0) flags |= 4;
+    comp_block[out0 + idx] = blk;
+    comp_slot[out0 + idx] = p % k_per_block;
+  };
+
+  bool nan_seen = false;
+  if (kk == n) {  // every candidate is kept, in position order
+    for (int p = tid; p < n; p += kTopkThreads) {
+      nan_seen |= score_key(row[p]) == 0u;
+      emit(p, p);
+    }
+  } else {
+    if (STAGED) {
+      for (int p = tid; p < n; p += kTopkThreads) {
+        const uint32_t key = score_key(row[p]);
+        nan_seen |= key == 0u;
+        s_keys[p] = key;
+      }
+      __syncthreads();
+    }
+    auto key_at = [&](int p) -> uint32_t { return STAGED ? s_keys[p] : score_key(__ldg(row + p)); };
+    uint32_t prefix = 0, mask = 0, need = static_cast<uint32_t>(kk);
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      if (tid < 256) hist[tid] = 0;
+      __syncthreads();
+      for (int p = tid; p < n; p += kTopkThreads) {
+        const uint32_t key = key_at(p);
+        if (!STAGED && shift == 24) nan_seen |= key == 0u;
+        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      // Suffix sums over the digits, largest digit first: thread i holds bin 255 - i.
+      const uint32_t h = tid < 256 ? hist[255 - tid] : 0u;
+      uint32_t total;
+      const uint32_t above = block_exclusive_scan(h, warp_sums, &total);  // keys in higher bins
+      if (tid < 256 && above < need && above + h >= need) {
+        s_digit = 255u - tid;
+        s_above = above;
+      }
+      __syncthreads();
+      prefix |= s_digit << shift;
+      mask |= 255u << shift;
+      need -= s_above;
+      __syncthreads();
+    }
+    // prefix = the k-th best key T; keep every key > T and the first `need`
+    // keys == T, each at its rank among the kept positions.
+    const uint32_t T = prefix;
+    uint32_t kept = 0, ties = 0;
+    for (int base = 0; base < n; base += kTopkThreads) {
+      const int p = base + tid;
+      const uint32_t key = p < n ? key_at(p) : 0u;
+      const uint32_t gt = (p < n && key > T) ? 1u : 0u;
+      const uint32_t eq = (p < n && key == T) ? 1u : 0u;
+      uint32_t tot;
+      const uint32_t ex = block_exclusive_scan((eq << 16) | gt, warp_sums, &tot);
+      const uint32_t gt_ex = ex & 0xffffu, eq_ex = ex >> 16;
+      const uint32_t room = need > ties ? need - ties : 0u;  // ties still to keep
+      if (gt || (eq && eq_ex < room)) emit(static_cast<int>(kept + gt_ex + min(eq_ex, room)), p);
+      const uint32_t gt_tot = tot & 0xffffu, eq_tot = tot >> 16;
+      kept += gt_tot + min(eq_tot, room);
+      ties += eq_tot;
+    }
+  }
+  if (nan_seen) flags |= 8;
+  if (__syncthreads_or(flags)) {
+    if (flags) atomicOr(status, flags);
+  }
+  pdl_trigger();
+}
+
+}  // namespace
+
+cudaError_t launch_topk_slots(const float* scores, int64_t score_stride, const int32_t* lengths,
+                              const int32_t* block_table, int64_t bt_stride, int N, int k,
+                              int k_per_block, int32_t* comp_indptr, int32_t* comp_block,
+                              int32_t* comp_slot, int64_t capacity, int32_t* status,
+                              cudaStream_t st) {
+  cudaError_t e = launch_pdl(topk_indptr_kernel, dim3(1), dim3(kTopkThreads), 0, st, lengths,
+                             score_stride, N, k, capacity, comp_indptr, status);
+  if (e != cudaSuccess || N == 0 || k == 0) return e;
+  if (score_stride <= kSmemKeys)
+    return launch_pdl(topk_select_kernel<true>, dim3(N), dim3(kTopkThreads), 0, st, scores,
+                      score_stride, lengths, block_table, bt_stride, k, k_per_block, comp_indptr,
+                      comp_block, comp_slot, status);
+  return launch_pdl(topk_select_kernel<false>, dim3(N), dim3(kTopkThreads), 0, st, scores,
+                    score_stride, lengths, block_table, bt_stride, k, k_per_block, comp_indptr,
+                    comp_block, comp_slot, status);
+}
+
+}  // namespace sda

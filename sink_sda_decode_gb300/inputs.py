@@ -206,6 +206,47 @@ def store_inputs(w: "Workload", rope_dim: int = ROPE_DIM, max_pos: int = MAX_POS
                               f"{rope_dim} dims, positions = ring head + win * U{{1..{max_pos // win - 1}}}")
 
 
+TOPK_K = 512          # compressed entries kept per token (the workloads' compressed lists)
+TOPK_CANDIDATES = 8192
+
+
+@dataclasses.dataclass
+class TopkInputs:
+    """Inputs of the top-k -> slot-list step: per-token indexer scores over
+    the token's compressed-cache positions and its block table."""
+    scores: torch.Tensor       # [N, S] fp32
+    lengths: torch.Tensor      # [N] int32 (0 for padded tokens)
+    block_table: torch.Tensor  # [N, S / k_per_block] int32, distinct blocks per token
+    k: int
+    recipe: str = ""
+
+
+def topk_inputs(w: "Workload", candidates: int = TOPK_CANDIDATES, k: int = TOPK_K,
+                seed: int | None = None, ragged: bool | None = None) -> TopkInputs:
+    """Top-k inputs matching a decode workload: scores ~ N(0,1) fp32 over
+    `candidates` positions per token (uniform U{0..candidates} lengths when
+    `ragged`, by default for workloads that pad tokens), length 0 for padded
+    tokens, and a block table of distinct random blocks of the workload's
+    compressed region."""
+    rng = np.random.default_rng(SEED_BASE + 900 + w.N % 997 if seed is None else seed)
+    dev = w.q.device
+    N, kpb = w.N, w.k_per_block
+    B = -(-candidates // kpb)
+    n_blocks = (w.total_pages - w.swa_pages) // kpb
+    scores = rng.standard_normal((N, candidates), dtype=np.float32)
+    if ragged is None:
+        ragged = bool((w.state_slot < 0).any())
+    lens = rng.integers(0, candidates + 1, N) if ragged else np.full(N, candidates)
+    lens[w.state_slot < 0] = 0
+    bt = np.stack([rng.choice(n_blocks, B, replace=False) for _ in range(N)]).astype(np.int32)
+    return TopkInputs(scores=torch.from_numpy(scores).to(dev),
+                      lengths=torch.from_numpy(lens.astype(np.int32)).to(dev),
+                      block_table=torch.from_numpy(bt).to(dev), k=k,
+                      recipe=f"scores N(0,1) fp32 over {candidates} positions"
+                             f"{' (lengths U{0..%d})' % candidates if ragged else ''}, k={k}, "
+                             f"{B} distinct random blocks per token")
+
+
 def fp8_rows_for(w: "Workload", pool: Fp8Pool, tokens=None):
     """Host copy of an FP8 pool restricted to the rows the given tokens read:
     (codes [R, D] uint8, scale [R] fp32, kv_indices remapped into [0, R),
