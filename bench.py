@@ -82,25 +82,34 @@ def peaks():
         return HBM_FALLBACK_GBS, BF16_FALLBACK_TFLOPS, "fallback"
 
 
-def kernel_source_hash():
+# The source files that define each measured kernel (its own file, the
+# headers it includes): a committed ncu figure is used only while these are
+# unchanged.
+KERNEL_SOURCES = {
+    "decode": ("sda_decode_umma.cu", "umma_ptx.cuh", "sda_internal.cuh"),
+    "store": ("sda_store.cu", "sda_internal.cuh"),
+    "topk": ("sda_topk.cu", "sda_internal.cuh"),
+}
+
+
+def kernel_source_hash(kernel="decode"):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sink_sda_decode_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in sorted(KERNEL_SOURCES[kernel]):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(config_name):
-    """DRAM bytes per launch of the attention kernel from the committed ncu
-    summary, only if it was taken on the current kernel sources."""
+def ncu_traffic(config_name, kernel="decode"):
+    """DRAM bytes per launch of the measured kernel from the committed ncu
+    summary, only if it was taken on the current sources of that kernel."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
         e = d.get(config_name)
-        if e and e.get("kernel_sources") == kernel_source_hash():
+        if e and e.get("kernel_sources") == kernel_source_hash(kernel):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -577,7 +586,8 @@ def report_line(args, w, ws, ms_step, ms_kernel, ms_e2e, tokens_total, r):
                      "peak": hbm if bound == "hbm" else bf16,
                      "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
                      "frac": achieved / (hbm if bound == "hbm" else bf16),
-                     "traffic": ncu_traffic(traffic_key),
+                     "traffic": ncu_traffic(traffic_key, path if path in ("store", "topk")
+                                            else "decode"),
                      "peak_source": peak_src,
                      "kernel": kernel, "kernel_ms": ms_kernel,
                      "algorithmic_bytes": nbytes, "algorithmic_flops": flops,

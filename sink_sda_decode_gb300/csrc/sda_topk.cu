@@ -14,11 +14,14 @@
 // larger score first, -0 equal to +0, NaN below -inf, equal scores by
 // increasing position.  Scores map to 32-bit keys that preserve that order,
 // so the selection is an exact radix select on integers:
-//   1. topk_indptr_kernel (one CTA): comp_indptr = prefix sums of min(k, n_t);
-//   2. topk_select_kernel (one CTA per token): four 8-bit digit passes (MSB
-//      first) find the key T of the k-th best candidate and how many
-//      candidates equal to T to keep; one ordered pass then keeps every key
-//      above T and the first `need` keys equal to T, writing each kept
+//   1. topk_indptr_kernel (one CTA): comp_indptr = prefix sums of min(k, n_t)
+//      (for batches of up to 4096 tokens each select CTA computes its own
+//      entry instead, and this launch is skipped);
+//   2. topk_select_kernel (one CTA per token): up to four 8-bit digit passes
+//      (MSB first) find the key T of the k-th best candidate and how many
+//      candidates equal to T to keep (stopping early once the digit bin that
+//      holds the k-th key is kept whole); one ordered pass then keeps every
+//      key above T and the first `need` keys equal to T, writing each kept
 //      position at its rank among kept positions (a block scan per chunk), so
 //      the output is in increasing position with no sort.
 // A token's keys are staged once in shared memory when its row fits
@@ -34,7 +37,7 @@ namespace sda {
 
 namespace {
 
-constexpr int kTopkThreads = 512;
+constexpr int kTopkThreads = 1024;
 constexpr int kSmemKeys = 11264;  // 44 KB of staged keys (static shared memory <= 48 KB)
 
 __device__ __forceinline__ uint32_t score_key(float f) {
@@ -127,26 +130,83 @@ __global__ void __launch_bounds__(kTopkThreads) topk_indptr_kernel(
   pdl_trigger();
 }
 
-template <bool STAGED>
-__global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(
+// Each thread handles groups of kIpt consecutive positions (one 16-byte
+// shared-memory access for staged keys), so that the histogram passes and
+// the ordered pass take a quarter of the loop trips and block scans.
+constexpr int kIpt = 4;
+
+// Sum over the block of two values per thread (FUSED offsets).
+__device__ __forceinline__ void block_sum2(uint32_t a, uint32_t b, uint32_t* sa, uint32_t* sb,
+                                           uint32_t (*parts)[2]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  a = __reduce_add_sync(0xffffffffu, a);
+  b = __reduce_add_sync(0xffffffffu, b);
+  if (lane == 0) parts[warp][0] = a, parts[warp][1] = b;
+  __syncthreads();
+  uint32_t x = 0, y = 0;
+  for (int w = 0; w < kTopkThreads / 32; ++w) x += parts[w][0], y += parts[w][1];
+  *sa = x;
+  *sb = y;
+  __syncthreads();
+}
+
+// FUSED (batches of at most kFusedTokens tokens whose kept counts sum below
+// 2^31): each CTA also sums the kept counts of the tokens before it and of
+// all tokens (lengths are a few KB, read from L2 by every CTA), writes its own
+// comp_indptr entry and checks the capacity, which saves the separate scan
+// launch.
+constexpr int kFusedTokens = 4096;
+
+template <bool STAGED, bool FUSED>
+__global__ void __launch_bounds__(kTopkThreads, 2) topk_select_kernel(
     const float* __restrict__ scores, int64_t score_stride, const int32_t* __restrict__ lengths,
-    const int32_t* __restrict__ block_table, int64_t bt_stride, int k, int k_per_block,
-    const int32_t* __restrict__ comp_indptr, int32_t* __restrict__ comp_block,
+    const int32_t* __restrict__ block_table, int64_t bt_stride, int N, int k, int k_per_block,
+    int64_t capacity, int32_t* __restrict__ comp_indptr, int32_t* __restrict__ comp_block,
     int32_t* __restrict__ comp_slot, int32_t* __restrict__ status) {
   pdl_wait();
-  __shared__ uint32_t s_keys[STAGED ? kSmemKeys : 1];
+  __shared__ __align__(16) uint32_t s_keys[STAGED ? kSmemKeys : kIpt];
   __shared__ uint32_t hist[256];
   __shared__ uint32_t warp_sums[kTopkThreads / 32];
-  __shared__ uint32_t s_digit, s_above;
+  __shared__ uint32_t parts[FUSED ? kTopkThreads / 32 : 1][2];
+  __shared__ uint32_t s_digit, s_above, s_count;
   const int t = blockIdx.x;
   const int tid = threadIdx.x;
   const int n = valid_length(lengths, t, score_stride);
   const int kk = n < k ? n : k;
-  const int32_t out0 = comp_indptr[t];
-  // kk == 0, or the lists were emptied for lack of capacity
-  if (kk == 0 || comp_indptr[t + 1] - out0 != kk) return;
+  int32_t out0;
+  if constexpr (FUSED) {
+    uint32_t before = 0, all = 0;
+    int bad = 0;
+    for (int u = tid; u < N; u += kTopkThreads) {
+      const int lu = lengths[u];
+      bad |= (lu < 0 || lu > score_stride) ? 1 : 0;
+      const int vu = (lu < 0 || lu > score_stride) ? 0 : lu;
+      const uint32_t c = static_cast<uint32_t>(vu < k ? vu : k);
+      all += c;
+      before += u < t ? c : 0u;
+    }
+    bad = __syncthreads_or(bad);
+    uint32_t s_before, s_all;
+    block_sum2(before, all, &s_before, &s_all, parts);
+    const bool over = static_cast<int64_t>(s_all) > capacity;
+    if (tid == 0) {
+      comp_indptr[t + 1] = over ? 0 : static_cast<int32_t>(s_before + kk);
+      if (t == 0) {
+        comp_indptr[0] = 0;
+        const int f = (bad ? 1 : 0) | (over ? 32 : 0);
+        if (f) atomicOr(status, f);
+      }
+    }
+    if (over || kk == 0) return;
+    out0 = static_cast<int32_t>(s_before);
+  } else {
+    out0 = comp_indptr[t];
+    // kk == 0, or the lists were emptied for lack of capacity
+    if (kk == 0 || comp_indptr[t + 1] - out0 != kk) return;
+  }
   const float* row = scores + static_cast<size_t>(t) * score_stride;
   const int32_t* bt = block_table + static_cast<size_t>(t) * bt_stride;
+  const int groups = (n + kIpt - 1) / kIpt;
   int flags = 0;
 
   auto emit = [&](int idx, int p) {
@@ -154,6 +214,20 @@ __global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(
     if (blk < 0) flags |= 4;
     comp_block[out0 + idx] = blk;
     comp_slot[out0 + idx] = p % k_per_block;
+  };
+  // The keys of positions kIpt*g .. kIpt*g+kIpt-1 (0 past the row's end;
+  // `valid` tells them apart from NaN keys).
+  auto keys_at = [&](int g, uint32_t (&key)[kIpt]) {
+    if (STAGED) {
+      const uint4 v = reinterpret_cast<const uint4*>(s_keys)[g];
+      key[0] = v.x, key[1] = v.y, key[2] = v.z, key[3] = v.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < kIpt; ++e) {
+        const int p = kIpt * g + e;
+        key[e] = p < n ? score_key(__ldg(row + p)) : 0u;
+      }
+    }
   };
 
   bool nan_seen = false;
@@ -164,22 +238,31 @@ __global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(
     }
   } else {
     if (STAGED) {
-      for (int p = tid; p < n; p += kTopkThreads) {
-        const uint32_t key = score_key(row[p]);
-        nan_seen |= key == 0u;
-        s_keys[p] = key;
+      for (int g = tid; g < groups; g += kTopkThreads) {
+        uint32_t key[kIpt];
+#pragma unroll
+        for (int e = 0; e < kIpt; ++e) {
+          const int p = kIpt * g + e;
+          key[e] = p < n ? score_key(row[p]) : 0u;
+          nan_seen |= p < n && key[e] == 0u;
+        }
+        reinterpret_cast<uint4*>(s_keys)[g] = make_uint4(key[0], key[1], key[2], key[3]);
       }
       __syncthreads();
     }
-    auto key_at = [&](int p) -> uint32_t { return STAGED ? s_keys[p] : score_key(__ldg(row + p)); };
     uint32_t prefix = 0, mask = 0, need = static_cast<uint32_t>(kk);
     for (int shift = 24; shift >= 0; shift -= 8) {
       if (tid < 256) hist[tid] = 0;
       __syncthreads();
-      for (int p = tid; p < n; p += kTopkThreads) {
-        const uint32_t key = key_at(p);
-        if (!STAGED && shift == 24) nan_seen |= key == 0u;
-        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+      for (int g = tid; g < groups; g += kTopkThreads) {
+        uint32_t key[kIpt];
+        keys_at(g, key);
+#pragma unroll
+        for (int e = 0; e < kIpt; ++e) {
+          const bool valid = kIpt * g + e < n;
+          if (!STAGED && shift == 24) nan_seen |= valid && key[e] == 0u;
+          if (valid && (key[e] & mask) == prefix) atomicAdd(&hist[(key[e] >> shift) & 255u], 1u);
+        }
       }
       __syncthreads();
       // Suffix sums over the digits, largest digit first: thread i holds bin 255 - i.
@@ -189,27 +272,46 @@ __global__ void __launch_bounds__(kTopkThreads) topk_select_kernel(
       if (tid < 256 && above < need && above + h >= need) {
         s_digit = 255u - tid;
         s_above = above;
+        s_count = h;
       }
       __syncthreads();
       prefix |= s_digit << shift;
       mask |= 255u << shift;
       need -= s_above;
+      const bool whole_bin = need == s_count;  // every key of the bin is kept: done
       __syncthreads();
+      if (whole_bin) break;
     }
-    // prefix = the k-th best key T; keep every key > T and the first `need`
-    // keys == T, each at its rank among the kept positions.
-    const uint32_t T = prefix;
+    // Keep every key whose leading (mask) bits exceed prefix, and the first
+    // `need` keys whose leading bits equal it (with the full mask: the k-th
+    // best key T itself), each at its rank among the kept positions.
     uint32_t kept = 0, ties = 0;
-    for (int base = 0; base < n; base += kTopkThreads) {
-      const int p = base + tid;
-      const uint32_t key = p < n ? key_at(p) : 0u;
-      const uint32_t gt = (p < n && key > T) ? 1u : 0u;
-      const uint32_t eq = (p < n && key == T) ? 1u : 0u;
+    for (int g0 = 0; g0 < groups; g0 += kTopkThreads) {
+      const int g = g0 + tid;
+      uint32_t key[kIpt] = {0u, 0u, 0u, 0u};
+      if (g < groups) keys_at(g, key);
+      uint32_t gt_bits = 0, eq_bits = 0;
+#pragma unroll
+      for (int e = 0; e < kIpt; ++e) {
+        const bool valid = g < groups && kIpt * g + e < n;
+        const uint32_t m = key[e] & mask;
+        gt_bits |= (valid && m > prefix) ? 1u << e : 0u;
+        eq_bits |= (valid && m == prefix) ? 1u << e : 0u;
+      }
       uint32_t tot;
-      const uint32_t ex = block_exclusive_scan((eq << 16) | gt, warp_sums, &tot);
-      const uint32_t gt_ex = ex & 0xffffu, eq_ex = ex >> 16;
+      const uint32_t ex =
+          block_exclusive_scan((static_cast<uint32_t>(__popc(eq_bits)) << 16) | __popc(gt_bits),
+                               warp_sums, &tot);
       const uint32_t room = need > ties ? need - ties : 0u;  // ties still to keep
-      if (gt || (eq && eq_ex < room)) emit(static_cast<int>(kept + gt_ex + min(eq_ex, room)), p);
+      uint32_t gt_before = ex & 0xffffu, eq_before = ex >> 16;
+#pragma unroll
+      for (int e = 0; e < kIpt; ++e) {
+        const bool gt = (gt_bits >> e) & 1u, eq = (eq_bits >> e) & 1u;
+        if (gt || (eq && eq_before < room))
+          emit(static_cast<int>(kept + gt_before + min(eq_before, room)), kIpt * g + e);
+        gt_before += gt;
+        eq_before += eq;
+      }
       const uint32_t gt_tot = tot & 0xffffu, eq_tot = tot >> 16;
       kept += gt_tot + min(eq_tot, room);
       ties += eq_tot;
@@ -229,16 +331,21 @@ cudaError_t launch_topk_slots(const float* scores, int64_t score_stride, const i
                               int k_per_block, int32_t* comp_indptr, int32_t* comp_block,
                               int32_t* comp_slot, int64_t capacity, int32_t* status,
                               cudaStream_t st) {
-  cudaError_t e = launch_pdl(topk_indptr_kernel, dim3(1), dim3(kTopkThreads), 0, st, lengths,
-                             score_stride, N, k, capacity, comp_indptr, status);
-  if (e != cudaSuccess || N == 0 || k == 0) return e;
-  if (score_stride <= kSmemKeys)
-    return launch_pdl(topk_select_kernel<true>, dim3(N), dim3(kTopkThreads), 0, st, scores,
-                      score_stride, lengths, block_table, bt_stride, k, k_per_block, comp_indptr,
-                      comp_block, comp_slot, status);
-  return launch_pdl(topk_select_kernel<false>, dim3(N), dim3(kTopkThreads), 0, st, scores,
-                    score_stride, lengths, block_table, bt_stride, k, k_per_block, comp_indptr,
-                    comp_block, comp_slot, status);
+  const int64_t max_keep = k < score_stride ? k : score_stride;
+  const bool fused = N > 0 && N <= kFusedTokens && k > 0 && N * max_keep < (int64_t{1} << 31);
+  if (!fused) {
+    cudaError_t e = launch_pdl(topk_indptr_kernel, dim3(1), dim3(kTopkThreads), 0, st, lengths,
+                               score_stride, N, k, capacity, comp_indptr, status);
+    if (e != cudaSuccess || N == 0 || k == 0) return e;
+  }
+  const bool staged = score_stride <= kSmemKeys;
+#define SDA_TOPK(S, F)                                                                    \
+  launch_pdl(topk_select_kernel<S, F>, dim3(N), dim3(kTopkThreads), 0, st, scores,      \
+             score_stride, lengths, block_table, bt_stride, N, k, k_per_block, capacity, \
+             comp_indptr, comp_block, comp_slot, status)
+  if (fused) return staged ? SDA_TOPK(true, true) : SDA_TOPK(false, true);
+  return staged ? SDA_TOPK(true, false) : SDA_TOPK(false, false);
+#undef SDA_TOPK
 }
 
 }  // namespace sda

@@ -178,3 +178,19 @@ def test_topk_build_decode_pipeline():
     want = oracle.sda_decode(w.q_bits()[tok], rows, sub_idx, sub_ptr, w.attn_sink.cpu().numpy(),
                              w.softmax_scale)
     parity.assert_parity(parity.compare(out[torch.from_numpy(tok).cuda()], want), "topk+build+decode")
+
+
+@pytest.mark.parametrize("N,S", [(4200, 200), (4097, 11268)])
+def test_topk_large_batches(N, S):
+    """More than 4096 tokens: comp_indptr comes from the separate scan kernel
+    (smaller batches compute it inside the selection kernel); rows staged in
+    shared memory and rows read from L2."""
+    rng = np.random.default_rng(N + S)
+    scores = special_scores(rng, N, S)
+    lens = rng.integers(0, S + 1, N).astype(np.int32)
+    lens[::7] = S
+    kpb = 32
+    bt = rng.integers(0, 10**5, (N, -(-S // kpb))).astype(np.int32)
+    got, ref = run_both(torch.from_numpy(scores).cuda(), torch.from_numpy(lens).cuda(),
+                        torch.from_numpy(bt).cuda(), 9, kpb)
+    assert_equal(got, ref, f"N={N} S={S}")
