@@ -378,7 +378,7 @@ def topk_slots(scores, lengths, block_table, k, k_per_block, lib=None):
     ln = _as(lengths, np.int32)
     bt = _as(block_table, np.int32)
     assert ln.shape == (N,) and bt.ndim == 2 and bt.shape[0] == N
-    cap = max(1, int(np.minimum(np.clip(ln, 0, S), k).sum()))
+    cap = max(1, N * int(k))  # room for k per token whatever the lengths say
     ptr = np.zeros(N + 1, np.int32)
     blk = np.zeros(cap, np.int32)
     slot = np.zeros(cap, np.int32)
