@@ -409,15 +409,36 @@ def longtail_h64(device="cpu", seed=SEED_BASE + 4):
                      longtail_h64.__doc__, q_rng=rng)
 
 
-GENERATORS = [tiny, h16, ragged_h64, h128, longtail_h64]
-CONFIG_NAMES = ["tiny", "h16", "ragged_h64", "h128", "longtail_h64"]
+def prefill_h64(device="cpu", seed=SEED_BASE + 5):
+    """Sparse prefill: one chunk of N=2048 consecutive tokens of a sequence,
+    H=64, D=512, pool 2^21 slots, no SWA region.  Token i attends over its
+    causal window of the chunk's own rows (slots max(0, i-127) .. i of a
+    staging region at the start of the pool, where the chunk's new K/V rows
+    sit: 1..128 entries) and over 512 compressed entries drawn for it from a
+    2048-entry candidate set the whole chunk shares (neighbouring tokens'
+    selections over the same context overlap heavily); sink ~ N(0,1).  The
+    lists go through the index builder as compressed (block, slot) pairs."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    N, H, D, P = 2048, 64, 512, 1 << 21
+    cand = N + rng.choice(P - N, 2048, replace=False)
+    lists, swa = [], []
+    for i in range(N):
+        window = np.arange(max(0, i - WIN + 1), i + 1)
+        lists.append(np.concatenate([window, rng.choice(cand, 512, replace=False)]))
+        swa.append((0, 0, 0))
+    return _assemble("N=2048 H=64 D=512 prefill chunk", N, H, D, P, lists, swa, 0, 1.0, seed,
+                     device, prefill_h64.__doc__, q_rng=rng)
+
+
+GENERATORS = [tiny, h16, ragged_h64, h128, longtail_h64, prefill_h64]
+CONFIG_NAMES = ["tiny", "h16", "ragged_h64", "h128", "longtail_h64", "prefill_h64"]
 
 
 SHARD_SEED_STRIDE = 1000
 
 
 def config(i: int, device="cpu", shard: int = 0) -> Workload:
-    """Workload i (0..4) with its fixed seed SEED_BASE + i.
+    """Workload i (0..5) with its fixed seed SEED_BASE + i.
 
     `shard` > 0 draws another batch of the same recipe (seed offset by
     SHARD_SEED_STRIDE per shard): under data parallelism each process decodes

@@ -33,7 +33,7 @@ def test_golden_example():
     assert st == g["status"][0]
 
 
-@pytest.mark.parametrize("cfg", range(5), ids=inputs.CONFIG_NAMES)
+@pytest.mark.parametrize("cfg", range(len(inputs.CONFIG_NAMES)), ids=inputs.CONFIG_NAMES)
 def test_workload_lists_bit_exact(cfg):
     w = inputs.config(cfg, device="cuda")
     args = (w.state_slot, w.swa_len, w.swa_head, w.comp_indptr, w.comp_block, w.comp_slot, w.win,

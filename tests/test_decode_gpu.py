@@ -44,7 +44,7 @@ def _force(monkeypatch, variant):
 
 
 @pytest.mark.parametrize("variant", TC_VARIANTS)
-@pytest.mark.parametrize("cfg,k", [(0, None), (1, None), (2, 40), (3, 24), (4, 24)],
+@pytest.mark.parametrize("cfg,k", [(0, None), (1, None), (2, 40), (3, 24), (4, 24), (5, 24)],
                          ids=inputs.CONFIG_NAMES)
 def test_workload_parity(monkeypatch, cfg, k, variant):
     _force(monkeypatch, variant)
@@ -346,3 +346,16 @@ def test_negative_and_large_softmax_scale():
     for scale in (-w.softmax_scale, 4.0 * w.softmax_scale):
         out = parity.run_gpu(w, scale=scale)
         parity.assert_parity(parity.compare(out, parity.run_oracle(w, scale=scale)), f"scale {scale}")
+
+
+def test_prefill_chunk_first_and_last_tokens():
+    """The sparse-prefill chunk: the first tokens (causal windows of 1..8 rows
+    of the chunk's own staging region) and the last ones (full windows) against
+    the oracle, through the same build + decode call sequence."""
+    w = inputs.config(5, device="cuda")
+    out = parity.run_gpu(w)
+    torch.cuda.synchronize()
+    toks = list(range(8)) + list(range(w.N - 4, w.N))
+    ref = parity.run_oracle(w, tokens=toks)
+    parity.assert_parity(parity.compare(out[torch.tensor(toks, device=out.device)], ref),
+                         "prefill first/last tokens")
