@@ -64,6 +64,27 @@ __device__ __forceinline__ void unpack8(const uint4& v, float f[8]) {
   }
 }
 
+// Packed fp32 pairs (Blackwell's f32x2 FMA pipe): one instruction, two IEEE
+// round-to-nearest results, bit-identical to two scalar operations.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
 __device__ __forceinline__ uint4 pack8_bf16(const float f[8]) {
   uint32_t w[4];
 #pragma unroll
@@ -126,13 +147,19 @@ __device__ __forceinline__ void process_row(const StoreParams& p, int lane, cons
   }
   // RMSNorm: one sum of squares over the row (lane partials, then the warp).
   float f[CPL][8];
-  float ss = 0.f;
+  uint64_t ss2 = 0;  // (even, odd) partial sums
 #pragma unroll
   for (int j = 0; j < CPL; ++j) {
     unpack8(x[j], f[j]);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) ss = fmaf(f[j][k], f[j][k], ss);
+    for (int k = 0; k < 8; k += 2) {
+      const uint64_t v = f2_pack(f[j][k], f[j][k + 1]);
+      ss2 = f2_fma(v, v, ss2);
+    }
   }
+  float ss_even, ss_odd;
+  f2_unpack(ss2, ss_even, ss_odd);
+  float ss = ss_even + ss_odd;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   const float inv_rms = 1.0f / sqrtf(ss / static_cast<float>(p.D) + p.eps);
@@ -143,8 +170,13 @@ __device__ __forceinline__ void process_row(const StoreParams& p, int lane, cons
     const int c = lane + 32 * j;
     float w[8];
     unpack8(c < chunks ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0), w);  // L1-resident
+    const uint64_t inv2 = f2_pack(inv_rms, inv_rms);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) f[j][k] = f[j][k] * inv_rms * w[k];
+    for (int k = 0; k < 8; k += 2) {  // (x * r) * w, as two scalar products would round
+      const uint64_t y = f2_mul(f2_mul(f2_pack(f[j][k], f[j][k + 1]), inv2),
+                                f2_pack(w[k], w[k + 1]));
+      f2_unpack(y, f[j][k], f[j][k + 1]);
+    }
     if (c >= rope_chunk0 && c < chunks && (!LASTJ || j == CPL - 1)) {
       // GPT-J rotation of the pairs (2i, 2i+1), i = 4 (c - rope_chunk0) + 0..3.
       float4 cs = cs_last, sn = sn_last;
@@ -201,31 +233,17 @@ __device__ __forceinline__ void process_row(const StoreParams& p, int lane, cons
   }
 }
 
-// State slot and position of the tokens of rows base .. base+RPW-1 (-1 past
-// the last row).  Row counts fit in 32 bits (checked on the host).
-template <int RPW>
-__device__ __forceinline__ void load_meta(const StoreParams& p, int base, int (&st)[RPW],
-                                          int (&pos)[RPW]) {
-#pragma unroll
-  for (int r = 0; r < RPW; ++r) {
-    const int row = base + r;
-    const bool valid = row < static_cast<int>(p.rows);
-    const int t = valid ? static_cast<int>(static_cast<unsigned>(row) / (p.H + 1)) : 0;
-    st[r] = valid ? __ldg(p.state_slot + t) : -1;
-    pos[r] = valid ? __ldg(p.positions + t) : -1;
-  }
-}
-
-// CPL: 16-byte chunks per lane (D <= 256 * CPL); RPW: rows a warp loads at
-// once (1: measured best with 5 CTAs = 40 warps per SM).  A warp walks its row batches grid-stride.  The state slots and
-// positions of the next batch are requested one batch ahead, so that a
-// batch's row loads and (LASTJ) its RoPE factor loads go out together: one
-// memory latency per batch rather than a position load followed by a
-// dependent cache load.
+// A warp owns one row at a time and walks the rows grid-stride (measured
+// best: one row per warp, 4-5 CTAs = 32-40 warps per SM; more rows per warp cost
+// warps).  The state slot and position of the next row are requested one row
+// ahead, so that a row's load and (LASTJ) its RoPE factor loads go out
+// together: one memory latency per row rather than a position load followed
+// by a dependent cache load.  The row -> (token, head) split is advanced
+// incrementally (one division per thread).
 template <int CPL>
-constexpr int store_ctas_per_sm() { return CPL <= 2 ? 5 : 2; }  // 48 / 128 registers a thread
+constexpr int store_ctas_per_sm() { return CPL <= 2 ? 4 : 2; }  // 64 / 128 registers a thread
 
-template <int CPL, int RPW, bool FP8, bool LASTJ>
+template <int CPL, bool FP8, bool LASTJ>
 __global__ void __launch_bounds__(kStoreThreads, store_ctas_per_sm<CPL>())
     qk_norm_rope_store_kernel(StoreParams p) {
   pdl_wait();
@@ -234,62 +252,49 @@ __global__ void __launch_bounds__(kStoreThreads, store_ctas_per_sm<CPL>())
   const int rope_chunk0 = (p.D - p.R) >> 3;
   const int half = p.R >> 1;
   const int rows = static_cast<int>(p.rows);
-  const int rows_per_token = p.H + 1;
-  const int warp = static_cast<int>((blockIdx.x * kStoreThreads + threadIdx.x) >> 5);
-  const int stride = static_cast<int>((gridDim.x * kStoreThreads) >> 5) * RPW;
-  int base = warp * RPW;
-  int nst[RPW], npos[RPW];
-  load_meta<RPW>(p, base, nst, npos);
-  for (; base < rows; base += stride) {
-    int st[RPW], pos[RPW], tok[RPW], head[RPW];
-    uint4 x[RPW][CPL];
-    float4 cs[RPW], sn[RPW];
+  const int rpt = p.H + 1;  // rows per token
+  const int stride = static_cast<int>((gridDim.x * kStoreThreads) >> 5);
+  const int stride_t = stride / rpt, stride_h = stride - stride_t * rpt;
+  int row = static_cast<int>((blockIdx.x * kStoreThreads + threadIdx.x) >> 5);
+  int t = row / rpt, head = row - t * rpt;
+  int st = row < rows ? __ldg(p.state_slot + t) : -1;
+  int pos = row < rows ? __ldg(p.positions + t) : -1;
+  for (; row < rows; row += stride) {
+    const uint16_t* src = head < p.H ? p.q + (static_cast<size_t>(t) * p.H + head) * p.D
+                                     : p.kv + static_cast<size_t>(t) * p.D;
+    uint4 x[CPL];
 #pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-      st[r] = nst[r];
-      pos[r] = npos[r];
-      const int row = base + r;
-      const bool valid = row < rows;
-      const int t = valid ? static_cast<int>(static_cast<unsigned>(row) / rows_per_token) : 0;
-      tok[r] = t;
-      head[r] = valid ? row - t * rows_per_token : -1;
-      const uint16_t* src = !valid            ? p.q
-                            : head[r] < p.H ? p.q + (static_cast<size_t>(t) * p.H + head[r]) * p.D
-                                            : p.kv + static_cast<size_t>(t) * p.D;
-#pragma unroll
-      for (int j = 0; j < CPL; ++j) {
-        const int c = lane + 32 * j;
-        x[r][j] = (valid && c < chunks) ? __ldcs(reinterpret_cast<const uint4*>(src) + c)
-                                        : make_uint4(0, 0, 0, 0);
-      }
-      cs[r] = sn[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (LASTJ) {
-        const int c = lane + 32 * (CPL - 1);
-        if (valid && st[r] >= 0 && pos[r] >= 0 && pos[r] < p.max_pos && c >= rope_chunk0 &&
-            c < chunks) {
-          const size_t off = static_cast<size_t>(pos[r]) * half + 4 * (c - rope_chunk0);
-          cs[r] = __ldg(reinterpret_cast<const float4*>(p.cos_cache + off));
-          sn[r] = __ldg(reinterpret_cast<const float4*>(p.sin_cache + off));
-        }
+    for (int j = 0; j < CPL; ++j) {
+      const int c = lane + 32 * j;
+      x[j] = c < chunks ? __ldcs(reinterpret_cast<const uint4*>(src) + c) : make_uint4(0, 0, 0, 0);
+    }
+    float4 cs = make_float4(0.f, 0.f, 0.f, 0.f), sn = cs;
+    if (LASTJ) {
+      const int c = lane + 32 * (CPL - 1);
+      if (st >= 0 && pos >= 0 && pos < p.max_pos && c >= rope_chunk0 && c < chunks) {
+        const size_t off = static_cast<size_t>(pos) * half + 4 * (c - rope_chunk0);
+        cs = __ldg(reinterpret_cast<const float4*>(p.cos_cache + off));
+        sn = __ldg(reinterpret_cast<const float4*>(p.sin_cache + off));
       }
     }
-    load_meta<RPW>(p, base + stride, nst, npos);
-#pragma unroll
-    for (int r = 0; r < RPW; ++r)
-      if (head[r] >= 0)
-        process_row<CPL, FP8, LASTJ>(p, lane, x[r], tok[r], head[r], st[r], pos[r], cs[r], sn[r]);
+    // the next row's token, and its state slot and position
+    int nt = t + stride_t, nh = head + stride_h;
+    if (nh >= rpt) nh -= rpt, ++nt;
+    const bool more = row + stride < rows;
+    const int nst = more ? __ldg(p.state_slot + nt) : -1;
+    const int npos = more ? __ldg(p.positions + nt) : -1;
+    process_row<CPL, FP8, LASTJ>(p, lane, x, t, head, st, pos, cs, sn);
+    t = nt, head = nh, st = nst, pos = npos;
   }
   pdl_trigger();
 }
 
 template <int CPL, bool FP8, bool LASTJ>
 cudaError_t launch_variant(const StoreParams& p, int num_sms, cudaStream_t st) {
-  constexpr int kRowsPerWarp = 1;  // more rows per warp measured slower (fewer warps per SM)
-  const int64_t warps = (p.rows + kRowsPerWarp - 1) / kRowsPerWarp;
-  const int64_t want = (warps * 32 + kStoreThreads - 1) / kStoreThreads;
+  const int64_t want = (p.rows * 32 + kStoreThreads - 1) / kStoreThreads;  // a warp per row
   const int64_t cap = static_cast<int64_t>(num_sms) * store_ctas_per_sm<CPL>();
   const int grid = static_cast<int>(want < cap ? want : cap);
-  return launch_pdl(qk_norm_rope_store_kernel<CPL, kRowsPerWarp, FP8, LASTJ>, dim3(grid),
+  return launch_pdl(qk_norm_rope_store_kernel<CPL, FP8, LASTJ>, dim3(grid),
                     dim3(kStoreThreads), 0, st, p);
 }
 
