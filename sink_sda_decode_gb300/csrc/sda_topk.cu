@@ -17,7 +17,7 @@
 //   1. topk_indptr_kernel (one CTA): comp_indptr = prefix sums of min(k, n_t)
 //      (for batches of up to 4096 tokens each select CTA computes its own
 //      entry instead, and this launch is skipped);
-//   2. topk_select_kernel (one CTA per token): up to four 8-bit digit passes
+//   2. topk_select_kernel (one CTA per token): up to three digit passes
 //      (MSB first) find the key T of the k-th best candidate and how many
 //      candidates equal to T to keep (stopping early once the digit bin that
 //      holds the k-th key is kept whole); one ordered pass then keeps every
@@ -26,7 +26,9 @@
 //      the output is in increasing position with no sort.
 // A token's keys are staged once in shared memory when its row fits
 // (<= kSmemKeys candidates); longer rows are re-read from global memory (L2)
-// by each pass.
+// by each pass.  Digits are 11, 11 and 10 bits wide: the leading bits of real
+// scores (sign and exponent) crowd into few values, and wide first digits
+// leave the threshold bin small, so the passes usually stop after the second.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -38,7 +40,9 @@ namespace sda {
 namespace {
 
 constexpr int kTopkThreads = 1024;
-constexpr int kSmemKeys = 11264;  // 44 KB of staged keys (static shared memory <= 48 KB)
+constexpr int kSmemKeys = 9216;  // 36 KB of staged keys (static shared memory <= 48 KB)
+constexpr int kBins = 2048;      // digit histogram (11-bit digits)
+static_assert(kBins == 2 * kTopkThreads, "two histogram bins per thread");
 
 __device__ __forceinline__ uint32_t score_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -165,7 +169,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_select_kernel(
     int32_t* __restrict__ comp_slot, int32_t* __restrict__ status) {
   pdl_wait();
   __shared__ __align__(16) uint32_t s_keys[STAGED ? kSmemKeys : kIpt];
-  __shared__ uint32_t hist[256];
+  __shared__ uint32_t hist[kBins];
   __shared__ uint32_t warp_sums[kTopkThreads / 32];
   __shared__ uint32_t parts[FUSED ? kTopkThreads / 32 : 1][2];
   __shared__ uint32_t s_digit, s_above, s_count;
@@ -250,9 +254,14 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_select_kernel(
       }
       __syncthreads();
     }
+    // Digits of 11, 11 and 10 bits (MSB first): bins 2047 - 2i and 2046 - 2i
+    // belong to thread i for the suffix sums.
     uint32_t prefix = 0, mask = 0, need = static_cast<uint32_t>(kk);
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      if (tid < 256) hist[tid] = 0;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+      const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+      const uint32_t dmask = pass == 2 ? 0x3ffu : 0x7ffu;
+      for (int b = tid; b < kBins; b += kTopkThreads) hist[b] = 0;
       __syncthreads();
       for (int g = tid; g < groups; g += kTopkThreads) {
         uint32_t key[kIpt];
@@ -260,23 +269,26 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_select_kernel(
 #pragma unroll
         for (int e = 0; e < kIpt; ++e) {
           const bool valid = kIpt * g + e < n;
-          if (!STAGED && shift == 24) nan_seen |= valid && key[e] == 0u;
-          if (valid && (key[e] & mask) == prefix) atomicAdd(&hist[(key[e] >> shift) & 255u], 1u);
+          if (!STAGED && pass == 0) nan_seen |= valid && key[e] == 0u;
+          if (valid && (key[e] & mask) == prefix) atomicAdd(&hist[(key[e] >> shift) & dmask], 1u);
         }
       }
       __syncthreads();
-      // Suffix sums over the digits, largest digit first: thread i holds bin 255 - i.
-      const uint32_t h = tid < 256 ? hist[255 - tid] : 0u;
+      const uint32_t hi = hist[kBins - 1 - 2 * tid], lo = hist[kBins - 2 - 2 * tid];
       uint32_t total;
-      const uint32_t above = block_exclusive_scan(h, warp_sums, &total);  // keys in higher bins
-      if (tid < 256 && above < need && above + h >= need) {
-        s_digit = 255u - tid;
+      const uint32_t above = block_exclusive_scan(hi + lo, warp_sums, &total);  // keys in higher bins
+      if (above < need && above + hi >= need) {
+        s_digit = kBins - 1 - 2 * tid;
         s_above = above;
-        s_count = h;
+        s_count = hi;
+      } else if (above + hi < need && above + hi + lo >= need) {
+        s_digit = kBins - 2 - 2 * tid;
+        s_above = above + hi;
+        s_count = lo;
       }
       __syncthreads();
       prefix |= s_digit << shift;
-      mask |= 255u << shift;
+      mask |= dmask << shift;
       need -= s_above;
       const bool whole_bin = need == s_count;  // every key of the bin is kept: done
       __syncthreads();
