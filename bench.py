@@ -7,7 +7,8 @@ attention kernel, log-sum-exp combine), replayed as one CUDA graph.
 
 Prints ONE JSON line.  Default workload: N=64 tokens, H=16, D=512, 640 slots
 per token (128 SWA ring slots + 512 random compressed slots) over a 2^20-slot
-pool.  `--config` picks another of the five workloads.
+pool.  `--config` picks another workload (the five decode workloads, or a
+2048-token sparse-prefill chunk, prefill_h64, through the same path).
 
   value     decode tokens/s with inputs resident in HBM (graph replays,
             CUDA events, L2 flushed between steps: a 256 MiB write, then a
