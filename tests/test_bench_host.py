@@ -64,3 +64,26 @@ def test_kernel_source_hash_is_stable_and_short():
     h = bench.kernel_source_hash()
     assert h == bench.kernel_source_hash() and len(h) == 16
     int(h, 16)
+
+
+def test_store_bytes_by_hand():
+    # H=16, D=512, R=64: q read + written 2*16*512*2, KV row read 1024 and
+    # stored 1024 (FP8: 512 codes + 4-byte scale), 8 bytes of slot/position,
+    # 64*4 bytes of cos/sin, plus the two 1 KB weights once
+    w = _W(64, 16, 512, 0)
+    per = 2 * 16 * 512 * 2 + 1024 + 1024 + 8 + 256
+    assert bench.store_algorithmic_bytes(w, 64) == 64 * per + 2048
+    assert bench.store_algorithmic_bytes(w, 64, "fp8") == 64 * (per - 1024 + 516) + 2048
+
+
+def test_topk_bytes_by_hand():
+    # lengths 0, 100, 8192 with k=512, K=64: scores 4 B each, lengths 4 B,
+    # block-table rows ceil(n/64)*4 B, indptr (N+1)*4 B, 8 B per kept position
+    b = bench.topk_algorithmic_bytes([0, 100, 8192], 512, 64)
+    assert b == (0 + 100 + 8192) * 4 + 3 * 4 + (0 + 2 + 128) * 4 + 4 * 4 + (0 + 100 + 512) * 8
+
+
+def test_kernel_source_hashes_cover_each_measured_kernel():
+    hs = {k: bench.kernel_source_hash(k) for k in ("decode", "store", "topk")}
+    assert len(set(hs.values())) == 3 and all(len(h) == 16 for h in hs.values())
+    assert bench.ncu_traffic("no such workload") is None
