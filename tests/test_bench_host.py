@@ -87,3 +87,25 @@ def test_kernel_source_hashes_cover_each_measured_kernel():
     hs = {k: bench.kernel_source_hash(k) for k in ("decode", "store", "topk")}
     assert len(set(hs.values())) == 3 and all(len(h) == 16 for h in hs.values())
     assert bench.ncu_traffic("no such workload") is None
+
+
+@pytest.mark.parametrize("path,metric", [("store", bench.STORE_METRIC), ("topk", bench.TOPK_METRIC),
+                                         ("layer", bench.METRIC)])
+def test_reference_arm_of_every_path(path, metric):
+    """`bench.py --impl reference --path P` times the oracle's share of that
+    path's step on the CPU and prints one line with the path's metric."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.abspath(bench.__file__))
+    cmd = [sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--path", path,
+           "--config", "h16", "--steps", "1", "--warmup", "1"]
+    p = subprocess.run(cmd, cwd=root, env=dict(os.environ, OMP_NUM_THREADS="2"),
+                       capture_output=True, text=True, timeout=300)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [l for l in p.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["metric"] == metric and line["value"] > 0
+    assert line["config"]["path"] == path
