@@ -55,6 +55,7 @@ class Workload:
     k_per_block: int
     swa_pages: int
     recipe: str = ""
+    seed: int = 0                # the generator seed (distinct per shard)
 
     @property
     def lengths(self) -> np.ndarray:
@@ -189,7 +190,7 @@ def store_inputs(w: "Workload", rope_dim: int = ROPE_DIM, max_pos: int = MAX_POS
     newest SWA entry of its own list) and at least win; new KV rows ~ N(0,1)
     bf16; norm weights ~ U[0.5, 1.5) bf16; RoPE tables of base 10000 on the
     last `rope_dim` dims.  Padded tokens keep state_slot < 0."""
-    rng = np.random.default_rng(SEED_BASE + 700 + (w.N * 7919 + w.H) % 1000 if seed is None else seed)
+    rng = np.random.default_rng(w.seed + 700 if seed is None else seed)
     dev = w.q.device
     N, D, win = w.N, w.D, w.win
     kv_new = _to_bf16(rng.standard_normal((N, D)), dev)
@@ -228,7 +229,7 @@ def topk_inputs(w: "Workload", candidates: int = TOPK_CANDIDATES, k: int = TOPK_
     `ragged`, by default for workloads that pad tokens), length 0 for padded
     tokens, and a block table of distinct random blocks of the workload's
     compressed region."""
-    rng = np.random.default_rng(SEED_BASE + 900 + w.N % 997 if seed is None else seed)
+    rng = np.random.default_rng(w.seed + 900 if seed is None else seed)
     dev = w.q.device
     N, kpb = w.N, w.k_per_block
     B = -(-candidates // kpb)
@@ -315,7 +316,7 @@ def _assemble(name, N, H, D, P, lists, swa_parts, swa_pages, sink_sigma, seed, d
                     q=q, unified_kv=kv, attn_sink=sink, kv_indices=idx,
                     kv_indptr=ptr.astype(np.int32), state_slot=desc[0], swa_len=desc[1],
                     swa_head=desc[2], comp_indptr=desc[3], comp_block=desc[4], comp_slot=desc[5],
-                    win=win, k_per_block=kpb, swa_pages=swa_pages, recipe=recipe)
+                    win=win, k_per_block=kpb, swa_pages=swa_pages, recipe=recipe, seed=seed)
 
 
 def tiny(device="cpu", seed=SEED_BASE + 0):
