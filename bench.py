@@ -1,9 +1,9 @@
 """Benchmark of the sparse sink decode attention hot path on one GB300.
 
-One step = the whole hot path over one batch: the index build
-(sda_build_indices: SWA ring slots + compressed slots -> ragged kv_indices)
-followed by the decode (sda_decode: device-side split plan, tensor-core
-attention kernel, log-sum-exp combine), replayed as one CUDA graph.
+One step = the whole hot path over one batch: the index build (SWA ring
+slots + compressed slots -> ragged kv_indices) followed by the decode
+(device-side split plan, tensor-core attention kernel, log-sum-exp combine),
+made by one sda_build_decode call and replayed as one CUDA graph.
 
 Prints ONE JSON line.  Default workload: N=64 tokens, H=16, D=512, 640 slots
 per token (128 SWA ring slots + 512 random compressed slots) over a 2^20-slot
@@ -342,7 +342,8 @@ class Step:
             self.q_rot = torch.empty_like(w.q)
             self.store_status = torch.empty(1, dtype=torch.int32, device=device)
         self.results = [self.q_rot if path == "store" else self.out]
-        self.launches_per_step = {"decode": 6, "store": 1, "layer": 7}[path]
+        # decode: builder lengths, scan + plan, scatter, attention, combine
+        self.launches_per_step = {"decode": 5, "store": 1, "layer": 6}[path]
 
     @property
     def rope_dim(self):
@@ -378,20 +379,18 @@ class Step:
             q = self.q_rot
         if self.path == "store":
             return
-        self.sda.build_indices(**{k: ins[k] for k in BUILDER_KEYS}, win=w.win,
-                               k_per_block=w.k_per_block, swa_pages=w.swa_pages,
-                               total_pages=w.total_pages, capacity=self.capacity,
-                               kv_indices=self.kv_indices, kv_indptr=self.kv_indptr,
-                               status=self.status, stream=stream)
+        # index build + decode in one call (the builder's scan and the decode's
+        # work plan share a CTA)
         if timing:
             self.sda.set_timing_events(*timing)
-        if self.pool is None:
-            self.sda.decode(q, w.unified_kv, self.kv_indices, self.kv_indptr, w.attn_sink,
-                            w.softmax_scale, out=self.out, workspace=self.ws, stream=stream)
-        else:
-            self.sda.decode_fp8(q, self.pool.codes, self.pool.scale, self.kv_indices,
-                                self.kv_indptr, w.attn_sink, w.softmax_scale, out=self.out,
-                                workspace=self.ws, stream=stream)
+        self.sda.build_decode(q, w.unified_kv if self.pool is None else self.pool.codes,
+                              w.attn_sink, w.softmax_scale,
+                              *(ins[k] for k in BUILDER_KEYS), win=w.win,
+                              k_per_block=w.k_per_block, swa_pages=w.swa_pages,
+                              kv_scale=None if self.pool is None else self.pool.scale,
+                              capacity=self.capacity, out=self.out, workspace=self.ws,
+                              kv_indices=self.kv_indices, kv_indptr=self.kv_indptr,
+                              status=self.status, stream=stream)
         self.sda.set_timing_events(None, None)
 
     def check_status(self):
@@ -530,7 +529,8 @@ def reduce_over_ranks(times_ms, units, ws, device):
 STEP_TEXT = {
     "topk": "top-k of each token's scores -> compressed (block, slot) lists (2 kernels) as one "
             "CUDA graph",
-    "decode": "index build + decode (plan, attention, combine) as one CUDA graph",
+    "decode": "index build + decode (plan, attention, combine), one sda_build_decode call, as "
+              "one CUDA graph",
     "store": "q/kv RMSNorm + GPT-J RoPE + SWA ring store (one kernel) as one CUDA graph",
     "layer": "q/kv norm + RoPE + SWA store, index build, decode as one CUDA graph",
 }

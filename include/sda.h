@@ -238,6 +238,26 @@ sda_status sda_build_indices(const int32_t* state_slot, const int32_t* swa_len,
                              void* stream);
 
 /*
+ * sda_build_indices followed by sda_decode (or sda_decode_fp8 when kv_scale is
+ * not NULL, unified_kv then holding the E4M3 codes), as one call: the same
+ * arguments, contracts, outputs and status bits as those two calls made back
+ * to back on the stream with total_indices = capacity, with one launch fewer
+ * (the builder's scan and the decode's work plan run in one CTA).  The
+ * workspace is sized by sda_decode_workspace_size (or
+ * sda_decode_fp8_workspace_size) with total_indices = capacity.  Lists the
+ * builder empties (bad descriptors, or bit 32: over capacity) decode to +0.
+ */
+sda_status sda_build_decode(const int32_t* state_slot, const int32_t* swa_len,
+                            const int32_t* swa_head, const int32_t* comp_indptr,
+                            const int32_t* comp_block, const int32_t* comp_slot,
+                            int64_t comp_total, int win, int k_per_block, int64_t swa_pages,
+                            int32_t* kv_indices, int64_t capacity, int32_t* kv_indptr,
+                            int32_t* status, const void* q, const void* unified_kv,
+                            const float* kv_scale, int64_t total_pages, const float* attn_sink,
+                            float softmax_scale, int N, int H, int D, void* out, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/*
  * Checks the docstring's index contract on the device.  status [2] int32
  * device memory receives: status[0] bits 1 = kv_indptr decreasing somewhere,
  * 2 = kv_indptr outside [0, total_indices], 4 = some entry of

@@ -21,7 +21,7 @@ import torch
 from . import _lib
 
 __all__ = ["decode", "workspace_size", "build_indices", "validate_indices", "decode_error_flag",
-           "decode_kernel", "decode_fp8", "workspace_size_fp8", "qk_norm_rope_swa_store", "topk_slots",
+           "decode_kernel", "decode_fp8", "workspace_size_fp8", "qk_norm_rope_swa_store", "topk_slots", "build_decode",
            "decode_host", "set_timing_events", "decode_noalloc", "library_path"]
 
 library_path = _lib.LIB_PATH
@@ -265,6 +265,62 @@ def build_indices(state_slot, swa_len, swa_head, comp_indptr, comp_block, comp_s
             int(capacity), kv_indptr.data_ptr(), status.data_ptr(), _stream_ptr(stream))
     _lib.check(rc, "sda_build_indices")
     return kv_indices, kv_indptr, status
+
+
+def build_decode(q, unified_kv, attn_sink, softmax_scale, state_slot, swa_len, swa_head,
+                 comp_indptr, comp_block, comp_slot, *, win, k_per_block, swa_pages,
+                 kv_scale=None, capacity=None, out=None, workspace=None, kv_indices=None,
+                 kv_indptr=None, status=None, stream=None):
+    """build_indices followed by decode (decode_fp8 when `kv_scale` is given;
+    `unified_kv` then holds the E4M3 codes) in one call with one launch fewer.
+    Returns (out, kv_indices, kv_indptr, status)."""
+    lib = _lib.load()
+    _req(q, "q", torch.bfloat16, 3)
+    dev = q.device
+    N, H, D = q.shape
+    if kv_scale is None:
+        _req(unified_kv, "unified_kv", torch.bfloat16, 2, dev)
+    else:
+        if unified_kv.dtype == torch.float8_e4m3fn:
+            unified_kv = unified_kv.view(torch.uint8)
+        _req(unified_kv, "kv_fp8", torch.uint8, 2, dev)
+        _req(kv_scale, "kv_scale", torch.float32, 1, dev)
+        if kv_scale.numel() != unified_kv.shape[0]:
+            raise ValueError("kv_scale must have one entry per pool row")
+    if unified_kv.shape[1] != D:
+        raise ValueError("pool rows must have D elements")
+    _req(attn_sink, "attn_sink", torch.float32, 1, dev)
+    _req(state_slot, "state_slot", torch.int32, 1, dev)
+    for name, t in (("swa_len", swa_len), ("swa_head", swa_head), ("comp_indptr", comp_indptr),
+                    ("comp_block", comp_block), ("comp_slot", comp_slot)):
+        _req(t, name, torch.int32, 1, dev)
+    if state_slot.numel() != N or attn_sink.numel() != H:
+        raise ValueError("state_slot must be [N] and attn_sink [H]")
+    if capacity is None:
+        capacity = N * int(win) + comp_block.numel()
+    if kv_indices is None:
+        kv_indices = torch.empty(max(int(capacity), 1), dtype=torch.int32, device=dev)
+    if kv_indptr is None:
+        kv_indptr = torch.empty(N + 1, dtype=torch.int32, device=dev)
+    if status is None:
+        status = torch.empty(1, dtype=torch.int32, device=dev)
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        size = (workspace_size if kv_scale is None else workspace_size_fp8)(N, H, D, int(capacity))
+        workspace = torch.empty(max(size, 1), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = lib.sda_build_decode(
+            state_slot.data_ptr(), swa_len.data_ptr(), swa_head.data_ptr(), comp_indptr.data_ptr(),
+            comp_block.data_ptr() if comp_block.numel() else None,
+            comp_slot.data_ptr() if comp_slot.numel() else None, comp_block.numel(), int(win),
+            int(k_per_block), int(swa_pages), kv_indices.data_ptr(), int(capacity),
+            kv_indptr.data_ptr(), status.data_ptr(), q.data_ptr(), unified_kv.data_ptr(),
+            None if kv_scale is None else kv_scale.data_ptr(), unified_kv.shape[0],
+            attn_sink.data_ptr(), float(softmax_scale), N, H, D, out.data_ptr(),
+            workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
+    _lib.check(rc, "sda_build_decode")
+    return out, kv_indices, kv_indptr, status
 
 
 def validate_indices(kv_indices, kv_indptr, total_pages, status=None, stream=None):

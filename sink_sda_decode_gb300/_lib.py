@@ -44,6 +44,9 @@ SIGNATURES = {
     "sda_build_indices": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i64, _i64,
                                  _vp, _i64, _vp, _vp, _vp]),
     "sda_validate_indices": (_i32, [_vp, _i64, _vp, _i32, _i64, _vp, _vp]),
+    "sda_build_decode": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i64, _vp, _i64, _vp,
+                                _vp, _vp, _vp, _vp, _i64, _vp, _f32, _i32, _i32, _i32, _vp, _vp,
+                                ctypes.c_size_t, _vp]),
     "sda_topk_slots": (_i32, [_vp, _i64, _vp, _vp, _i64, _i32, _i32, _i32, _vp, _vp, _vp, _i64, _vp,
                               _vp]),
     "sda_qk_norm_rope_swa_store": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32,

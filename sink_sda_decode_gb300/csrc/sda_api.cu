@@ -308,6 +308,86 @@ sda_status sda_decode_fp8(const void* q, const void* kv_fp8, const float* kv_sca
   return SDA_OK;
 }
 
+sda_status sda_build_decode(const int32_t* state_slot, const int32_t* swa_len,
+                            const int32_t* swa_head, const int32_t* comp_indptr,
+                            const int32_t* comp_block, const int32_t* comp_slot,
+                            int64_t comp_total, int win, int k_per_block, int64_t swa_pages,
+                            int32_t* kv_indices, int64_t capacity, int32_t* kv_indptr,
+                            int32_t* status, const void* q, const void* unified_kv,
+                            const float* kv_scale, int64_t total_pages, const float* attn_sink,
+                            float softmax_scale, int N, int H, int D, void* out, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  // the builder's checks (sda_build_indices)
+  if (N < 0 || win <= 0 || k_per_block <= 0 || swa_pages < 0 || total_pages <= 0 ||
+      total_pages > 0x7fffffffll || swa_pages > total_pages || capacity < 0 ||
+      capacity > 0x7fffffffll || comp_total < 0 || comp_total > 0x7fffffffll)
+    return SDA_ERR_INVALID_ARG;
+  if (!kv_indptr || !status) return SDA_ERR_INVALID_ARG;
+  if (N > 0 && (!state_slot || !swa_len || !swa_head || !comp_indptr)) return SDA_ERR_INVALID_ARG;
+  if (comp_total > 0 && (!comp_block || !comp_slot)) return SDA_ERR_INVALID_ARG;
+  if (capacity > 0 && !kv_indices) return SDA_ERR_INVALID_ARG;
+  // the decode's checks (sda_decode / sda_decode_fp8)
+  const bool fp8 = kv_scale != nullptr;
+  if (fp8 ? !tc_shape_supported(H, D) : !shape_supported(H, D)) return SDA_ERR_UNSUPPORTED;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (N == 0) {  // the builder still writes kv_indptr[0] and the status word
+    const cudaError_t e = launch_build_indices(state_slot, swa_len, swa_head, comp_indptr,
+                                               comp_block, comp_slot, comp_total, N, win,
+                                               k_per_block, swa_pages, total_pages, kv_indices,
+                                               capacity, kv_indptr, status, st);
+    if (e != cudaSuccess) {
+      note_cuda_error(e, "sda_build_decode");
+      return SDA_ERR_CUDA;
+    }
+    return SDA_OK;
+  }
+  if (!q || !unified_kv || !attn_sink || !out || !workspace) return SDA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(unified_kv, 16) || !aligned(out, 16) || !aligned(kv_indptr, 4) ||
+      !aligned(attn_sink, 4) || (kv_indices && !aligned(kv_indices, 4)) ||
+      (fp8 && !aligned(kv_scale, 4)))
+    return SDA_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return SDA_ERR_WORKSPACE;
+  DeviceCaps caps;
+  cudaError_t e = device_caps(&caps);
+  if (e != cudaSuccess) {
+    note_cuda_error(e, "sda_build_decode");
+    return SDA_ERR_CUDA;
+  }
+  LaunchPlan lp;
+  if (fp8) fp8_plan(H, D, caps, &lp);
+  else choose_plan(H, D, caps, &lp);
+  const WsLayout L = workspace_layout(N, H, D, capacity, lp);
+  if (workspace_bytes < L.total) return SDA_ERR_WORKSPACE;
+  e = launch_build_len(state_slot, swa_len, swa_head, comp_indptr, comp_block, comp_slot,
+                       comp_total, N, win, k_per_block, swa_pages, total_pages, kv_indptr, st);
+  if (e == cudaSuccess) e = launch_scan_plan(N, capacity, kv_indptr, status, lp, workspace, L, st);
+  if (e == cudaSuccess)
+    e = launch_build_scatter(state_slot, swa_len, swa_head, comp_indptr, comp_block, comp_slot, N,
+                             win, k_per_block, swa_pages, kv_indptr, kv_indices, st);
+  if (e == cudaSuccess && g_ev_before && g_ev_after) e = cudaEventRecord(g_ev_before, st);
+  if (e == cudaSuccess) {
+    if (fp8)
+      e = launch_decode_umma(q, unified_kv, kv_scale, total_pages, kv_indices, attn_sink,
+                             softmax_scale, N, H, D, out, workspace, L, lp, st);
+    else if (lp.variant == kPair)
+      e = launch_decode_pair(q, unified_kv, kv_indices, attn_sink, softmax_scale, N, H, D, out,
+                             workspace, L, lp, st);
+    else if (lp.variant == kUmma)
+      e = launch_decode_umma(q, unified_kv, nullptr, total_pages, kv_indices, attn_sink,
+                             softmax_scale, N, H, D, out, workspace, L, lp, st);
+    else
+      e = launch_decode_simt(q, unified_kv, kv_indices, attn_sink, softmax_scale, N, H, D, out,
+                             workspace, L, lp, st);
+  }
+  if (e == cudaSuccess && g_ev_before && g_ev_after) e = cudaEventRecord(g_ev_after, st);
+  if (e == cudaSuccess) e = launch_combine(attn_sink, N, H, D, out, workspace, L, caps.num_sms, st);
+  if (e != cudaSuccess) {
+    note_cuda_error(e, "sda_build_decode");
+    return SDA_ERR_CUDA;
+  }
+  return SDA_OK;
+}
+
 sda_status sda_decode_kernel(int H, int D, int* kernel) {
   if (!kernel) return SDA_ERR_INVALID_ARG;
   if (!shape_supported(H, D)) return SDA_ERR_UNSUPPORTED;

@@ -12,12 +12,11 @@
 // failure the sglang PR 25898 summary page describes; here win and
 // k_per_block are checked on the host and every emitted slot is in range).
 #include "sda_internal.cuh"
+#include "sda_scan.cuh"
 
 namespace sda {
 
 namespace {
-
-constexpr int kScanThreads = 1024;
 
 // One CTA per token in the length and scatter passes; 1024 threads and loops
 // unrolled 8 deep keep a long list (e.g. 64 K compressed entries) to a few
@@ -67,65 +66,12 @@ build_len_kernel(const int32_t* __restrict__ state_slot, const int32_t* __restri
   }
 }
 
-// One CTA: in-place inclusive scan of the lengths in kv_indptr[1..N] (int64
-// running total), kv_indptr[0] = 0; negative entries are bad tokens (empty
-// slice, their bits OR-ed into *status).  If the total exceeds capacity,
-// every slice is emptied and bit 32 is raised.  Writes *status.
 __global__ void __launch_bounds__(kScanThreads)
 build_scan_kernel(int N, int64_t capacity, int32_t* __restrict__ kv_indptr,
                   int32_t* __restrict__ status) {
-  __shared__ long long warp_sums[32];
-  __shared__ long long s_carry;
-  __shared__ int s_over;
-  __shared__ int s_flags;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (threadIdx.x == 0) {
-    s_carry = 0;
-    s_over = 0;
-    s_flags = 0;
-  }
   pdl_wait();
   pdl_trigger();
-  __syncthreads();
-  for (int t0 = 0; t0 < N; t0 += kScanThreads) {
-    const int t = t0 + threadIdx.x;
-    long long v = t < N ? kv_indptr[t + 1] : 0;
-    if (v < 0) {
-      atomicOr(&s_flags, (int)(-v));
-      v = 0;
-    }
-    long long x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      long long y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) warp_sums[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-      long long w = warp_sums[lane], s = w;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        long long y = __shfl_up_sync(0xffffffffu, s, o);
-        if (lane >= o) s += y;
-      }
-      warp_sums[lane] = s - w;
-    }
-    __syncthreads();
-    const long long incl = s_carry + warp_sums[warp] + x;
-    if (t < N) {
-      if (incl > capacity) s_over = 1;
-      kv_indptr[t + 1] = (int32_t)(incl > capacity ? capacity : incl);
-    }
-    __syncthreads();
-    if (threadIdx.x == kScanThreads - 1) s_carry = incl;
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) kv_indptr[0] = 0;
-  __syncthreads();
-  if (s_over)
-    for (int t = threadIdx.x; t <= N; t += kScanThreads) kv_indptr[t] = 0;
-  if (threadIdx.x == 0) *status = s_flags | (s_over ? 32 : 0);
+  build_scan_body(N, capacity, kv_indptr, status);
 }
 
 // One CTA per token: write its slots at kv_indices[kv_indptr[t] ...].
@@ -186,6 +132,31 @@ __global__ void validate_kernel(const int32_t* __restrict__ kv_indices, int64_t 
 
 }  // namespace
 
+cudaError_t launch_build_len(const int32_t* state_slot, const int32_t* swa_len,
+                             const int32_t* swa_head, const int32_t* comp_indptr,
+                             const int32_t* comp_block, const int32_t* comp_slot,
+                             int64_t comp_total, int N, int win, int k_per_block,
+                             int64_t swa_pages, int64_t total_pages, int32_t* kv_indptr,
+                             cudaStream_t st) {
+  if (N <= 0) return cudaSuccess;
+  const int blocks = N < 65535 ? N : 65535;
+  return launch_pdl(build_len_kernel, dim3(blocks), dim3(kTokThreads), 0, st, state_slot, swa_len,
+                    swa_head, comp_indptr, comp_block, comp_slot, comp_total, N, win, k_per_block,
+                    swa_pages, total_pages, kv_indptr);
+}
+
+cudaError_t launch_build_scatter(const int32_t* state_slot, const int32_t* swa_len,
+                                 const int32_t* swa_head, const int32_t* comp_indptr,
+                                 const int32_t* comp_block, const int32_t* comp_slot, int N,
+                                 int win, int k_per_block, int64_t swa_pages,
+                                 const int32_t* kv_indptr, int32_t* kv_indices, cudaStream_t st) {
+  if (N <= 0) return cudaSuccess;
+  const int blocks = N < 65535 ? N : 65535;
+  return launch_pdl(build_scatter_kernel, dim3(blocks), dim3(kTokThreads), 0, st, state_slot,
+                    swa_len, swa_head, comp_indptr, comp_block, comp_slot, N, win, k_per_block,
+                    swa_pages, kv_indptr, kv_indices);
+}
+
 cudaError_t launch_build_indices(const int32_t* state_slot, const int32_t* swa_len,
                                  const int32_t* swa_head, const int32_t* comp_indptr,
                                  const int32_t* comp_block, const int32_t* comp_slot,
@@ -193,19 +164,15 @@ cudaError_t launch_build_indices(const int32_t* state_slot, const int32_t* swa_l
                                  int64_t swa_pages, int64_t total_pages, int32_t* kv_indices,
                                  int64_t capacity, int32_t* kv_indptr, int32_t* status,
                                  cudaStream_t st) {
-  const int blocks = N < 65535 ? N : 65535;
-  cudaError_t e = cudaSuccess;
-  if (N > 0)
-    e = launch_pdl(build_len_kernel, dim3(blocks), dim3(kTokThreads), 0, st, state_slot, swa_len,
-                   swa_head, comp_indptr, comp_block, comp_slot, comp_total, N, win, k_per_block,
-                   swa_pages, total_pages, kv_indptr);
+  cudaError_t e = launch_build_len(state_slot, swa_len, swa_head, comp_indptr, comp_block,
+                                   comp_slot, comp_total, N, win, k_per_block, swa_pages,
+                                   total_pages, kv_indptr, st);
   if (e == cudaSuccess)
     e = launch_pdl(build_scan_kernel, dim3(1), dim3(kScanThreads), 0, st, N, capacity, kv_indptr,
                    status);
-  if (e == cudaSuccess && N > 0)
-    e = launch_pdl(build_scatter_kernel, dim3(blocks), dim3(kTokThreads), 0, st, state_slot, swa_len,
-                   swa_head, comp_indptr, comp_block, comp_slot, N, win, k_per_block, swa_pages,
-                   (const int32_t*)kv_indptr, kv_indices);
+  if (e == cudaSuccess)
+    e = launch_build_scatter(state_slot, swa_len, swa_head, comp_indptr, comp_block, comp_slot, N,
+                             win, k_per_block, swa_pages, kv_indptr, kv_indices, st);
   return e;
 }
 

@@ -85,6 +85,9 @@ WsLayout workspace_layout(int N, int H, int D, int64_t total_indices, const Laun
 // All launchers only enqueue; they return cudaGetLastError().
 cudaError_t launch_plan(const int32_t* kv_indptr, int N, int64_t total_indices,
                         const LaunchPlan& lp, void* ws, const WsLayout& L, cudaStream_t st);
+// The builder's scan and the work plan in one CTA (sda_build_decode).
+cudaError_t launch_scan_plan(int N, int64_t capacity, int32_t* kv_indptr, int32_t* status,
+                             const LaunchPlan& lp, void* ws, const WsLayout& L, cudaStream_t st);
 cudaError_t launch_combine(const float* attn_sink, int N, int H, int D, void* out, void* ws,
                            const WsLayout& L, int num_sms, cudaStream_t st);
 cudaError_t launch_decode_simt(const void* q, const void* kv, const int32_t* kv_indices,
@@ -117,6 +120,20 @@ cudaError_t launch_build_indices(const int32_t* state_slot, const int32_t* swa_l
                                  int64_t swa_pages, int64_t total_pages, int32_t* kv_indices,
                                  int64_t capacity, int32_t* kv_indptr, int32_t* status,
                                  cudaStream_t st);
+// The index builder as separate launches, for callers that put another
+// kernel between its scan and its scatter: per-token lengths, then (after
+// the scan) the scatter.
+cudaError_t launch_build_len(const int32_t* state_slot, const int32_t* swa_len,
+                             const int32_t* swa_head, const int32_t* comp_indptr,
+                             const int32_t* comp_block, const int32_t* comp_slot,
+                             int64_t comp_total, int N, int win, int k_per_block,
+                             int64_t swa_pages, int64_t total_pages, int32_t* kv_indptr,
+                             cudaStream_t st);
+cudaError_t launch_build_scatter(const int32_t* state_slot, const int32_t* swa_len,
+                                 const int32_t* swa_head, const int32_t* comp_indptr,
+                                 const int32_t* comp_block, const int32_t* comp_slot, int N,
+                                 int win, int k_per_block, int64_t swa_pages,
+                                 const int32_t* kv_indptr, int32_t* kv_indices, cudaStream_t st);
 cudaError_t launch_validate(const int32_t* kv_indices, int64_t total_indices,
                             const int32_t* kv_indptr, int N, int64_t total_pages,
                             int32_t* status, cudaStream_t st);

@@ -10,6 +10,7 @@
 #include <cuda_bf16.h>
 
 #include "sda_internal.cuh"
+#include "sda_scan.cuh"
 
 namespace sda {
 
@@ -63,10 +64,10 @@ __device__ __forceinline__ TokenSplit token_split(const int32_t* indptr, int t, 
   return s;
 }
 
-__global__ void __launch_bounds__(kPlanThreads)
-plan_kernel(const int32_t* __restrict__ indptr, int N, long long total_indices, int hg, int grid,
-            int tile, int min_chunk, WsHeader* __restrict__ hdr, int4* __restrict__ units,
-            int4* __restrict__ splits) {
+__device__ __forceinline__ void plan_body(const int32_t* __restrict__ indptr, int N,
+                                          long long total_indices, int hg, int grid, int tile,
+                                          int min_chunk, WsHeader* __restrict__ hdr,
+                                          int4* __restrict__ units, int4* __restrict__ splits) {
   __shared__ int warp_sums[32];
   __shared__ int s_total[2];
   __shared__ int bucket_count[kBuckets];
@@ -74,8 +75,7 @@ plan_kernel(const int32_t* __restrict__ indptr, int N, long long total_indices, 
   __shared__ int s_chunk;
 
   if (threadIdx.x < kBuckets) bucket_count[threadIdx.x] = 0;
-  pdl_wait();
-  pdl_trigger();
+  __syncthreads();
   // kv_indptr must be a true prefix sum inside [0, total_indices]; otherwise
   // nothing is planned (out is left unwritten) and the error word reads 2, so
   // that no kernel ever reads kv_indices out of bounds.
@@ -160,6 +160,30 @@ plan_kernel(const int32_t* __restrict__ indptr, int N, long long total_indices, 
     hdr->chunk = chunk;
     hdr->error = 0;
   }
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+plan_kernel(const int32_t* __restrict__ indptr, int N, long long total_indices, int hg, int grid,
+            int tile, int min_chunk, WsHeader* __restrict__ hdr, int4* __restrict__ units,
+            int4* __restrict__ splits) {
+  pdl_wait();
+  pdl_trigger();
+  plan_body(indptr, N, total_indices, hg, grid, tile, min_chunk, hdr, units, splits);
+}
+
+// The index builder's scan and the plan in one CTA (sda_build_decode): the
+// scan turns the per-token lengths into kv_indptr, and the plan reads it
+// straight back, which saves the plan's own launch.
+static_assert(kPlanThreads == kScanThreads, "one CTA runs both bodies");
+__global__ void __launch_bounds__(kPlanThreads)
+scan_plan_kernel(int N, int64_t capacity, int32_t* __restrict__ kv_indptr,
+                 int32_t* __restrict__ status, int hg, int grid, int tile, int min_chunk,
+                 WsHeader* __restrict__ hdr, int4* __restrict__ units, int4* __restrict__ splits) {
+  pdl_wait();
+  pdl_trigger();
+  build_scan_body(N, capacity, kv_indptr, status);
+  __syncthreads();  // kv_indptr is final (this CTA wrote it)
+  plan_body(kv_indptr, N, (long long)capacity, hg, grid, tile, min_chunk, hdr, units, splits);
 }
 
 // Merge the pieces of each split token:
@@ -256,6 +280,16 @@ cudaError_t launch_plan(const int32_t* kv_indptr, int N, int64_t total_indices,
   char* base = static_cast<char*>(ws);
   return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, kv_indptr, N,
                     (long long)total_indices, lp.hg, lp.grid, lp.tile, lp.min_chunk,
+                    reinterpret_cast<WsHeader*>(base),
+                    reinterpret_cast<int4*>(base + L.units_off),
+                    reinterpret_cast<int4*>(base + L.split_off));
+}
+
+cudaError_t launch_scan_plan(int N, int64_t capacity, int32_t* kv_indptr, int32_t* status,
+                             const LaunchPlan& lp, void* ws, const WsLayout& L, cudaStream_t st) {
+  char* base = static_cast<char*>(ws);
+  return launch_pdl(scan_plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, N, capacity, kv_indptr,
+                    status, lp.hg, lp.grid, lp.tile, lp.min_chunk,
                     reinterpret_cast<WsHeader*>(base),
                     reinterpret_cast<int4*>(base + L.units_off),
                     reinterpret_cast<int4*>(base + L.split_off));

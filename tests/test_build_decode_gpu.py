@@ -1,0 +1,122 @@
+"""sda_build_decode: the index build and the decode as one call (the builder's
+scan and the decode's work plan share one CTA).  It must give exactly what
+the two calls give back to back -- bit-identical lists, status and output --
+and therefore match the oracle's build + decode."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity
+import sink_sda_decode_gb300 as sda
+from sink_sda_decode_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def two_calls(w, bi, pool=None, capacity=None):
+    idx, ptr, st = sda.build_indices(**bi, win=w.win, k_per_block=w.k_per_block,
+                                     swa_pages=w.swa_pages, total_pages=w.total_pages,
+                                     capacity=capacity)
+    if pool is None:
+        out = sda.decode(w.q, w.unified_kv, idx, ptr, w.attn_sink, w.softmax_scale)
+    else:
+        out = sda.decode_fp8(w.q, pool.codes, pool.scale, idx, ptr, w.attn_sink, w.softmax_scale)
+    return out, idx, ptr, st
+
+
+def fused(w, bi, pool=None, capacity=None):
+    kv = w.unified_kv if pool is None else pool.codes
+    return sda.build_decode(w.q, kv, w.attn_sink, w.softmax_scale, bi["state_slot"], bi["swa_len"],
+                            bi["swa_head"], bi["comp_indptr"], bi["comp_block"], bi["comp_slot"],
+                            win=w.win, k_per_block=w.k_per_block, swa_pages=w.swa_pages,
+                            kv_scale=None if pool is None else pool.scale, capacity=capacity)
+
+
+def assert_same(a, b):
+    out_a, idx_a, ptr_a, st_a = a
+    out_b, idx_b, ptr_b, st_b = b
+    torch.cuda.synchronize()
+    n = int(ptr_a[-1].item())
+    assert int(st_a.item()) == int(st_b.item())
+    assert torch.equal(ptr_a, ptr_b) and torch.equal(idx_a[:n], idx_b[:n])
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 4], ids=[inputs.CONFIG_NAMES[c] for c in (0, 1, 2, 4)])
+def test_fused_equals_two_calls(cfg):
+    w = inputs.config(cfg, device="cuda")
+    bi = w.builder_inputs("cuda")
+    assert_same(fused(w, bi), two_calls(w, bi))
+
+
+def test_fused_fp8_equals_two_calls():
+    w = inputs.config(2, device="cuda")
+    bi = w.builder_inputs("cuda")
+    pool = inputs.fp8_pool(w)
+    assert_same(fused(w, bi, pool), two_calls(w, bi, pool))
+
+
+def test_fused_matches_the_oracle_chain():
+    w = inputs.config(1, device="cuda")
+    bi = w.builder_inputs("cuda")
+    out, idx, ptr, st = fused(w, bi)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    o_idx, o_ptr, o_st = oracle.build_indices(w.state_slot, w.swa_len, w.swa_head, w.comp_indptr,
+                                              w.comp_block, w.comp_slot, w.win, w.k_per_block,
+                                              w.swa_pages, w.total_pages)
+    assert o_st == 0 and np.array_equal(ptr.cpu().numpy(), o_ptr)
+    assert np.array_equal(idx.cpu().numpy()[: o_ptr[-1]], o_idx)
+    parity.assert_parity(parity.compare(out, parity.run_oracle(w)), "fused build + decode")
+
+
+def test_fused_bad_descriptors_and_capacity():
+    """Bad tokens get empty slices (output +0) and their status bits; too
+    small a capacity empties every list (bit 32) and every output is +0."""
+    w = inputs.config(1, device="cuda")
+    bi = {k: v.clone() for k, v in w.builder_inputs("cuda").items()}
+    bi["swa_len"][3] = w.win + 1          # bit 1
+    bi["comp_slot"][bi["comp_indptr"][5]] = w.k_per_block  # bit 8
+    out, idx, ptr, st = fused(w, bi)
+    ref = two_calls(w, bi)
+    assert_same((out, idx, ptr, st), ref)
+    assert int(st.item()) == 1 | 8
+    assert not out[3].view(torch.int16).any() and not out[5].view(torch.int16).any()
+    out, idx, ptr, st = fused(w, bi, capacity=100)
+    torch.cuda.synchronize()
+    assert int(st.item()) & 32 and not ptr.any() and not out.view(torch.int16).any()
+
+
+def test_fused_graph_capture_and_empty_batch():
+    w = inputs.config(1, device="cuda")
+    bi = w.builder_inputs("cuda")
+    cap = w.N * w.win + int(w.comp_block.size)
+    idx = torch.empty(cap, dtype=torch.int32, device="cuda")
+    ptr = torch.empty(w.N + 1, dtype=torch.int32, device="cuda")
+    st = torch.empty(1, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(w.q)
+    ws = torch.empty(sda.workspace_size(w.N, w.H, w.D, cap), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    kw = dict(win=w.win, k_per_block=w.k_per_block, swa_pages=w.swa_pages, capacity=cap, out=out,
+              workspace=ws, kv_indices=idx, kv_indptr=ptr, status=st, stream=s)
+    args = (w.q, w.unified_kv, w.attn_sink, w.softmax_scale, bi["state_slot"], bi["swa_len"],
+            bi["swa_head"], bi["comp_indptr"], bi["comp_block"], bi["comp_slot"])
+    with torch.cuda.stream(s):
+        sda.build_decode(*args, **kw)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        sda.build_decode(*args, **kw)
+    out.zero_()
+    ptr.fill_(-1)
+    g.replay()
+    torch.cuda.synchronize()
+    assert_same((out, idx, ptr, st), two_calls(w, bi))
+    # N = 0: the builder still writes kv_indptr[0] = 0 and a zero status
+    e = torch.zeros(0, dtype=torch.int32, device="cuda")
+    o, i, p, s0 = sda.build_decode(w.q[:0], w.unified_kv, w.attn_sink, w.softmax_scale, e, e, e,
+                                   torch.zeros(1, dtype=torch.int32, device="cuda"), e, e,
+                                   win=w.win, k_per_block=w.k_per_block, swa_pages=w.swa_pages)
+    torch.cuda.synchronize()
+    assert p.tolist() == [0] and int(s0.item()) == 0 and o.shape[0] == 0
