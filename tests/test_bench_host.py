@@ -109,3 +109,32 @@ def test_reference_arm_of_every_path(path, metric):
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["metric"] == metric and line["value"] > 0
     assert line["config"]["path"] == path
+
+
+@pytest.mark.parametrize("path", ["decode", "store", "topk", "layer"])
+def test_report_line_of_every_path(path):
+    """The JSON line each path prints: its metric, the byte count its
+    roofline divides by, its launch count and the keys the contract asks for."""
+    class Args:
+        steps, warmup, config, kv = 10, 3, "h16", "bf16"
+    Args.path = path
+    w = inputs.config(1)
+    ti_bytes = 1234567
+    r = {"h2d": 10, "d2h": 20, "clocks": {"sm_mhz": 2070.0}, "rope_dim": 64,
+         "topk_bytes": ti_bytes, "launches_per_step": {"decode": 5, "store": 1, "topk": 2,
+                                                       "layer": 6}[path]}
+    line = bench.report_line(Args, w, 1, 0.040, 0.020, 0.060, w.N, r)
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "roofline", "e2e", "gpu_launches", "clocks"):
+        assert key in line
+    rf = line["roofline"]
+    assert rf["bound"] == "hbm" and rf["kernel_ms"] == 0.020
+    want = {"store": bench.store_algorithmic_bytes(w, 64), "topk": ti_bytes}.get(
+        path, bench.algorithmic_bytes(w))
+    assert rf["algorithmic_bytes"] == want
+    assert rf["achieved"] == pytest.approx(want / 1e9 / 20e-6)
+    assert line["gpu_launches"] == r["launches_per_step"] * 10
+    assert line["metric"] == {"store": bench.STORE_METRIC, "topk": bench.TOPK_METRIC}.get(path, bench.METRIC)
+    assert line["value"] == pytest.approx(w.N / 40e-6) and line["e2e"]["value"] == pytest.approx(w.N / 60e-6)
+    assert line["config"]["path"] == path
