@@ -15,8 +15,10 @@ pool.  `--config` picks another workload (the five decode workloads, or a
             256 MiB read so that the written lines are back in HBM and the
             step pays for none of the flush's write-backs)
   e2e       the same metric through the public API from pinned host
-            memory: one packed H2D copy of q + the index descriptors, build +
-            decode, D2H of out, replayed as one CUDA graph
+            memory: sda_build_decode_host reads q and the index descriptors
+            from page-locked host memory in a kernel, builds and decodes, and
+            writes out back the same way, replayed as one CUDA graph (other
+            paths: one packed H2D copy in, D2H copies of the result out)
   roofline  the attention kernel alone (events recorded around it by the
             library's timing hook): algorithmic bytes / time vs measured HBM
   cpu_baseline  the fp64 CPU oracle on the host cores (bounded sample)
@@ -482,6 +484,28 @@ def gpu_arm(args, w, device, ws, rank, pool=None):
         step.run(ins=views, stream=s)
         for o, t_ in zip(outs_h, step.results):
             o.copy_(t_, non_blocking=True)
+
+    if step.path == "decode":
+        # The decode step's own host-buffer call: kernels read q and the
+        # builder's descriptors from page-locked host memory and write out and
+        # the status word back (sda_build_decode_host), no copy-engine transfer.
+        hq = w.q.cpu().pin_memory()
+        hd = {k: step.ins[k].cpu().pin_memory() for k in BUILDER_KEYS}
+        h_out = torch.empty(w.q.shape, dtype=w.q.dtype, pin_memory=True)
+        h_st = torch.empty(1, dtype=torch.int32, pin_memory=True)
+        pool = step.pool
+        ws_host = torch.empty(step.sda.build_decode_host_workspace_size(
+            w.N, w.H, w.D, int(w.comp_block.size), step.capacity, pool is not None),
+            dtype=torch.uint8, device=device)
+        h2d = hq.numel() * hq.element_size() + sum(t_.numel() * 4 for t_ in hd.values())
+        d2h = h_out.numel() * h_out.element_size() + 4
+
+        def e2e_step():
+            step.sda.build_decode_host(
+                hq, w.unified_kv if pool is None else pool.codes, w.attn_sink, w.softmax_scale,
+                *(hd[k] for k in BUILDER_KEYS), win=w.win, k_per_block=w.k_per_block,
+                swa_pages=w.swa_pages, kv_scale=None if pool is None else pool.scale,
+                capacity=step.capacity, out=h_out, status=h_st, workspace=ws_host, stream=s)
 
     with torch.cuda.stream(s):
         for _ in range(max(args.warmup, 3)):

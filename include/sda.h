@@ -258,6 +258,36 @@ sda_status sda_build_decode(const int32_t* state_slot, const int32_t* swa_len,
                             size_t workspace_bytes, void* stream);
 
 /*
+ * sda_build_decode from HOST buffers: q [N,H,D] bf16, the builder's
+ * descriptors (state_slot, swa_len, swa_head [N], comp_indptr [N+1],
+ * comp_block, comp_slot [comp_total]) and the outputs out [N,H,D] bf16 and
+ * status [1] int32 are page-locked host memory (cudaHostAlloc /
+ * cudaMallocHost / torch pin_memory; q and out 16-byte aligned); the pool
+ * (unified_kv, kv_scale) and attn_sink stay in device memory.  The call
+ * gathers the inputs into `workspace` (device, 256-byte aligned, at least
+ * sda_build_decode_host_workspace_size bytes) with one kernel that reads the
+ * host memory directly, runs sda_build_decode there (kv_indices and kv_indptr
+ * live in the workspace) and writes out and status back to the host with
+ * another kernel -- no copy-engine transfer, so the whole step is one
+ * sequence of kernels on `stream` (graph-capturable).  Asynchronous: the host
+ * buffers must stay valid, and out/status are ready once the stream reaches
+ * this point.  SDA_ERR_INVALID_ARG if a host buffer is not page-locked or is
+ * misaligned.
+ */
+sda_status sda_build_decode_host_workspace_size(int N, int H, int D, int64_t comp_total,
+                                                int64_t capacity, int fp8, size_t* bytes);
+
+sda_status sda_build_decode_host(const int32_t* state_slot, const int32_t* swa_len,
+                                 const int32_t* swa_head, const int32_t* comp_indptr,
+                                 const int32_t* comp_block, const int32_t* comp_slot,
+                                 int64_t comp_total, int win, int k_per_block, int64_t swa_pages,
+                                 int64_t capacity, const void* q, const void* unified_kv,
+                                 const float* kv_scale, int64_t total_pages,
+                                 const float* attn_sink, float softmax_scale, int N, int H, int D,
+                                 void* out, int32_t* status, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/*
  * Checks the docstring's index contract on the device.  status [2] int32
  * device memory receives: status[0] bits 1 = kv_indptr decreasing somewhere,
  * 2 = kv_indptr outside [0, total_indices], 4 = some entry of

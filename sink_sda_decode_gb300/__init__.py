@@ -22,6 +22,7 @@ from . import _lib
 
 __all__ = ["decode", "workspace_size", "build_indices", "validate_indices", "decode_error_flag",
            "decode_kernel", "decode_fp8", "workspace_size_fp8", "qk_norm_rope_swa_store", "topk_slots", "build_decode",
+           "build_decode_host", "build_decode_host_workspace_size",
            "decode_host", "set_timing_events", "decode_noalloc", "library_path"]
 
 library_path = _lib.LIB_PATH
@@ -321,6 +322,76 @@ def build_decode(q, unified_kv, attn_sink, softmax_scale, state_slot, swa_len, s
             workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
     _lib.check(rc, "sda_build_decode")
     return out, kv_indices, kv_indptr, status
+
+
+def build_decode_host_workspace_size(N, H, D, comp_total, capacity, fp8=False) -> int:
+    """Device workspace bytes build_decode_host needs."""
+    lib = _lib.load()
+    n = ctypes.c_size_t(0)
+    _lib.check(lib.sda_build_decode_host_workspace_size(int(N), int(H), int(D), int(comp_total),
+                                                        int(capacity), int(bool(fp8)),
+                                                        ctypes.byref(n)),
+               "sda_build_decode_host_workspace_size")
+    return int(n.value)
+
+
+def build_decode_host(q, unified_kv, attn_sink, softmax_scale, state_slot, swa_len, swa_head,
+                      comp_indptr, comp_block, comp_slot, *, win, k_per_block, swa_pages,
+                      kv_scale=None, capacity=None, out=None, status=None, workspace=None,
+                      stream=None):
+    """build_decode from page-locked HOST tensors (q, the descriptors, and the
+    outputs out / status): kernels read the inputs from host memory and write
+    the result back, with no copy-engine transfer.  The pool and attn_sink stay
+    on the device.  Asynchronous on `stream`; returns (out, status) host
+    tensors, valid once the stream has reached this call."""
+    lib = _lib.load()
+    dev = unified_kv.device
+
+    def host(t, name, dtype, ndim):
+        if not isinstance(t, torch.Tensor) or t.dtype != dtype or t.dim() != ndim:
+            raise TypeError(f"{name} must be a {ndim}-d {dtype} tensor")
+        if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous page-locked (pinned) host tensor")
+    host(q, "q", torch.bfloat16, 3)
+    N, H, D = q.shape
+    for name, t in (("state_slot", state_slot), ("swa_len", swa_len), ("swa_head", swa_head),
+                    ("comp_indptr", comp_indptr), ("comp_block", comp_block),
+                    ("comp_slot", comp_slot)):
+        host(t, name, torch.int32, 1)
+    if kv_scale is None:
+        _req(unified_kv, "unified_kv", torch.bfloat16, 2, dev)
+    else:
+        if unified_kv.dtype == torch.float8_e4m3fn:
+            unified_kv = unified_kv.view(torch.uint8)
+        _req(unified_kv, "kv_fp8", torch.uint8, 2, dev)
+        _req(kv_scale, "kv_scale", torch.float32, 1, dev)
+    _req(attn_sink, "attn_sink", torch.float32, 1, dev)
+    if capacity is None:
+        capacity = N * int(win) + comp_block.numel()
+    if out is None:
+        out = torch.empty((N, H, D), dtype=torch.bfloat16, pin_memory=True)
+    else:
+        host(out, "out", torch.bfloat16, 3)
+    if status is None:
+        status = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    if workspace is None:
+        with torch.cuda.device(dev):
+            size = build_decode_host_workspace_size(N, H, D, comp_block.numel(), capacity,
+                                                    kv_scale is not None)
+        workspace = torch.empty(size, dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = lib.sda_build_decode_host(
+            state_slot.data_ptr() if N else None, swa_len.data_ptr() if N else None,
+            swa_head.data_ptr() if N else None, comp_indptr.data_ptr(),
+            comp_block.data_ptr() if comp_block.numel() else None,
+            comp_slot.data_ptr() if comp_slot.numel() else None, comp_block.numel(), int(win),
+            int(k_per_block), int(swa_pages), int(capacity), q.data_ptr() if N else None,
+            unified_kv.data_ptr(), None if kv_scale is None else kv_scale.data_ptr(),
+            unified_kv.shape[0], attn_sink.data_ptr(), float(softmax_scale), N, H, D,
+            out.data_ptr() if N else None, status.data_ptr(), workspace.data_ptr(),
+            workspace.numel(), _stream_ptr(stream))
+    _lib.check(rc, "sda_build_decode_host")
+    return out, status
 
 
 def validate_indices(kv_indices, kv_indptr, total_pages, status=None, stream=None):

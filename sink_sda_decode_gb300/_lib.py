@@ -44,6 +44,11 @@ SIGNATURES = {
     "sda_build_indices": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i64, _i64,
                                  _vp, _i64, _vp, _vp, _vp]),
     "sda_validate_indices": (_i32, [_vp, _i64, _vp, _i32, _i64, _vp, _vp]),
+    "sda_build_decode_host_workspace_size": (_i32, [_i32, _i32, _i32, _i64, _i64, _i32,
+                                                    ctypes.POINTER(ctypes.c_size_t)]),
+    "sda_build_decode_host": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i64, _i64, _vp,
+                                     _vp, _vp, _i64, _vp, _f32, _i32, _i32, _i32, _vp, _vp, _vp,
+                                     ctypes.c_size_t, _vp]),
     "sda_build_decode": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i64, _vp, _i64, _vp,
                                 _vp, _vp, _vp, _vp, _i64, _vp, _f32, _i32, _i32, _i32, _vp, _vp,
                                 ctypes.c_size_t, _vp]),

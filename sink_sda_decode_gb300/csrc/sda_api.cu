@@ -308,15 +308,17 @@ sda_status sda_decode_fp8(const void* q, const void* kv_fp8, const float* kv_sca
   return SDA_OK;
 }
 
-sda_status sda_build_decode(const int32_t* state_slot, const int32_t* swa_len,
-                            const int32_t* swa_head, const int32_t* comp_indptr,
-                            const int32_t* comp_block, const int32_t* comp_slot,
-                            int64_t comp_total, int win, int k_per_block, int64_t swa_pages,
-                            int32_t* kv_indices, int64_t capacity, int32_t* kv_indptr,
-                            int32_t* status, const void* q, const void* unified_kv,
-                            const float* kv_scale, int64_t total_pages, const float* attn_sink,
-                            float softmax_scale, int N, int H, int D, void* out, void* workspace,
-                            size_t workspace_bytes, void* stream) {
+static sda_status build_decode_impl(const int32_t* state_slot, const int32_t* swa_len,
+                                    const int32_t* swa_head, const int32_t* comp_indptr,
+                                    const int32_t* comp_block, const int32_t* comp_slot,
+                                    int64_t comp_total, int win, int k_per_block,
+                                    int64_t swa_pages, int32_t* kv_indices, int64_t capacity,
+                                    int32_t* kv_indptr, int32_t* status, const void* q,
+                                    const void* unified_kv, const float* kv_scale,
+                                    int64_t total_pages, const float* attn_sink,
+                                    float softmax_scale, int N, int H, int D, void* out,
+                                    void* workspace, size_t workspace_bytes, void* stream,
+                                    const char* who) {
   // the builder's checks (sda_build_indices)
   if (N < 0 || win <= 0 || k_per_block <= 0 || swa_pages < 0 || total_pages <= 0 ||
       total_pages > 0x7fffffffll || swa_pages > total_pages || capacity < 0 ||
@@ -336,7 +338,7 @@ sda_status sda_build_decode(const int32_t* state_slot, const int32_t* swa_len,
                                                k_per_block, swa_pages, total_pages, kv_indices,
                                                capacity, kv_indptr, status, st);
     if (e != cudaSuccess) {
-      note_cuda_error(e, "sda_build_decode");
+      note_cuda_error(e, who);
       return SDA_ERR_CUDA;
     }
     return SDA_OK;
@@ -350,7 +352,7 @@ sda_status sda_build_decode(const int32_t* state_slot, const int32_t* swa_len,
   DeviceCaps caps;
   cudaError_t e = device_caps(&caps);
   if (e != cudaSuccess) {
-    note_cuda_error(e, "sda_build_decode");
+    note_cuda_error(e, who);
     return SDA_ERR_CUDA;
   }
   LaunchPlan lp;
@@ -382,7 +384,172 @@ sda_status sda_build_decode(const int32_t* state_slot, const int32_t* swa_len,
   if (e == cudaSuccess && g_ev_before && g_ev_after) e = cudaEventRecord(g_ev_after, st);
   if (e == cudaSuccess) e = launch_combine(attn_sink, N, H, D, out, workspace, L, caps.num_sms, st);
   if (e != cudaSuccess) {
-    note_cuda_error(e, "sda_build_decode");
+    note_cuda_error(e, who);
+    return SDA_ERR_CUDA;
+  }
+  return SDA_OK;
+}
+
+sda_status sda_build_decode(const int32_t* state_slot, const int32_t* swa_len,
+                            const int32_t* swa_head, const int32_t* comp_indptr,
+                            const int32_t* comp_block, const int32_t* comp_slot,
+                            int64_t comp_total, int win, int k_per_block, int64_t swa_pages,
+                            int32_t* kv_indices, int64_t capacity, int32_t* kv_indptr,
+                            int32_t* status, const void* q, const void* unified_kv,
+                            const float* kv_scale, int64_t total_pages, const float* attn_sink,
+                            float softmax_scale, int N, int H, int D, void* out, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  return build_decode_impl(state_slot, swa_len, swa_head, comp_indptr, comp_block, comp_slot,
+                           comp_total, win, k_per_block, swa_pages, kv_indices, capacity,
+                           kv_indptr, status, q, unified_kv, kv_scale, total_pages, attn_sink,
+                           softmax_scale, N, H, D, out, workspace, workspace_bytes, stream,
+                           "sda_build_decode");
+}
+
+// Layout of sda_build_decode_host's device workspace: the staged inputs, the
+// builder's outputs, the staged output, then sda_build_decode's workspace.
+struct HostWs {
+  size_t q, ss, sl, sh, cptr, cb, cs, idx, iptr, st, out, dec, total;
+};
+
+static HostWs host_ws_layout(int N, int H, int D, int64_t comp_total, int64_t capacity,
+                             size_t dec_bytes) {
+  HostWs w;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + (bytes > 0 ? bytes : 1), 256);
+    return at;
+  };
+  const size_t qb = (size_t)N * H * D * 2;
+  w.q = take(qb);
+  w.ss = take((size_t)N * 4);
+  w.sl = take((size_t)N * 4);
+  w.sh = take((size_t)N * 4);
+  w.cptr = take((size_t)(N + 1) * 4);
+  w.cb = take((size_t)comp_total * 4);
+  w.cs = take((size_t)comp_total * 4);
+  w.idx = take((size_t)capacity * 4);
+  w.iptr = take((size_t)(N + 1) * 4);
+  w.st = take(4);
+  w.out = take(qb);
+  w.dec = take(dec_bytes);
+  w.total = off;
+  return w;
+}
+
+// Device view of page-locked host memory (NULL if `p` is not page-locked host memory).
+static const void* host_view(const void* p) {
+  if (!p) return nullptr;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+static sda_status build_decode_ws(int N, int H, int D, int64_t capacity, bool fp8, size_t* bytes) {
+  DeviceCaps caps;
+  const cudaError_t e = device_caps(&caps);
+  if (e != cudaSuccess) {
+    note_cuda_error(e, "sda_build_decode_host_workspace_size");
+    return SDA_ERR_CUDA;
+  }
+  LaunchPlan lp;
+  if (fp8) fp8_plan(H, D, caps, &lp);
+  else choose_plan(H, D, caps, &lp);
+  *bytes = workspace_layout(N, H, D, capacity, lp).total;
+  return SDA_OK;
+}
+
+sda_status sda_build_decode_host_workspace_size(int N, int H, int D, int64_t comp_total,
+                                                int64_t capacity, int fp8, size_t* bytes) {
+  if (!bytes || N < 0 || comp_total < 0 || capacity < 0) return SDA_ERR_INVALID_ARG;
+  if (fp8 ? !tc_shape_supported(H, D) : !shape_supported(H, D)) return SDA_ERR_UNSUPPORTED;
+  size_t dec = 0;
+  const sda_status r = build_decode_ws(N, H, D, capacity, fp8 != 0, &dec);
+  if (r != SDA_OK) return r;
+  *bytes = host_ws_layout(N, H, D, comp_total, capacity, dec).total;
+  return SDA_OK;
+}
+
+sda_status sda_build_decode_host(const int32_t* state_slot, const int32_t* swa_len,
+                                 const int32_t* swa_head, const int32_t* comp_indptr,
+                                 const int32_t* comp_block, const int32_t* comp_slot,
+                                 int64_t comp_total, int win, int k_per_block, int64_t swa_pages,
+                                 int64_t capacity, const void* q, const void* unified_kv,
+                                 const float* kv_scale, int64_t total_pages,
+                                 const float* attn_sink, float softmax_scale, int N, int H, int D,
+                                 void* out, int32_t* status, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  if (N < 0 || comp_total < 0 || comp_total > 0x7fffffffll || capacity < 0 ||
+      capacity > 0x7fffffffll || !status || !workspace)
+    return SDA_ERR_INVALID_ARG;
+  const bool fp8 = kv_scale != nullptr;
+  if (fp8 ? !tc_shape_supported(H, D) : !shape_supported(H, D)) return SDA_ERR_UNSUPPORTED;
+  if (!aligned(workspace, 256)) return SDA_ERR_WORKSPACE;
+  // every host array must be page-locked; q and out 16-byte aligned
+  const void* d_st = host_view(status);
+  const void* d_ss = N > 0 ? host_view(state_slot) : nullptr;
+  const void* d_sl = N > 0 ? host_view(swa_len) : nullptr;
+  const void* d_sh = N > 0 ? host_view(swa_head) : nullptr;
+  const void* d_cp = host_view(comp_indptr);
+  const void* d_cb = comp_total > 0 ? host_view(comp_block) : nullptr;
+  const void* d_cs = comp_total > 0 ? host_view(comp_slot) : nullptr;
+  const void* d_q = N > 0 ? host_view(q) : nullptr;
+  const void* d_out = N > 0 ? host_view(out) : nullptr;
+  if (!d_st || !d_cp || (N > 0 && (!d_ss || !d_sl || !d_sh || !d_q || !d_out)) ||
+      (comp_total > 0 && (!d_cb || !d_cs)))
+    return SDA_ERR_INVALID_ARG;
+  if ((N > 0 && (!aligned(d_q, 16) || !aligned(d_out, 16))) || !aligned(d_st, 4) ||
+      !aligned(d_cp, 4) || (N > 0 && (!aligned(d_ss, 4) || !aligned(d_sl, 4) || !aligned(d_sh, 4))) ||
+      (comp_total > 0 && (!aligned(d_cb, 4) || !aligned(d_cs, 4))))
+    return SDA_ERR_INVALID_ARG;
+  size_t dec = 0;
+  sda_status r = build_decode_ws(N, H, D, capacity, fp8, &dec);
+  if (r != SDA_OK) return r;
+  const HostWs w = host_ws_layout(N, H, D, comp_total, capacity, dec);
+  if (workspace_bytes < w.total) return SDA_ERR_WORKSPACE;
+  char* base = static_cast<char*>(workspace);
+  DeviceCaps caps;
+  cudaError_t e = device_caps(&caps);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t q_words = (int64_t)N * H * D / 2;
+  CopySegments in = {};
+  auto add = [](CopySegments& c, const void* src, void* dst, int64_t words) {
+    if (words > 0) c.seg[c.n++] = CopySegment{src, dst, words};
+  };
+  add(in, d_q, base + w.q, q_words);
+  add(in, d_ss, base + w.ss, N);
+  add(in, d_sl, base + w.sl, N);
+  add(in, d_sh, base + w.sh, N);
+  add(in, d_cp, base + w.cptr, N + 1);
+  add(in, d_cb, base + w.cb, comp_total);
+  add(in, d_cs, base + w.cs, comp_total);
+  if (e == cudaSuccess) e = launch_gather_copy(in, caps.num_sms, st);
+  if (e != cudaSuccess) {
+    note_cuda_error(e, "sda_build_decode_host");
+    return SDA_ERR_CUDA;
+  }
+  r = build_decode_impl(reinterpret_cast<const int32_t*>(base + w.ss),
+                        reinterpret_cast<const int32_t*>(base + w.sl),
+                        reinterpret_cast<const int32_t*>(base + w.sh),
+                        reinterpret_cast<const int32_t*>(base + w.cptr),
+                        reinterpret_cast<const int32_t*>(base + w.cb),
+                        reinterpret_cast<const int32_t*>(base + w.cs), comp_total, win,
+                        k_per_block, swa_pages, reinterpret_cast<int32_t*>(base + w.idx), capacity,
+                        reinterpret_cast<int32_t*>(base + w.iptr),
+                        reinterpret_cast<int32_t*>(base + w.st), base + w.q, unified_kv, kv_scale,
+                        total_pages, attn_sink, softmax_scale, N, H, D, base + w.out,
+                        base + w.dec, dec > 0 ? dec : 1, stream, "sda_build_decode_host");
+  if (r != SDA_OK) return r;
+  CopySegments back = {};
+  add(back, base + w.out, const_cast<void*>(d_out), q_words);
+  add(back, base + w.st, const_cast<void*>(d_st), 1);
+  e = launch_gather_copy(back, caps.num_sms, st);
+  if (e != cudaSuccess) {
+    note_cuda_error(e, "sda_build_decode_host");
     return SDA_ERR_CUDA;
   }
   return SDA_OK;

@@ -120,3 +120,76 @@ def test_fused_graph_capture_and_empty_batch():
                                    win=w.win, k_per_block=w.k_per_block, swa_pages=w.swa_pages)
     torch.cuda.synchronize()
     assert p.tolist() == [0] and int(s0.item()) == 0 and o.shape[0] == 0
+
+
+def pinned(t):
+    return t.cpu().pin_memory()
+
+
+def host_call(w, bi, pool=None, out=None, status=None, workspace=None, stream=None):
+    kv = w.unified_kv if pool is None else pool.codes
+    h = {k: pinned(v) for k, v in bi.items()}
+    return sda.build_decode_host(pinned(w.q), kv, w.attn_sink, w.softmax_scale, h["state_slot"],
+                                 h["swa_len"], h["swa_head"], h["comp_indptr"], h["comp_block"],
+                                 h["comp_slot"], win=w.win, k_per_block=w.k_per_block,
+                                 swa_pages=w.swa_pages, kv_scale=None if pool is None else pool.scale,
+                                 out=out, status=status, workspace=workspace, stream=stream)
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2], ids=[inputs.CONFIG_NAMES[c] for c in (0, 1, 2)])
+def test_host_buffers_equal_the_device_call(cfg):
+    """Inputs read by kernels straight from page-locked host memory and the
+    result written back to it: bit-identical to the device-buffer call."""
+    w = inputs.config(cfg, device="cuda")
+    bi = w.builder_inputs("cuda")
+    out_h, st_h = host_call(w, bi)
+    out_d, _, _, st_d = fused(w, bi)
+    torch.cuda.synchronize()
+    assert int(st_h.item()) == int(st_d.item())
+    assert torch.equal(out_h.view(torch.int16), out_d.cpu().view(torch.int16))
+
+
+def test_host_buffers_fp8_and_bad_descriptors():
+    w = inputs.config(1, device="cuda")
+    bi = {k: v.clone() for k, v in w.builder_inputs("cuda").items()}
+    bi["swa_len"][2] = -1  # bit 1: token 2 decodes to +0
+    pool = inputs.fp8_pool(w)
+    out_h, st_h = host_call(w, bi, pool)
+    out_d, _, _, st_d = fused(w, bi, pool)
+    torch.cuda.synchronize()
+    assert int(st_h.item()) == int(st_d.item()) == 1
+    assert torch.equal(out_h.view(torch.int16), out_d.cpu().view(torch.int16))
+    assert not out_h[2].view(torch.int16).any()
+
+
+def test_host_buffers_graph_replay_and_rejects_pageable():
+    w = inputs.config(1, device="cuda")
+    bi = w.builder_inputs("cuda")
+    h = {k: pinned(v) for k, v in bi.items()}
+    q_h = pinned(w.q)
+    out_h = torch.empty(w.q.shape, dtype=torch.bfloat16, pin_memory=True)
+    st_h = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    cap = w.N * w.win + int(w.comp_block.size)
+    ws = torch.empty(sda.build_decode_host_workspace_size(w.N, w.H, w.D, int(w.comp_block.size), cap),
+                     dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    args = (q_h, w.unified_kv, w.attn_sink, w.softmax_scale, h["state_slot"], h["swa_len"],
+            h["swa_head"], h["comp_indptr"], h["comp_block"], h["comp_slot"])
+    kw = dict(win=w.win, k_per_block=w.k_per_block, swa_pages=w.swa_pages, capacity=cap,
+              out=out_h, status=st_h, workspace=ws, stream=s)
+    with torch.cuda.stream(s):
+        sda.build_decode_host(*args, **kw)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        sda.build_decode_host(*args, **kw)
+    out_h.zero_()
+    st_h.fill_(-1)
+    g.replay()
+    torch.cuda.synchronize()
+    out_d, _, _, st_d = fused(w, bi)
+    torch.cuda.synchronize()
+    assert int(st_h.item()) == int(st_d.item()) == 0
+    assert torch.equal(out_h.view(torch.int16), out_d.cpu().view(torch.int16))
+    with pytest.raises(ValueError):  # pageable host memory
+        sda.build_decode_host(w.q.cpu(), *args[1:], **{**kw, "stream": None})
