@@ -11,6 +11,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "sda_copy.cuh"
 #include "sda_internal.cuh"
 
 namespace sda {

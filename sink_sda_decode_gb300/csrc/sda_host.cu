@@ -12,6 +12,7 @@
 
 #include <cstdint>
 
+#include "sda_copy.cuh"
 #include "sda_internal.cuh"
 
 namespace sda {

@@ -85,20 +85,6 @@ WsLayout workspace_layout(int N, int H, int D, int64_t total_indices, const Laun
 // All launchers only enqueue; they return cudaGetLastError().
 cudaError_t launch_plan(const int32_t* kv_indptr, int N, int64_t total_indices,
                         const LaunchPlan& lp, void* ws, const WsLayout& L, cudaStream_t st);
-// Copies between arrays the SMs can address (device memory, page-locked host
-// memory), in one grid-stride launch; every segment 4-byte aligned.
-struct CopySegment {
-  const void* src;
-  void* dst;
-  int64_t words;  // 4-byte words
-};
-constexpr int kMaxCopySegments = 8;
-struct CopySegments {
-  CopySegment seg[kMaxCopySegments];
-  int n;
-};
-cudaError_t launch_gather_copy(const CopySegments& segs, int num_sms, cudaStream_t st);
-
 // The builder's scan and the work plan in one CTA (sda_build_decode).
 cudaError_t launch_scan_plan(int N, int64_t capacity, int32_t* kv_indptr, int32_t* status,
                              const LaunchPlan& lp, void* ws, const WsLayout& L, cudaStream_t st);
