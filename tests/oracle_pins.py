@@ -267,6 +267,15 @@ def pin_builder_capacity(lib):
     assert st == 32 and ptr.tolist() == [0, 0, 0] and idx.size == 0
 
 
+def pin_builder_comp_range(lib):
+    """A compressed range that ends past the last entry: that token is empty
+    with status bit 4, the token before it is unaffected (worked by hand:
+    t0 = ring slot 0*4 + 0 and compressed 8 + 0*4 + 2)."""
+    idx, ptr, st = oracle.build_indices([0, 1], [1, 1], [0, 0], [0, 1, 3], [0], [2], 4, 4, 8, 16,
+                                        lib=lib)
+    assert st == 4 and ptr.tolist() == [0, 2, 2] and idx.tolist() == [0, 10]
+
+
 def pin_validate(lib):
     """Validation flags: decreasing indptr, indptr out of range, bad slots (counted)."""
     assert oracle.validate_indices([0, 1, 2], [0, 1, 3], 3, lib=lib) == (0, 0)
@@ -590,7 +599,8 @@ ROUNDING_PINS = [pin_bf16_rne, pin_e4m3_rne, pin_fp8_scale]
 DECODE_PINS = [pin_sdpa, pin_sink_minus_inf_is_softmax, pin_single_slot, pin_duplicate_adds_ln2,
                pin_zero_length, pin_permutation, pin_sink_factor, pin_scale_zero, pin_convexity,
                pin_hard_attention_limit, pin_sink_plus_inf, pin_token_subset]
-BUILDER_PINS = [pin_builder_golden, pin_builder_ring_closed_form, pin_builder_capacity]
+BUILDER_PINS = [pin_builder_golden, pin_builder_ring_closed_form, pin_builder_capacity,
+                pin_builder_comp_range]
 VALIDATE_PINS = [pin_validate]
 ALL_PINS = (DECODE_PINS + BUILDER_PINS + VALIDATE_PINS + FP8_PINS + STORE_PINS + ROUNDING_PINS
             + TOPK_PINS)

@@ -99,6 +99,11 @@ MUTANTS = {
                            pins.BUILDER_PINS),
     "padded_not_empty": ("if (state_slot[t] < 0) continue;", "if (state_slot[t] < -1) continue;",
                          pins.BUILDER_PINS),
+    "swa_head_unchecked": ("else if (n_swa > 0 && (swa_head[t] < 0 || swa_head[t] >= win)) bad |= 2;",
+                           "else if (0) bad |= 2;", pins.BUILDER_PINS),
+    "comp_indptr_decrease_unchecked": ("if (c0 < 0 || c1 < c0 || (int64_t)c1 > comp_total) bad |= 4;",
+                                       "if (c0 < 0 || (int64_t)c1 > comp_total) bad |= 4;",
+                                       pins.BUILDER_PINS),
     # validation
     "validate_off_by_one": ("(int64_t)kv_indices[e] >= total_pages) ++n_bad;",
                             "(int64_t)kv_indices[e] > total_pages) ++n_bad;", pins.VALIDATE_PINS),
