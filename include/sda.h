@@ -167,19 +167,15 @@ sda_status sda_decode_noalloc(const void* q, const void* unified_kv, int64_t tot
 
 /*
  * Which attention kernel sda_decode launches for (H, D) on the current
- * device: *kernel = SDA_KERNEL_SIMT (CUDA cores, any supported shape),
- * SDA_KERNEL_ONE_CTA (tensor cores, one CTA per unit) or SDA_KERNEL_CLUSTER
- * (tensor cores, a two-CTA cluster per unit, each CTA holding half of D).
- * The tensor-core kernels need D = 512 and H in {16, 32} or a multiple of
- * 64; the one-CTA kernel is the default there, the cluster kernel runs only
- * when forced (and when the device can run it).  The
- * environment variable SDA_FORCE_VARIANT=simt|umma|pair overrides the choice
- * where the shape allows (for testing).  Errors: SDA_ERR_INVALID_ARG (kernel
+ * device: *kernel = SDA_KERNEL_SIMT (CUDA cores, any supported shape) or
+ * SDA_KERNEL_ONE_CTA (tensor cores, one CTA per unit; D = 512 and H in
+ * {16, 32} or a multiple of 64, the default there).  The environment
+ * variable SDA_FORCE_VARIANT=simt|umma overrides the choice where the shape
+ * allows (for testing).  Errors: SDA_ERR_INVALID_ARG (kernel
  * is NULL), SDA_ERR_UNSUPPORTED, SDA_ERR_CUDA.
  */
 #define SDA_KERNEL_SIMT 0
 #define SDA_KERNEL_ONE_CTA 1
-#define SDA_KERNEL_CLUSTER 2
 sda_status sda_decode_kernel(int H, int D, int* kernel);
 
 /*

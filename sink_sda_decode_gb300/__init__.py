@@ -189,12 +189,12 @@ def decode_noalloc(q: torch.Tensor, unified_kv: torch.Tensor, kv_indices: torch.
     return out
 
 
-KERNEL_NAMES = {0: "simt", 1: "one_cta", 2: "cluster"}
+KERNEL_NAMES = {0: "simt", 1: "one_cta"}
 
 
 def decode_kernel(H: int, D: int, device=None) -> str:
     """Name of the attention kernel decode() launches for (H, D) on `device`
-    ("simt", "one_cta" or "cluster")."""
+    ("simt" or "one_cta")."""
     lib = _lib.load()
     k = ctypes.c_int(-1)
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):

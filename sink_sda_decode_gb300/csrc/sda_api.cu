@@ -36,9 +36,8 @@ struct DeviceInfo {
 };
 DeviceInfo g_dev[kMaxDevices];
 
-// SM count of the current device and how many CTA pairs of the cluster
-// kernel fit at once, queried once per device; also sets the tensor-core
-// kernels' shared-memory attributes on that device.
+// SM count of the current device, queried once per device; also sets the
+// tensor-core kernels' shared-memory attributes on that device.
 cudaError_t device_caps(DeviceCaps* caps) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -49,10 +48,6 @@ cudaError_t device_caps(DeviceCaps* caps) {
     d.err = cudaDeviceGetAttribute(&d.caps.num_sms, cudaDevAttrMultiProcessorCount, dev);
     for (int nh : {16, 32, 64})
       if (d.err == cudaSuccess) d.err = umma_prepare(nh);
-    for (int i = 0; i < 3 && d.err == cudaSuccess; ++i) {
-      const cudaError_t pe = pair_prepare(16 << i, &d.caps.pairs[i]);
-      if (pe != cudaSuccess) note_cuda_error(pe, "cluster kernel unavailable");
-    }
   });
   *caps = d.caps;
   return d.err;
@@ -62,14 +57,13 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) &
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Optional A/B switch for tests: SDA_FORCE_VARIANT=simt|umma|pair forces a
-// decode kernel (pair and umma only where the shape allows them).
+// Optional A/B switch for tests: SDA_FORCE_VARIANT=simt|umma forces a
+// decode kernel (umma only where the shape allows it).
 int forced_variant() {
   const char* v = std::getenv("SDA_FORCE_VARIANT");
   if (!v) return -1;
   if (std::strcmp(v, "simt") == 0) return kSimt;
   if (std::strcmp(v, "umma") == 0) return kUmma;
-  if (std::strcmp(v, "pair") == 0) return kPair;
   return -1;
 }
 
@@ -88,26 +82,11 @@ bool choose_plan(int H, int D, const DeviceCaps& caps, LaunchPlan* lp) {
   lp->num_sms = caps.num_sms;
   const bool tc_shape = tc_shape_supported(H, D);
   const int nh = H < 64 ? H : 64;
-  const int pairs = tc_shape ? caps.pairs[nh == 16 ? 0 : nh == 32 ? 1 : 2] : 0;
   const int forced = forced_variant();
-  // The one-CTA kernel is the default: the cluster kernel's exchange of
-  // partial scores through distributed shared memory (~25 GB/s per SM
-  // measured) costs more per tile than the MMAs it saves.
   Variant v = tc_shape ? kUmma : kSimt;
-  if (forced == kSimt || (forced == kUmma && tc_shape) || (forced == kPair && pairs > 0))
-    v = static_cast<Variant>(forced);
+  if (forced == kSimt || (forced == kUmma && tc_shape)) v = static_cast<Variant>(forced);
   lp->variant = v;
-  if (v == kPair) {
-    // two CTAs (one cluster) per unit, each holding half of D; units are
-    // spread over the clusters that fit on the device at once
-    lp->nh = nh;
-    lp->hg = H / nh;
-    lp->grid = pairs;
-    lp->threads = 640;
-    lp->smem = pair_smem_bytes(nh);
-    lp->tile = kPairTileSlots;
-    lp->min_chunk = kPairTileSlots;
-  } else if (v == kUmma) {
+  if (v == kUmma) {
     lp->nh = nh;
     lp->hg = H / lp->nh;
     lp->grid = caps.num_sms;  // one CTA per SM (about 200 KB of shared memory each)
@@ -218,10 +197,7 @@ sda_status sda_decode(const void* q, const void* unified_kv, int64_t total_pages
   e = launch_plan(kv_indptr, N, total_indices, lp, workspace, L, st);
   if (e == cudaSuccess && g_ev_before && g_ev_after) e = cudaEventRecord(g_ev_before, st);
   if (e == cudaSuccess) {
-    if (lp.variant == kPair)
-      e = launch_decode_pair(q, unified_kv, kv_indices, attn_sink, softmax_scale, N, H, D, out,
-                             workspace, L, lp, st);
-    else if (lp.variant == kUmma)
+    if (lp.variant == kUmma)
       e = launch_decode_umma(q, unified_kv, nullptr, total_pages, kv_indices, attn_sink,
                              softmax_scale, N, H, D, out, workspace, L, lp, st);
     else
@@ -372,9 +348,6 @@ static sda_status build_decode_impl(const int32_t* state_slot, const int32_t* sw
     if (fp8)
       e = launch_decode_umma(q, unified_kv, kv_scale, total_pages, kv_indices, attn_sink,
                              softmax_scale, N, H, D, out, workspace, L, lp, st);
-    else if (lp.variant == kPair)
-      e = launch_decode_pair(q, unified_kv, kv_indices, attn_sink, softmax_scale, N, H, D, out,
-                             workspace, L, lp, st);
     else if (lp.variant == kUmma)
       e = launch_decode_umma(q, unified_kv, nullptr, total_pages, kv_indices, attn_sink,
                              softmax_scale, N, H, D, out, workspace, L, lp, st);
@@ -567,8 +540,7 @@ sda_status sda_decode_kernel(int H, int D, int* kernel) {
   }
   LaunchPlan lp;
   choose_plan(H, D, caps, &lp);
-  static_assert(SDA_KERNEL_SIMT == kSimt && SDA_KERNEL_ONE_CTA == kUmma && SDA_KERNEL_CLUSTER == kPair,
-                "public kernel codes");
+  static_assert(SDA_KERNEL_SIMT == kSimt && SDA_KERNEL_ONE_CTA == kUmma, "public kernel codes");
   *kernel = lp.variant;
   return SDA_OK;
 }

@@ -62,9 +62,10 @@ constexpr int kMaxStages = 3;
 constexpr int kSmWarps = 8;                // warps 0..7: softmax / epilogue (warps q, q+4 share TMEM quadrant q)
 constexpr int kLoaderWarp0 = 8;            // warps 8..15: KV row loaders
 constexpr int kLoaderWarps = 8;
-constexpr int kMmaWarp = 16;               // warp 16: QK issuer + q loads
+constexpr int kMmaWarp = 16;               // warp 16: QK issuer (first half of D) + q loads
 constexpr int kPvWarp = 17;                // warp 17: PV issuer
-// 20 warps (18, 19 idle): warps are spread over the SM's four sub-partitions,
+constexpr int kMmaWarpB = 18;              // warp 18: QK issuer (second half of D)
+// 20 warps (19 idle): warps are spread over the SM's four sub-partitions,
 // each with 16 K registers, so 18 or 20 warps (5 on some) allow 96 registers
 constexpr int kThreads = 640;
 constexpr int kRowsPerLoader = kTileSlots / kLoaderWarps;  // 8 rows of a tile per loader warp
@@ -88,6 +89,7 @@ enum Bar : int {
   kBarOEmpty,
   kBarDrain,
   kBarDrainPv,
+  kBarDrainQb,
   kNumBars
 };
 
@@ -124,8 +126,10 @@ struct Cfg {
   static constexpr int kOffHMax = kOffLSum + 4 * 128;
   static constexpr int kSmemUsed = kOffHMax + 4 * 256;
   static constexpr int kSmem = kSmemUsed + 1024;  // slack for 1024-byte alignment
-  static constexpr int kTmemCols = (128 + 4 * NH) <= 256 ? 256 : 512;
   static constexpr int kOCol = 128;  // O^T block b at columns [128 + b*NH, +NH)
+  static constexpr int kSbCol = kOCol + 4 * NH;  // S_b buffers (second half of D) after O^T
+  static constexpr int kTmemCols = (kSbCol + 128) <= 256 ? 256 : 512;
+  static_assert(kSbCol + 128 <= 512, "TMEM columns");
   static constexpr uint32_t kIdescQK = idesc_bf16_f32(64, 64, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, NH, true, false);
   static_assert(kOffP % 1024 == 0 && kPBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
@@ -256,13 +260,13 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQFull), 1);
-    mbar_init(bar(kBarQEmpty), 1);
+    mbar_init(bar(kBarQEmpty), 2);  // both QK issuers' commits
     for (int i = 0; i < 2 * C::kStages; ++i) {
       mbar_init(bar(kBarKVFull0 + i), kLoaderWarps);
       mbar_init(bar(kBarPVDone0 + i), 1);
     }
-    mbar_init(bar(kBarSFull0), 1);
-    mbar_init(bar(kBarSFull1), 1);
+    mbar_init(bar(kBarSFull0), 2);  // S_a and S_b
+    mbar_init(bar(kBarSFull1), 2);
     mbar_init(bar(kBarSEmpty0), kSmWarps);
     mbar_init(bar(kBarSEmpty1), kSmWarps);
     mbar_init(bar(kBarPFull0), kSmWarps);
@@ -270,6 +274,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
     mbar_init(bar(kBarOEmpty), kSmWarps);
     mbar_init(bar(kBarDrain), 1);
     mbar_init(bar(kBarDrainPv), 1);
+    mbar_init(bar(kBarDrainQb), 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmap_q);
@@ -401,32 +406,23 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         hv[PF - 1] = hpf;
       }
     } else {
+    // bf16 pool: rows go straight from global to shared memory with 16-byte
+    // cp.async (no register round trip, no separate shared stores).  Each
+    // half of D of the warp's 8 rows is one commit group, issued as soon as
+    // the PV MMAs that last read that half of the stage are done; the warp
+    // then waits for its own copies, fences them to the async proxy (the
+    // tensor cores read the stage through it) and arrives, half by half.
     for (int g = 0; hv[0] && ok; ++g) {
       const int s = g % KS;  // KV stage
-      uint4 v[2 * kRowsPerLoader];
-#pragma unroll
-      for (int r = 0; r < kRowsPerLoader; ++r) {
-        const int slot = __shfl_sync(0xffffffffu, sl[0], r);
-        if (slot >= 0) {
-          const uint4* src = kv4 + (size_t)slot * (kD / 8);
-          v[2 * r] = __ldcg(src + lane);
-          v[2 * r + 1] = __ldcg(src + 32 + lane);
-        } else {  // tail row of a partial tile: zeros (its p is forced to 0)
-          v[2 * r] = make_uint4(0, 0, 0, 0);
-          v[2 * r + 1] = make_uint4(0, 0, 0, 0);
-        }
-      }
       if (g == 0) {
 #pragma unroll
         for (int j = 1; j < PF; ++j) prefetch_rows(sl[j]);
       }
-      const bool hpf = c.valid;  // tile g + PF
+      const bool hpf = c.valid;  // tile g + PF: its slot indices are read now
       const int spf = hpf ? tile_slot() : -1;
       if (hpf) c.next();
-      // store the tile in two halves of D (each row's loads v[2r] and
-      // v[2r + 1]), each as soon as the PV MMAs that read that half of the
-      // tile last in this stage are done
-      uint8_t* stage = smem + C::kOffKV + s * kKVBytes;
+      const uint32_t stage = sKV + s * kKVBytes;
+      int issued = 0;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         if (g >= KS) {  // the tile KS back in this stage
@@ -435,16 +431,31 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
           if (!ok) break;
         }
         // 16-byte chunk q = 32*hh + lane of each row: panel q/8, chunk q%8;
-        // the warp's 8 rows are one 8-row swizzle atom of every panel
+        // the warp's 8 rows are one 8-row swizzle atom of every panel.  A
+        // tail row of a partial tile is zero-filled (its p is forced to 0).
         const int q = hh * 32 + lane, k = q & 7;
-        uint8_t* atom = stage + (q >> 3) * kPanelKV + lw * 1024;
+        const uint32_t atom = stage + (q >> 3) * kPanelKV + lw * 1024;
         static_assert(kRowsPerLoader == 8, "one swizzle atom per loader warp");
 #pragma unroll
-        for (int r = 0; r < kRowsPerLoader; ++r)
-          *reinterpret_cast<uint4*>(atom + r * 128 + ((k ^ r) << 4)) = v[2 * r + hh];
-        fence_proxy_async_smem();  // generic-proxy stores -> read by the tensor cores
+        for (int r = 0; r < kRowsPerLoader; ++r) {
+          const int slot = __shfl_sync(0xffffffffu, sl[0], r);
+          const uint4* src = slot >= 0 ? kv4 + (size_t)slot * (kD / 8) + q : kv4;
+          cp_async16(atom + r * 128 + ((k ^ r) << 4), src, slot >= 0 ? 16u : 0u);
+        }
+        cp_async_commit();
+        ++issued;
+      }
+      if (issued == 2) {
+        cp_async_wait_group<1>();  // first half landed
+        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kv_full(s, hh)));
+        if (lane == 0) mbar_arrive(bar(kv_full(s, 0)));
+      }
+      cp_async_wait_group<0>();
+      if (issued == 2) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kv_full(s, 1)));
       }
       prefetch_rows(spf);
 #pragma unroll
@@ -456,27 +467,31 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
       hv[PF - 1] = hpf;
     }
     }
-  } else if (warp == kMmaWarp || warp == kPvWarp) {
+  } else if (warp == kMmaWarp || warp == kPvWarp || warp == kMmaWarpB) {
     // ===================================================== MMA issuers
-    // Two threads issue tcgen05 MMAs, so that one waiting for the tensor
-    // pipe to accept its instructions never delays the other:
-    //  - warp 16, lane 0: S = Q K^T of every tile, as soon as the tile has
-    //    landed and its S buffer is free, and q of the next unit (tiled TMA)
-    //    as soon as this unit's last QK has read q;
+    // Three threads issue tcgen05 MMAs; one thread's MMAs run one after the
+    // other, but MMAs of different threads overlap in the tensor pipe, so
+    // splitting the work keeps it busy:
+    //  - warps 16 and 18, lane 0: S = Q K^T of every tile, K split in two:
+    //    warp 16 the columns [0, 256) of D into S_a, warp 18 the columns
+    //    [256, 512) into S_b (the softmax adds the two), each as soon as its
+    //    half of the tile has landed and the S buffer is free; warp 16 also
+    //    loads q of the next unit (tiled TMA) once both halves of this unit's
+    //    last QK have read q;
     //  - warp 17, lane 0: O^T += V^T P^T of every tile as soon as its P is
     //    written (a commit after blocks 1 and 3 releases each half of the KV
     //    stage; the second also frees the P buffer).
-    // Each thread's commits track only its own MMAs.
-    // Each has a single next event at any time, so it sleeps in the
-    // mbarrier wait (hardware suspend) instead of spinning, which leaves the
-    // issue slots of its sub-partition to the softmax and loader warps.
+    // Each thread's commits track only its own MMAs.  Each has a single next
+    // event at any time, so it sleeps in the mbarrier wait (hardware suspend)
+    // instead of spinning, leaving the issue slots to the other warps.
     if (lane == 0) {
-      const bool qk_role = warp == kMmaWarp;
+      const bool qk_role = warp != kPvWarp;
+      const int qh = warp == kMmaWarpB ? 1 : 0;  // QK: half of D (of the K dimension)
       TileCursor cq;
       cq.init(p.units, n_units);
       int q_issued = 0;
       bool ok = true;
-      if (qk_role && cq.valid) {  // q of the first unit
+      if (qk_role && qh == 0 && cq.valid) {  // q of the first unit
         mbar_arrive_expect_tx(bar(kBarQFull), NH * 128 * kPanels);
         const int qrow = cq.u.x * H + unit_head_group(cq.u.w) * NH;
 #pragma unroll
@@ -488,32 +503,29 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         if (qk_role) {
           if (g >= 2) ok = wait_bar(bar(kBarSEmpty0 + s), ((g >> 1) - 1) & 1, abort_flag, p.hdr);
           if (ok && cq.i == 0) ok = wait_bar(bar(kBarQFull), cq.nu & 1, abort_flag, p.hdr);
+          if (ok) ok = wait_bar(bar(kv_full(ks, qh)), (g / KS) & 1, abort_flag, p.hdr);
           if (!ok) break;
+          tc_fence_after();
           const uint32_t kvs = sKV + ks * kKVBytes;
           // descriptors of the first K step; the others only move the start address
           const uint64_t a0 = sdesc_sw128(sQ, 16, 1024), b0 = sdesc_sw128(kvs, 16, 1024);
+          const uint32_t sacc = tmem + (qh ? C::kSbCol : 0) + s * 64;
 #pragma unroll
-          for (int c = 0; c < kPanels; ++c) {
-            if ((c & 3) == 0) {  // panels 4h..4h+3 = half h of the stage
-              ok = wait_bar(bar(kv_full(ks, c >> 2)), (g / KS) & 1, abort_flag, p.hdr);
-              if (!ok) break;
-              tc_fence_after();
-            }
+          for (int c = 4 * qh; c < 4 * qh + 4; ++c) {  // panels of this half of D
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t a = sdesc_advance(a0, c * C::kPanelQ + kk * 32);
               const uint64_t bd = sdesc_advance(b0, c * kPanelKV + kk * 32);
-              mma_bf16(tmem + s * 64, a, bd, C::kIdescQK, (c | kk) ? 1u : 0u);
+              mma_bf16(sacc, a, bd, C::kIdescQK, (c != 4 * qh || kk) ? 1u : 0u);
             }
           }
-          if (!ok) break;
           mma_commit(bar(kBarSFull0 + s));
           const bool last = cq.i == cq.ntiles - 1;
           const int nu = cq.nu;
           if (last) mma_commit(bar(kBarQEmpty));
           cq.next();
-          if (last && cq.valid) {
-            // q of the next unit once this unit's QKs have read q
+          if (qh == 0 && last && cq.valid) {
+            // q of the next unit once this unit's QKs (both halves) have read q
             ok = wait_bar(bar(kBarQEmpty), nu & 1, abort_flag, p.hdr);
             if (!ok) break;
             mbar_arrive_expect_tx(bar(kBarQFull), NH * 128 * kPanels);
@@ -548,10 +560,10 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         }
       }
       // drain this thread's MMAs (and the last q copy) before TMEM and smem go away
-      const int drain = qk_role ? kBarDrain : kBarDrainPv;
+      const int drain = qk_role ? (qh ? kBarDrainQb : kBarDrain) : kBarDrainPv;
       mma_commit(bar(drain));
       drain_bar(bar(drain), 0, p.hdr);
-      if (qk_role && q_issued >= 1) drain_bar(bar(kBarQFull), (q_issued - 1) & 1, p.hdr);
+      if (qk_role && qh == 0 && q_issued >= 1) drain_bar(bar(kBarQFull), (q_issued - 1) & 1, p.hdr);
     }
     __syncwarp();
   } else if (warp < kSmWarps) {
@@ -560,8 +572,18 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
     // each tile, hc = w / 4, with the 16x256b shape: thread t holds heads
     // hA = 16q + t/4 and hB = hA + 8 (the M = 64 accumulator keeps row r in
     // lane 32*(r/16) + r%16) for the 8 slots 32hc + 8rep + 2(t%4) + {0,1},
-    // rep = 0..3.  A head's row max over the tile is two quad shuffles and
-    // one exchange with warp w ^ 4 through shared memory.
+    // rep = 0..3, as the sum of the two K halves S_a + S_b.
+    //
+    // Weights are taken against a per-head running reference m (log2
+    // units): p = 2^(score * scale * log2 e - m).  On a unit's first tile m
+    // is the tile's exact per-head maximum (two quad shuffles and an
+    // exchange with warp w ^ 4).  On later tiles the weights are computed
+    // against the current m straight away, and only when a scaled score
+    // exceeds m by more than the threshold (2^8 headroom, so p <= 256 in
+    // bf16) do the eight warps take the exact path: the tile's maxima, a
+    // raised m, O^T rescaled in TMEM and the tile's weights recomputed.  So
+    // a tile after the first needs one block-wide vote and no exchange, and
+    // the weights are those of a running maximum raised lazily.
     const int q4 = warp & 3, hc = warp >> 2;
     const int st = threadIdx.x;  // 0..255
     const int tq = lane & 3;
@@ -569,7 +591,6 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
     const bool vA = hA < NH, vB = hB < NH;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const float sc = p.qk_scale_log2;
-    const bool pos_sc = sc >= 0.f;  // a negative scale makes the smallest score the largest logit
     // Control flow here is identical in the eight warps (it depends only on
     // the unit list and on block-wide votes), so every named barrier is
     // reached by all of them even after a wait timed out: a timed-out wait
@@ -596,116 +617,141 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         const int n = min(kTileN, len - i * kTileN);
         wait_bar(bar(kBarSFull0 + s), (g >> 1) & 1, abort_flag, p.hdr);
         tc_fence_after();
-        uint32_t sv[16];
-        tmem_ld_16x256b_x4(tmem + lane_base + s * 64 + 32 * hc, sv);
-        tmem_wait_ld();
+        float x[16];  // raw scores of this thread's 16 (head, slot) pairs: S_a + S_b
+        {
+          uint32_t sv[16];
+          tmem_ld_16x256b_x4(tmem + lane_base + s * 64 + 32 * hc, sv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) x[e] = __uint_as_float(sv[e]);
+          tmem_ld_16x256b_x4(tmem + lane_base + C::kSbCol + s * 64 + 32 * hc, sv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) x[e] += __uint_as_float(sv[e]);
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarSEmpty0 + s));  // S buffer s may be overwritten
-        // largest scaled logit per head over this warp's valid slots
-        float eA = pos_sc ? -INFINITY : INFINITY, eB = eA;
+        uint32_t valid = 0;  // bit e: element e is a slot of the list (not past the tile's end)
 #pragma unroll
         for (int rep = 0; rep < 4; ++rep) {
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            if (32 * hc + 8 * rep + 2 * tq + kk < n) {
-              const float a = __uint_as_float(sv[4 * rep + kk]), b = __uint_as_float(sv[4 * rep + 2 + kk]);
-              eA = pos_sc ? fmaxf(eA, a) : fminf(eA, a);
-              eB = pos_sc ? fmaxf(eB, b) : fminf(eB, b);
-            }
+          for (int kk = 0; kk < 4; ++kk) {
+            const int j = 32 * hc + 8 * rep + 2 * tq + (kk & 1);
+            valid |= (j < n ? 1u : 0u) << (4 * rep + kk);
           }
-        }
-#pragma unroll
-        for (int o = 1; o <= 2; o <<= 1) {
-          const float xa = __shfl_xor_sync(0xffffffffu, eA, o), xb = __shfl_xor_sync(0xffffffffu, eB, o);
-          eA = pos_sc ? fmaxf(eA, xa) : fminf(eA, xa);
-          eB = pos_sc ? fmaxf(eB, xb) : fminf(eB, xb);
-        }
-        {  // combine with the other half of the tile (warp w ^ 4)
-          float* hm = s_hmax + (g & 1) * 128;
-          if (tq == 0) {
-            hm[hc * 64 + hA] = eA;
-            hm[hc * 64 + hB] = eB;
-          }
-          named_bar_sync(2 + q4, 64);
-          const float oA = hm[(hc ^ 1) * 64 + hA], oB = hm[(hc ^ 1) * 64 + hB];
-          eA = pos_sc ? fmaxf(eA, oA) : fminf(eA, oA);
-          eB = pos_sc ? fmaxf(eB, oB) : fminf(eB, oB);
-        }
-        const float tA = eA * sc, tB = eB * sc;
-        float alphaA = 1.f, alphaB = 1.f;
-        bool need = false;
-        if (vA && tA > mA + kRescaleThreshold) {
-          alphaA = ex2_approx(mA - tA);  // 0 on the first tile (m = -inf)
-          need = i > 0;
-          lA *= alphaA;
-          mA = tA;
-        }
-        if (vB && tB > mB + kRescaleThreshold) {
-          alphaB = ex2_approx(mB - tB);
-          need = need || i > 0;
-          lB *= alphaB;
-          mB = tB;
         }
         // P buffer s is free once the PV of tile g-2 is done
         if (g >= 2) {
           if (lane == 0) wait_bar(bar(pv_done((g - 2) % KS, 1)), ((g - 2) / KS) & 1, abort_flag, p.hdr);
           __syncwarp();
         }
-        // p = 2^(s*scale - m) in bf16 into rows hA, hB of P (K-major, 128-byte
+        // p = 2^(x*scale - m) in bf16 into rows hA, hB of P (K-major, 128-byte
         // swizzle: 16-byte chunk c of 8 slots at (c ^ (h & 7)) * 16, this
-        // thread's slot pair at byte 4*tq of the chunk)
+        // thread's slot pair at byte 4*tq of the chunk); returns whether a
+        // weight exceeded the headroom.  The denominator sums the same bf16
+        // weights the PV MMA multiplies, so rounding p perturbs the weights
+        // of an exact weighted average but biases nothing.
         uint8_t* pbase = smem + C::kOffP + s * C::kPBytes;
         uint8_t* prowA = pbase + (hA >> 3) * 1024 + (hA & 7) * 128 + 4 * tq;
         uint8_t* prowB = pbase + (hB >> 3) * 1024 + (hB & 7) * 128 + 4 * tq;
-        float sA = 0.f, sB = 0.f;
+        float sA, sB;
+        auto weights = [&]() {
+          bool over = false;
+          sA = 0.f;
+          sB = 0.f;
 #pragma unroll
-        for (int rep = 0; rep < 4; ++rep) {
-          const int c = 4 * hc + rep;  // chunk of 8 slots within the tile
-          const int j = 8 * c + 2 * tq;
-          const float a0 = j < n ? ex2_approx(fmaf(__uint_as_float(sv[4 * rep + 0]), sc, -mA)) : 0.f;
-          const float a1 = j + 1 < n ? ex2_approx(fmaf(__uint_as_float(sv[4 * rep + 1]), sc, -mA)) : 0.f;
-          const float b0 = j < n ? ex2_approx(fmaf(__uint_as_float(sv[4 * rep + 2]), sc, -mB)) : 0.f;
-          const float b1 = j + 1 < n ? ex2_approx(fmaf(__uint_as_float(sv[4 * rep + 3]), sc, -mB)) : 0.f;
-          __nv_bfloat162 pa = __floats2bfloat162_rn(a0, a1), pb = __floats2bfloat162_rn(b0, b1);
-          // the denominator sums the same bf16 weights the PV MMA multiplies,
-          // so rounding p perturbs the weights but biases nothing
-          const float2 fa = __bfloat1622float2(pa), fb = __bfloat1622float2(pb);
-          sA += fa.x + fa.y;
-          sB += fb.x + fb.y;
-          if (vA) *reinterpret_cast<uint32_t*>(prowA + ((c ^ (hA & 7)) << 4)) = *reinterpret_cast<uint32_t*>(&pa);
-          if (vB) *reinterpret_cast<uint32_t*>(prowB + ((c ^ (hB & 7)) << 4)) = *reinterpret_cast<uint32_t*>(&pb);
+          for (int rep = 0; rep < 4; ++rep) {
+            float e[4];
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const bool ok_e = (valid >> (4 * rep + kk)) & 1u;
+              const float arg = fmaf(x[4 * rep + kk], sc, -((kk < 2) ? mA : mB));
+              over = over || (ok_e && arg > kRescaleThreshold);
+              e[kk] = ok_e ? ex2_approx(arg) : 0.f;
+            }
+            __nv_bfloat162 pa = __floats2bfloat162_rn(e[0], e[1]), pb = __floats2bfloat162_rn(e[2], e[3]);
+            const float2 fa = __bfloat1622float2(pa), fb = __bfloat1622float2(pb);
+            sA += fa.x + fa.y;
+            sB += fb.x + fb.y;
+            const int c = 4 * hc + rep;  // chunk of 8 slots within the tile
+            if (vA) *reinterpret_cast<uint32_t*>(prowA + ((c ^ (hA & 7)) << 4)) = *reinterpret_cast<uint32_t*>(&pa);
+            if (vB) *reinterpret_cast<uint32_t*>(prowB + ((c ^ (hB & 7)) << 4)) = *reinterpret_cast<uint32_t*>(&pb);
+          }
+          return over;
+        };
+        // exact path on a unit's first tile (block-uniform), else by vote (an
+        // invalid head's weights are never stored, so it casts no vote)
+        const bool exact = i == 0 || named_bar_or(1, kSoftmaxThreads, weights() && vA);
+        if (exact) {
+          // exact path: the tile's largest scaled score per head
+          float eA = -INFINITY, eB = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            if ((valid >> e) & 1u) {
+              if ((e & 3) < 2) eA = fmaxf(eA, x[e] * sc);
+              else eB = fmaxf(eB, x[e] * sc);
+            }
+          }
+#pragma unroll
+          for (int o = 1; o <= 2; o <<= 1) {
+            eA = fmaxf(eA, __shfl_xor_sync(0xffffffffu, eA, o));
+            eB = fmaxf(eB, __shfl_xor_sync(0xffffffffu, eB, o));
+          }
+          {  // combine with the other half of the tile (warp w ^ 4)
+            float* hm = s_hmax + (g & 1) * 128;
+            if (tq == 0) {
+              hm[hc * 64 + hA] = eA;
+              hm[hc * 64 + hB] = eB;
+            }
+            named_bar_sync(2 + q4, 64);
+            eA = fmaxf(eA, hm[(hc ^ 1) * 64 + hA]);
+            eB = fmaxf(eB, hm[(hc ^ 1) * 64 + hB]);
+          }
+          float alphaA = 1.f, alphaB = 1.f;
+          if (vA && eA > mA + kRescaleThreshold) {
+            alphaA = ex2_approx(mA - eA);  // 0 when m was -inf
+            lA *= alphaA;
+            mA = eA;
+          }
+          if (vB && eB > mB + kRescaleThreshold) {
+            alphaB = ex2_approx(mB - eB);
+            lB *= alphaB;
+            mB = eB;
+          }
+          weights();  // against the raised reference (the scores die here)
+          if (i > 0) {
+            // O^T already holds this unit's earlier tiles: scale its head columns
+            if (tq == 0 && hc == 0) {
+              if (vA) s_alpha[hA] = alphaA;
+              if (vB) s_alpha[hB] = alphaB;
+            }
+            named_bar_sync(1, kSoftmaxThreads);
+            // O^T must be quiescent: wait for the PV of tile g-1
+            if (lane == 0) wait_bar(bar(pv_done((g - 1) % KS, 1)), ((g - 1) / KS) & 1, abort_flag, p.hdr);
+            __syncwarp();
+            tc_fence_after();
+            // this warp's lanes of O^T blocks 2hc, 2hc + 1
+#pragma unroll
+            for (int b = 2 * hc; b < 2 * hc + 2; ++b) {
+#pragma unroll
+              for (int c = 0; c < NH / 16; ++c) {
+                uint32_t ov[16];
+                const uint32_t ta = tmem + lane_base + C::kOCol + b * NH + c * 16;
+                tmem_ld16(ta, ov);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * s_alpha[c * 16 + e]);
+                tmem_st16(ta, ov);
+              }
+            }
+            tmem_wait_st();
+            named_bar_sync(1, kSoftmaxThreads);  // s_alpha is rewritten next time
+          }
         }
         lA += sA;
         lB += sB;
         fence_proxy_async_smem();
-        if (named_bar_or(1, kSoftmaxThreads, need)) {
-          if (tq == 0 && hc == 0) {
-            if (vA) s_alpha[hA] = alphaA;
-            if (vB) s_alpha[hB] = alphaB;
-          }
-          named_bar_sync(1, kSoftmaxThreads);
-          // O^T must be quiescent: wait for the PV of tile g-1
-          if (lane == 0) wait_bar(bar(pv_done((g - 1) % KS, 1)), ((g - 1) / KS) & 1, abort_flag, p.hdr);
-          __syncwarp();
-          tc_fence_after();
-          // this warp's lanes of O^T blocks 2hc, 2hc + 1
-#pragma unroll
-          for (int b = 2 * hc; b < 2 * hc + 2; ++b) {
-#pragma unroll
-            for (int c = 0; c < NH / 16; ++c) {
-              uint32_t ov[16];
-              const uint32_t ta = tmem + lane_base + C::kOCol + b * NH + c * 16;
-              tmem_ld16(ta, ov);
-              tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * s_alpha[c * 16 + e]);
-              tmem_st16(ta, ov);
-            }
-          }
-          tmem_wait_st();
-          named_bar_sync(1, kSoftmaxThreads);  // s_alpha is rewritten next time
-        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarPFull0 + s));

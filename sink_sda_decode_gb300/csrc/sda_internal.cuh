@@ -43,18 +43,17 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
 // Split list entry: x = token, y = first partial row, z = number of pieces.
-constexpr int kTileSlots = 64;      // slots per KV tile of the one-CTA tensor-core kernel
-constexpr int kPairTileSlots = 128; // slots per KV tile of the two-CTA (cluster) kernel
+constexpr int kTileSlots = 64;      // slots per KV tile of the tensor-core kernel
 
 // Decode variants.
-enum Variant : int { kSimt = 0, kUmma = 1, kPair = 2 };
+enum Variant : int { kSimt = 0, kUmma = 1 };
 
 struct LaunchPlan {
   Variant variant;
   int nh;        // heads per CTA
   int num_sms;   // SMs of the device
   int hg;        // head groups per token (H / nh)
-  int grid;      // persistent workers the units are spread over (CTAs, or CTA pairs)
+  int grid;      // persistent CTAs the units are spread over
   int threads;   // threads per CTA
   size_t smem;   // dynamic shared memory bytes
   int tile;      // pieces of split lists are multiples of this many slots
@@ -69,7 +68,6 @@ struct WsLayout {
 // What the plan needs to know about the device.
 struct DeviceCaps {
   int num_sms = 0;
-  int pairs[3] = {0, 0, 0};  // resident CTA pairs of the cluster kernel for nh = 16, 32, 64
 };
 
 // Picks the kernel variant and grid for (H, D) on a device.  Returns false
@@ -103,15 +101,6 @@ cudaError_t launch_decode_umma(const void* q, const void* kv, const float* kv_sc
                                cudaStream_t st);
 size_t umma_smem_bytes(int nh);
 cudaError_t umma_prepare(int nh);  // one-time kernel attribute set-up
-cudaError_t launch_decode_pair(const void* q, const void* kv, const int32_t* kv_indices,
-                               const float* attn_sink, float softmax_scale, int N, int H, int D,
-                               void* out, void* ws, const WsLayout& L, const LaunchPlan& lp,
-                               cudaStream_t st);
-size_t pair_smem_bytes(int nh);
-// One-time set-up of the cluster kernel for `nh`; *pairs receives how many
-// two-CTA clusters can be resident at once (0: the kernel cannot run, and
-// the returned error says why; the caller then uses the one-CTA kernel).
-cudaError_t pair_prepare(int nh, int* pairs);
 
 cudaError_t launch_build_indices(const int32_t* state_slot, const int32_t* swa_len,
                                  const int32_t* swa_head, const int32_t* comp_indptr,

@@ -5,7 +5,8 @@ array inside the library.
 
 Checked through the C ABI (ctypes, no Python wrapper in between): two calls
 in a row, on different workloads, each against the regular sda_decode entry
-point on the same inputs, within the parity tolerance of the other GPU tests.
+point on the same inputs and against the fp64 oracle, within the parity
+tolerance of the other GPU tests.
 This file is collected last on purpose; it passes alone in a fresh process
 and after the rest of the suite.
 """
@@ -32,13 +33,18 @@ def _noalloc(lib, w, idx, ptr, out):
                                   w.H, w.D, out.data_ptr(), stream)
 
 
-def _check_against_decode(w, out):
+def _check_against_decode(w, out, ref64=None):
     idx, ptr = parity.to_dev(w)
     ref = sda.decode(w.q, w.unified_kv, idx, ptr, w.attn_sink, w.softmax_scale)
     torch.cuda.synchronize()
     d = (out.double() - ref.double()).abs()
     assert d.max().item() <= parity.MAX_ABS and d.mean().item() <= parity.MEAN_ABS
     assert torch.all(out[torch.from_numpy(np.nonzero(w.lengths == 0)[0]).cuda()].view(torch.int16) == 0)
+    # and against the fp64 oracle on the same inputs
+    if ref64 is None:
+        ref64 = parity.run_oracle(w)
+    parity.assert_parity(parity.compare(out, ref64), "noalloc vs oracle")
+    return ref64
 
 
 def test_noalloc_two_calls_match_decode():
@@ -50,7 +56,7 @@ def test_noalloc_two_calls_match_decode():
     o1 = torch.full_like(w1.q, 9.0)
     assert _noalloc(lib, w1, i1, p1, o1) == 0
     torch.cuda.synchronize()
-    _check_against_decode(w1, o1)
+    ref1 = _check_against_decode(w1, o1)
     # call 2 right after, different shapes and lengths (empty, ragged, long)
     w2 = inputs.random_small(seed=77, N=6, H=32, D=512, P=40000,
                              lengths=[0, 1, 65, 640, 5000, 129], device="cuda")
@@ -60,7 +66,7 @@ def test_noalloc_two_calls_match_decode():
     torch.cuda.synchronize()
     _check_against_decode(w2, o2)
     # and call 1's output was not disturbed by call 2 sharing the scratch
-    _check_against_decode(w1, o1)
+    _check_against_decode(w1, o1, ref1)
 
 
 def test_noalloc_rejects_sizes_beyond_the_array():
