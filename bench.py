@@ -5,10 +5,15 @@ slots + compressed slots -> ragged kv_indices) followed by the decode
 (device-side split plan, tensor-core attention kernel, log-sum-exp combine),
 made by one sda_build_decode call and replayed as one CUDA graph.
 
-Prints ONE JSON line.  Default workload: N=64 tokens, H=16, D=512, 640 slots
-per token (128 SWA ring slots + 512 random compressed slots) over a 2^20-slot
-pool.  `--config` picks another workload (the five decode workloads, or a
-2048-token sparse-prefill chunk, prefill_h64, through the same path).
+Prints ONE JSON line.  Default workload: N=1024 tokens, H=128, D=512, 640
+slots per token (128 SWA ring slots + 512 random compressed slots) over a
+2^21-slot pool, the largest of the five decode workloads that fits one GPU.
+`--config` picks another workload (the five decode workloads, or a
+2048-token sparse-prefill chunk, prefill_h64, through the same path).  The
+default decode run also times the five decode workloads one after another
+in the same way (`per_config`: tokens/s, attention-kernel time, roofline
+fraction) and, in its CPU-baseline leg, compares a bounded token sample of
+each with the fp64 oracle (`parity_sample`).
 
   value     decode tokens/s with inputs resident in HBM (graph replays,
             CUDA events, L2 flushed between steps: a 256 MiB write, then a
@@ -61,7 +66,7 @@ METRIC = "decode tokens/s and gathered-KV GB/s; % of binding roofline (HBM vs bf
 STORE_METRIC = "q/kv RMSNorm + RoPE + SWA store tokens/s; % of HBM roofline"
 TOPK_METRIC = "top-k -> slot list tokens/s; % of HBM roofline"
 BUILDER_KEYS = ("state_slot", "swa_len", "swa_head", "comp_indptr", "comp_block", "comp_slot")
-DEFAULT_CONFIG = 1
+DEFAULT_CONFIG = 3  # h128: N=1024 H=128 D=512 L=640, the largest single-GPU workload
 L2_FLUSH_BYTES = 256 << 20
 HBM_FALLBACK_GBS = 6800.0
 BF16_FALLBACK_TFLOPS = 1900.0
@@ -533,6 +538,58 @@ def gpu_arm(args, w, device, ws, rank, pool=None):
                                                    w.k_per_block) if step.path == "topk" else None))
 
 
+def measure_decode(w, device, steps, warmup):
+    """Step and attention-kernel time (ms) of the decode step on workload w,
+    timed as in gpu_arm (graph replays after an L2 flush; the kernel alone
+    through the library's timing hook).  Returns the output of the last step
+    too, for the sampled oracle comparison."""
+    step = Step(w, device, None, "decode")
+    flush = L2Flush(device)
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(s):
+        for _ in range(max(warmup, 3)):
+            step.run(stream=s)
+    torch.cuda.synchronize(device)
+    step.check_status()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step.run(stream=s)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    torch.cuda.synchronize(device)
+    with torch.cuda.stream(s):
+        for a, b in evs:
+            flush()
+            a.record(s)
+            g.replay()
+            b.record(s)
+        for a, b in kev:
+            flush()
+            step.run(stream=s, timing=(a, b))
+    torch.cuda.synchronize(device)
+    ms_step = sum(a.elapsed_time(b) for a, b in evs) / steps
+    ms_kernel = sum(a.elapsed_time(b) for a, b in kev) / steps
+    return ms_step, ms_kernel, step.out.clone()
+
+
+def per_config_entry(w, ms_step, ms_kernel):
+    hbm, bf16, _ = peaks()
+    nbytes, flops = algorithmic_bytes(w), algorithmic_flops(w)
+    bound = "hbm" if nbytes / (hbm * 1e9) >= flops / (bf16 * 1e12) else "tensor"
+    achieved = (nbytes / 1e9 if bound == "hbm" else flops / 1e12) / (ms_kernel * 1e-3)
+    return {"workload": w.name, "N": w.N, "H": w.H, "total_slots": int(w.total_len),
+            "value": w.N / (ms_step * 1e-3), "unit": "tokens/s", "ms_per_step": ms_step,
+            "kernel_ms": ms_kernel, "bound": bound,
+            "frac": achieved / (hbm if bound == "hbm" else bf16),
+            "gathered_kv_gbs": int(w.total_len) * w.D * 2 / (ms_kernel * 1e-3) / 1e9}
+
+
+PER_CONFIGS = ("tiny", "h16", "ragged_h64", "h128", "longtail_h64")
+
+
 # ----------------------------------------------------------------------------- job-wide report
 def reduce_over_ranks(times_ms, units, ws, device):
     """Job-wide timings and units of a data-parallel run.
@@ -694,6 +751,28 @@ def oracle_budget(w, path):
     return w.N if path in ("store", "topk") or w.total_len <= 200000 else 16
 
 
+def sampled_parity(w, out, max_tokens=48):
+    """The CPU-baseline leg's check of the GPU output: a deterministic sample
+    of tokens (always the longest and the shortest list) against the fp64
+    oracle, with the tolerance of the parity tests (max |err| <= 8e-3 or one
+    bf16 ULP of the reference where that is larger, mean |err| <= 1e-3)."""
+    lens = w.lengths
+    rng = np.random.default_rng(1)
+    toks = set(rng.choice(w.N, min(w.N, max_tokens), replace=False).tolist())
+    toks |= {int(np.argmax(lens)), int(np.argmin(lens))}
+    toks = np.array(sorted(toks))
+    ref = oracle_decode(oracle_inputs(w, toks), w)
+    got = out[torch.from_numpy(toks).to(out.device)].float().cpu().numpy().astype(np.float64)
+    err = np.abs(got - ref)
+    ax = np.abs(ref)
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(ax, 2.0 ** -126))) - 7)
+    return {"tokens": int(toks.size), "elements": int(err.size),
+            "max_abs": float(err.max()) if err.size else 0.0,
+            "mean_abs": float(err.mean()) if err.size else 0.0,
+            "raw_violations": int((err > 8e-3).sum()),
+            "rounding_aware_violations": int((err > np.maximum(8e-3, ulp)).sum())}
+
+
 def time_oracle(w, seconds, max_tokens, pool=None, path="decode"):
     import oracle
     toks = oracle_sample(w, max_tokens)
@@ -727,6 +806,8 @@ def main():
                          "layer: store + build + decode; topk: top-k -> slot lists")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false",
+                    help="skip timing the five decode workloads after the main one")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     ws, rank, local = dist_env()
@@ -779,12 +860,35 @@ def main():
         return
 
     line = report_line(args, w, ws, ms_step, ms_kernel, ms_e2e, tokens_total, r)
+    outs = {}
+    if args.per_config and ws == 1 and args.path == "decode" and args.kv == "bf16":
+        # the five decode workloads, one after another, timed the same way
+        per = []
+        for name in PER_CONFIGS:
+            wc = w if name == args.config else inputs.config(inputs.CONFIG_NAMES.index(name),
+                                                             device=device)
+            ms_s, ms_k, outs[name] = measure_decode(wc, device, args.steps, args.warmup)
+            per.append(dict(config=name, **per_config_entry(wc, ms_s, ms_k)))
+            if wc is not w:
+                del wc
+                torch.cuda.empty_cache()
+        line["per_config"] = per
     if not args.no_cpu_baseline and ws == 1:
         tps, cores, toks, passes, el = time_oracle(w, args.cpu_seconds,
                                                    oracle_budget(w, args.path), pool, args.path)
         line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": f"{len(toks)} of {w.N} tokens x {passes} passes, "
                                           f"{el:.1f} s"}
+        if outs:
+            # the same leg checks each workload's GPU output on a token sample
+            for entry in line["per_config"]:
+                name = entry["config"]
+                wc = w if name == args.config else inputs.config(inputs.CONFIG_NAMES.index(name),
+                                                                 device=device)
+                entry["parity_sample"] = sampled_parity(wc, outs[name])
+                if wc is not w:
+                    del wc
+                    torch.cuda.empty_cache()
     print(json.dumps(line))
     if ws > 1:
         torch.distributed.destroy_process_group()

@@ -199,6 +199,20 @@ sda_status sda_decode_error_flag(const void* workspace, int32_t* device_flag, vo
 sda_status sda_set_timing_events(void* before, void* after);
 
 /*
+ * Test hook for the bounded pipeline waits of the tensor-core kernels (no
+ * counterpart on the pages: it exists so that the failure path can be run
+ * without faulting anything).  Every later launch of those kernels from any
+ * host thread bounds each mbarrier wait by `timeout_ns` (0 = the default of
+ * 2 s), and, when withhold_arrive is 1, the first loader warp of CTA 0 skips
+ * its arrive on the first half of its first tile, so that the QK issuer's
+ * wait runs out: the kernel raises the error word (1), every role drains its
+ * own copies and MMAs, and the call completes with unspecified outputs.
+ * withhold_arrive must be 0 or 1 (else SDA_ERR_INVALID_ARG).  Reset with
+ * (0, 0) before any normal use.
+ */
+sda_status sda_debug_wait_fault(int withhold_arrive, uint64_t timeout_ns);
+
+/*
  * Index builder (the decode index scatter the docstring calls
  * write_v4_paged_decode_indices; its inputs are not on the page, these are
  * the plainest inputs that produce its two slot formulas).  Per token t:

@@ -215,6 +215,16 @@ def decode_error_flag(workspace: torch.Tensor, stream=None) -> int:
     return int(flag.item())
 
 
+def debug_wait_fault(withhold_arrive: bool, timeout_ns: int = 0) -> None:
+    """Test hook of the tensor-core kernels' bounded waits: every later launch
+    bounds each pipeline wait by `timeout_ns` (0 = the default 2 s) and, with
+    withhold_arrive, CTA 0's first loader warp skips one arrive so that a wait
+    runs out (the error word then reads 1).  Reset with (False, 0)."""
+    lib = _lib.load()
+    _lib.check(lib.sda_debug_wait_fault(1 if withhold_arrive else 0, int(timeout_ns)),
+               "sda_debug_wait_fault")
+
+
 def set_timing_events(before: torch.cuda.Event | None, after: torch.cuda.Event | None) -> None:
     """Record `before` / `after` around the attention kernel of every later
     decode() / decode_fp8() and around the kernel of every later

@@ -41,6 +41,7 @@ SIGNATURES = {
     "sda_decode_error_flag": (_i32, [_vp, _vp, _vp]),
     "sda_decode_kernel": (_i32, [_i32, _i32, _vp]),
     "sda_set_timing_events": (_i32, [_vp, _vp]),
+    "sda_debug_wait_fault": (_i32, [_i32, ctypes.c_uint64]),
     "sda_build_indices": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i64, _i64,
                                  _vp, _i64, _vp, _vp, _vp]),
     "sda_validate_indices": (_i32, [_vp, _i64, _vp, _i32, _i64, _vp, _vp]),

@@ -19,6 +19,11 @@ namespace sda {
 namespace {
 
 thread_local char g_last_error[256] = "";
+// sda_debug_wait_fault: pipeline-wait bound (0 = the default 2 s) and the
+// withheld-arrive switch, read by every tensor-core kernel launch.
+std::atomic<unsigned long long> g_wait_timeout_ns{0};
+std::atomic<int> g_withhold_arrive{0};
+constexpr unsigned long long kDefaultWaitTimeoutNs = 2000000000ull;
 thread_local cudaEvent_t g_ev_before = nullptr;
 thread_local cudaEvent_t g_ev_after = nullptr;
 
@@ -68,6 +73,11 @@ int forced_variant() {
 }
 
 }  // namespace
+
+WaitFault current_wait_fault() {
+  const unsigned long long t = g_wait_timeout_ns.load();
+  return WaitFault{g_withhold_arrive.load(), t ? t : kDefaultWaitTimeoutNs};
+}
 
 bool shape_supported(int H, int D) {
   return (D == 64 || D == 128 || D == 256 || D == 512) && H >= 1 && H <= 256;
@@ -542,6 +552,13 @@ sda_status sda_decode_kernel(int H, int D, int* kernel) {
   choose_plan(H, D, caps, &lp);
   static_assert(SDA_KERNEL_SIMT == kSimt && SDA_KERNEL_ONE_CTA == kUmma, "public kernel codes");
   *kernel = lp.variant;
+  return SDA_OK;
+}
+
+sda_status sda_debug_wait_fault(int withhold_arrive, uint64_t timeout_ns) {
+  if (withhold_arrive != 0 && withhold_arrive != 1) return SDA_ERR_INVALID_ARG;
+  g_withhold_arrive.store(withhold_arrive);
+  g_wait_timeout_ns.store(timeout_ns);
   return SDA_OK;
 }
 

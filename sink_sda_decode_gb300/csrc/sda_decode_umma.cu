@@ -73,7 +73,6 @@ constexpr int kPrefetchTiles = 2;          // L2 prefetch distance of the loader
 static_assert(kPrefetchTiles >= 2, "the loaders read the next tile's slots one tile early");
 constexpr int kSoftmaxThreads = kSmWarps * 32;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
 enum Bar : int {
   kBarQFull = 0,
@@ -153,23 +152,31 @@ struct Params {
   float* part_o;
   float qk_scale_log2;
   int H;
+  uint64_t wait_timeout_ns;  // bound of every pipeline wait (2 s unless a test shortens it)
+  int withhold_arrive;       // test only: CTA 0's first loader warp skips one arrive
+};
+
+// Where a bounded wait reports a timeout, and after how long.
+struct WaitCtx {
+  volatile int* abort_flag;  // shared: set once any role of the CTA gave up
+  WsHeader* hdr;             // global error word (1 = a wait timed out)
+  uint64_t timeout_ns;
 };
 
 // Bounded wait.  Returns false (and raises the abort flags) on timeout; once
 // any role has aborted, every later wait returns false at once, so all roles
 // run to the end of their loops quickly and the CTA exits.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                         WsHeader* hdr) {
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtx& wc) {
   if (mbar_try_wait(bar, parity)) return true;
-  if (*abort_flag) return false;
+  if (*wc.abort_flag) return false;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-        *abort_flag = 1;
-        atomicExch(&hdr->error, 1);
+      if (*wc.abort_flag) return false;
+      if (globaltimer_ns() - t0 > wc.timeout_ns) {
+        *wc.abort_flag = 1;
+        atomicExch(&wc.hdr->error, 1);
         return false;
       }
     }
@@ -178,11 +185,11 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 
 // Wait used only while draining copies / MMAs this CTA started: bounded by
 // the timeout, but not cut short by the abort flag.
-__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, WsHeader* hdr) {
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, const WaitCtx& wc) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-      atomicExch(&hdr->error, 1);
+    if (globaltimer_ns() - t0 > wc.timeout_ns) {
+      atomicExch(&wc.hdr->error, 1);
       return;
     }
   }
@@ -293,6 +300,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
   pdl_trigger();
   const int n_units = p.hdr->n_units;
   const int H = p.H;
+  const WaitCtx wc{abort_flag, p.hdr, p.wait_timeout_ns};
 
   if (warp >= kLoaderWarp0 && warp < kLoaderWarp0 + kLoaderWarps) {
     // ===================================================== KV row loaders
@@ -381,7 +389,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           if (g >= KS) {  // the tile KS back in this stage
-            if (lane == 0) ok = wait_bar(bar(pv_done(s, hh)), ((g / KS) - 1) & 1, abort_flag, p.hdr);
+            if (lane == 0) ok = wait_bar(bar(pv_done(s, hh)), ((g / KS) - 1) & 1, wc);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
           }
@@ -426,7 +434,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         if (g >= KS) {  // the tile KS back in this stage
-          if (lane == 0) ok = wait_bar(bar(pv_done(s, hh)), ((g / KS) - 1) & 1, abort_flag, p.hdr);
+          if (lane == 0) ok = wait_bar(bar(pv_done(s, hh)), ((g / KS) - 1) & 1, wc);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
         }
@@ -449,7 +457,10 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         cp_async_wait_group<1>();  // first half landed
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kv_full(s, 0)));
+        // (a test can make CTA 0's first loader warp withhold this arrive
+        // once, so that the QK issuer's bounded wait runs out)
+        const bool withhold = p.withhold_arrive && blockIdx.x == 0 && lw == 0 && g == 0;
+        if (lane == 0 && !withhold) mbar_arrive(bar(kv_full(s, 0)));
       }
       cp_async_wait_group<0>();
       if (issued == 2) {
@@ -501,9 +512,9 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
       while (cq.valid && ok) {
         const int g = cq.g, s = g & 1, ks = g % KS;  // S / P buffer, KV stage
         if (qk_role) {
-          if (g >= 2) ok = wait_bar(bar(kBarSEmpty0 + s), ((g >> 1) - 1) & 1, abort_flag, p.hdr);
-          if (ok && cq.i == 0) ok = wait_bar(bar(kBarQFull), cq.nu & 1, abort_flag, p.hdr);
-          if (ok) ok = wait_bar(bar(kv_full(ks, qh)), (g / KS) & 1, abort_flag, p.hdr);
+          if (g >= 2) ok = wait_bar(bar(kBarSEmpty0 + s), ((g >> 1) - 1) & 1, wc);
+          if (ok && cq.i == 0) ok = wait_bar(bar(kBarQFull), cq.nu & 1, wc);
+          if (ok) ok = wait_bar(bar(kv_full(ks, qh)), (g / KS) & 1, wc);
           if (!ok) break;
           tc_fence_after();
           const uint32_t kvs = sKV + ks * kKVBytes;
@@ -526,7 +537,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
           cq.next();
           if (qh == 0 && last && cq.valid) {
             // q of the next unit once this unit's QKs (both halves) have read q
-            ok = wait_bar(bar(kBarQEmpty), nu & 1, abort_flag, p.hdr);
+            ok = wait_bar(bar(kBarQEmpty), nu & 1, wc);
             if (!ok) break;
             mbar_arrive_expect_tx(bar(kBarQFull), NH * 128 * kPanels);
             const int qrow = cq.u.x * H + unit_head_group(cq.u.w) * NH;
@@ -536,8 +547,8 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
           }
         } else {
           const bool first = cq.i == 0;
-          ok = wait_bar(bar(kBarPFull0 + s), (g >> 1) & 1, abort_flag, p.hdr);
-          if (ok && first && cq.nu >= 1) ok = wait_bar(bar(kBarOEmpty), (cq.nu - 1) & 1, abort_flag, p.hdr);
+          ok = wait_bar(bar(kBarPFull0 + s), (g >> 1) & 1, wc);
+          if (ok && first && cq.nu >= 1) ok = wait_bar(bar(kBarOEmpty), (cq.nu - 1) & 1, wc);
           if (!ok) break;
           tc_fence_after();
           const uint32_t kvs = sKV + ks * kKVBytes;
@@ -562,8 +573,8 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
       // drain this thread's MMAs (and the last q copy) before TMEM and smem go away
       const int drain = qk_role ? (qh ? kBarDrainQb : kBarDrain) : kBarDrainPv;
       mma_commit(bar(drain));
-      drain_bar(bar(drain), 0, p.hdr);
-      if (qk_role && qh == 0 && q_issued >= 1) drain_bar(bar(kBarQFull), (q_issued - 1) & 1, p.hdr);
+      drain_bar(bar(drain), 0, wc);
+      if (qk_role && qh == 0 && q_issued >= 1) drain_bar(bar(kBarQFull), (q_issued - 1) & 1, wc);
     }
     __syncwarp();
   } else if (warp < kSmWarps) {
@@ -615,7 +626,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
       for (int i = 0; i < ntiles; ++i, ++g) {
         const int s = g & 1;
         const int n = min(kTileN, len - i * kTileN);
-        wait_bar(bar(kBarSFull0 + s), (g >> 1) & 1, abort_flag, p.hdr);
+        wait_bar(bar(kBarSFull0 + s), (g >> 1) & 1, wc);
         tc_fence_after();
         float x[16];  // raw scores of this thread's 16 (head, slot) pairs: S_a + S_b
         {
@@ -643,7 +654,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         }
         // P buffer s is free once the PV of tile g-2 is done
         if (g >= 2) {
-          if (lane == 0) wait_bar(bar(pv_done((g - 2) % KS, 1)), ((g - 2) / KS) & 1, abort_flag, p.hdr);
+          if (lane == 0) wait_bar(bar(pv_done((g - 2) % KS, 1)), ((g - 2) / KS) & 1, wc);
           __syncwarp();
         }
         // p = 2^(x*scale - m) in bf16 into rows hA, hB of P (K-major, 128-byte
@@ -728,7 +739,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
             }
             named_bar_sync(1, kSoftmaxThreads);
             // O^T must be quiescent: wait for the PV of tile g-1
-            if (lane == 0) wait_bar(bar(pv_done((g - 1) % KS, 1)), ((g - 1) / KS) & 1, abort_flag, p.hdr);
+            if (lane == 0) wait_bar(bar(pv_done((g - 1) % KS, 1)), ((g - 1) / KS) & 1, wc);
             __syncwarp();
             tc_fence_after();
             // this warp's lanes of O^T blocks 2hc, 2hc + 1
@@ -767,7 +778,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         s_lsum[hc * 64 + hB] = lB;
       }
       const int gl = g - 1;
-      if (lane == 0) wait_bar(bar(pv_done(gl % KS, 1)), (gl / KS) & 1, abort_flag, p.hdr);
+      if (lane == 0) wait_bar(bar(pv_done(gl % KS, 1)), (gl / KS) & 1, wc);
       __syncwarp();
       tc_fence_after();
       named_bar_sync(1, kSoftmaxThreads);
@@ -947,6 +958,9 @@ cudaError_t launch_nh(const void* q, const void* kv, const float* kv_scale, int6
   p.part_o = reinterpret_cast<float*>(base + L.o_off);
   p.qk_scale_log2 = scale * kLog2e;
   p.H = H;
+  const WaitFault wf = current_wait_fault();
+  p.wait_timeout_ns = wf.timeout_ns;
+  p.withhold_arrive = wf.withhold;
   return launch_pdl(decode_umma_kernel<NH, FP8>, dim3(lp.grid), dim3(kThreads), (size_t)Cfg<NH>::kSmem,
                     st, tq, tout, p);
 }

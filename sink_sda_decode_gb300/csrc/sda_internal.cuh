@@ -100,6 +100,13 @@ cudaError_t launch_decode_umma(const void* q, const void* kv, const float* kv_sc
                                void* out, void* ws, const WsLayout& L, const LaunchPlan& lp,
                                cudaStream_t st);
 size_t umma_smem_bytes(int nh);
+// Bound of the tensor-core kernel's pipeline waits, and whether CTA 0's
+// first loader warp withholds one arrive (sda_debug_wait_fault; tests only).
+struct WaitFault {
+  int withhold;
+  uint64_t timeout_ns;
+};
+WaitFault current_wait_fault();
 cudaError_t umma_prepare(int nh);  // one-time kernel attribute set-up
 
 cudaError_t launch_build_indices(const int32_t* state_slot, const int32_t* swa_len,
