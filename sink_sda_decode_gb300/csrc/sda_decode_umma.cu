@@ -114,7 +114,7 @@ struct Cfg {
   // written into the other
   static constexpr int kOffStage2 = kOffP + kStages * kPBytes;
   static constexpr int kOffBar = kOffStage2 + NH * 256;
-  static constexpr int kOffMisc = kOffBar + 192;  // kNumBars <= 24
+  static constexpr int kOffMisc = kOffBar + 256;  // kNumBars <= 32
   // misc: tmem base (4), abort flag (4), pad, then per-head float arrays:
   // l-sum [2 halves][64]; alpha aliases its first half (used only inside a
   // unit's tiles) and fac its second (each thread reads its head's l-sums
@@ -430,6 +430,9 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
       const int spf = hpf ? tile_slot() : -1;
       if (hpf) c.next();
       const uint32_t stage = sKV + s * kKVBytes;
+      int slot_r[kRowsPerLoader];  // slots of this warp's 8 rows (-1: past the tile's end)
+#pragma unroll
+      for (int r = 0; r < kRowsPerLoader; ++r) slot_r[r] = __shfl_sync(0xffffffffu, sl[0], r);
       int issued = 0;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -446,7 +449,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         static_assert(kRowsPerLoader == 8, "one swizzle atom per loader warp");
 #pragma unroll
         for (int r = 0; r < kRowsPerLoader; ++r) {
-          const int slot = __shfl_sync(0xffffffffu, sl[0], r);
+          const int slot = slot_r[r];
           const uint4* src = slot >= 0 ? kv4 + (size_t)slot * (kD / 8) + q : kv4;
           cp_async16(atom + r * 128 + ((k ^ r) << 4), src, slot >= 0 ? 16u : 0u);
         }
@@ -658,19 +661,23 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
           __syncwarp();
         }
         // p = 2^(x*scale - m) in bf16 into rows hA, hB of P (K-major, 128-byte
-        // swizzle: 16-byte chunk c of 8 slots at (c ^ (h & 7)) * 16, this
-        // thread's slot pair at byte 4*tq of the chunk); returns whether a
-        // weight exceeded the headroom.  The denominator sums the same bf16
-        // weights the PV MMA multiplies, so rounding p perturbs the weights
-        // of an exact weighted average but biases nothing.
-        uint8_t* pbase = smem + C::kOffP + s * C::kPBytes;
-        uint8_t* prowA = pbase + (hA >> 3) * 1024 + (hA & 7) * 128 + 4 * tq;
-        uint8_t* prowB = pbase + (hB >> 3) * 1024 + (hB & 7) * 128 + 4 * tq;
+        // swizzle: 16-byte chunk c of 8 slots at (c ^ (h & 7)) * 16).  The
+        // 16x256b load left this thread's weights in the layout of stmatrix
+        // fragments (row = head t/4 of an 8-head group, columns = slot pair
+        // 2(t%4) of an 8-slot chunk), so each warp stores its 16 heads x 32
+        // slots with two stmatrix.x4 (matrix i = chunk 4hc + i; lane 8i + j
+        // addresses head row j).  Returns whether a weight exceeded the
+        // headroom.  The denominator sums the same bf16 weights the PV MMA
+        // multiplies, so rounding p perturbs the weights of an exact weighted
+        // average but biases nothing.
+        const uint32_t prow = sP + s * C::kPBytes + (2 * q4) * 1024 + (lane & 7) * 128 +
+                              ((((4 * hc) + (lane >> 3)) ^ (lane & 7)) << 4);
         float sA, sB;
         auto weights = [&]() {
           bool over = false;
           sA = 0.f;
           sB = 0.f;
+          uint32_t pa[4], pb[4];
 #pragma unroll
           for (int rep = 0; rep < 4; ++rep) {
             float e[4];
@@ -681,13 +688,16 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
               over = over || (ok_e && arg > kRescaleThreshold);
               e[kk] = ok_e ? ex2_approx(arg) : 0.f;
             }
-            __nv_bfloat162 pa = __floats2bfloat162_rn(e[0], e[1]), pb = __floats2bfloat162_rn(e[2], e[3]);
-            const float2 fa = __bfloat1622float2(pa), fb = __bfloat1622float2(pb);
+            __nv_bfloat162 va = __floats2bfloat162_rn(e[0], e[1]), vb = __floats2bfloat162_rn(e[2], e[3]);
+            const float2 fa = __bfloat1622float2(va), fb = __bfloat1622float2(vb);
             sA += fa.x + fa.y;
             sB += fb.x + fb.y;
-            const int c = 4 * hc + rep;  // chunk of 8 slots within the tile
-            if (vA) *reinterpret_cast<uint32_t*>(prowA + ((c ^ (hA & 7)) << 4)) = *reinterpret_cast<uint32_t*>(&pa);
-            if (vB) *reinterpret_cast<uint32_t*>(prowB + ((c ^ (hB & 7)) << 4)) = *reinterpret_cast<uint32_t*>(&pb);
+            pa[rep] = *reinterpret_cast<uint32_t*>(&va);
+            pb[rep] = *reinterpret_cast<uint32_t*>(&vb);
+          }
+          if (vA) {  // warp-uniform (vA == vB)
+            stmatrix_x4(prow, pa[0], pa[1], pa[2], pa[3]);
+            stmatrix_x4(prow + 1024, pb[0], pb[1], pb[2], pb[3]);
           }
           return over;
         };

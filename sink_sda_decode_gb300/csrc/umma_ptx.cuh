@@ -225,6 +225,15 @@ __device__ __forceinline__ void stmatrix_x4_trans(uint32_t addr, uint32_t r0, ui
                "r"(r0), "r"(r1), "r"(r2), "r"(r3)
                : "memory");
 }
+// Four 8x8 b16 matrices stored as they are held (stmatrix, no transpose):
+// this thread's 32-bit register i holds row t/4, columns 2*(t%4), +1 of
+// matrix i; thread 8i + j gives the shared address of row j of matrix i.
+__device__ __forceinline__ void stmatrix_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                            uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
