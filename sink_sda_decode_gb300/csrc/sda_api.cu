@@ -100,7 +100,7 @@ bool choose_plan(int H, int D, const DeviceCaps& caps, LaunchPlan* lp) {
     lp->nh = nh;
     lp->hg = H / lp->nh;
     lp->grid = caps.num_sms;  // one CTA per SM (about 200 KB of shared memory each)
-    lp->threads = 640;
+    lp->threads = 896;
     lp->smem = umma_smem_bytes(lp->nh);
     lp->tile = kTileSlots;
     lp->min_chunk = kTileSlots;
@@ -231,7 +231,7 @@ static bool fp8_plan(int H, int D, const DeviceCaps& caps, LaunchPlan* lp) {
     lp->nh = H < 64 ? H : 64;
     lp->hg = H / lp->nh;
     lp->grid = caps.num_sms;
-    lp->threads = 640;
+    lp->threads = 896;
     lp->smem = umma_smem_bytes(lp->nh);
     lp->tile = kTileSlots;
     lp->min_chunk = kTileSlots;

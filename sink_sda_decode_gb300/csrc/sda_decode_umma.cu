@@ -60,17 +60,28 @@ constexpr int kPanelKV = kTileN * 128;     // bytes of one KV panel
 constexpr int kKVBytes = kPanels * kPanelKV;   // 64 KB per stage
 constexpr int kMaxStages = 3;
 constexpr int kSmWarps = 8;                // warps 0..7: softmax / epilogue (warps q, q+4 share TMEM quadrant q)
-constexpr int kLoaderWarp0 = 8;            // warps 8..15: KV row loaders
-constexpr int kLoaderWarps = 8;
-constexpr int kMmaWarp = 16;               // warp 16: QK issuer (first half of D) + q loads
-constexpr int kPvWarp = 17;                // warp 17: PV issuer
-constexpr int kMmaWarpB = 18;              // warp 18: QK issuer (second half of D)
-// 20 warps (19 idle): warps are spread over the SM's four sub-partitions,
-// each with 16 K registers, so 18 or 20 warps (5 on some) allow 96 registers
-constexpr int kThreads = 640;
+constexpr int kLoaderWarp0 = 8;            // warps 8..23: KV row loaders, two groups of 8
+constexpr int kLoaderWarps = 8;            // warps per loader group (group g loads tiles of parity g)
+constexpr int kLoaderGroups = 2;
+constexpr int kMmaWarp = 24;               // warp 24: QK issuer (first half of D) + q loads
+constexpr int kPvWarp = 25;                // warp 25: PV issuer
+constexpr int kMmaWarpB = 26;              // warp 26: QK issuer (second half of D)
+// 28 warps (27 idle) = 7 warpgroups; registers are split by setmaxnreg:
+// softmax warpgroups 0-1 grow to kSmRegs, loader warpgroups 2-5 and the MMA
+// warpgroup 6 shrink.  The split must fit the launch allocation of
+// kThreads x kLaunchRegs (checked on the host before the first launch).
+constexpr int kThreads = 896;
+constexpr int kLaunchRegs = 72;            // 65536 / 896, rounded down to a multiple of 8
+template <bool FP8>
+struct RegSplit {  // the FP8 loaders dequantise in registers, so they get more
+  static constexpr int kSm = 96;
+  static constexpr int kLoader = FP8 ? 64 : 56;
+  static constexpr int kMma = FP8 ? 56 : 72;
+  static_assert(kSmWarps * 32 * kSm + kLoaderGroups * kLoaderWarps * 32 * kLoader + 4 * 32 * kMma <=
+                    kThreads * kLaunchRegs,
+                "register split exceeds the launch allocation");
+};
 constexpr int kRowsPerLoader = kTileSlots / kLoaderWarps;  // 8 rows of a tile per loader warp
-constexpr int kPrefetchTiles = 2;          // L2 prefetch distance of the loaders, in tiles
-static_assert(kPrefetchTiles >= 2, "the loaders read the next tile's slots one tile early");
 constexpr int kSoftmaxThreads = kSmWarps * 32;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -269,7 +280,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
     mbar_init(bar(kBarQFull), 1);
     mbar_init(bar(kBarQEmpty), 2);  // both QK issuers' commits
     for (int i = 0; i < 2 * C::kStages; ++i) {
-      mbar_init(bar(kBarKVFull0 + i), kLoaderWarps);
+      mbar_init(bar(kBarKVFull0 + i), FP8 ? kLoaderWarps : kLoaderGroups * kLoaderWarps);
       mbar_init(bar(kBarPVDone0 + i), 1);
     }
     mbar_init(bar(kBarSFull0), 2);  // S_a and S_b
@@ -302,19 +313,19 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
   const int H = p.H;
   const WaitCtx wc{abort_flag, p.hdr, p.wait_timeout_ns};
 
-  if (warp >= kLoaderWarp0 && warp < kLoaderWarp0 + kLoaderWarps) {
+  if (warp >= kLoaderWarp0 && warp < kLoaderWarp0 + kLoaderGroups * kLoaderWarps) {
     // ===================================================== KV row loaders
-    // Loader warp w owns rows [8w, 8w+8) of every 64-slot tile.  Each row
-    // (1 KB) is read by the whole warp as two contiguous 512-byte loads, so a
-    // thread keeps 16 x 16 B in flight and an SM 64 KB; the loads of a tile
-    // are issued before the warp waits for the tile's shared-memory stage,
-    // then stored into the 128-byte-swizzled K-major layout the MMAs read.
-    // The rows of the tile kPrefetchTiles ahead are brought into L2 with one
-    // bulk prefetch per row, so that their loads wait on L2, not on DRAM.
-    const int lw = warp - kLoaderWarp0;
+    // Two groups of 8 loader warps; warp w of a group owns rows [8w, 8w+8)
+    // of the group's 64-slot tiles (bf16 pool: group 0 the even tiles,
+    // group 1 the odd ones, so that one group waits for its rows to land
+    // while the other issues; FP8 pool: group 0 all tiles).  The rows of a
+    // later tile are brought into L2 with one bulk prefetch per row, so that
+    // their loads wait on L2, not on DRAM.
+    setmaxnreg_dec<RegSplit<FP8>::kLoader>();
+    const int grp = (warp - kLoaderWarp0) / kLoaderWarps;
+    const int lw = (warp - kLoaderWarp0) % kLoaderWarps;
     const uint4* kv4 = reinterpret_cast<const uint4*>(p.kv);
-    TileCursor c;  // the next tile whose slots are read
-    c.init(p.units, n_units);
+    TileCursor c{};  // the next tile whose slots are read
     auto tile_slot = [&]() {  // lanes 0..7: slot of row 8w + lane of tile c, else -1
       const int n = min(kTileN, c.len() - c.i * kTileN);
       const int r = lw * kRowsPerLoader + lane;
@@ -327,112 +338,108 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         if constexpr (FP8) bulk_prefetch_l2(p.kv_scale + (slot_of_lane & ~3), 16);  // the row's scale
       }
     };
-    constexpr int PF = kPrefetchTiles;
-    int sl[PF];    // slots of tiles g .. g + PF - 1
-    bool hv[PF];   // whether those tiles exist
-#pragma unroll
-    for (int j = 0; j < PF; ++j) {
-      hv[j] = c.valid;
-      sl[j] = c.valid ? tile_slot() : -1;
-      if (c.valid) c.next();
-    }
     bool ok = true;
+    TileCursor t;  // this group's current tile (the groups take every other tile)
+    t.init(p.units, n_units);
+    if (grp == 1 && t.valid) t.next();
+    c = t;  // c: this group's next tile (slots read one tile early)
+    auto skip2 = [&](TileCursor& x) {
+      if (x.valid) x.next();
+      if (x.valid) x.next();
+    };
     if constexpr (FP8) {
       // E4M3 pool: each row is 512 bytes of codes; lane l reads bytes
       // [8l, 8l+8) of each half (one 8-byte load per row and half, 256 bytes
-      // per warp instruction), lanes 0..7 also read the row's scale; the
-      // codes are dequantised (code * scale, rounded to bf16) into the same
-      // swizzled bf16 tile as the bf16 pool's rows.
+      // per warp instruction), lanes 0..7 also read their row's scale one tile
+      // early; the codes are dequantised (code * scale, rounded to bf16) into
+      // the same swizzled bf16 tile as the bf16 pool's rows, half by half.
       const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
-      // lanes 0..7: scale of their row of the current tile, read one tile early
-      float scl = (lane < kRowsPerLoader && hv[0] && sl[0] >= 0) ? __ldg(p.kv_scale + sl[0]) : 0.f;
-      for (int g = 0; hv[0] && ok; ++g) {
+      bool hv0 = t.valid;
+      int sl0 = hv0 ? tile_slot() : -1;
+      float scl0 = (lane < kRowsPerLoader && sl0 >= 0) ? __ldg(p.kv_scale + sl0) : 0.f;
+      skip2(c);
+      for (int g = grp; hv0 && ok; g += 2) {
         const int s = g % KS;  // KV stage
-        uint2 w[2 * kRowsPerLoader];
+        const bool hv1 = c.valid;
+        const int sl1 = hv1 ? tile_slot() : -1;
+        skip2(c);
+        int slot_r[kRowsPerLoader];
+        float sc_r[kRowsPerLoader];
 #pragma unroll
         for (int r = 0; r < kRowsPerLoader; ++r) {
-          const int slot = __shfl_sync(0xffffffffu, sl[0], r);
-          if (slot >= 0) {
-            const uint2* src = reinterpret_cast<const uint2*>(kv8 + (size_t)slot * kD);
-            w[2 * r] = __ldcg(src + lane);
-            w[2 * r + 1] = __ldcg(src + 32 + lane);
-          } else {  // tail row of a partial tile: zeros (its p is forced to 0)
-            w[2 * r] = make_uint2(0, 0);
-            w[2 * r + 1] = make_uint2(0, 0);
-          }
-        }
-        const float scl_next =
-            (lane < kRowsPerLoader && hv[1] && sl[1] >= 0) ? __ldg(p.kv_scale + sl[1]) : 0.f;
-        if (g == 0) {
-#pragma unroll
-          for (int j = 1; j < PF; ++j) prefetch_rows(sl[j]);
-        }
-        const bool hpf = c.valid;  // tile g + PF
-        const int spf = hpf ? tile_slot() : -1;
-        if (hpf) c.next();
-        // dequantise both halves now, while the stage may still be busy, so
-        // that the conversion stays off the path from "stage free" to "stored"
-        uint4 v[2 * kRowsPerLoader];
-#pragma unroll
-        for (int r = 0; r < kRowsPerLoader; ++r) {
-          const float sr = __shfl_sync(0xffffffffu, scl, r);
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const uint2 c8 = w[2 * r + hh];
-            v[2 * r + hh] = make_uint4(e4m3x2_to_bf16x2_scaled(c8.x & 0xffffu, sr),
-                                       e4m3x2_to_bf16x2_scaled(c8.x >> 16, sr),
-                                       e4m3x2_to_bf16x2_scaled(c8.y & 0xffffu, sr),
-                                       e4m3x2_to_bf16x2_scaled(c8.y >> 16, sr));
-          }
+          slot_r[r] = __shfl_sync(0xffffffffu, sl0, r);
+          sc_r[r] = __shfl_sync(0xffffffffu, scl0, r);
         }
         uint8_t* stage = smem + C::kOffKV + s * kKVBytes;
-#pragma unroll
+#pragma unroll 1
         for (int hh = 0; hh < 2; ++hh) {
+          uint2 w[kRowsPerLoader];
+#pragma unroll
+          for (int r = 0; r < kRowsPerLoader; ++r) {
+            // a tail row of a partial tile is zeros (its p is forced to 0)
+            w[r] = slot_r[r] >= 0
+                       ? __ldcg(reinterpret_cast<const uint2*>(kv8 + (size_t)slot_r[r] * kD) + 32 * hh + lane)
+                       : make_uint2(0, 0);
+          }
           if (g >= KS) {  // the tile KS back in this stage
             if (lane == 0) ok = wait_bar(bar(pv_done(s, hh)), ((g / KS) - 1) & 1, wc);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
           }
-          // 16-byte chunk q = 32*hh + lane (8 bf16) of each row: panel q/8, chunk q%8
+          // 16-byte chunk q = 32*hh + lane of each row: panel q/8, chunk q%8
           const int q = hh * 32 + lane, k = q & 7;
           uint8_t* atom = stage + (q >> 3) * kPanelKV + lw * 1024;
 #pragma unroll
-          for (int r = 0; r < kRowsPerLoader; ++r)
-            *reinterpret_cast<uint4*>(atom + r * 128 + ((k ^ r) << 4)) = v[2 * r + hh];
+          for (int r = 0; r < kRowsPerLoader; ++r) {
+            const uint2 c8 = w[r];
+            const float sr = sc_r[r];
+            *reinterpret_cast<uint4*>(atom + r * 128 + ((k ^ r) << 4)) =
+                make_uint4(e4m3x2_to_bf16x2_scaled(c8.x & 0xffffu, sr),
+                           e4m3x2_to_bf16x2_scaled(c8.x >> 16, sr),
+                           e4m3x2_to_bf16x2_scaled(c8.y & 0xffffu, sr),
+                           e4m3x2_to_bf16x2_scaled(c8.y >> 16, sr));
+          }
           fence_proxy_async_smem();  // generic-proxy stores -> read by the tensor cores
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kv_full(s, hh)));
         }
-        prefetch_rows(spf);
-        scl = scl_next;
-#pragma unroll
-        for (int j = 0; j + 1 < PF; ++j) {
-          sl[j] = sl[j + 1];
-          hv[j] = hv[j + 1];
-        }
-        sl[PF - 1] = spf;
-        hv[PF - 1] = hpf;
+        // the next tile's scales (lanes 0..7) and rows (into L2)
+        scl0 = (lane < kRowsPerLoader && sl1 >= 0) ? __ldg(p.kv_scale + sl1) : 0.f;
+        prefetch_rows(sl1);
+        sl0 = sl1;
+        hv0 = hv1;
       }
     } else {
-    // bf16 pool: rows go straight from global to shared memory with 16-byte
-    // cp.async (no register round trip, no separate shared stores).  Each
-    // half of D of the warp's 8 rows is one commit group, issued as soon as
-    // the PV MMAs that last read that half of the stage are done; the warp
-    // then waits for its own copies, fences them to the async proxy (the
-    // tensor cores read the stage through it) and arrives, half by half.
-    for (int g = 0; hv[0] && ok; ++g) {
+    // bf16 pool: all 16 loader warps share every tile, warp v (0..15) rows
+    // [4v, 4v+4).  Rows go straight from global to shared memory with
+    // 16-byte cp.async (no register round trip, no separate shared stores).
+    // Each half of D of the warp's rows is one commit group, issued as soon
+    // as the PV MMAs that last read that half of the stage are done; the
+    // warp then waits for its own copies, fences them to the async proxy
+    // (the tensor cores read the stage through it) and arrives, half by half.
+    constexpr int kRows = kTileN / (kLoaderGroups * kLoaderWarps);  // 4 rows per warp
+    const int v = warp - kLoaderWarp0;
+    auto slot_of = [&](const TileCursor& x) {  // lanes 0..3: slot of row 4v + lane of tile x, else -1
+      const int n = min(kTileN, x.len() - x.i * kTileN);
+      const int r = v * kRows + lane;
+      return (lane < kRows && r < n) ? __ldg(p.kv_indices + x.u.y + x.i * kTileN + r) : -1;
+    };
+    TileCursor cu;  // the current tile
+    cu.init(p.units, n_units);
+    TileCursor nx = cu;  // the next tile
+    if (nx.valid) nx.next();
+    TileCursor n2 = nx;  // the one after: its slots are read a tile early, its rows prefetched
+    if (n2.valid) n2.next();
+    int sl0 = cu.valid ? slot_of(cu) : -1;
+    int sl1 = nx.valid ? slot_of(nx) : -1;
+    if (sl1 >= 0) prefetch_rows(sl1);
+    for (int g = 0; cu.valid && ok; ++g) {
       const int s = g % KS;  // KV stage
-      if (g == 0) {
-#pragma unroll
-        for (int j = 1; j < PF; ++j) prefetch_rows(sl[j]);
-      }
-      const bool hpf = c.valid;  // tile g + PF: its slot indices are read now
-      const int spf = hpf ? tile_slot() : -1;
-      if (hpf) c.next();
+      const int sl2 = n2.valid ? slot_of(n2) : -1;
       const uint32_t stage = sKV + s * kKVBytes;
-      int slot_r[kRowsPerLoader];  // slots of this warp's 8 rows (-1: past the tile's end)
+      int slot_r[kRows];  // slots of this warp's rows (-1: past the tile's end)
 #pragma unroll
-      for (int r = 0; r < kRowsPerLoader; ++r) slot_r[r] = __shfl_sync(0xffffffffu, sl[0], r);
+      for (int r = 0; r < kRows; ++r) slot_r[r] = __shfl_sync(0xffffffffu, sl0, r);
       int issued = 0;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -442,16 +449,16 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
           if (!ok) break;
         }
         // 16-byte chunk q = 32*hh + lane of each row: panel q/8, chunk q%8;
-        // the warp's 8 rows are one 8-row swizzle atom of every panel.  A
-        // tail row of a partial tile is zero-filled (its p is forced to 0).
+        // row 4v + r sits at row (4v + r) % 8 of 8-row swizzle atom (4v + r) / 8
+        // of every panel.  A tail row of a partial tile is zero-filled (its p
+        // is forced to 0).
         const int q = hh * 32 + lane, k = q & 7;
-        const uint32_t atom = stage + (q >> 3) * kPanelKV + lw * 1024;
-        static_assert(kRowsPerLoader == 8, "one swizzle atom per loader warp");
+        const uint32_t atom = stage + (q >> 3) * kPanelKV + (v >> 1) * 1024;
 #pragma unroll
-        for (int r = 0; r < kRowsPerLoader; ++r) {
-          const int slot = slot_r[r];
+        for (int r = 0; r < kRows; ++r) {
+          const int slot = slot_r[r], r8 = 4 * (v & 1) + r;
           const uint4* src = slot >= 0 ? kv4 + (size_t)slot * (kD / 8) + q : kv4;
-          cp_async16(atom + r * 128 + ((k ^ r) << 4), src, slot >= 0 ? 16u : 0u);
+          cp_async16(atom + r8 * 128 + ((k ^ r8) << 4), src, slot >= 0 ? 16u : 0u);
         }
         cp_async_commit();
         ++issued;
@@ -462,7 +469,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         __syncwarp();
         // (a test can make CTA 0's first loader warp withhold this arrive
         // once, so that the QK issuer's bounded wait runs out)
-        const bool withhold = p.withhold_arrive && blockIdx.x == 0 && lw == 0 && g == 0;
+        const bool withhold = p.withhold_arrive && blockIdx.x == 0 && v == 0 && g == 0;
         if (lane == 0 && !withhold) mbar_arrive(bar(kv_full(s, 0)));
       }
       cp_async_wait_group<0>();
@@ -471,17 +478,17 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kv_full(s, 1)));
       }
-      prefetch_rows(spf);
-#pragma unroll
-      for (int j = 0; j + 1 < PF; ++j) {
-        sl[j] = sl[j + 1];
-        hv[j] = hv[j + 1];
-      }
-      sl[PF - 1] = spf;
-      hv[PF - 1] = hpf;
+      prefetch_rows(sl2);  // rows of tile g + 2 into L2
+      cu = nx;
+      nx = n2;
+      if (n2.valid) n2.next();
+      sl0 = sl1;
+      sl1 = sl2;
     }
     }
-  } else if (warp == kMmaWarp || warp == kPvWarp || warp == kMmaWarpB) {
+  } else if (warp >= kMmaWarp) {
+    if constexpr (RegSplit<FP8>::kMma < kLaunchRegs) setmaxnreg_dec<RegSplit<FP8>::kMma>();  // the whole warpgroup (warp 27 idles)
+    if (warp == kMmaWarp || warp == kPvWarp || warp == kMmaWarpB) {
     // ===================================================== MMA issuers
     // Three threads issue tcgen05 MMAs; one thread's MMAs run one after the
     // other, but MMAs of different threads overlap in the tensor pipe, so
@@ -580,7 +587,9 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
       if (qk_role && qh == 0 && q_issued >= 1) drain_bar(bar(kBarQFull), (q_issued - 1) & 1, wc);
     }
     __syncwarp();
+    }
   } else if (warp < kSmWarps) {
+    setmaxnreg_inc<RegSplit<FP8>::kSm>();
     // ===================================================== softmax + epilogue
     // Warp w reads TMEM lane quadrant q = w % 4 and slots [32hc, 32hc + 32) of
     // each tile, hc = w / 4, with the 16x256b shape: thread t holds heads
@@ -986,13 +995,26 @@ size_t umma_smem_bytes(int nh) {
   }
 }
 
+// The warp roles resize their registers with setmaxnreg, and an increase
+// waits until the others have released enough of the CTA's launch
+// allocation: never launch a build whose allocation is smaller than the split
+// assumes (the increase would wait forever).
+template <int NH, bool FP8>
+cudaError_t prepare_variant() {
+  cudaError_t e = cudaFuncSetAttribute(decode_umma_kernel<NH, FP8>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<NH>::kSmem);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes a;
+  e = cudaFuncGetAttributes(&a, decode_umma_kernel<NH, FP8>);
+  if (e != cudaSuccess) return e;
+  if (a.numRegs < kLaunchRegs || a.maxThreadsPerBlock < kThreads) return cudaErrorInvalidConfiguration;
+  return cudaSuccess;
+}
+
 template <int NH>
 cudaError_t prepare_nh() {
-  cudaError_t e = cudaFuncSetAttribute(decode_umma_kernel<NH, false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<NH>::kSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_umma_kernel<NH, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<NH>::kSmem);
+  cudaError_t e = prepare_variant<NH, false>();
+  if (e == cudaSuccess) e = prepare_variant<NH, true>();
   return e;
 }
 
