@@ -280,9 +280,16 @@ sda_status sda_build_decode(const int32_t* state_slot, const int32_t* swa_len,
  * live in the workspace) and writes out and status back to the host with
  * another kernel -- no copy-engine transfer, so the whole step is one
  * sequence of kernels on `stream` (graph-capturable).  Asynchronous: the host
- * buffers must stay valid, and out/status are ready once the stream reaches
- * this point.  SDA_ERR_INVALID_ARG if a host buffer is not page-locked or is
- * misaligned.
+ * buffers must stay valid (and keep their page-locking) until the stream has
+ * passed this call, and out/status are ready once the stream reaches this
+ * point.  SDA_ERR_INVALID_ARG if a host buffer is not page-locked or is
+ * misaligned, or on any argument sda_build_decode would reject; those checks
+ * all run before anything is enqueued.  Only the start of each host buffer
+ * can be checked: the library cannot learn the size of a page-locked
+ * allocation, so a host buffer shorter than its stated extent (N*H*D*2 bytes
+ * for q and out, 4*N for the per-token descriptors, 4*(N+1) for comp_indptr,
+ * 4*comp_total for comp_block / comp_slot) is undefined behaviour: the
+ * kernels would read or write past it.
  */
 sda_status sda_build_decode_host_workspace_size(int N, int H, int D, int64_t comp_total,
                                                 int64_t capacity, int fp8, size_t* bytes);

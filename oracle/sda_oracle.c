@@ -26,7 +26,7 @@
  *     written below (2^(x*log2 e) = e^x), so the oracle uses the plain
  *     definition with libm exp() in double precision.
  *
- * Readings where the page is silent (each also listed in the design notes):
+ * Readings where the page is silent:
  *   - the sink is a natural-log logit that is NOT multiplied by softmax_scale;
  *     its value vector is zero (a "virtual key" that only adds e^sink to the
  *     denominator);
@@ -323,7 +323,7 @@ int oracle_validate_indices(const int32_t* kv_indices, int64_t total_indices,
  * slot of an entry is state_slot * win + ring (the paged_decode.py docstring
  * on the PR 28392 page).
  *
- * Readings where the pages are silent (each also in the design notes):
+ * Readings where the pages are silent:
  *   - RMSNorm of a row x of length D with weight w:
  *       y_d = x_d / sqrt(mean_d x_d^2 + eps) * w_d      (one weight [D] per
  *     tensor, shared by all heads of q);
@@ -486,7 +486,7 @@ void oracle_e4m3_rne_array(const double* v, int64_t n, uint8_t* out) {
  * paged_decode.py docstring (PR 28392 page): block_id * K_PER_BLOCK +
  * slot_in_block, the block being the token's block_table entry.
  *
- * Readings where the page is silent (each also in the design notes):
+ * Readings where the page is silent:
  *   - token t's candidates are positions p in [0, n_t), n_t = lengths[t], with
  *     scores[t * score_stride + p]; positions at or past n_t are padding and
  *     are never read or selected; lengths outside [0, score_stride] count as

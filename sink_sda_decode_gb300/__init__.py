@@ -33,6 +33,16 @@ def _stream_ptr(stream) -> int:
     return int(s.cuda_stream)
 
 
+def _workspace_for(nbytes: int, dev, stream) -> torch.Tensor:
+    """A workspace from torch's caching allocator that the allocator knows is
+    in use on `stream` (the stream the kernels run on), so that the block is
+    not handed out again while those kernels may still touch it."""
+    ws = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=dev)
+    if isinstance(stream, torch.cuda.Stream):
+        ws.record_stream(stream)
+    return ws
+
+
 def _req(t: torch.Tensor, name: str, dtype, ndim=None, device=None):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
@@ -91,7 +101,7 @@ def decode(q: torch.Tensor, unified_kv: torch.Tensor, kv_indices: torch.Tensor,
     with torch.cuda.device(dev):
         need = workspace_size(N, H, D, kv_indices.numel())
         if workspace is None:
-            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+            workspace = _workspace_for(need, dev, stream)
         else:
             _req(workspace, "workspace", torch.uint8, 1, dev)
         rc = lib.sda_decode(q.data_ptr(), unified_kv.data_ptr(), unified_kv.shape[0],
@@ -148,7 +158,7 @@ def decode_fp8(q: torch.Tensor, kv_fp8: torch.Tensor, kv_scale: torch.Tensor,
     with torch.cuda.device(dev):
         need = workspace_size_fp8(N, H, D, kv_indices.numel())
         if workspace is None:
-            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+            workspace = _workspace_for(need, dev, stream)
         else:
             _req(workspace, "workspace", torch.uint8, 1, dev)
         rc = lib.sda_decode_fp8(q.data_ptr(), kv_fp8.data_ptr(), kv_scale.data_ptr(),
@@ -319,7 +329,7 @@ def build_decode(q, unified_kv, attn_sink, softmax_scale, state_slot, swa_len, s
         out = torch.empty_like(q)
     if workspace is None:
         size = (workspace_size if kv_scale is None else workspace_size_fp8)(N, H, D, int(capacity))
-        workspace = torch.empty(max(size, 1), dtype=torch.uint8, device=dev)
+        workspace = _workspace_for(size, dev, stream)
     with torch.cuda.device(dev):
         rc = lib.sda_build_decode(
             state_slot.data_ptr(), swa_len.data_ptr(), swa_head.data_ptr(), comp_indptr.data_ptr(),
@@ -353,21 +363,48 @@ def build_decode_host(q, unified_kv, attn_sink, softmax_scale, state_slot, swa_l
     outputs out / status): kernels read the inputs from host memory and write
     the result back, with no copy-engine transfer.  The pool and attn_sink stay
     on the device.  Asynchronous on `stream`; returns (out, status) host
-    tensors, valid once the stream has reached this call."""
+    tensors, valid once the stream has reached this call.  The caller must
+    keep every host tensor passed in alive (and pinned) until then: the
+    kernels read and write them after this function returns."""
     lib = _lib.load()
-    dev = unified_kv.device
 
-    def host(t, name, dtype, ndim):
+    def kind(t, name, dtype, ndim):
         if not isinstance(t, torch.Tensor) or t.dtype != dtype or t.dim() != ndim:
             raise TypeError(f"{name} must be a {ndim}-d {dtype} tensor")
+
+    def host(t, name, dtype, ndim):
+        kind(t, name, dtype, ndim)
         if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous page-locked (pinned) host tensor")
-    host(q, "q", torch.bfloat16, 3)
+    descriptors = (("state_slot", state_slot), ("swa_len", swa_len), ("swa_head", swa_head),
+                   ("comp_indptr", comp_indptr), ("comp_block", comp_block),
+                   ("comp_slot", comp_slot))
+    kind(q, "q", torch.bfloat16, 3)
     N, H, D = q.shape
-    for name, t in (("state_slot", state_slot), ("swa_len", swa_len), ("swa_head", swa_head),
-                    ("comp_indptr", comp_indptr), ("comp_block", comp_block),
-                    ("comp_slot", comp_slot)):
+    for name, t in descriptors:
+        kind(t, name, torch.int32, 1)
+    # the kernels trust these extents: check every one (host memory is reached
+    # over the chip-to-chip link, and an undersized buffer would be read past)
+    if state_slot.numel() != N or swa_len.numel() != N or swa_head.numel() != N:
+        raise ValueError("state_slot, swa_len and swa_head must have N entries")
+    if comp_indptr.numel() != N + 1:
+        raise ValueError("comp_indptr must have N + 1 entries")
+    if comp_block.numel() != comp_slot.numel():
+        raise ValueError("comp_block and comp_slot must have the same length")
+    if out is not None:
+        kind(out, "out", torch.bfloat16, 3)
+        if tuple(out.shape) != (N, H, D):
+            raise ValueError("out must have q's shape")
+    if status is not None:
+        kind(status, "status", torch.int32, 1)
+        if status.numel() < 1:
+            raise ValueError("status must hold one int32")
+    host(q, "q", torch.bfloat16, 3)
+    for name, t in descriptors:
         host(t, name, torch.int32, 1)
+    if not isinstance(unified_kv, torch.Tensor):
+        raise TypeError("unified_kv must be a torch.Tensor")
+    dev = unified_kv.device
     if kv_scale is None:
         _req(unified_kv, "unified_kv", torch.bfloat16, 2, dev)
     else:
@@ -375,7 +412,13 @@ def build_decode_host(q, unified_kv, attn_sink, softmax_scale, state_slot, swa_l
             unified_kv = unified_kv.view(torch.uint8)
         _req(unified_kv, "kv_fp8", torch.uint8, 2, dev)
         _req(kv_scale, "kv_scale", torch.float32, 1, dev)
+        if kv_scale.numel() != unified_kv.shape[0]:
+            raise ValueError("kv_scale must have one entry per pool row")
+    if unified_kv.shape[1] != D:
+        raise ValueError("pool rows must have D elements")
     _req(attn_sink, "attn_sink", torch.float32, 1, dev)
+    if attn_sink.numel() != H:
+        raise ValueError("attn_sink must have H entries")
     if capacity is None:
         capacity = N * int(win) + comp_block.numel()
     if out is None:
@@ -384,11 +427,13 @@ def build_decode_host(q, unified_kv, attn_sink, softmax_scale, state_slot, swa_l
         host(out, "out", torch.bfloat16, 3)
     if status is None:
         status = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    else:
+        host(status, "status", torch.int32, 1)
     if workspace is None:
         with torch.cuda.device(dev):
             size = build_decode_host_workspace_size(N, H, D, comp_block.numel(), capacity,
                                                     kv_scale is not None)
-        workspace = torch.empty(size, dtype=torch.uint8, device=dev)
+        workspace = _workspace_for(size, dev, stream)
     with torch.cuda.device(dev):
         rc = lib.sda_build_decode_host(
             state_slot.data_ptr() if N else None, swa_len.data_ptr() if N else None,

@@ -295,6 +295,26 @@ sda_status sda_decode_fp8(const void* q, const void* kv_fp8, const float* kv_sca
   return SDA_OK;
 }
 
+// The scalar and pool-argument checks of sda_build_decode(_host) that need
+// no workspace-derived pointer; the host-buffer entry point runs them before
+// it enqueues its input gather, so that an invalid call enqueues nothing.
+static sda_status build_decode_scalars_ok(int N, int win, int k_per_block, int64_t swa_pages,
+                                          int64_t total_pages, int64_t capacity,
+                                          int64_t comp_total, const void* unified_kv,
+                                          const float* kv_scale, const float* attn_sink, int H,
+                                          int D) {
+  if (N < 0 || win <= 0 || k_per_block <= 0 || swa_pages < 0 || total_pages <= 0 ||
+      total_pages > 0x7fffffffll || swa_pages > total_pages || capacity < 0 ||
+      capacity > 0x7fffffffll || comp_total < 0 || comp_total > 0x7fffffffll)
+    return SDA_ERR_INVALID_ARG;
+  const bool fp8 = kv_scale != nullptr;
+  if (fp8 ? !tc_shape_supported(H, D) : !shape_supported(H, D)) return SDA_ERR_UNSUPPORTED;
+  if (N > 0 && (!unified_kv || !attn_sink || !aligned(unified_kv, 16) || !aligned(attn_sink, 4) ||
+                (fp8 && !aligned(kv_scale, 4))))
+    return SDA_ERR_INVALID_ARG;
+  return SDA_OK;
+}
+
 static sda_status build_decode_impl(const int32_t* state_slot, const int32_t* swa_len,
                                     const int32_t* swa_head, const int32_t* comp_indptr,
                                     const int32_t* comp_block, const int32_t* comp_slot,
@@ -467,11 +487,12 @@ sda_status sda_build_decode_host(const int32_t* state_slot, const int32_t* swa_l
                                  const float* attn_sink, float softmax_scale, int N, int H, int D,
                                  void* out, int32_t* status, void* workspace,
                                  size_t workspace_bytes, void* stream) {
-  if (N < 0 || comp_total < 0 || comp_total > 0x7fffffffll || capacity < 0 ||
-      capacity > 0x7fffffffll || !status || !workspace)
-    return SDA_ERR_INVALID_ARG;
+  if (!status || !workspace) return SDA_ERR_INVALID_ARG;
+  // everything checkable on the host is checked before the input gather is enqueued
+  sda_status r0 = build_decode_scalars_ok(N, win, k_per_block, swa_pages, total_pages, capacity,
+                                          comp_total, unified_kv, kv_scale, attn_sink, H, D);
+  if (r0 != SDA_OK) return r0;
   const bool fp8 = kv_scale != nullptr;
-  if (fp8 ? !tc_shape_supported(H, D) : !shape_supported(H, D)) return SDA_ERR_UNSUPPORTED;
   if (!aligned(workspace, 256)) return SDA_ERR_WORKSPACE;
   // every host array must be page-locked; q and out 16-byte aligned
   const void* d_st = host_view(status);

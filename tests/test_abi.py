@@ -5,6 +5,7 @@ import re
 
 import pytest
 
+import sink_sda_decode_gb300 as sda
 from sink_sda_decode_gb300 import _lib
 
 
@@ -109,3 +110,27 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no fallback"):
         _lib.load()
+
+
+def test_build_decode_host_extent_checks():
+    """build_decode_host checks every host extent the kernels trust before it
+    touches CUDA: a descriptor, comp_indptr, comp list or out of the wrong
+    length raises ValueError (CPU tensors suffice: these checks come first)."""
+    import torch
+    N, H, D = 3, 16, 512
+    q = torch.zeros(N, H, D, dtype=torch.bfloat16)
+    i32 = lambda n: torch.zeros(n, dtype=torch.int32)  # noqa: E731
+    good = dict(state_slot=i32(N), swa_len=i32(N), swa_head=i32(N), comp_indptr=i32(N + 1),
+                comp_block=i32(5), comp_slot=i32(5))
+    kw = dict(win=4, k_per_block=8, swa_pages=64)
+    cases = [("state_slot", i32(N - 1)), ("swa_len", i32(N + 1)), ("swa_head", i32(0)),
+             ("comp_indptr", i32(N)), ("comp_slot", i32(4))]
+    for name, bad in cases:
+        args = dict(good, **{name: bad})
+        with pytest.raises(ValueError):
+            sda.build_decode_host(q, None, None, 1.0, args["state_slot"], args["swa_len"],
+                                  args["swa_head"], args["comp_indptr"], args["comp_block"],
+                                  args["comp_slot"], **kw)
+    with pytest.raises(ValueError):
+        sda.build_decode_host(q, None, None, 1.0, *good.values(),
+                              out=torch.zeros(N, H, D - 8, dtype=torch.bfloat16), **kw)

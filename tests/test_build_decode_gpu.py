@@ -127,13 +127,19 @@ def pinned(t):
 
 
 def host_call(w, bi, pool=None, out=None, status=None, workspace=None, stream=None):
+    """One build_decode_host call on pinned copies of the inputs.  The copies
+    are temporaries, so the call's stream is synchronised before they go out
+    of scope (the kernels read them asynchronously)."""
     kv = w.unified_kv if pool is None else pool.codes
     h = {k: pinned(v) for k, v in bi.items()}
-    return sda.build_decode_host(pinned(w.q), kv, w.attn_sink, w.softmax_scale, h["state_slot"],
-                                 h["swa_len"], h["swa_head"], h["comp_indptr"], h["comp_block"],
-                                 h["comp_slot"], win=w.win, k_per_block=w.k_per_block,
-                                 swa_pages=w.swa_pages, kv_scale=None if pool is None else pool.scale,
-                                 out=out, status=status, workspace=workspace, stream=stream)
+    hq = pinned(w.q)
+    res = sda.build_decode_host(hq, kv, w.attn_sink, w.softmax_scale, h["state_slot"],
+                                h["swa_len"], h["swa_head"], h["comp_indptr"], h["comp_block"],
+                                h["comp_slot"], win=w.win, k_per_block=w.k_per_block,
+                                swa_pages=w.swa_pages, kv_scale=None if pool is None else pool.scale,
+                                out=out, status=status, workspace=workspace, stream=stream)
+    (stream if stream is not None else torch.cuda.current_stream()).synchronize()
+    return res
 
 
 @pytest.mark.parametrize("cfg", [0, 1, 2], ids=[inputs.CONFIG_NAMES[c] for c in (0, 1, 2)])
