@@ -850,13 +850,18 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
               fac[2 * rep] = s_fac[h0 + 8 * rep + 2 * tq];
               fac[2 * rep + 1] = s_fac[h0 + 8 * rep + 2 * tq + 1];
             }
+            // both 16-row bands of the quadrant in flight before one wait
+            uint32_t rr[2][kCH / 2];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               const uint32_t taddr = tmem + ((uint32_t)(q4 * 32 + 16 * half) << 16) + C::kOCol + b * NH + h0;
-              uint32_t r[kCH / 2];
-              if constexpr (kCH == 32) tmem_ld_16x256b_x4(taddr, r);
-              else tmem_ld_16x256b_x2(taddr, r);
-              tmem_wait_ld();
+              if constexpr (kCH == 32) tmem_ld_16x256b_x4(taddr, rr[half]);
+              else tmem_ld_16x256b_x2(taddr, rr[half]);
+            }
+            tmem_wait_ld();
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const uint32_t (&r)[kCH / 2] = rr[half];
               // "+ 0.f" turns -0 into +0 when the factor is 0 (sink = +inf)
               uint32_t pk[kCH / 4];  // [rep][row d or d+8]
 #pragma unroll
