@@ -103,7 +103,6 @@ bool choose_plan(int H, int D, const DeviceCaps& caps, LaunchPlan* lp) {
     lp->threads = 896;
     lp->smem = umma_smem_bytes(lp->nh);
     lp->tile = kTileSlots;
-    lp->min_chunk = kTileSlots;
   } else {
     lp->nh = H;
     lp->hg = 1;
@@ -111,17 +110,17 @@ bool choose_plan(int H, int D, const DeviceCaps& caps, LaunchPlan* lp) {
     lp->threads = 256;
     lp->smem = 0;
     lp->tile = kTileSlots;
-    lp->min_chunk = kTileSlots;
   }
+  if (lp->grid > kMaxPlanGrid) lp->grid = kMaxPlanGrid;
   return true;
 }
 
 WsLayout workspace_layout(int N, int H, int D, int64_t total_indices, const LaunchPlan& lp) {
   WsLayout L;
-  // Partial rows: fewer than 2 * grid / hg (pieces are >= T*hg/grid slots)
-  // and fewer than 2 * T / min_chunk + 1 (chunk >= min_chunk slots); T <= total_indices.
+  // Partial rows: fewer than 2 * grid / hg (each interior range boundary
+  // cuts one token) and no more than one per tile (T <= total_indices).
   int64_t p1 = 2 * ((int64_t)(lp.grid + lp.hg - 1) / lp.hg) + 2;
-  int64_t p2 = 2 * ((total_indices + lp.min_chunk - 1) / lp.min_chunk) + 2;
+  int64_t p2 = 2 * ((total_indices + lp.tile - 1) / lp.tile) + 2;
   int64_t p_max = p1 < p2 ? p1 : p2;
   int64_t s_max = p_max / 2 + 1;
   if (s_max > N) s_max = N;
@@ -131,6 +130,12 @@ WsLayout workspace_layout(int N, int H, int D, int64_t total_indices, const Laun
   size_t off = sizeof(WsHeader);
   L.units_off = off;
   off = align_up(off + (size_t)L.u_max * 16, 256);
+  L.cta_off = off;
+  off = align_up(off + (size_t)(lp.grid + 1) * 4, 256);
+  L.ctok_off = off;
+  off = align_up(off + (size_t)(N > 0 ? N : 1) * 4, 256);
+  L.ctp_off = off;
+  off = align_up(off + (size_t)(N + 1) * 4, 256);
   L.split_off = off;
   off = align_up(off + (size_t)(s_max > 0 ? s_max : 1) * 16, 256);
   L.ml_off = off;
@@ -234,7 +239,6 @@ static bool fp8_plan(int H, int D, const DeviceCaps& caps, LaunchPlan* lp) {
     lp->threads = 896;
     lp->smem = umma_smem_bytes(lp->nh);
     lp->tile = kTileSlots;
-    lp->min_chunk = kTileSlots;
   }
   return true;
 }

@@ -80,16 +80,15 @@ __global__ void __launch_bounds__(kSimtThreads)
 decode_simt_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kv,
                    const int32_t* __restrict__ kv_indices, const float* __restrict__ attn_sink,
                    float qk_scale_log2, int H, __nv_bfloat16* __restrict__ out,
-                   const WsHeader* __restrict__ hdr, const int4* __restrict__ units,
+                   const int* __restrict__ cta_start, const int4* __restrict__ units,
                    float2* __restrict__ part_ml, float* __restrict__ part_o) {
   using S = LaneShape<D>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   pdl_wait();
   pdl_trigger();
-  const int n_units = hdr->n_units;
-  for (int k = 0;; ++k) {
-    const int pos = unit_position(k, blockIdx.x, gridDim.x);
-    if (pos >= n_units) break;
+  // this CTA's run of the unit list
+  const int u0 = cta_start[blockIdx.x], u1 = cta_start[blockIdx.x + 1];
+  for (int pos = u0; pos < u1; ++pos) {
     const int4 u = units[pos];
     const int t = u.x, begin = u.y, len = u.z, row = unit_part_row(u.w);
     for (int h = warp; h < H; h += kSimtWarps) {
@@ -176,7 +175,7 @@ cudaError_t launch_simt_d(const void* q, const void* kv, const int32_t* kv_indic
   return launch_pdl(decode_simt_kernel<D>, dim3(lp.grid), dim3(kSimtThreads), 0, st,
                     static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kv),
                     kv_indices, attn_sink, scale * kLog2e, H, static_cast<__nv_bfloat16*>(out),
-                    reinterpret_cast<const WsHeader*>(base),
+                    reinterpret_cast<const int*>(base + L.cta_off),
                     reinterpret_cast<const int4*>(base + L.units_off),
                     reinterpret_cast<float2*>(base + L.ml_off),
                     reinterpret_cast<float*>(base + L.o_off));

@@ -159,6 +159,7 @@ struct Params {
   __nv_bfloat16* out;
   WsHeader* hdr;
   const int4* units;
+  const int* cta_start;  // CTA b's units are units[cta_start[b] .. cta_start[b + 1])
   float2* part_ml;
   float* part_o;
   float qk_scale_log2;
@@ -206,12 +207,12 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, const W
   }
 }
 
-// Walks the tiles of the units a CTA owns, in the same order in every role:
-// unit k of CTA b is unit_position(k, b, G); units without slots are skipped.
+// Walks the tiles of the units a CTA owns (its contiguous run of the unit
+// list), in the same order in every role; units without slots are skipped.
 struct TileCursor {
   const int4* units;
   int n_units;
-  int k;       // unit slot in the CTA's sequence
+  int k;       // unit of the CTA's run
   int4 u;      // current unit
   int ntiles;  // tiles of the current unit
   int i;       // tile within the unit
@@ -221,12 +222,11 @@ struct TileCursor {
   __device__ __forceinline__ int len() const { return u.z; }
   __device__ __forceinline__ void seek() {
     for (;; ++k) {
-      const int pos = unit_position(k, blockIdx.x, gridDim.x);
-      if (pos >= n_units) {
+      if (k >= n_units) {
         valid = false;
         return;
       }
-      u = units[pos];
+      u = units[k];
       if (u.z > 0) {
         ntiles = (u.z + kTileN - 1) / kTileN;
         i = 0;
@@ -309,7 +309,8 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
   // everything above overlaps the previous kernel (PDL); global memory only below
   pdl_wait();
   pdl_trigger();
-  const int n_units = p.hdr->n_units;
+  const int4* const my_units = p.units + p.cta_start[blockIdx.x];
+  const int n_units = p.cta_start[blockIdx.x + 1] - p.cta_start[blockIdx.x];
   const int H = p.H;
   const WaitCtx wc{abort_flag, p.hdr, p.wait_timeout_ns};
 
@@ -340,7 +341,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
     };
     bool ok = true;
     TileCursor t;  // this group's current tile (the groups take every other tile)
-    t.init(p.units, n_units);
+    t.init(my_units, n_units);
     if (grp == 1 && t.valid) t.next();
     c = t;  // c: this group's next tile (slots read one tile early)
     auto skip2 = [&](TileCursor& x) {
@@ -425,7 +426,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
       return (lane < kRows && r < n) ? __ldg(p.kv_indices + x.u.y + x.i * kTileN + r) : -1;
     };
     TileCursor cu;  // the current tile
-    cu.init(p.units, n_units);
+    cu.init(my_units, n_units);
     TileCursor nx = cu;  // the next tile
     if (nx.valid) nx.next();
     TileCursor n2 = nx;  // the one after: its slots are read a tile early, its rows prefetched
@@ -509,7 +510,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
       const bool qk_role = warp != kPvWarp;
       const int qh = warp == kMmaWarpB ? 1 : 0;  // QK: half of D (of the K dimension)
       TileCursor cq;
-      cq.init(p.units, n_units);
+      cq.init(my_units, n_units);
       int q_issued = 0;
       bool ok = true;
       if (qk_role && qh == 0 && cq.valid) {  // q of the first unit
@@ -619,10 +620,8 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
     // reached by all of them even after a wait timed out: a timed-out wait
     // only leaves garbage in the outputs and the error word raised.
     int g = 0;
-    for (int k = 0;; ++k) {
-      const int pos = unit_position(k, blockIdx.x, gridDim.x);
-      if (pos >= n_units) break;
-      const int4 u = p.units[pos];
+    for (int k = 0; k < n_units; ++k) {
+      const int4 u = my_units[k];
       const int t = u.x, len = u.z, hg = unit_head_group(u.w), row = unit_part_row(u.w);
       if (len <= 0) {
         // padded token: out = 0 for its NH heads (contiguous NH*D bf16)
@@ -978,6 +977,7 @@ cudaError_t launch_nh(const void* q, const void* kv, const float* kv_scale, int6
   p.out = static_cast<__nv_bfloat16*>(out);
   p.hdr = reinterpret_cast<WsHeader*>(base);
   p.units = reinterpret_cast<const int4*>(base + L.units_off);
+  p.cta_start = reinterpret_cast<const int*>(base + L.cta_off);
   p.part_ml = reinterpret_cast<float2*>(base + L.ml_off);
   p.part_o = reinterpret_cast<float*>(base + L.o_off);
   p.qk_scale_log2 = scale * kLog2e;

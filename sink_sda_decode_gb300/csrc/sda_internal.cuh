@@ -14,10 +14,12 @@ namespace sda {
 // ---------------------------------------------------------------- work units
 //
 // A work unit is one piece of one token's slot list, for one group of heads.
-// Long lists are cut into pieces so that every CTA of a persistent grid gets
-// about the same number of slots ("split-L"); the pieces of a split token
-// each write an unnormalised partial (m, l, acc) that the combine kernel
-// merges with the sink.  Unsplit tokens are finished by the decode kernel.
+// Each CTA of the persistent grid owns a contiguous run of units covering
+// about the same number of KV tiles (the plan cuts each head group's tile
+// sequence into equal ranges, "split-L"); the pieces of a token cut by a
+// range boundary each write an unnormalised partial (m, l, acc) that the
+// combine kernel merges with the sink.  Unsplit tokens are finished by the
+// decode kernel.
 //
 // int4 layout: x = token, y = first index into kv_indices (absolute),
 //              z = number of slots, w = head_group | ((partial_row + 1) << 4)
@@ -44,6 +46,7 @@ static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
 // Split list entry: x = token, y = first partial row, z = number of pieces.
 constexpr int kTileSlots = 64;      // slots per KV tile of the tensor-core kernel
+constexpr int kMaxPlanGrid = 1024;  // largest persistent grid the plan partitions for
 
 // Decode variants.
 enum Variant : int { kSimt = 0, kUmma = 1 };
@@ -57,11 +60,12 @@ struct LaunchPlan {
   int threads;   // threads per CTA
   size_t smem;   // dynamic shared memory bytes
   int tile;      // pieces of split lists are multiples of this many slots
-  int min_chunk; // smallest piece a list is cut into (a multiple of tile)
 };
 
 struct WsLayout {
-  size_t units_off, split_off, ml_off, o_off, total;
+  // units_off: the unit list; cta_off: int [grid + 1], CTA b's units are
+  // [cta[b], cta[b+1]); ctok_off / ctp_off: the plan's scratch (int [N], [N+1])
+  size_t units_off, cta_off, ctok_off, ctp_off, split_off, ml_off, o_off, total;
   int u_max, s_max, p_max;
 };
 
@@ -74,9 +78,10 @@ struct DeviceCaps {
 // if (H, D) is unsupported.
 bool choose_plan(int H, int D, const DeviceCaps& caps, LaunchPlan* lp);
 
-// Workspace layout for a plan.  p_max bounds the partial rows: a piece is
-// at least ceil(T * hg / grid) slots, so split tokens (L > chunk) use fewer
-// than 2 * L / chunk pieces each, and in total fewer than 2 * grid / hg.
+// Workspace layout for a plan.  p_max bounds the partial rows: each of the
+// at most grid / hg - 1 interior range boundaries cuts one token, so the
+// split tokens have fewer than 2 * grid / hg pieces in total (and no more
+// than one per tile).
 WsLayout workspace_layout(int N, int H, int D, int64_t total_indices, const LaunchPlan& lp);
 
 // ---------------------------------------------------------------- launchers
@@ -189,12 +194,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 constexpr float kLog2e = 1.4426950408889634f;
 
-__device__ __forceinline__ int unit_position(int k, int cta, int grid) {
-  // "snake" order over a list sorted by decreasing size: CTA b takes
-  // positions b, 2G-1-b, 2G+b, 4G-1-b, ... so that big and small units pair up.
-  const int round = k >> 1;
-  return round * 2 * grid + ((k & 1) ? (2 * grid - 1 - cta) : cta);
-}
 #endif
 
 }  // namespace sda

@@ -17,9 +17,7 @@ namespace sda {
 namespace {
 
 constexpr int kPlanThreads = 1024;
-constexpr int kBuckets = 33;  // bucket b holds units of length in [2^(b-1), 2^b); 0 = empty
-
-__device__ __forceinline__ int len_bucket(int len) { return len <= 0 ? 0 : 32 - __clz(len); }
+static_assert(kMaxPlanGrid <= kPlanThreads, "one plan thread per CTA of the grid");
 
 // Exclusive block-wide scan of one int per thread (1024 threads); returns the
 // prefix and stores the block total in *total (smem scratch of 32 ints).
@@ -50,32 +48,54 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
   return r;
 }
 
-struct TokenSplit {
-  int len, pieces, piece_len;
-};
-
-__device__ __forceinline__ TokenSplit token_split(const int32_t* indptr, int t, int chunk, int tile) {
-  TokenSplit s;
-  int L = indptr[t + 1] - indptr[t];
-  s.len = L > 0 ? L : 0;
-  s.pieces = s.len == 0 ? 1 : (s.len + chunk - 1) / chunk;
-  const int even = (s.len + s.pieces - 1) / s.pieces;
-  s.piece_len = s.pieces == 1 ? s.len : ((even + tile - 1) / tile) * tile;
-  return s;
+// First index i in [lo, hi) with a[i] > x (hi if none); a non-decreasing.
+__device__ __forceinline__ int upper_index(const int* a, int lo, int hi, int x) {
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (a[mid] > x) hi = mid;
+    else lo = mid + 1;
+  }
+  return lo;
+}
+// First index i in [lo, hi) with a[i] >= x (hi if none); a non-decreasing.
+__device__ __forceinline__ int lower_index(const int* a, int lo, int hi, int x) {
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (a[mid] >= x) hi = mid;
+    else lo = mid + 1;
+  }
+  return lo;
 }
 
+// The work plan: each head group's sequence of KV tiles (the non-empty
+// tokens in token order, ceil(L_t / tile) tiles each) is cut into at most
+// grid / hg contiguous ranges of nearly equal tile counts, one per CTA.  The
+// number of ranges Ga is the smallest that reaches the least possible
+// maximum, Wmin = ceil(T / (grid / hg)) tiles; a range boundary that falls
+// within Wmin / 16 tiles of a token boundary moves onto it, so that a token
+// is cut only where that buys balance.  A token cut by k boundaries becomes
+// k + 1 pieces (units with partial rows, merged by the combine kernel).
+// CTA g * (grid / hg) + r takes range r of head group g, so the CTAs that
+// read a token's rows for different head groups run in step and share them
+// through L2.  Zero-length tokens (out = 0) are dealt round-robin over all
+// CTAs, ahead of each CTA's range.
+//
+// Outputs: cta_start[b] .. cta_start[b + 1] is CTA b's contiguous run of
+// the unit list; the split list holds (token, first partial row, pieces).
+// Scratch: ctok[j] = j-th non-empty token (zero-length tokens from the back),
+// ctp[j] = tiles before it (ctp[NNZ] = T).
 __device__ __forceinline__ void plan_body(const int32_t* __restrict__ indptr, int N,
                                           long long total_indices, int hg, int grid, int tile,
-                                          int min_chunk, WsHeader* __restrict__ hdr,
-                                          int4* __restrict__ units, int4* __restrict__ splits) {
+                                          WsHeader* __restrict__ hdr, int4* __restrict__ units,
+                                          int4* __restrict__ splits, int* __restrict__ cta_start,
+                                          int* __restrict__ ctok, int* __restrict__ ctp) {
   __shared__ int warp_sums[32];
   __shared__ int s_total[2];
-  __shared__ int bucket_count[kBuckets];
-  __shared__ int bucket_cursor[kBuckets];
-  __shared__ int s_chunk;
+  __shared__ int sB[kMaxPlanGrid + 1];      // range boundaries (tiles)
+  __shared__ int s_lo[kMaxPlanGrid];        // first non-empty token of range r
+  __shared__ int s_start[kMaxPlanGrid + 1]; // start of CTA b's unit run
+  __shared__ int s_nz[kMaxPlanGrid];        // zero-length units of CTA b
 
-  if (threadIdx.x < kBuckets) bucket_count[threadIdx.x] = 0;
-  __syncthreads();
   // kv_indptr must be a true prefix sum inside [0, total_indices]; otherwise
   // nothing is planned (out is left unwritten) and the error word reads 2, so
   // that no kernel ever reads kv_indices out of bounds.
@@ -85,6 +105,7 @@ __device__ __forceinline__ void plan_body(const int32_t* __restrict__ indptr, in
     if (v < 0 || (long long)v > total_indices || (t < N && indptr[t + 1] < v)) bad = 1;
   }
   if (__syncthreads_or(bad)) {
+    for (int b = threadIdx.x; b <= grid; b += kPlanThreads) cta_start[b] = 0;
     if (threadIdx.x == 0) {
       hdr->n_units = 0;
       hdr->n_split = 0;
@@ -94,81 +115,140 @@ __device__ __forceinline__ void plan_body(const int32_t* __restrict__ indptr, in
     }
     return;
   }
-  if (threadIdx.x == 0) {
-    long long T = N > 0 ? (long long)indptr[N] - (long long)indptr[0] : 0;
-    if (T < 0) T = 0;
-    long long target = (T * hg + grid - 1) / grid;
-    // a multiple of the tile, so that every piece but the last is whole
-    // tiles and no piece is empty
-    long long chunk = ((target + tile - 1) / tile) * tile;
-    if (chunk < min_chunk) chunk = min_chunk;
-    if (chunk > (1ll << 30)) chunk = 1ll << 30;
-    s_chunk = (int)chunk;
-  }
-  __syncthreads();
-  const int chunk = s_chunk;
 
-  // pass 1: unit counts per length bucket
+  // pass 1: compact the non-empty tokens and scan their tile counts
+  int nnz = 0, T = 0;
   for (int t0 = 0; t0 < N; t0 += kPlanThreads) {
     const int t = t0 + threadIdx.x;
+    const int L = t < N ? indptr[t + 1] - indptr[t] : 0;
+    const int nz = L > 0 ? 1 : 0;
+    const int nt = (L + tile - 1) / tile;
+    const int rank = block_exclusive_scan(nz, warp_sums, &s_total[0]) + nnz;
+    const int tp = block_exclusive_scan(nt, warp_sums, &s_total[1]) + T;
     if (t < N) {
-      TokenSplit s = token_split(indptr, t, chunk, tile);
-      for (int k = 0; k < s.pieces; ++k) {
-        int plen = s.pieces == 1 ? s.len : min(s.piece_len, s.len - k * s.piece_len);
-        atomicAdd(&bucket_count[len_bucket(plen)], hg);
+      if (nz) {
+        ctok[rank] = t;
+        ctp[rank] = tp;
+      } else {
+        ctok[N - 1 - (t - rank)] = t;  // zero-length token number t - rank
       }
     }
+    nnz += s_total[0];
+    T += s_total[1];
+    __syncthreads();  // s_total is rewritten by the next chunk
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int b = kBuckets - 1; b >= 0; --b) {  // longest pieces first
-      bucket_cursor[b] = acc;
-      acc += bucket_count[b];
+  if (threadIdx.x == 0) ctp[nnz] = T;
+  __syncthreads();  // ctok / ctp visible to the whole CTA
+  const int NZ = N - nnz;
+  const int Gh = grid / hg;
+  const int Wmin = T > 0 ? (T + Gh - 1) / Gh : 0;
+  const int Ga = T > 0 ? (T + Wmin - 1) / Wmin : 0;  // ranges in use per head group (<= Gh)
+  const int snap = Wmin / 16;
+
+  // range boundaries: nominal r*T/Ga, moved onto a token boundary within
+  // snap tiles (nominal boundaries are >= Wmin/2 apart and move by at most
+  // Wmin/16, so they stay strictly increasing: no range is empty)
+  for (int r = threadIdx.x; r <= Ga; r += kPlanThreads) {
+    int x = Ga > 0 ? (int)(((long long)r * T) / Ga) : 0;
+    if (r > 0 && r < Ga) {
+      const int a = upper_index(ctp, 0, nnz + 1, x) - 1;  // ctp[a] <= x < ctp[a + 1]
+      const int dl = x - ctp[a], dh = ctp[a + 1] - x;
+      if (dl <= dh && dl <= snap) x = ctp[a];
+      else if (dh < dl && dh <= snap) x = ctp[a + 1];
     }
-    hdr->n_units = acc;
+    sB[r] = x;
   }
   __syncthreads();
 
-  // pass 2: emit units, partial rows and the split list
+  // units per CTA: its share of the zero-length (token, head group) pairs,
+  // then one per token its range touches
+  const int zp_total = hg * NZ;
+  {
+    const int b = threadIdx.x;  // grid <= kMaxPlanGrid <= kPlanThreads
+    int total = 0;
+    if (b < grid) {
+      const int nzb = b < zp_total ? (zp_total - 1 - b) / grid + 1 : 0;
+      const int g = b / Gh, r = b % Gh;
+      int cnt = 0;
+      if (g < hg && r < Ga) {
+        const int lo = upper_index(ctp, 1, nnz + 1, sB[r]) - 1;  // first j with ctp[j+1] > B[r]
+        const int hi = lower_index(ctp, 0, nnz, sB[r + 1]) - 1;  // last j with ctp[j] < B[r+1]
+        cnt = hi - lo + 1;
+        if (g == 0) s_lo[r] = lo;
+      }
+      s_nz[b] = nzb;
+      total = nzb + cnt;
+    }
+    const int start = block_exclusive_scan(total, warp_sums, &s_total[0]);
+    if (b < grid) {
+      s_start[b] = start;
+      cta_start[b] = start;
+    }
+    if (b == 0) {
+      s_start[grid] = s_total[0];
+      cta_start[grid] = s_total[0];
+    }
+  }
+  __syncthreads();
+
+  // pass 2: the units of every non-empty token and the split list
   int part_carry = 0, split_carry = 0;
-  for (int t0 = 0; t0 < N; t0 += kPlanThreads) {
-    const int t = t0 + threadIdx.x;
-    TokenSplit s{0, 1, 0};
-    if (t < N) s = token_split(indptr, t, chunk, tile);
-    const bool split = t < N && s.pieces > 1;
-    const int part_base = block_exclusive_scan(split ? s.pieces : 0, warp_sums, &s_total[0]) + part_carry;
+  for (int j0 = 0; j0 < nnz; j0 += kPlanThreads) {
+    const int j = j0 + threadIdx.x;
+    int f = 0, l = -1, a0 = 0, a1 = 0;
+    if (j < nnz) {
+      a0 = ctp[j];
+      a1 = ctp[j + 1];
+      f = upper_index(sB, 0, Ga + 1, a0) - 1;      // range holding the token's first tile
+      l = upper_index(sB, 0, Ga + 1, a1 - 1) - 1;  // and its last
+    }
+    const int pieces = l - f + 1;
+    const bool split = pieces > 1;
+    const int part_base = block_exclusive_scan(split ? pieces : 0, warp_sums, &s_total[0]) + part_carry;
     const int split_idx = block_exclusive_scan(split ? 1 : 0, warp_sums, &s_total[1]) + split_carry;
-    if (t < N) {
-      const int begin = indptr[t];
-      for (int k = 0; k < s.pieces; ++k) {
-        const int plen = s.pieces == 1 ? s.len : min(s.piece_len, s.len - k * s.piece_len);
-        const int pos = atomicAdd(&bucket_cursor[len_bucket(plen)], hg);
-        const int row = split ? part_base + k : -1;
-        for (int g = 0; g < hg; ++g)
-          units[pos + g] = make_int4(t, begin + k * s.piece_len, plen, make_unit_meta(g, row));
+    if (j < nnz) {
+      const int t = ctok[j];
+      const int begin0 = indptr[t], L = indptr[t + 1] - begin0;
+      if (split) splits[split_idx] = make_int4(t, part_base, pieces, 0);
+      for (int r = f; r <= l; ++r) {
+        const int lo_t = max(a0, sB[r]) - a0, hi_t = min(a1, sB[r + 1]) - a0;  // tiles of the token
+        const int begin = begin0 + lo_t * tile;
+        const int len = min(L, hi_t * tile) - lo_t * tile;
+        const int row = split ? part_base + (r - f) : -1;
+        for (int g = 0; g < hg; ++g) {
+          const int b = g * Gh + r;
+          units[s_start[b] + s_nz[b] + (j - s_lo[r])] = make_int4(t, begin, len, make_unit_meta(g, row));
+        }
       }
-      if (split) splits[split_idx] = make_int4(t, part_base, s.pieces, 0);
     }
     part_carry += s_total[0];
     split_carry += s_total[1];
     __syncthreads();
   }
+  // zero-length (token, head group) pairs, round-robin over the CTAs
+  for (int zp = threadIdx.x; zp < zp_total; zp += kPlanThreads) {
+    const int g = zp / NZ, z = zp % NZ;
+    const int t = ctok[N - 1 - z];
+    const int b = zp % grid, k = zp / grid;
+    units[s_start[b] + k] = make_int4(t, indptr[t], 0, make_unit_meta(g, -1));
+  }
   if (threadIdx.x == 0) {
+    hdr->n_units = s_start[grid];
     hdr->n_split = split_carry;
     hdr->n_parts = part_carry;
-    hdr->chunk = chunk;
+    hdr->chunk = Wmin * tile;
     hdr->error = 0;
   }
 }
 
 __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(const int32_t* __restrict__ indptr, int N, long long total_indices, int hg, int grid,
-            int tile, int min_chunk, WsHeader* __restrict__ hdr, int4* __restrict__ units,
-            int4* __restrict__ splits) {
+            int tile, WsHeader* __restrict__ hdr, int4* __restrict__ units,
+            int4* __restrict__ splits, int* __restrict__ cta_start, int* __restrict__ ctok,
+            int* __restrict__ ctp) {
   pdl_wait();
   pdl_trigger();
-  plan_body(indptr, N, total_indices, hg, grid, tile, min_chunk, hdr, units, splits);
+  plan_body(indptr, N, total_indices, hg, grid, tile, hdr, units, splits, cta_start, ctok, ctp);
 }
 
 // The index builder's scan and the plan in one CTA (sda_build_decode): the
@@ -177,13 +257,15 @@ plan_kernel(const int32_t* __restrict__ indptr, int N, long long total_indices, 
 static_assert(kPlanThreads == kScanThreads, "one CTA runs both bodies");
 __global__ void __launch_bounds__(kPlanThreads)
 scan_plan_kernel(int N, int64_t capacity, int32_t* __restrict__ kv_indptr,
-                 int32_t* __restrict__ status, int hg, int grid, int tile, int min_chunk,
-                 WsHeader* __restrict__ hdr, int4* __restrict__ units, int4* __restrict__ splits) {
+                 int32_t* __restrict__ status, int hg, int grid, int tile,
+                 WsHeader* __restrict__ hdr, int4* __restrict__ units, int4* __restrict__ splits,
+                 int* __restrict__ cta_start, int* __restrict__ ctok, int* __restrict__ ctp) {
   pdl_wait();
   pdl_trigger();
   build_scan_body(N, capacity, kv_indptr, status);
   __syncthreads();  // kv_indptr is final (this CTA wrote it)
-  plan_body(kv_indptr, N, (long long)capacity, hg, grid, tile, min_chunk, hdr, units, splits);
+  plan_body(kv_indptr, N, (long long)capacity, hg, grid, tile, hdr, units, splits, cta_start, ctok,
+            ctp);
 }
 
 // Merge the pieces of each split token:
@@ -279,20 +361,24 @@ cudaError_t launch_plan(const int32_t* kv_indptr, int N, int64_t total_indices,
                         const LaunchPlan& lp, void* ws, const WsLayout& L, cudaStream_t st) {
   char* base = static_cast<char*>(ws);
   return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, kv_indptr, N,
-                    (long long)total_indices, lp.hg, lp.grid, lp.tile, lp.min_chunk,
+                    (long long)total_indices, lp.hg, lp.grid, lp.tile,
                     reinterpret_cast<WsHeader*>(base),
                     reinterpret_cast<int4*>(base + L.units_off),
-                    reinterpret_cast<int4*>(base + L.split_off));
+                    reinterpret_cast<int4*>(base + L.split_off),
+                    reinterpret_cast<int*>(base + L.cta_off), reinterpret_cast<int*>(base + L.ctok_off),
+                    reinterpret_cast<int*>(base + L.ctp_off));
 }
 
 cudaError_t launch_scan_plan(int N, int64_t capacity, int32_t* kv_indptr, int32_t* status,
                              const LaunchPlan& lp, void* ws, const WsLayout& L, cudaStream_t st) {
   char* base = static_cast<char*>(ws);
   return launch_pdl(scan_plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, N, capacity, kv_indptr,
-                    status, lp.hg, lp.grid, lp.tile, lp.min_chunk,
+                    status, lp.hg, lp.grid, lp.tile,
                     reinterpret_cast<WsHeader*>(base),
                     reinterpret_cast<int4*>(base + L.units_off),
-                    reinterpret_cast<int4*>(base + L.split_off));
+                    reinterpret_cast<int4*>(base + L.split_off),
+                    reinterpret_cast<int*>(base + L.cta_off), reinterpret_cast<int*>(base + L.ctok_off),
+                    reinterpret_cast<int*>(base + L.ctp_off));
 }
 
 cudaError_t launch_combine(const float* attn_sink, int N, int H, int D, void* out, void* ws,
