@@ -241,13 +241,29 @@ __device__ __forceinline__ void plan_body(const int32_t* __restrict__ indptr, in
   }
 }
 
+// Batches of up to kPlanSmemTokens tokens keep the plan's token arrays (ctok,
+// ctp) in the CTA's shared memory: the boundary and token passes run binary
+// searches over them, and a search through global memory would pay a
+// dependent round trip per step.  Larger batches use the workspace copies.
+constexpr int kPlanSmemTokens = 12288;
+__host__ __device__ constexpr size_t plan_dyn_smem(int N) {
+  return N <= kPlanSmemTokens ? (size_t)(2 * (N > 0 ? N : 1) + 1) * 4 : 0;
+}
+__device__ __forceinline__ void plan_token_arrays(int N, int*& ctok, int*& ctp) {
+  extern __shared__ int plan_dyn[];
+  if (N <= kPlanSmemTokens) {
+    ctok = plan_dyn;
+    ctp = plan_dyn + (N > 0 ? N : 1);
+  }
+}
+
 __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(const int32_t* __restrict__ indptr, int N, long long total_indices, int hg, int grid,
             int tile, WsHeader* __restrict__ hdr, int4* __restrict__ units,
-            int4* __restrict__ splits, int* __restrict__ cta_start, int* __restrict__ ctok,
-            int* __restrict__ ctp) {
+            int4* __restrict__ splits, int* __restrict__ cta_start, int* ctok, int* ctp) {
   pdl_wait();
   pdl_trigger();
+  plan_token_arrays(N, ctok, ctp);
   plan_body(indptr, N, total_indices, hg, grid, tile, hdr, units, splits, cta_start, ctok, ctp);
 }
 
@@ -259,11 +275,12 @@ __global__ void __launch_bounds__(kPlanThreads)
 scan_plan_kernel(int N, int64_t capacity, int32_t* __restrict__ kv_indptr,
                  int32_t* __restrict__ status, int hg, int grid, int tile,
                  WsHeader* __restrict__ hdr, int4* __restrict__ units, int4* __restrict__ splits,
-                 int* __restrict__ cta_start, int* __restrict__ ctok, int* __restrict__ ctp) {
+                 int* __restrict__ cta_start, int* ctok, int* ctp) {
   pdl_wait();
   pdl_trigger();
   build_scan_body(N, capacity, kv_indptr, status);
   __syncthreads();  // kv_indptr is final (this CTA wrote it)
+  plan_token_arrays(N, ctok, ctp);
   plan_body(kv_indptr, N, (long long)capacity, hg, grid, tile, hdr, units, splits, cta_start, ctok,
             ctp);
 }
@@ -360,7 +377,10 @@ combine_kernel(const float* __restrict__ attn_sink, int H, __nv_bfloat16* __rest
 cudaError_t launch_plan(const int32_t* kv_indptr, int N, int64_t total_indices,
                         const LaunchPlan& lp, void* ws, const WsLayout& L, cudaStream_t st) {
   char* base = static_cast<char*>(ws);
-  return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, kv_indptr, N,
+  static const cudaError_t attr = cudaFuncSetAttribute(
+      plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_dyn_smem(kPlanSmemTokens));
+  if (attr != cudaSuccess) return attr;
+  return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), plan_dyn_smem(N), st, kv_indptr, N,
                     (long long)total_indices, lp.hg, lp.grid, lp.tile,
                     reinterpret_cast<WsHeader*>(base),
                     reinterpret_cast<int4*>(base + L.units_off),
@@ -372,7 +392,10 @@ cudaError_t launch_plan(const int32_t* kv_indptr, int N, int64_t total_indices,
 cudaError_t launch_scan_plan(int N, int64_t capacity, int32_t* kv_indptr, int32_t* status,
                              const LaunchPlan& lp, void* ws, const WsLayout& L, cudaStream_t st) {
   char* base = static_cast<char*>(ws);
-  return launch_pdl(scan_plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, N, capacity, kv_indptr,
+  static const cudaError_t attr = cudaFuncSetAttribute(
+      scan_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_dyn_smem(kPlanSmemTokens));
+  if (attr != cudaSuccess) return attr;
+  return launch_pdl(scan_plan_kernel, dim3(1), dim3(kPlanThreads), plan_dyn_smem(N), st, N, capacity, kv_indptr,
                     status, lp.hg, lp.grid, lp.tile,
                     reinterpret_cast<WsHeader*>(base),
                     reinterpret_cast<int4*>(base + L.units_off),
