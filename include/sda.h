@@ -279,7 +279,22 @@ sda_status sda_build_decode(const int32_t* state_slot, const int32_t* swa_len,
  * host memory directly, runs sda_build_decode there (kv_indices and kv_indptr
  * live in the workspace) and writes out and status back to the host with
  * another kernel -- no copy-engine transfer, so the whole step is one
- * sequence of kernels on `stream` (graph-capturable).  Asynchronous: the host
+ * sequence of kernels on `stream` (graph-capturable).
+ * Batches whose q is 8 MB or more (N*H*D*2 >= 2^23) take another route,
+ * because the host link then costs more than the step (about 210 GB/s in and
+ * 190 GB/s out on a GB300 with NVLink-C2C): the descriptors and q travel by
+ * copy engine on a library-owned inbound stream, in 2..8 token chunks (chunk
+ * boundaries depend on N only); the index build runs once for the whole
+ * batch on `stream`, then the decode chunk by chunk as each chunk's q lands,
+ * and each chunk's out goes back on a library-owned outbound stream as soon
+ * as its decode is done, so both link directions and the SMs work at once.
+ * `stream` forks to those two streams at the start of the call and joins
+ * them at its end (graph-capturable; the first such call on a device creates
+ * the two streams and their events, so make it before any capture; calls
+ * from several host threads are serialised while they enqueue).  Each chunk
+ * has its own work plan, so the result can differ from the one-call path in
+ * the last bf16 bit (both are within the decode's tolerance); status is the
+ * whole batch's, as in sda_build_decode.  Asynchronous: the host
  * buffers must stay valid (and keep their page-locking) until the stream has
  * passed this call, and out/status are ready once the stream reaches this
  * point.  SDA_ERR_INVALID_ARG if a host buffer is not page-locked or is

@@ -482,6 +482,158 @@ sda_status sda_build_decode_host_workspace_size(int N, int H, int D, int64_t com
   return SDA_OK;
 }
 
+// ---------------------------------------------------------------- large host batches
+// A batch whose q (and out) is at least kPipelineBytes moves through the
+// host link in token chunks so that the link's two directions and the SMs
+// work at once: two streams of this library carry copy-engine transfers (the
+// descriptors and each chunk's q in; each chunk's out back as soon as its
+// decode is done) while the caller's stream builds the whole batch's lists
+// once and decodes chunk after chunk (the decode takes absolute kv_indptr
+// offsets, so a chunk decodes from a slice of the batch's lists).  The
+// chunk boundaries depend on N only, never on the contents of the host
+// arrays, so a captured graph stays valid when the caller refills them.
+constexpr int64_t kPipelineBytes = 8ll << 20;
+constexpr int kMaxChunks = 8;
+
+struct PipeRes {
+  cudaStream_t cin = nullptr, cout = nullptr;
+  cudaEvent_t fork = nullptr, desc = nullptr, built = nullptr, done = nullptr;
+  cudaEvent_t q_in[kMaxChunks] = {}, dec_done[kMaxChunks] = {};
+  bool ok = false;
+};
+
+// Streams and events of the current device, created on its first large
+// call (which should therefore come before any stream capture); calls that
+// enqueue concurrently from several host threads are serialised.
+static std::mutex g_pipe_mu;
+static PipeRes g_pipe[64];
+
+static cudaError_t pipe_resources(PipeRes** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  PipeRes& r = g_pipe[dev];
+  if (!r.ok) {
+    const unsigned fl = cudaEventDisableTiming;
+    if ((e = cudaStreamCreateWithFlags(&r.cin, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithFlags(&r.cout, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    cudaEvent_t* evs[] = {&r.fork, &r.desc, &r.built, &r.done};
+    for (cudaEvent_t* p : evs)
+      if ((e = cudaEventCreateWithFlags(p, fl)) != cudaSuccess) return e;
+    for (int c = 0; c < kMaxChunks; ++c) {
+      if ((e = cudaEventCreateWithFlags(&r.q_in[c], fl)) != cudaSuccess) return e;
+      if ((e = cudaEventCreateWithFlags(&r.dec_done[c], fl)) != cudaSuccess) return e;
+    }
+    r.ok = true;
+  }
+  *out = &r;
+  return cudaSuccess;
+}
+
+static sda_status build_decode_host_pipelined(
+    const int32_t* state_slot, const int32_t* swa_len, const int32_t* swa_head,
+    const int32_t* comp_indptr, const int32_t* comp_block, const int32_t* comp_slot,
+    int64_t comp_total, int win, int k_per_block, int64_t swa_pages, int64_t capacity,
+    const void* q, const void* unified_kv, const float* kv_scale, int64_t total_pages,
+    const float* attn_sink, float softmax_scale, int N, int H, int D, void* out, int32_t* status,
+    char* base, const HostWs& w, cudaStream_t st) {
+  const char* who = "sda_build_decode_host";
+  const bool fp8 = kv_scale != nullptr;
+  DeviceCaps caps;
+  cudaError_t e = device_caps(&caps);
+  if (e != cudaSuccess) {
+    note_cuda_error(e, who);
+    return SDA_ERR_CUDA;
+  }
+  LaunchPlan lp;
+  if (fp8) fp8_plan(H, D, caps, &lp);
+  else choose_plan(H, D, caps, &lp);
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  PipeRes* r = nullptr;
+  e = pipe_resources(&r);
+  const int64_t row_bytes = (int64_t)H * D * 2;  // q / out bytes per token
+  const int64_t q_bytes = (int64_t)N * row_bytes;
+  int chunks = (int)(q_bytes / kPipelineBytes);
+  chunks = chunks < 2 ? 2 : (chunks > kMaxChunks ? kMaxChunks : chunks);
+  if (chunks > N) chunks = N;
+  const int per = (N + chunks - 1) / chunks;
+  auto H2D = [&](void* dst, const void* src, size_t bytes) {
+    return bytes ? cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, r->cin) : cudaSuccess;
+  };
+  // fork: the copy streams start after everything already on the caller's stream
+  if (e == cudaSuccess) e = cudaEventRecord(r->fork, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(r->cin, r->fork, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(r->cout, r->fork, 0);
+  // descriptors, then the q chunks, on the inbound stream
+  if (e == cudaSuccess) e = H2D(base + w.ss, state_slot, (size_t)N * 4);
+  if (e == cudaSuccess) e = H2D(base + w.sl, swa_len, (size_t)N * 4);
+  if (e == cudaSuccess) e = H2D(base + w.sh, swa_head, (size_t)N * 4);
+  if (e == cudaSuccess) e = H2D(base + w.cptr, comp_indptr, (size_t)(N + 1) * 4);
+  if (e == cudaSuccess) e = H2D(base + w.cb, comp_block, (size_t)comp_total * 4);
+  if (e == cudaSuccess) e = H2D(base + w.cs, comp_slot, (size_t)comp_total * 4);
+  if (e == cudaSuccess) e = cudaEventRecord(r->desc, r->cin);
+  for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
+    const int t0 = c * per, nc = (t0 + per <= N ? per : N - t0);
+    if (nc <= 0) break;
+    e = H2D(base + w.q + (size_t)t0 * row_bytes, static_cast<const char*>(q) + (size_t)t0 * row_bytes,
+            (size_t)nc * row_bytes);
+    if (e == cudaSuccess) e = cudaEventRecord(r->q_in[c], r->cin);
+  }
+  // the whole batch's lists and status on the caller's stream
+  int32_t* idx = reinterpret_cast<int32_t*>(base + w.idx);
+  int32_t* iptr = reinterpret_cast<int32_t*>(base + w.iptr);
+  int32_t* dst_st = reinterpret_cast<int32_t*>(base + w.st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, r->desc, 0);
+  if (e == cudaSuccess)
+    e = launch_build_indices(reinterpret_cast<const int32_t*>(base + w.ss),
+                             reinterpret_cast<const int32_t*>(base + w.sl),
+                             reinterpret_cast<const int32_t*>(base + w.sh),
+                             reinterpret_cast<const int32_t*>(base + w.cptr),
+                             reinterpret_cast<const int32_t*>(base + w.cb),
+                             reinterpret_cast<const int32_t*>(base + w.cs), comp_total, N, win,
+                             k_per_block, swa_pages, total_pages, idx, capacity, iptr, dst_st, st);
+  if (e == cudaSuccess) e = cudaEventRecord(r->built, st);
+  // the status word goes back as soon as the build is done
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(r->cout, r->built, 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(status, dst_st, 4, cudaMemcpyDeviceToHost, r->cout);
+  // decode chunk after chunk; each chunk's out goes back on the outbound stream
+  void* dec = base + w.dec;
+  for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
+    const int t0 = c * per, nc = (t0 + per <= N ? per : N - t0);
+    if (nc <= 0) break;
+    const WsLayout L = workspace_layout(nc, H, D, capacity, lp);
+    const char* qc = base + w.q + (size_t)t0 * row_bytes;
+    char* oc = base + w.out + (size_t)t0 * row_bytes;
+    e = cudaStreamWaitEvent(st, r->q_in[c], 0);
+    if (e == cudaSuccess) e = launch_plan(iptr + t0, nc, capacity, lp, dec, L, st);
+    if (e == cudaSuccess) {
+      if (fp8 || lp.variant == kUmma)
+        e = launch_decode_umma(qc, unified_kv, kv_scale, total_pages, idx, attn_sink, softmax_scale,
+                               nc, H, D, oc, dec, L, lp, st);
+      else
+        e = launch_decode_simt(qc, unified_kv, idx, attn_sink, softmax_scale, nc, H, D, oc, dec,
+                               L, lp, st);
+    }
+    if (e == cudaSuccess) e = launch_combine(attn_sink, nc, H, D, oc, dec, L, caps.num_sms, st);
+    if (e == cudaSuccess) e = cudaEventRecord(r->dec_done[c], st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(r->cout, r->dec_done[c], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(static_cast<char*>(out) + (size_t)t0 * row_bytes, oc, (size_t)nc * row_bytes,
+                          cudaMemcpyDeviceToHost, r->cout);
+  }
+  // join: the caller's stream continues after every copy of this call
+  if (e == cudaSuccess) e = cudaEventRecord(r->done, r->cout);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, r->done, 0);
+  if (e == cudaSuccess) e = cudaEventRecord(r->fork, r->cin);  // the inbound stream joins too
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, r->fork, 0);
+  if (e != cudaSuccess) {
+    note_cuda_error(e, who);
+    return SDA_ERR_CUDA;
+  }
+  return SDA_OK;
+}
+
 sda_status sda_build_decode_host(const int32_t* state_slot, const int32_t* swa_len,
                                  const int32_t* swa_head, const int32_t* comp_indptr,
                                  const int32_t* comp_block, const int32_t* comp_slot,
@@ -521,9 +673,14 @@ sda_status sda_build_decode_host(const int32_t* state_slot, const int32_t* swa_l
   const HostWs w = host_ws_layout(N, H, D, comp_total, capacity, dec);
   if (workspace_bytes < w.total) return SDA_ERR_WORKSPACE;
   char* base = static_cast<char*>(workspace);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((int64_t)N * H * D * 2 >= kPipelineBytes && N >= 2)
+    return build_decode_host_pipelined(state_slot, swa_len, swa_head, comp_indptr, comp_block,
+                                       comp_slot, comp_total, win, k_per_block, swa_pages, capacity,
+                                       q, unified_kv, kv_scale, total_pages, attn_sink,
+                                       softmax_scale, N, H, D, out, status, base, w, st);
   DeviceCaps caps;
   cudaError_t e = device_caps(&caps);
-  const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t q_words = (int64_t)N * H * D / 2;
   CopySegments in = {};
   auto add = [](CopySegments& c, const void* src, void* dst, int64_t words) {
