@@ -20,10 +20,11 @@ each with the fp64 oracle (`parity_sample`).
             256 MiB read so that the written lines are back in HBM and the
             step pays for none of the flush's write-backs)
   e2e       the same metric through the public API from pinned host
-            memory: sda_build_decode_host reads q and the index descriptors
-            from page-locked host memory in a kernel, builds and decodes, and
-            writes out back the same way, replayed as one CUDA graph (other
-            paths: one packed H2D copy in, D2H copies of the result out)
+            memory: sda_build_decode_host, replayed as one CUDA graph (small
+            batches: kernels read q and the index descriptors from page-
+            locked host memory and write out back; batches with >= 8 MB of
+            q: token chunks over copy-engine streams, overlapped with the
+            decode); other paths: one packed H2D copy in, D2H copies out
   roofline  the attention kernel alone (events recorded around it by the
             library's timing hook): algorithmic bytes / time vs measured HBM
   cpu_baseline  the fp64 CPU oracle on the host cores (bounded sample)
@@ -493,7 +494,8 @@ def gpu_arm(args, w, device, ws, rank, pool=None):
     if step.path == "decode":
         # The decode step's own host-buffer call: kernels read q and the
         # builder's descriptors from page-locked host memory and write out and
-        # the status word back (sda_build_decode_host), no copy-engine transfer.
+        # the status word back (sda_build_decode_host; large batches go through
+        # its chunked copy-engine pipeline).
         hq = w.q.cpu().pin_memory()
         hd = {k: step.ins[k].cpu().pin_memory() for k in BUILDER_KEYS}
         h_out = torch.empty(w.q.shape, dtype=w.q.dtype, pin_memory=True)
