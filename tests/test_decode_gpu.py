@@ -313,3 +313,34 @@ def test_negative_and_large_softmax_scale():
     for scale in (-w.softmax_scale, 4.0 * w.softmax_scale):
         out = parity.run_gpu(w, scale=scale)
         parity.assert_parity(parity.compare(out, parity.run_oracle(w, scale=scale)), f"scale {scale}")
+
+
+@pytest.mark.parametrize("variant", ["simt", "default"])
+def test_plan_large_batch_with_tail_padding(monkeypatch, variant):
+    """13 000 tokens (more than the work plan keeps in shared memory, so its
+    token arrays live in the workspace), short ragged lists and a tail of
+    3 000 padded tokens (zero-length slices, dealt round-robin over the CTAs):
+    every token matches the oracle and every padded token is +0."""
+    _force(monkeypatch, variant)
+    rng = np.random.default_rng(31)
+    N, pad = 13000, 3000
+    lengths = list(rng.integers(0, 41, size=N - pad)) + [0] * pad
+    w = inputs.random_small(seed=31, N=N, H=16, D=512, P=1 << 16, lengths=lengths, device="cuda")
+    out = parity.run_gpu(w)
+    parity.assert_parity(parity.compare(out, parity.run_oracle(w)), f"N={N} tail padding {variant}")
+    assert not out[N - pad:].view(torch.int16).any()
+
+
+@pytest.mark.parametrize("variant", ["simt", "default"])
+def test_batch_without_slots(monkeypatch, variant):
+    """Every slice empty: the plan has no ranges, every output is +0 and no
+    error is raised."""
+    _force(monkeypatch, variant)
+    w = inputs.random_small(seed=32, N=300, H=64, D=512, P=4096, lengths=[0] * 300, device="cuda")
+    idx, ptr = parity.to_dev(w)
+    ws = torch.empty(sda.workspace_size(w.N, w.H, w.D, 0), dtype=torch.uint8, device="cuda")
+    out = torch.full_like(w.q, 7.0)
+    sda.decode(w.q, w.unified_kv, idx, ptr, w.attn_sink, w.softmax_scale, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    assert not out.view(torch.int16).any()
+    assert sda.decode_error_flag(ws) == 0
