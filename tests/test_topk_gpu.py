@@ -194,3 +194,20 @@ def test_topk_large_batches(N, S):
     got, ref = run_both(torch.from_numpy(scores).cuda(), torch.from_numpy(lens).cuda(),
                         torch.from_numpy(bt).cuda(), 9, kpb)
     assert_equal(got, ref, f"N={N} S={S}")
+
+
+@pytest.mark.parametrize("N,S", [(100, 3000), (150, 12000), (76, 700)])
+def test_topk_mid_size_batches(N, S):
+    """Mid-size batches with special values and ties, rows staged in shared
+    memory and rows read from L2, lengths from 0 to the whole row, k from 1
+    to past most lengths."""
+    rng = np.random.default_rng(N * 7 + S)
+    scores = special_scores(rng, N, S)
+    lens = rng.integers(0, S + 1, N).astype(np.int32)
+    lens[:4] = [0, 1, 40, S]
+    kpb = 16
+    bt = rng.integers(0, 10**5, (N, -(-S // kpb))).astype(np.int32)
+    for k in (1, 40, 1000):
+        got, ref = run_both(torch.from_numpy(scores).cuda(), torch.from_numpy(lens).cuda(),
+                            torch.from_numpy(bt).cuda(), k, kpb)
+        assert_equal(got, ref, f"N={N} S={S} k={k}")
