@@ -168,7 +168,8 @@ sda_status sda_decode_noalloc(const void* q, const void* unified_kv, int64_t tot
 /*
  * Which attention kernel sda_decode launches for (H, D) on the current
  * device: *kernel = SDA_KERNEL_SIMT (CUDA cores, any supported shape) or
- * SDA_KERNEL_ONE_CTA (tensor cores, one CTA per unit; D = 512 and H in
+ * SDA_KERNEL_ONE_CTA (tensor cores, one persistent CTA per SM, each owning an
+ * equal share of the batch's KV tiles; D = 512 and H in
  * {16, 32} or a multiple of 64, the default there).  The environment
  * variable SDA_FORCE_VARIANT=simt|umma overrides the choice where the shape
  * allows (for testing).  Errors: SDA_ERR_INVALID_ARG (kernel
