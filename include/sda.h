@@ -290,9 +290,11 @@ sda_status sda_build_decode(const int32_t* state_slot, const int32_t* swa_len,
  * and each chunk's out goes back on a library-owned outbound stream as soon
  * as its decode is done, so both link directions and the SMs work at once.
  * `stream` forks to those two streams at the start of the call and joins
- * them at its end (graph-capturable; the first such call on a device creates
- * the two streams and their events, so make it before any capture; calls
- * from several host threads are serialised while they enqueue).  Each chunk
+ * them at its end (graph-capturable; the two streams and their events are
+ * created on the device by the first sda_build_decode_host_workspace_size
+ * query or call for such a batch, which must therefore come before any
+ * capture; calls from several host threads are serialised while they
+ * enqueue).  Each chunk
  * has its own work plan, so the result can differ from the one-call path in
  * the last bf16 bit (both are within the decode's tolerance); status is the
  * whole batch's, as in sda_build_decode.  Asynchronous: the host

@@ -471,17 +471,6 @@ static sda_status build_decode_ws(int N, int H, int D, int64_t capacity, bool fp
   return SDA_OK;
 }
 
-sda_status sda_build_decode_host_workspace_size(int N, int H, int D, int64_t comp_total,
-                                                int64_t capacity, int fp8, size_t* bytes) {
-  if (!bytes || N < 0 || comp_total < 0 || capacity < 0) return SDA_ERR_INVALID_ARG;
-  if (fp8 ? !tc_shape_supported(H, D) : !shape_supported(H, D)) return SDA_ERR_UNSUPPORTED;
-  size_t dec = 0;
-  const sda_status r = build_decode_ws(N, H, D, capacity, fp8 != 0, &dec);
-  if (r != SDA_OK) return r;
-  *bytes = host_ws_layout(N, H, D, comp_total, capacity, dec).total;
-  return SDA_OK;
-}
-
 // ---------------------------------------------------------------- large host batches
 // A batch whose q (and out) is at least kPipelineBytes moves through the
 // host link in token chunks so that the link's two directions and the SMs
@@ -515,17 +504,27 @@ static cudaError_t pipe_resources(PipeRes** out) {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   PipeRes& r = g_pipe[dev];
   if (!r.ok) {
+    // all or nothing: a failure destroys whatever this attempt created
+    PipeRes n;
     const unsigned fl = cudaEventDisableTiming;
-    if ((e = cudaStreamCreateWithFlags(&r.cin, cudaStreamNonBlocking)) != cudaSuccess) return e;
-    if ((e = cudaStreamCreateWithFlags(&r.cout, cudaStreamNonBlocking)) != cudaSuccess) return e;
-    cudaEvent_t* evs[] = {&r.fork, &r.desc, &r.built, &r.done};
-    for (cudaEvent_t* p : evs)
-      if ((e = cudaEventCreateWithFlags(p, fl)) != cudaSuccess) return e;
+    cudaEvent_t* evs[4 + 2 * kMaxChunks] = {&n.fork, &n.desc, &n.built, &n.done};
     for (int c = 0; c < kMaxChunks; ++c) {
-      if ((e = cudaEventCreateWithFlags(&r.q_in[c], fl)) != cudaSuccess) return e;
-      if ((e = cudaEventCreateWithFlags(&r.dec_done[c], fl)) != cudaSuccess) return e;
+      evs[4 + 2 * c] = &n.q_in[c];
+      evs[5 + 2 * c] = &n.dec_done[c];
     }
-    r.ok = true;
+    e = cudaStreamCreateWithFlags(&n.cin, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&n.cout, cudaStreamNonBlocking);
+    for (cudaEvent_t* p : evs)
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(p, fl);
+    if (e != cudaSuccess) {
+      for (cudaEvent_t* p : evs)
+        if (*p) cudaEventDestroy(*p);
+      if (n.cin) cudaStreamDestroy(n.cin);
+      if (n.cout) cudaStreamDestroy(n.cout);
+      return e;
+    }
+    n.ok = true;
+    r = n;
   }
   *out = &r;
   return cudaSuccess;
@@ -630,6 +629,28 @@ static sda_status build_decode_host_pipelined(
   if (e != cudaSuccess) {
     note_cuda_error(e, who);
     return SDA_ERR_CUDA;
+  }
+  return SDA_OK;
+}
+
+sda_status sda_build_decode_host_workspace_size(int N, int H, int D, int64_t comp_total,
+                                                int64_t capacity, int fp8, size_t* bytes) {
+  if (!bytes || N < 0 || comp_total < 0 || capacity < 0) return SDA_ERR_INVALID_ARG;
+  if (fp8 ? !tc_shape_supported(H, D) : !shape_supported(H, D)) return SDA_ERR_UNSUPPORTED;
+  size_t dec = 0;
+  const sda_status r = build_decode_ws(N, H, D, capacity, fp8 != 0, &dec);
+  if (r != SDA_OK) return r;
+  *bytes = host_ws_layout(N, H, D, comp_total, capacity, dec).total;
+  if ((int64_t)N * H * D * 2 >= kPipelineBytes && N >= 2) {
+    // a large batch takes the chunked route: create this device's copy
+    // streams now, so that the first call can already be captured
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    PipeRes* res = nullptr;
+    const cudaError_t e = pipe_resources(&res);
+    if (e != cudaSuccess) {
+      note_cuda_error(e, "sda_build_decode_host_workspace_size");
+      return SDA_ERR_CUDA;
+    }
   }
   return SDA_OK;
 }
