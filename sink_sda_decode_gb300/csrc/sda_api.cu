@@ -41,6 +41,8 @@ struct DeviceInfo {
 };
 DeviceInfo g_dev[kMaxDevices];
 
+}  // namespace
+
 // SM count of the current device, queried once per device; also sets the
 // tensor-core kernels' shared-memory attributes on that device.
 cudaError_t device_caps(DeviceCaps* caps) {
@@ -57,6 +59,8 @@ cudaError_t device_caps(DeviceCaps* caps) {
   *caps = d.caps;
   return d.err;
 }
+
+namespace {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -371,12 +375,14 @@ static sda_status build_decode_impl(const int32_t* state_slot, const int32_t* sw
   else choose_plan(H, D, caps, &lp);
   const WsLayout L = workspace_layout(N, H, D, capacity, lp);
   if (workspace_bytes < L.total) return SDA_ERR_WORKSPACE;
-  e = launch_build_len(state_slot, swa_len, swa_head, comp_indptr, comp_block, comp_slot,
-                       comp_total, N, win, k_per_block, swa_pages, total_pages, kv_indptr, st);
-  if (e == cudaSuccess) e = launch_scan_plan(N, capacity, kv_indptr, status, lp, workspace, L, st);
+  const EntryCheck ec = entry_check_layout(state_slot, comp_indptr, comp_block, comp_slot,
+                                           comp_total, N, k_per_block, swa_pages, total_pages,
+                                           capacity, kv_indices, status, caps.num_sms);
+  e = launch_build_len(swa_len, swa_head, N, win, kv_indptr, ec, st);
+  if (e == cudaSuccess) e = launch_scan_plan(N, capacity, kv_indptr, status, ec, lp, workspace, L, st);
   if (e == cudaSuccess)
     e = launch_build_scatter(state_slot, swa_len, swa_head, comp_indptr, comp_block, comp_slot, N,
-                             win, k_per_block, swa_pages, kv_indptr, kv_indices, st);
+                             win, k_per_block, swa_pages, capacity, kv_indptr, kv_indices, st);
   if (e == cudaSuccess && g_ev_before && g_ev_after) e = cudaEventRecord(g_ev_before, st);
   if (e == cudaSuccess) {
     if (fp8)

@@ -73,6 +73,8 @@ struct WsLayout {
 struct DeviceCaps {
   int num_sms = 0;
 };
+// The current device's capabilities (queried once per device).
+cudaError_t device_caps(DeviceCaps* caps);
 
 // Picks the kernel variant and grid for (H, D) on a device.  Returns false
 // if (H, D) is unsupported.
@@ -89,8 +91,31 @@ WsLayout workspace_layout(int N, int H, int D, int64_t total_indices, const Laun
 cudaError_t launch_plan(const int32_t* kv_indptr, int N, int64_t total_indices,
                         const LaunchPlan& lp, void* ws, const WsLayout& L, cudaStream_t st);
 // The builder's scan and the work plan in one CTA (sda_build_decode).
+// Where the length pass left its findings on the compressed entries.  That
+// pass checks the entry array in equal slices of chunks_per_cta 4-entry
+// chunks, one slice per CTA, without knowing which token an entry belongs
+// to, and writes flags[b] != 0 if slice b holds a bad entry; the tokens'
+// lengths it writes assume good entries.  The scan then re-checks, entry by
+// entry, every token whose entries overlap a flagged slice.
+struct EntryCheck {
+  const int32_t* state_slot;
+  const int32_t* comp_indptr;
+  const int32_t* comp_block;
+  const int32_t* comp_slot;
+  int64_t comp_total;
+  int k_per_block;
+  int64_t swa_pages;
+  int64_t total_pages;
+  const int32_t* flags;  // [n_flags]
+  int n_flags;
+  int64_t chunks_per_cta;
+};
+
+// The index builder's scan (with the entry re-check) and the work plan in
+// one CTA.
 cudaError_t launch_scan_plan(int N, int64_t capacity, int32_t* kv_indptr, int32_t* status,
-                             const LaunchPlan& lp, void* ws, const WsLayout& L, cudaStream_t st);
+                             const EntryCheck& ec, const LaunchPlan& lp, void* ws,
+                             const WsLayout& L, cudaStream_t st);
 cudaError_t launch_combine(const float* attn_sink, int N, int H, int D, void* out, void* ws,
                            const WsLayout& L, int num_sms, cudaStream_t st);
 cudaError_t launch_decode_simt(const void* q, const void* kv, const int32_t* kv_indices,
@@ -121,19 +146,23 @@ cudaError_t launch_build_indices(const int32_t* state_slot, const int32_t* swa_l
                                  int64_t swa_pages, int64_t total_pages, int32_t* kv_indices,
                                  int64_t capacity, int32_t* kv_indptr, int32_t* status,
                                  cudaStream_t st);
+
+// The layout of the length pass's entry check: its grid (one flag per CTA),
+// its slices, and where the flags go (kv_indices, or the status word).
+EntryCheck entry_check_layout(const int32_t* state_slot, const int32_t* comp_indptr,
+                              const int32_t* comp_block, const int32_t* comp_slot,
+                              int64_t comp_total, int N, int k_per_block, int64_t swa_pages,
+                              int64_t total_pages, int64_t capacity, int32_t* kv_indices,
+                              int32_t* status, int num_sms);
 // The index builder as separate launches, for callers that put another
-// kernel between its scan and its scatter: per-token lengths, then (after
-// the scan) the scatter.
-cudaError_t launch_build_len(const int32_t* state_slot, const int32_t* swa_len,
-                             const int32_t* swa_head, const int32_t* comp_indptr,
-                             const int32_t* comp_block, const int32_t* comp_slot,
-                             int64_t comp_total, int N, int win, int k_per_block,
-                             int64_t swa_pages, int64_t total_pages, int32_t* kv_indptr,
-                             cudaStream_t st);
+// kernel between its scan and its scatter: lengths and the entry check, then
+// (after the scan, which takes the same EntryCheck) the scatter.
+cudaError_t launch_build_len(const int32_t* swa_len, const int32_t* swa_head, int N, int win,
+                             int32_t* kv_indptr, const EntryCheck& ec, cudaStream_t st);
 cudaError_t launch_build_scatter(const int32_t* state_slot, const int32_t* swa_len,
                                  const int32_t* swa_head, const int32_t* comp_indptr,
                                  const int32_t* comp_block, const int32_t* comp_slot, int N,
-                                 int win, int k_per_block, int64_t swa_pages,
+                                 int win, int k_per_block, int64_t swa_pages, int64_t capacity,
                                  const int32_t* kv_indptr, int32_t* kv_indices, cudaStream_t st);
 cudaError_t launch_validate(const int32_t* kv_indices, int64_t total_indices,
                             const int32_t* kv_indptr, int N, int64_t total_pages,

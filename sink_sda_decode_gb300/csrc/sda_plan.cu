@@ -88,7 +88,8 @@ __device__ __forceinline__ void plan_body(const int32_t* __restrict__ indptr, in
                                           long long total_indices, int hg, int grid, int tile,
                                           WsHeader* __restrict__ hdr, int4* __restrict__ units,
                                           int4* __restrict__ splits, int* __restrict__ cta_start,
-                                          int* __restrict__ ctok, int* __restrict__ ctp) {
+                                          int* __restrict__ ctok, int* __restrict__ ctp,
+                                          bool check_indptr) {
   __shared__ int warp_sums[32];
   __shared__ int s_total[2];
   __shared__ int sB[kMaxPlanGrid + 1];      // range boundaries (tiles)
@@ -98,9 +99,10 @@ __device__ __forceinline__ void plan_body(const int32_t* __restrict__ indptr, in
 
   // kv_indptr must be a true prefix sum inside [0, total_indices]; otherwise
   // nothing is planned (out is left unwritten) and the error word reads 2, so
-  // that no kernel ever reads kv_indices out of bounds.
+  // that no kernel ever reads kv_indices out of bounds.  (A prefix sum the
+  // builder's scan just wrote in this CTA is one by construction.)
   int bad = 0;
-  for (int t = threadIdx.x; t <= N; t += kPlanThreads) {
+  for (int t = threadIdx.x; check_indptr && t <= N; t += kPlanThreads) {
     const int v = indptr[t];
     if (v < 0 || (long long)v > total_indices || (t < N && indptr[t + 1] < v)) bad = 1;
   }
@@ -264,7 +266,7 @@ plan_kernel(const int32_t* __restrict__ indptr, int N, long long total_indices, 
   pdl_wait();
   pdl_trigger();
   plan_token_arrays(N, ctok, ctp);
-  plan_body(indptr, N, total_indices, hg, grid, tile, hdr, units, splits, cta_start, ctok, ctp);
+  plan_body(indptr, N, total_indices, hg, grid, tile, hdr, units, splits, cta_start, ctok, ctp, true);
 }
 
 // The index builder's scan and the plan in one CTA (sda_build_decode): the
@@ -273,16 +275,16 @@ plan_kernel(const int32_t* __restrict__ indptr, int N, long long total_indices, 
 static_assert(kPlanThreads == kScanThreads, "one CTA runs both bodies");
 __global__ void __launch_bounds__(kPlanThreads)
 scan_plan_kernel(int N, int64_t capacity, int32_t* __restrict__ kv_indptr,
-                 int32_t* __restrict__ status, int hg, int grid, int tile,
+                 int32_t* __restrict__ status, EntryCheck ec, int hg, int grid, int tile,
                  WsHeader* __restrict__ hdr, int4* __restrict__ units, int4* __restrict__ splits,
                  int* __restrict__ cta_start, int* ctok, int* ctp) {
   pdl_wait();
   pdl_trigger();
-  build_scan_body(N, capacity, kv_indptr, status);
+  build_scan_body(N, capacity, kv_indptr, status, ec);
   __syncthreads();  // kv_indptr is final (this CTA wrote it)
   plan_token_arrays(N, ctok, ctp);
   plan_body(kv_indptr, N, (long long)capacity, hg, grid, tile, hdr, units, splits, cta_start, ctok,
-            ctp);
+            ctp, false);
 }
 
 // Merge the pieces of each split token:
@@ -294,7 +296,9 @@ scan_plan_kernel(int N, int64_t capacity, int32_t* __restrict__ kv_indptr,
 // One warp per (split token, head): lane k loads (m_k, l_k) of piece k, the
 // maxima and denominator are warp reductions, then every lane accumulates
 // 16 values of D (D = 512; 4 x 16-byte loads per piece, independent across
-// pieces) and stores them as bf16.  Warps past the actual number of split
+// pieces) and stores them as bf16.  The split entry is read together with
+// the header, and the first two pieces' values together with the (m, l)
+// pairs, so a warp waits on two memory round trips.  Warps past the actual number of split
 // tokens exit at once (the grid is sized for the worst case so that it can
 // be captured in a CUDA graph).
 constexpr int kCombineWarps = 8;
@@ -302,7 +306,7 @@ constexpr int kCombineWarps = 8;
 template <int D>
 __global__ void __launch_bounds__(kCombineWarps * 32)
 combine_kernel(const float* __restrict__ attn_sink, int H, __nv_bfloat16* __restrict__ out,
-               const WsHeader* __restrict__ hdr, const int4* __restrict__ splits,
+               const WsHeader* __restrict__ hdr, const int4* __restrict__ splits, int s_cap,
                const float2* __restrict__ part_ml, const float* __restrict__ part_o) {
   // lane l owns the 4-value groups at d = 4l + 128g (16 values for D = 512;
   // for D = 64 only lanes 0..15 hold a group)
@@ -311,20 +315,36 @@ combine_kernel(const float* __restrict__ attn_sink, int H, __nv_bfloat16* __rest
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int item = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
-  if (item >= hdr->n_split * H) return;
   const int si = item / H, h = item % H;
-  const int4 sp = splits[si];
-  const int t = sp.x, row0 = sp.y, np = sp.z;
+  const int n_split = hdr->n_split;
+  const int4 sp = splits[si < s_cap ? si : 0];  // read together with the header
+  if (item >= n_split * H) return;
+  const int t = sp.x, row0 = sp.y, np = sp.z;  // np >= 2
   const float ms = attn_sink[h] * kLog2e;
+  const int d0 = lane * 4;  // this lane's 4-value groups at d0 + 128*g
+  const bool holds = D >= 128 || d0 < D;
+  // the pieces' (m, l) (lane k: piece k) and the first two pieces' partial
+  // outputs, all in flight together
+  const float2 ml0 = lane < np ? part_ml[(size_t)(row0 + lane) * H + h] : make_float2(-INFINITY, 0.f);
+  float4 v0[kGroups], v1[kGroups];
+  {
+    const float* o0 = part_o + ((size_t)row0 * H + h) * D + d0;
+    const float* o1 = part_o + ((size_t)(row0 + 1) * H + h) * D + d0;
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) {
+      v0[g] = holds ? *reinterpret_cast<const float4*>(o0 + 128 * g) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v1[g] = holds ? *reinterpret_cast<const float4*>(o1 + 128 * g) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
   // maxima and denominator over the pieces (lanes stride over them)
-  float mk = -INFINITY;
-  for (int k = lane; k < np; k += 32) mk = fmaxf(mk, part_ml[(size_t)(row0 + k) * H + h].x);
+  float mk = ml0.x;
+  for (int k = lane + 32; k < np; k += 32) mk = fmaxf(mk, part_ml[(size_t)(row0 + k) * H + h].x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, o));
   const float M = fmaxf(ms, mk);
   const bool dead = (ms == INFINITY) || (M == -INFINITY);
-  float den = 0.f;
-  for (int k = lane; k < np; k += 32) {
+  float den = (dead || lane >= np) ? 0.f : ml0.y * ex2_approx(ml0.x - M);
+  for (int k = lane + 32; k < np; k += 32) {
     const float2 ml = part_ml[(size_t)(row0 + k) * H + h];
     den += dead ? 0.f : ml.y * ex2_approx(ml.x - M);
   }
@@ -335,19 +355,34 @@ combine_kernel(const float* __restrict__ attn_sink, int H, __nv_bfloat16* __rest
 #pragma unroll
   for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
   if (!dead) {
-    const int d0 = lane * 4;  // this lane's 4-value groups at d0 + 128*j
     for (int k0 = 0; k0 < np; k0 += 32) {
       // weight of piece k0 + j lives in lane j
       const int kk = k0 + lane;
-      const float wl = kk < np ? ex2_approx(part_ml[(size_t)(row0 + kk) * H + h].x - M) : 0.f;
+      const float wl = kk < np ? ex2_approx((k0 == 0 ? ml0.x : part_ml[(size_t)(row0 + kk) * H + h].x) - M) : 0.f;
       const int nk = min(32, np - k0);
+      int j = 0;
+      if (k0 == 0) {  // the two pieces already loaded
+#pragma unroll
+        for (int p2 = 0; p2 < 2; ++p2) {
+          const float wk = __shfl_sync(0xffffffffu, wl, p2);
+#pragma unroll
+          for (int g = 0; g < kGroups; ++g) {
+            const float4 v = p2 ? v1[g] : v0[g];
+            acc[4 * g + 0] += wk * v.x;
+            acc[4 * g + 1] += wk * v.y;
+            acc[4 * g + 2] += wk * v.z;
+            acc[4 * g + 3] += wk * v.w;
+          }
+        }
+        j = 2;
+      }
 #pragma unroll 4
-      for (int j = 0; j < nk; ++j) {
+      for (; j < nk; ++j) {
         const float wk = __shfl_sync(0xffffffffu, wl, j);
         const float* o = part_o + ((size_t)(row0 + k0 + j) * H + h) * D + d0;
 #pragma unroll
         for (int g = 0; g < kGroups; ++g) {
-          if (D < 128 && d0 >= D) break;
+          if (!holds) break;
           const float4 v = *reinterpret_cast<const float4*>(o + 128 * g);
           acc[4 * g + 0] += wk * v.x;
           acc[4 * g + 1] += wk * v.y;
@@ -390,13 +425,14 @@ cudaError_t launch_plan(const int32_t* kv_indptr, int N, int64_t total_indices,
 }
 
 cudaError_t launch_scan_plan(int N, int64_t capacity, int32_t* kv_indptr, int32_t* status,
-                             const LaunchPlan& lp, void* ws, const WsLayout& L, cudaStream_t st) {
+                             const EntryCheck& ec, const LaunchPlan& lp, void* ws,
+                             const WsLayout& L, cudaStream_t st) {
   char* base = static_cast<char*>(ws);
   static const cudaError_t attr = cudaFuncSetAttribute(
       scan_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_dyn_smem(kPlanSmemTokens));
   if (attr != cudaSuccess) return attr;
   return launch_pdl(scan_plan_kernel, dim3(1), dim3(kPlanThreads), plan_dyn_smem(N), st, N, capacity, kv_indptr,
-                    status, lp.hg, lp.grid, lp.tile,
+                    status, ec, lp.hg, lp.grid, lp.tile,
                     reinterpret_cast<WsHeader*>(base),
                     reinterpret_cast<int4*>(base + L.units_off),
                     reinterpret_cast<int4*>(base + L.split_off),
@@ -415,7 +451,7 @@ cudaError_t launch_combine(const float* attn_sink, int N, int H, int D, void* ou
   auto args = [&](auto kernel) {
     return launch_pdl(kernel, dim3(blocks), dim3(kCombineWarps * 32), 0, st, attn_sink, H,
                       static_cast<__nv_bfloat16*>(out), reinterpret_cast<const WsHeader*>(base),
-                      reinterpret_cast<const int4*>(base + L.split_off),
+                      reinterpret_cast<const int4*>(base + L.split_off), L.s_max,
                       reinterpret_cast<const float2*>(base + L.ml_off),
                       reinterpret_cast<const float*>(base + L.o_off));
   };
