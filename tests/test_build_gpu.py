@@ -124,3 +124,98 @@ def test_validate_matches_oracle():
             ptr[-1] = n + 4
         st = sda.validate_indices(dev(idx), dev(ptr), 997).cpu().numpy()
         assert tuple(int(x) for x in st) == oracle.validate_indices(idx, ptr, 997)
+
+
+def check_against_oracle(args, capacity=None, offset=0):
+    """GPU build of `args` (capacity as given) against the oracle.  offset > 0
+    passes comp_block / comp_slot as views that start `offset` entries into
+    larger arrays, so that their addresses are not 16-byte aligned."""
+    ss, sl, sh, cp, cb, cs, win, kpb, swa_pages, total_pages = args
+    cbd, csd = dev(np.concatenate([np.zeros(offset, np.int32), cb])), \
+        dev(np.concatenate([np.zeros(offset, np.int32), cs]))
+    idx, ptr, st = sda.build_indices(dev(ss), dev(sl), dev(sh), dev(cp), cbd[offset:], csd[offset:],
+                                     win=win, k_per_block=kpb, swa_pages=swa_pages,
+                                     total_pages=total_pages, capacity=capacity)
+    ptr_h = ptr.cpu().numpy()
+    o_idx, o_ptr, o_st = oracle.build_indices(*args, capacity=capacity)
+    assert int(st.item()) == o_st
+    assert np.array_equal(ptr_h, o_ptr)
+    assert np.array_equal(idx.cpu().numpy()[:ptr_h[-1]], o_idx)
+    return o_st
+
+
+def test_entry_check_overlapping_and_stray_entries():
+    """The length pass checks the entry array in slices without knowing the
+    tokens, and the scan re-checks the tokens that overlap a flagged slice.
+    With a non-monotone comp_indptr, token ranges overlap: an entry listed
+    by two tokens marks both, an entry listed only by a token whose range is
+    bad (bit 4) or by a padded token marks none, nor does one that no token
+    lists."""
+    win, kpb, n_blocks = 8, 4, 50
+    swa_pages = 4 * win
+    total_pages = swa_pages + n_blocks * kpb
+    n_entries = 20003  # not a multiple of 4: the last chunk runs past the arrays' end
+    rng = np.random.default_rng(11)
+    cb = rng.integers(0, n_blocks, n_entries).astype(np.int32)
+    cs = rng.integers(0, kpb, n_entries).astype(np.int32)
+    # token 0 [0, 9000); token 1 [9000, 3000): bit 4; token 2 [3000, 5000)
+    # and token 3 [5000, 15000), both inside token 0's range in part;
+    # token 4 padded over [15000, 20000); token 5 [20000, 15000): bit 4;
+    # entries [20000, 20003) belong to no token
+    ss = np.array([0, 1, 2, 3, -1, 0], np.int32)
+    sl = np.array([2, 0, 3, 1, 0, 0], np.int32)
+    sh = np.array([1, 0, 5, 7, 0, 0], np.int32)
+    cp = np.array([0, 9000, 3000, 5000, 15000, 20000, 15000], np.int32)
+    cap = 40000  # overlapping ranges list some entries twice
+    assert check_against_oracle((ss, sl, sh, cp, cb, cs, win, kpb, swa_pages, total_pages), cap) == 4
+    cases = {  # entry -> the bit it raises
+        "listed by tokens 0 and 3": (6000, 8),
+        "listed by tokens 0 and 2": (4000, 16),
+        "listed by token 0 (and the bad-range token 1)": (8999, 8),
+        "listed only by the padded token 4": (17000, 8),
+        "listed by no token": (20001, 16),
+    }
+    for what, (e, bit) in cases.items():
+        cb2, cs2 = cb.copy(), cs.copy()
+        if bit == 16:
+            cb2[e] = n_blocks + 3
+        else:
+            cs2[e] = kpb
+        st = check_against_oracle((ss, sl, sh, cp, cb2, cs2, win, kpb, swa_pages, total_pages), cap)
+        assert st & 4 and not st & 32, what
+    # every entry bad: every token with a good range and a real slot is marked
+    check_against_oracle((ss, sl, sh, cp, np.full_like(cb, -1), cs, win, kpb, swa_pages, total_pages),
+                         cap)
+
+
+@pytest.mark.parametrize("offset", [0, 1, 3])
+@pytest.mark.parametrize("capacity", ["auto", 0, 5, 2000])
+def test_entry_check_alignment_and_capacity(offset, capacity):
+    """Entry arrays that are not 16-byte aligned (checked one entry per
+    load), and capacities that leave the flags little room or none (0: the
+    single flag goes through the status word)."""
+    rng = np.random.default_rng(offset * 31 + (7 if capacity == "auto" else capacity))
+    args = random_descriptors(rng, 400, win=16, kpb=8, n_states=200, n_blocks=3000, max_comp=900)
+    cap = None if capacity == "auto" else capacity
+    check_against_oracle(args, capacity=cap, offset=offset)
+
+
+@pytest.mark.parametrize("N", [305, 2000])
+def test_long_lists_flat_scatter(N):
+    """Batches above one wave of one-token CTAs take the scatter that is flat
+    over the packed output: a 65 536-entry list among short ones, lists that
+    end inside a thread's four outputs, empty and padded tokens between."""
+    rng = np.random.default_rng(N)
+    ss, sl, sh, cp, cb, cs, win, kpb, swa_pages, total_pages = random_descriptors(
+        rng, N, win=16, kpb=8, n_states=N, n_blocks=20000, bad=False, max_comp=7)
+    lens = np.diff(cp.astype(np.int64))
+    lens[N // 3] = 65536
+    lens[N // 2] = 0
+    ss[N // 2 + 1] = -1
+    cp = np.zeros(N + 1, np.int64)
+    cp[1:] = np.cumsum(lens)
+    cb = rng.integers(0, 20000, cp[-1]).astype(np.int32)
+    cs = rng.integers(0, kpb, cp[-1]).astype(np.int32)
+    st = check_against_oracle((ss, sl, sh, cp.astype(np.int32), cb, cs, win, kpb, swa_pages,
+                               total_pages))
+    assert st == 0
