@@ -13,6 +13,7 @@
 
 #include "sda_copy.cuh"
 #include "sda_internal.cuh"
+#include "sda_scatter.cuh"
 
 namespace sda {
 
@@ -379,10 +380,12 @@ static sda_status build_decode_impl(const int32_t* state_slot, const int32_t* sw
                                            comp_total, N, k_per_block, swa_pages, total_pages,
                                            capacity, kv_indices, status, caps.num_sms);
   e = launch_build_len(swa_len, swa_head, N, win, kv_indptr, ec, st);
-  if (e == cudaSuccess) e = launch_scan_plan(N, capacity, kv_indptr, status, ec, lp, workspace, L, st);
-  if (e == cudaSuccess)
-    e = launch_build_scatter(state_slot, swa_len, swa_head, comp_indptr, comp_block, comp_slot, N,
-                             win, k_per_block, swa_pages, capacity, kv_indptr, kv_indices, st);
+  if (e == cudaSuccess) e = launch_build_scan(N, capacity, kv_indptr, status, ec, st);
+  if (e == cudaSuccess) {
+    const ScatterArgs sa{state_slot, swa_len, swa_head, comp_indptr, comp_block, comp_slot, N, win,
+                         k_per_block, swa_pages, kv_indptr, kv_indices};
+    e = launch_scatter_plan(sa, capacity, lp, workspace, L, caps.num_sms, st);
+  }
   if (e == cudaSuccess && g_ev_before && g_ev_after) e = cudaEventRecord(g_ev_before, st);
   if (e == cudaSuccess) {
     if (fp8)

@@ -13,6 +13,7 @@
 // k_per_block are checked on the host and every emitted slot is in range).
 #include "sda_internal.cuh"
 #include "sda_scan.cuh"
+#include "sda_scatter.cuh"
 
 namespace sda {
 
@@ -105,119 +106,21 @@ build_scan_kernel(int N, int64_t capacity, int32_t* __restrict__ kv_indptr,
   build_scan_body(N, capacity, kv_indptr, status, ec);
 }
 
-// Scatter pass for batches that fit one wave of CTAs: one CTA per token
-// writes its slots at kv_indices[kv_indptr[t] ...]; the token's fields are
-// loaded together with its slice bounds (two dependent round trips before
-// the compressed entries).
-constexpr int kTokThreads = 1024;
+// Scatter pass (bodies in sda_scatter.cuh): one-token CTAs for a batch that
+// fits one wave of them, else flat over the packed output.
+constexpr int kScatterThreads = 256;
 
-__global__ void __launch_bounds__(kTokThreads)
-build_scatter_tok_kernel(const int32_t* __restrict__ state_slot, const int32_t* __restrict__ swa_len,
-                         const int32_t* __restrict__ swa_head, const int32_t* __restrict__ comp_indptr,
-                         const int32_t* __restrict__ comp_block, const int32_t* __restrict__ comp_slot,
-                         int N, int win, int k_per_block, int64_t swa_pages,
-                         const int32_t* __restrict__ kv_indptr, int32_t* __restrict__ kv_indices) {
+__global__ void __launch_bounds__(kTokThreads) build_scatter_tok_kernel(ScatterArgs a) {
   pdl_wait();
   pdl_trigger();
-  for (int t = blockIdx.x; t < N; t += gridDim.x) {
-    const int32_t o0 = kv_indptr[t], o1 = kv_indptr[t + 1];
-    const int32_t ss = state_slot[t], n_swa = swa_len[t], head = swa_head[t], c0 = comp_indptr[t];
-    if (o1 <= o0) continue;  // padded, bad or over capacity (uniform)
-    const int32_t ns = n_swa > 0 ? n_swa : 0;
-    for (int32_t j = threadIdx.x; j < ns; j += kTokThreads) {
-      int32_t ring = (int32_t)(((int64_t)head - n_swa + 1 + j) % win);
-      if (ring < 0) ring += win;
-      kv_indices[o0 + j] = (int32_t)((int64_t)ss * win + ring);
-    }
-    const int32_t nc = o1 - o0 - ns;
-#pragma unroll 8
-    for (int32_t i = threadIdx.x; i < nc; i += kTokThreads)
-      kv_indices[o0 + ns + i] =
-          (int32_t)(swa_pages + (int64_t)comp_block[c0 + i] * k_per_block + comp_slot[c0 + i]);
-  }
+  scatter_tok_body(a, blockIdx.x, gridDim.x);
 }
 
-// Scatter pass for larger batches, flat over the packed output: thread i writes the outputs
-// [4i, 4i + 4) (grid-stride), finding the token of the first by a binary
-// search in kv_indptr (staged in shared memory for batches of up to
-// kScatterSmemTokens tokens) and walking on from there.  Every token's list
-// is spread over as many threads as it has outputs / 4, however long it is.
-constexpr int kScatterThreads = 256;
-constexpr int kScatterPer = 4;
-constexpr int kScatterSmemTokens = 8191;
-
-__global__ void __launch_bounds__(kScatterThreads)
-build_scatter_kernel(const int32_t* __restrict__ state_slot, const int32_t* __restrict__ swa_len,
-                     const int32_t* __restrict__ swa_head, const int32_t* __restrict__ comp_indptr,
-                     const int32_t* __restrict__ comp_block, const int32_t* __restrict__ comp_slot,
-                     int N, int win, int k_per_block, int64_t swa_pages,
-                     const int32_t* __restrict__ kv_indptr, int32_t* __restrict__ kv_indices) {
+__global__ void __launch_bounds__(kScatterThreads) build_scatter_kernel(ScatterArgs a) {
   extern __shared__ int32_t s_ptr[];
   pdl_wait();
   pdl_trigger();
-  const bool staged = N <= kScatterSmemTokens;
-  if (staged) {  // (uniform)
-    for (int i = threadIdx.x; i <= N; i += kScatterThreads) s_ptr[i] = kv_indptr[i];
-    __syncthreads();
-  }
-  const int32_t* ptr = staged ? s_ptr : kv_indptr;
-  const int32_t total = ptr[N];  // 0 when the lists were emptied (over capacity)
-  const int64_t first = (int64_t)blockIdx.x * kScatterThreads * kScatterPer;
-  if (first >= total) return;  // the whole CTA: uniform
-  const int64_t stride = (int64_t)gridDim.x * kScatterThreads * kScatterPer;
-  for (int64_t o0 = first + (int64_t)threadIdx.x * kScatterPer; o0 < total; o0 += stride) {
-    // token of each output: a binary search for the first (last t with
-    // ptr[t] <= o0; ptr is non-decreasing, ptr[0] = 0 <= o0 < ptr[N]), then
-    // a walk past the next list ends
-    int lo = 0, hi = N - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (ptr[mid] <= o0) lo = mid;
-      else hi = mid - 1;
-    }
-    int tk[kScatterPer];
-    int32_t jk[kScatterPer];
-    int t = lo;
-#pragma unroll
-    for (int k = 0; k < kScatterPer; ++k) {
-      const int64_t o = o0 + k;
-      if (o < total)
-        while (o >= ptr[t + 1]) ++t;
-      tk[k] = t;
-      jk[k] = (int32_t)(o - ptr[t]);
-    }
-    // every load of the kScatterPer outputs in flight together
-    int32_t ss[kScatterPer], ns[kScatterPer], hd[kScatterPer], c0[kScatterPer];
-#pragma unroll
-    for (int k = 0; k < kScatterPer; ++k) {
-      ss[k] = state_slot[tk[k]];
-      ns[k] = swa_len[tk[k]];
-      hd[k] = swa_head[tk[k]];
-      c0[k] = comp_indptr[tk[k]];
-    }
-    int32_t cb[kScatterPer], cs[kScatterPer];
-#pragma unroll
-    for (int k = 0; k < kScatterPer; ++k) {
-      const bool comp = o0 + k < total && jk[k] >= ns[k];
-      const int32_t e = c0[k] + (jk[k] - (ns[k] > 0 ? ns[k] : 0));
-      cb[k] = comp ? comp_block[e] : 0;
-      cs[k] = comp ? comp_slot[e] : 0;
-    }
-#pragma unroll
-    for (int k = 0; k < kScatterPer; ++k) {
-      const int64_t o = o0 + k;
-      if (o >= total) break;
-      int32_t v;
-      if (jk[k] < ns[k]) {
-        int32_t ring = (int32_t)(((int64_t)hd[k] - ns[k] + 1 + jk[k]) % win);
-        if (ring < 0) ring += win;
-        v = (int32_t)((int64_t)ss[k] * win + ring);
-      } else {
-        v = (int32_t)(swa_pages + (int64_t)cb[k] * k_per_block + cs[k]);
-      }
-      kv_indices[o] = v;
-    }
-  }
+  scatter_flat_body(a, blockIdx.x, gridDim.x, s_ptr);
 }
 
 __global__ void validate_kernel(const int32_t* __restrict__ kv_indices, int64_t total_indices,
@@ -293,6 +196,12 @@ cudaError_t launch_build_len(const int32_t* swa_len, const int32_t* swa_head, in
                     kv_indptr, const_cast<int32_t*>(ec.flags));
 }
 
+cudaError_t launch_build_scan(int N, int64_t capacity, int32_t* kv_indptr, int32_t* status,
+                              const EntryCheck& ec, cudaStream_t st) {
+  return launch_pdl(build_scan_kernel, dim3(1), dim3(kScanThreads), 0, st, N, capacity, kv_indptr,
+                    status, ec);
+}
+
 cudaError_t launch_build_scatter(const int32_t* state_slot, const int32_t* swa_len,
                                  const int32_t* swa_head, const int32_t* comp_indptr,
                                  const int32_t* comp_block, const int32_t* comp_slot, int N,
@@ -302,19 +211,12 @@ cudaError_t launch_build_scatter(const int32_t* state_slot, const int32_t* swa_l
   DeviceCaps caps;
   const cudaError_t ce = device_caps(&caps);
   if (ce != cudaSuccess) return ce;
-  if (N <= 2 * caps.num_sms)  // one wave of one-token CTAs
-    return launch_pdl(build_scatter_tok_kernel, dim3(N), dim3(kTokThreads), 0, st, state_slot,
-                      swa_len, swa_head, comp_indptr, comp_block, comp_slot, N, win, k_per_block,
-                      swa_pages, kv_indptr, kv_indices);
-  // enough threads for the capacity, at most one wave (grid-stride beyond)
-  const long long per_cta = (long long)kScatterThreads * kScatterPer;
-  const long long need = (capacity + per_cta - 1) / per_cta;
-  const long long wave = (long long)caps.num_sms * (2048 / kScatterThreads);
-  const int blocks = (int)(need < wave ? need : wave);
-  const size_t smem = N <= kScatterSmemTokens ? (size_t)(N + 1) * sizeof(int32_t) : 0;
-  return launch_pdl(build_scatter_kernel, dim3(blocks), dim3(kScatterThreads), smem, st, state_slot,
-                    swa_len, swa_head, comp_indptr, comp_block, comp_slot, N, win, k_per_block,
-                    swa_pages, kv_indptr, kv_indices);
+  const ScatterArgs a{state_slot, swa_len, swa_head, comp_indptr, comp_block, comp_slot, N, win,
+                      k_per_block, swa_pages, kv_indptr, kv_indices};
+  const ScatterShape sh = scatter_shape(N, capacity, caps.num_sms, kScatterThreads);
+  if (!sh.flat)
+    return launch_pdl(build_scatter_tok_kernel, dim3(sh.ctas), dim3(kTokThreads), 0, st, a);
+  return launch_pdl(build_scatter_kernel, dim3(sh.ctas), dim3(kScatterThreads), sh.smem, st, a);
 }
 
 cudaError_t launch_build_indices(const int32_t* state_slot, const int32_t* swa_len,
@@ -331,9 +233,7 @@ cudaError_t launch_build_indices(const int32_t* state_slot, const int32_t* swa_l
                                            comp_total, N, k_per_block, swa_pages, total_pages,
                                            capacity, kv_indices, status, caps.num_sms);
   e = launch_build_len(swa_len, swa_head, N, win, kv_indptr, ec, st);
-  if (e == cudaSuccess)
-    e = launch_pdl(build_scan_kernel, dim3(1), dim3(kScanThreads), 0, st, N, capacity, kv_indptr,
-                   status, ec);
+  if (e == cudaSuccess) e = launch_build_scan(N, capacity, kv_indptr, status, ec, st);
   if (e == cudaSuccess)
     e = launch_build_scatter(state_slot, swa_len, swa_head, comp_indptr, comp_block, comp_slot, N,
                              win, k_per_block, swa_pages, capacity, kv_indptr, kv_indices, st);

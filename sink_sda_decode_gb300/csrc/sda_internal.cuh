@@ -111,11 +111,11 @@ struct EntryCheck {
   int64_t chunks_per_cta;
 };
 
-// The index builder's scan (with the entry re-check) and the work plan in
-// one CTA.
-cudaError_t launch_scan_plan(int N, int64_t capacity, int32_t* kv_indptr, int32_t* status,
-                             const EntryCheck& ec, const LaunchPlan& lp, void* ws,
-                             const WsLayout& L, cudaStream_t st);
+struct ScatterArgs;  // sda_scatter.cuh
+// The work plan beside the index builder's scatter, one launch (after the
+// builder's scan).
+cudaError_t launch_scatter_plan(const ScatterArgs& sa, int64_t capacity, const LaunchPlan& lp,
+                               void* ws, const WsLayout& L, int num_sms, cudaStream_t st);
 cudaError_t launch_combine(const float* attn_sink, int N, int H, int D, void* out, void* ws,
                            const WsLayout& L, int num_sms, cudaStream_t st);
 cudaError_t launch_decode_simt(const void* q, const void* kv, const int32_t* kv_indices,
@@ -159,6 +159,8 @@ EntryCheck entry_check_layout(const int32_t* state_slot, const int32_t* comp_ind
 // (after the scan, which takes the same EntryCheck) the scatter.
 cudaError_t launch_build_len(const int32_t* swa_len, const int32_t* swa_head, int N, int win,
                              int32_t* kv_indptr, const EntryCheck& ec, cudaStream_t st);
+cudaError_t launch_build_scan(int N, int64_t capacity, int32_t* kv_indptr, int32_t* status,
+                              const EntryCheck& ec, cudaStream_t st);
 cudaError_t launch_build_scatter(const int32_t* state_slot, const int32_t* swa_len,
                                  const int32_t* swa_head, const int32_t* comp_indptr,
                                  const int32_t* comp_block, const int32_t* comp_slot, int N,

@@ -10,7 +10,7 @@
 #include <cuda_bf16.h>
 
 #include "sda_internal.cuh"
-#include "sda_scan.cuh"
+#include "sda_scatter.cuh"
 
 namespace sda {
 
@@ -99,8 +99,8 @@ __device__ __forceinline__ void plan_body(const int32_t* __restrict__ indptr, in
 
   // kv_indptr must be a true prefix sum inside [0, total_indices]; otherwise
   // nothing is planned (out is left unwritten) and the error word reads 2, so
-  // that no kernel ever reads kv_indices out of bounds.  (A prefix sum the
-  // builder's scan just wrote in this CTA is one by construction.)
+  // that no kernel ever reads kv_indices out of bounds.  (A prefix sum that
+  // the builder's scan wrote is one by construction.)
   int bad = 0;
   for (int t = threadIdx.x; check_indptr && t <= N; t += kPlanThreads) {
     const int v = indptr[t];
@@ -269,22 +269,26 @@ plan_kernel(const int32_t* __restrict__ indptr, int N, long long total_indices, 
   plan_body(indptr, N, total_indices, hg, grid, tile, hdr, units, splits, cta_start, ctok, ctp, true);
 }
 
-// The index builder's scan and the plan in one CTA (sda_build_decode): the
-// scan turns the per-token lengths into kv_indptr, and the plan reads it
-// straight back, which saves the plan's own launch.
-static_assert(kPlanThreads == kScanThreads, "one CTA runs both bodies");
+// The work plan beside the index builder's scatter (sda_build_decode): both
+// need only the scanned kv_indptr, so CTA 0 plans while the other CTAs
+// scatter (one-token CTAs, or FLAT over the packed output).
+template <bool FLAT>
 __global__ void __launch_bounds__(kPlanThreads)
-scan_plan_kernel(int N, int64_t capacity, int32_t* __restrict__ kv_indptr,
-                 int32_t* __restrict__ status, EntryCheck ec, int hg, int grid, int tile,
-                 WsHeader* __restrict__ hdr, int4* __restrict__ units, int4* __restrict__ splits,
-                 int* __restrict__ cta_start, int* ctok, int* ctp) {
+scatter_plan_kernel(ScatterArgs sa, long long capacity, int hg, int grid, int tile,
+                    WsHeader* __restrict__ hdr, int4* __restrict__ units, int4* __restrict__ splits,
+                    int* __restrict__ cta_start, int* ctok, int* ctp) {
   pdl_wait();
   pdl_trigger();
-  build_scan_body(N, capacity, kv_indptr, status, ec);
-  __syncthreads();  // kv_indptr is final (this CTA wrote it)
-  plan_token_arrays(N, ctok, ctp);
-  plan_body(kv_indptr, N, (long long)capacity, hg, grid, tile, hdr, units, splits, cta_start, ctok,
-            ctp, false);
+  if (blockIdx.x == 0) {
+    plan_token_arrays(sa.N, ctok, ctp);
+    plan_body(sa.kv_indptr, sa.N, capacity, hg, grid, tile, hdr, units, splits, cta_start, ctok, ctp,
+              false);
+  } else if (FLAT) {
+    extern __shared__ int32_t scatter_dyn[];
+    scatter_flat_body(sa, blockIdx.x - 1, gridDim.x - 1, scatter_dyn);
+  } else {
+    scatter_tok_body(sa, blockIdx.x - 1, gridDim.x - 1);
+  }
 }
 
 // Merge the pieces of each split token:
@@ -424,20 +428,34 @@ cudaError_t launch_plan(const int32_t* kv_indptr, int N, int64_t total_indices,
                     reinterpret_cast<int*>(base + L.ctp_off));
 }
 
-cudaError_t launch_scan_plan(int N, int64_t capacity, int32_t* kv_indptr, int32_t* status,
-                             const EntryCheck& ec, const LaunchPlan& lp, void* ws,
-                             const WsLayout& L, cudaStream_t st) {
+cudaError_t launch_scatter_plan(const ScatterArgs& sa, int64_t capacity, const LaunchPlan& lp,
+                               void* ws, const WsLayout& L, int num_sms, cudaStream_t st) {
   char* base = static_cast<char*>(ws);
-  static const cudaError_t attr = cudaFuncSetAttribute(
-      scan_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_dyn_smem(kPlanSmemTokens));
+  const ScatterShape sh = scatter_shape(sa.N, capacity, num_sms, kPlanThreads);
+  const size_t pd = plan_dyn_smem(sa.N);
+  const size_t smem = pd > sh.smem ? pd : sh.smem;
+  auto go = [&](auto kernel, int ctas) {
+    return launch_pdl(kernel, dim3(1 + ctas), dim3(kPlanThreads), smem, st, sa, (long long)capacity,
+                      lp.hg, lp.grid, lp.tile, reinterpret_cast<WsHeader*>(base),
+                      reinterpret_cast<int4*>(base + L.units_off),
+                      reinterpret_cast<int4*>(base + L.split_off),
+                      reinterpret_cast<int*>(base + L.cta_off),
+                      reinterpret_cast<int*>(base + L.ctok_off),
+                      reinterpret_cast<int*>(base + L.ctp_off));
+  };
+  static const cudaError_t attr = [] {
+    const int most = (int)plan_dyn_smem(kPlanSmemTokens);
+    cudaError_t e = cudaFuncSetAttribute(scatter_plan_kernel<true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(scatter_plan_kernel<false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    return e;
+  }();
   if (attr != cudaSuccess) return attr;
-  return launch_pdl(scan_plan_kernel, dim3(1), dim3(kPlanThreads), plan_dyn_smem(N), st, N, capacity, kv_indptr,
-                    status, ec, lp.hg, lp.grid, lp.tile,
-                    reinterpret_cast<WsHeader*>(base),
-                    reinterpret_cast<int4*>(base + L.units_off),
-                    reinterpret_cast<int4*>(base + L.split_off),
-                    reinterpret_cast<int*>(base + L.cta_off), reinterpret_cast<int*>(base + L.ctok_off),
-                    reinterpret_cast<int*>(base + L.ctp_off));
+  // no lists to write (capacity 0): CTA 0 alone
+  if (capacity <= 0) return go(scatter_plan_kernel<false>, 0);
+  return sh.flat ? go(scatter_plan_kernel<true>, sh.ctas) : go(scatter_plan_kernel<false>, sh.ctas);
 }
 
 cudaError_t launch_combine(const float* attn_sink, int N, int H, int D, void* out, void* ws,

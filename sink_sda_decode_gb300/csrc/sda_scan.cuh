@@ -1,5 +1,5 @@
-// sda_scan.cuh -- the index builder's one-CTA scan, shared by its own kernel
-// (sda_build.cu) and by the fused scan + work-plan kernel (sda_plan.cu).
+// sda_scan.cuh -- the index builder's one-CTA scan (with the re-check of
+// flagged compressed entries), run by build_scan_kernel (sda_build.cu).
 #pragma once
 
 #include <cstdint>
