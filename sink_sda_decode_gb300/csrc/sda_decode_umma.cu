@@ -641,15 +641,12 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         tc_fence_after();
         float x[16];  // raw scores of this thread's 16 (head, slot) pairs: S_a + S_b
         {
-          uint32_t sv[16];
-          tmem_ld_16x256b_x4(tmem + lane_base + s * 64 + 32 * hc, sv);
+          uint32_t sa[16], sb[16];  // both halves in flight before one wait
+          tmem_ld_16x256b_x4(tmem + lane_base + s * 64 + 32 * hc, sa);
+          tmem_ld_16x256b_x4(tmem + lane_base + C::kSbCol + s * 64 + 32 * hc, sb);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) x[e] = __uint_as_float(sv[e]);
-          tmem_ld_16x256b_x4(tmem + lane_base + C::kSbCol + s * 64 + 32 * hc, sv);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) x[e] += __uint_as_float(sv[e]);
+          for (int e = 0; e < 16; ++e) x[e] = __uint_as_float(sa[e]) + __uint_as_float(sb[e]);
         }
         tc_fence_before();
         __syncwarp();
