@@ -48,6 +48,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -101,12 +102,20 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(src):
+    """The source without comments and blank lines: a comment edit leaves the
+    compiled kernel, and so its measured figures, unchanged."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
 def kernel_source_hash(kernel="decode"):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sink_sda_decode_gb300", "csrc")
     for name in sorted(KERNEL_SOURCES[kernel]):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

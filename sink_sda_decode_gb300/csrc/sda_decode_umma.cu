@@ -10,36 +10,38 @@
 // out in bf16.
 //
 // Design for GB300 (not from the page, whose kernel targets AMD GPUs):
-//  * One persistent CTA per SM owns one work unit at a time: a piece of one
-//    token's slot list for NH <= 64 heads (H = 128 uses two CTAs per token).
-//    All heads of a token share each gathered KV row, so a row is read from
-//    HBM once per CTA.
-//  * Warps 8..15 load KV tiles of 64 slots: each 1 KB row is read by a whole
-//    warp as two contiguous 512-byte loads (16 x 16 B in flight per thread,
-//    64 KB per SM), then stored 128-byte-swizzled into a shared-memory stage
-//    (2 stages, 3 for NH = 16), one half of D at a time: a half is refilled
-//    as soon as the PV MMAs that read it (blocks 0-1 or 2-3) are done, and
-//    the next QK starts on the first half while the second is still stored.
-//    Whole-row loads keep DRAM accesses contiguous; TMA tile::gather4, which
+//  * One persistent CTA per SM owns a contiguous run of work units: a unit
+//    is a piece of one token's slot list for NH <= 64 heads (H = 128 uses
+//    two CTAs per token, which read the same rows at about the same time,
+//    the second mostly from L2).  All heads of a unit share each gathered KV
+//    row, so a row is read from memory once per CTA.
+//  * Warps 8..23 load KV tiles of 64 slots: warp v copies rows 4v .. 4v+3
+//    straight from global to a 128-byte-swizzled shared-memory stage with
+//    16-byte cp.async, one half of D per commit group, each half as soon as
+//    the PV MMAs that last read it are done (2 stages, 3 for NH = 16); the
+//    rows of the tile two ahead are brought into L2 with bulk prefetches.
+//    (FP8 pool: two groups of 8 warps on alternate tiles dequantise E4M3
+//    codes in registers into the same bf16 tile.)  TMA tile::gather4, which
 //    fetches 128 bytes of four rows per instruction, topped out near a third
 //    of HBM bandwidth on this GPU.
-//  * Warps 16 and 17 issue tcgen05 MMAs, event driven and apart, so that one
-//    waiting for the tensor pipe never delays the other:  S = Q K^T  (M = 64
-//    padded heads, N = 64 slots, K = 512) into TMEM by warp 16, which also
-//    loads q[t] with tiled TMA, and  O^T += V^T P^T  (M = 128 rows of D,
-//    N = NH heads, K = 64 slots) into a TMEM accumulator by warp 17; the
-//    same shared tile is K (K-major operand) and V (MN-major operand).
-//    (Warps 18 and 19 only fill out the register split: 20 warps on four
-//    sub-partitions of 16 K registers leave 96 registers per thread.)
-//  * Warps 0..7 read S from TMEM (warps q and q + 4 share lane quadrant q
-//    and take slots 0..31 and 32..63; two heads per quad of threads), run
-//    the online softmax, write P (bf16) to shared memory, rescale O^T in
-//    TMEM only when a head's running max grows by more than 8 (2^8
-//    headroom, so p <= 256), and finally normalise with the sink and write
-//    out through stmatrix + TMA stores (or, for a piece of a split token,
-//    write the unnormalised partial for the combine kernel).
-//  * Every mbarrier wait is bounded (2 s); on timeout the kernel raises the
-//    workspace error word, drains its own copies and returns.
+//  * Warps 24 and 26 issue the QK MMAs (tcgen05, M = 64 padded heads, N = 64
+//    slots), warp 24 the first half of D into S_a and warp 26 the second
+//    into S_b, so that their MMAs overlap in the tensor pipe; warp 24 also
+//    loads q of each unit with tiled TMA.  Warp 25 issues  O^T += V^T P^T
+//    (M = 128 rows of D, N = NH heads, K = 64 slots) into a TMEM
+//    accumulator; the same shared tile is K (K-major operand) and V
+//    (MN-major operand).  Warp 27 only fills out its warpgroup.
+//  * Warps 0..7 read S_a + S_b from TMEM (warps q and q + 4 share lane
+//    quadrant q and take slots 0..31 and 32..63), run the online softmax,
+//    write P (bf16) to shared memory, rescale O^T in TMEM only when a
+//    head's running max grows by more than 8 (2^8 headroom, so p <= 256),
+//    and finally normalise with the sink and write out through stmatrix +
+//    TMA stores (or, for a piece of a split token, write the unnormalised
+//    partial for the combine kernel).
+//  * Registers are redistributed with setmaxnreg (softmax warps grow, the
+//    loader and MMA warpgroups shrink); every mbarrier wait is bounded (2 s),
+//    and on timeout the kernel raises the workspace error word, drains its
+//    own copies and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -494,13 +496,13 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
     // Three threads issue tcgen05 MMAs; one thread's MMAs run one after the
     // other, but MMAs of different threads overlap in the tensor pipe, so
     // splitting the work keeps it busy:
-    //  - warps 16 and 18, lane 0: S = Q K^T of every tile, K split in two:
-    //    warp 16 the columns [0, 256) of D into S_a, warp 18 the columns
+    //  - warps 24 and 26, lane 0: S = Q K^T of every tile, K split in two:
+    //    warp 24 the columns [0, 256) of D into S_a, warp 26 the columns
     //    [256, 512) into S_b (the softmax adds the two), each as soon as its
-    //    half of the tile has landed and the S buffer is free; warp 16 also
+    //    half of the tile has landed and the S buffer is free; warp 24 also
     //    loads q of the next unit (tiled TMA) once both halves of this unit's
     //    last QK have read q;
-    //  - warp 17, lane 0: O^T += V^T P^T of every tile as soon as its P is
+    //  - warp 25, lane 0: O^T += V^T P^T of every tile as soon as its P is
     //    written (a commit after blocks 1 and 3 releases each half of the KV
     //    stage; the second also frees the P buffer).
     // Each thread's commits track only its own MMAs.  Each has a single next
