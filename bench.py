@@ -359,7 +359,7 @@ class Step:
             self.q_rot = torch.empty_like(w.q)
             self.store_status = torch.empty(1, dtype=torch.int32, device=device)
         self.results = [self.q_rot if path == "store" else self.out]
-        # decode: builder lengths, scan + plan, scatter, attention, combine
+        # decode: builder lengths, scan, plan + scatter, attention, combine
         self.launches_per_step = {"decode": 5, "store": 1, "layer": 6}[path]
 
     @property

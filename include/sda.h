@@ -225,8 +225,9 @@ sda_status sda_debug_wait_fault(int withhold_arrive, uint64_t timeout_ns);
  *     in input order, emitted as swa_pages + comp_block[e] * k_per_block +
  *     comp_slot[e].
  * kv_indptr [N + 1] receives the prefix sum (kv_indptr[0] = 0) and
- * kv_indices [capacity] the packed slots.  All arrays are int32 device
- * memory.  A token with a bad field gets an empty slice and sets bits of
+ * kv_indices [capacity] the packed slots; entries past kv_indptr[N] are
+ * unspecified (the builder uses them as scratch).  All arrays are int32
+ * device memory.  A token with a bad field gets an empty slice and sets bits of
  * *status (device int32, overwritten):
  *   1  swa_len outside [0, win]
  *   2  swa_head outside [0, win) while swa_len > 0
@@ -235,7 +236,10 @@ sda_status sda_debug_wait_fault(int withhold_arrive, uint64_t timeout_ns);
  *   16 a slot outside its region (state_slot*win + win > swa_pages, or a
  *      compressed slot >= total_pages)
  *   32 the packed lists exceed `capacity`: then every slice is empty
- * So every emitted slot is valid for sda_decode by construction.
+ * So every emitted slot is valid for sda_decode by construction.  The
+ * compressed entries are checked in parallel slices of the entry array; a
+ * batch that holds bad entries is then re-checked token by token by one CTA
+ * (slower, same result).
  * Host errors (SDA_ERR_INVALID_ARG): N < 0, win <= 0, k_per_block <= 0,
  * swa_pages < 0, total_pages outside (0, 2^31), swa_pages > total_pages,
  * capacity < 0 or > 2^31 - 1, a null pointer that would be read.
@@ -253,7 +257,7 @@ sda_status sda_build_indices(const int32_t* state_slot, const int32_t* swa_len,
  * not NULL, unified_kv then holding the E4M3 codes), as one call: the same
  * arguments, contracts, outputs and status bits as those two calls made back
  * to back on the stream with total_indices = capacity, with one launch fewer
- * (the builder's scan and the decode's work plan run in one CTA).  The
+ * (the decode's work plan runs in the same launch as the builder's scatter).  The
  * workspace is sized by sda_decode_workspace_size (or
  * sda_decode_fp8_workspace_size) with total_indices = capacity.  Lists the
  * builder empties (bad descriptors, or bit 32: over capacity) decode to +0.
