@@ -5,9 +5,11 @@
 // slot_in_block) into the ragged kv_indices / kv_indptr pair the decode
 // kernel reads (paged_decode.py docstring, caller convention for unified_kv
 // and kv_indices: ragged-packed, no sentinels, padded tokens get an empty
-// slice).  Three launches: per-token validation + length, one-CTA scan,
-// scatter over the packed output.  Bad descriptors never reach the decode kernel: the
-// token's slice is emptied and a status bit is raised (a divide-by-zero in a
+// slice).  Three launches: lengths and an entry check (flat over the tokens
+// and the compressed entries), a one-CTA scan (which re-checks the tokens
+// whose entries were flagged), and the scatter.  Bad descriptors never reach
+// the decode kernel: the token's slice is emptied and a status bit is raised
+// (a divide-by-zero in a
 // slot translation that produced out-of-range slots and a GPU fault is the
 // failure the sglang PR 25898 summary page describes; here win and
 // k_per_block are checked on the host and every emitted slot is in range).
