@@ -9,10 +9,10 @@
 // and the compressed entries), a one-CTA scan (which re-checks the tokens
 // whose entries were flagged), and the scatter.  Bad descriptors never reach
 // the decode kernel: the token's slice is emptied and a status bit is raised
-// (a divide-by-zero in a
-// slot translation that produced out-of-range slots and a GPU fault is the
-// failure the sglang PR 25898 summary page describes; here win and
-// k_per_block are checked on the host and every emitted slot is in range).
+// (a divide-by-zero in a slot translation that produced out-of-range slots
+// and a GPU fault is the failure the sglang PR 25898 summary page
+// describes; here win and k_per_block are checked on the host and every
+// emitted slot is in range).
 #include "sda_internal.cuh"
 #include "sda_scan.cuh"
 #include "sda_scatter.cuh"
