@@ -263,3 +263,14 @@ def test_host_buffers_large_batch_bad_descriptors_and_graph_replay():
     tokens = [t for t in range(w.N) if t != bad]
     ref = parity.run_oracle(w, tokens=tokens)
     parity.assert_parity(parity.compare(out_h[tokens].cuda(), ref), "chunked host batch, bad token")
+
+
+def test_fused_large_batch_equals_two_calls():
+    """9000 tokens: the plan beside the flat scatter, whose kv_indptr search
+    runs in global memory (no shared-memory copy above 8191 tokens)."""
+    rng = np.random.default_rng(9000)
+    lens = rng.integers(0, 130, 9000)
+    lens[::97] = 0
+    w = inputs.random_small(9000, 9000, 16, 512, 1 << 16, lens, device="cuda")
+    bi = w.builder_inputs("cuda")
+    assert_same(fused(w, bi), two_calls(w, bi))

@@ -219,3 +219,12 @@ def test_long_lists_flat_scatter(N):
     st = check_against_oracle((ss, sl, sh, cp.astype(np.int32), cb, cs, win, kpb, swa_pages,
                                total_pages))
     assert st == 0
+
+
+@pytest.mark.parametrize("N", [9000, 13000])
+def test_large_batches_unstaged_scatter(N):
+    """Batches above 8191 tokens: the flat scatter searches kv_indptr in
+    global memory instead of a shared-memory copy."""
+    rng = np.random.default_rng(N + 17)
+    args = random_descriptors(rng, N, win=16, kpb=8, n_states=N, n_blocks=5000, max_comp=30)
+    check_against_oracle(args)
