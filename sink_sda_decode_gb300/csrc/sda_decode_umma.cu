@@ -27,10 +27,12 @@
 //  * Warps 24 and 26 issue the QK MMAs (tcgen05, M = 64 padded heads, N = 64
 //    slots), warp 24 the first half of D into S_a and warp 26 the second
 //    into S_b, so that their MMAs overlap in the tensor pipe; warp 24 also
-//    loads q of each unit with tiled TMA.  Warp 25 issues  O^T += V^T P^T
-//    (M = 128 rows of D, N = NH heads, K = 64 slots) into a TMEM
-//    accumulator; the same shared tile is K (K-major operand) and V
-//    (MN-major operand).  Warp 27 only fills out its warpgroup.
+//    loads q of each unit with tiled TMA.  Softmax thread 0 issues
+//    O^T += V^T P^T  (M = 128 rows of D, N = NH heads, K = 64 slots) into a
+//    TMEM accumulator right after the barrier at which every softmax warp
+//    has written the tile's P; the same shared tile is K (K-major operand)
+//    and V (MN-major operand).  Warps 25 and 27 only fill out their
+//    warpgroup.
 //  * Warps 0..7 read S_a + S_b from TMEM (warps q and q + 4 share lane
 //    quadrant q and take slots 0..31 and 32..63), run the online softmax,
 //    write P (bf16) to shared memory, rescale O^T in TMEM only when a
@@ -66,7 +68,7 @@ constexpr int kLoaderWarp0 = 8;            // warps 8..23: KV row loaders, two g
 constexpr int kLoaderWarps = 8;            // warps per loader group (group g loads tiles of parity g)
 constexpr int kLoaderGroups = 2;
 constexpr int kMmaWarp = 24;               // warp 24: QK issuer (first half of D) + q loads
-constexpr int kPvWarp = 25;                // warp 25: PV issuer
+// warps 25 and 27 only fill out the MMA warpgroup (softmax thread 0 issues the PV MMAs)
 constexpr int kMmaWarpB = 26;              // warp 26: QK issuer (second half of D)
 // 28 warps (27 idle) = 7 warpgroups; registers are split by setmaxnreg:
 // softmax warpgroups 0-1 grow to kSmRegs, loader warpgroups 2-5 and the MMA
@@ -96,9 +98,6 @@ enum Bar : int {
   kBarSFull1,
   kBarSEmpty0,
   kBarSEmpty1,
-  kBarPFull0,
-  kBarPFull1,
-  kBarOEmpty,
   kBarDrain,
   kBarDrainPv,
   kBarDrainQb,
@@ -289,9 +288,6 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
     mbar_init(bar(kBarSFull1), 2);
     mbar_init(bar(kBarSEmpty0), kSmWarps);
     mbar_init(bar(kBarSEmpty1), kSmWarps);
-    mbar_init(bar(kBarPFull0), kSmWarps);
-    mbar_init(bar(kBarPFull1), kSmWarps);
-    mbar_init(bar(kBarOEmpty), kSmWarps);
     mbar_init(bar(kBarDrain), 1);
     mbar_init(bar(kBarDrainPv), 1);
     mbar_init(bar(kBarDrainQb), 1);
@@ -491,31 +487,28 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
     }
   } else if (warp >= kMmaWarp) {
     if constexpr (RegSplit<FP8>::kMma < kLaunchRegs) setmaxnreg_dec<RegSplit<FP8>::kMma>();  // the whole warpgroup (warp 27 idles)
-    if (warp == kMmaWarp || warp == kPvWarp || warp == kMmaWarpB) {
+    if (warp == kMmaWarp || warp == kMmaWarpB) {
     // ===================================================== MMA issuers
-    // Three threads issue tcgen05 MMAs; one thread's MMAs run one after the
+    // Two threads issue the QK MMAs; one thread's MMAs run one after the
     // other, but MMAs of different threads overlap in the tensor pipe, so
-    // splitting the work keeps it busy:
-    //  - warps 24 and 26, lane 0: S = Q K^T of every tile, K split in two:
-    //    warp 24 the columns [0, 256) of D into S_a, warp 26 the columns
-    //    [256, 512) into S_b (the softmax adds the two), each as soon as its
-    //    half of the tile has landed and the S buffer is free; warp 24 also
-    //    loads q of the next unit (tiled TMA) once both halves of this unit's
-    //    last QK have read q;
-    //  - warp 25, lane 0: O^T += V^T P^T of every tile as soon as its P is
-    //    written (a commit after blocks 1 and 3 releases each half of the KV
-    //    stage; the second also frees the P buffer).
-    // Each thread's commits track only its own MMAs.  Each has a single next
-    // event at any time, so it sleeps in the mbarrier wait (hardware suspend)
-    // instead of spinning, leaving the issue slots to the other warps.
+    // splitting the work keeps it busy: warps 24 and 26, lane 0, compute
+    // S = Q K^T of every tile, K split in two: warp 24 the columns [0, 256)
+    // of D into S_a, warp 26 the columns [256, 512) into S_b (the softmax
+    // adds the two), each as soon as its half of the tile has landed and the
+    // S buffer is free; warp 24 also loads q of the next unit (tiled TMA) once
+    // both halves of this unit's last QK have read q.  (The PV MMAs are
+    // issued by softmax thread 0 right after the barrier at which every
+    // softmax warp has written the tile's P.)  Each thread's commits track
+    // only its own MMAs.  Each has a single next event at any time, so it
+    // sleeps in the mbarrier wait (hardware suspend) instead of spinning,
+    // leaving the issue slots to the other warps.
     if (lane == 0) {
-      const bool qk_role = warp != kPvWarp;
       const int qh = warp == kMmaWarpB ? 1 : 0;  // QK: half of D (of the K dimension)
       TileCursor cq;
       cq.init(my_units, n_units);
       int q_issued = 0;
       bool ok = true;
-      if (qk_role && qh == 0 && cq.valid) {  // q of the first unit
+      if (qh == 0 && cq.valid) {  // q of the first unit
         mbar_arrive_expect_tx(bar(kBarQFull), NH * 128 * kPanels);
         const int qrow = cq.u.x * H + unit_head_group(cq.u.w) * NH;
 #pragma unroll
@@ -523,8 +516,8 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         q_issued = 1;
       }
       while (cq.valid && ok) {
-        const int g = cq.g, s = g & 1, ks = g % KS;  // S / P buffer, KV stage
-        if (qk_role) {
+        const int g = cq.g, s = g & 1, ks = g % KS;  // S buffer, KV stage
+        {
           if (g >= 2) ok = wait_bar(bar(kBarSEmpty0 + s), ((g >> 1) - 1) & 1, wc);
           if (ok && cq.i == 0) ok = wait_bar(bar(kBarQFull), cq.nu & 1, wc);
           if (ok) ok = wait_bar(bar(kv_full(ks, qh)), (g / KS) & 1, wc);
@@ -558,36 +551,13 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
             for (int c = 0; c < kPanels; ++c) tma_load_2d(sQ + c * C::kPanelQ, &tmap_q, c * 64, qrow, bar(kBarQFull));
             q_issued = cq.nu + 1;
           }
-        } else {
-          const bool first = cq.i == 0;
-          ok = wait_bar(bar(kBarPFull0 + s), (g >> 1) & 1, wc);
-          if (ok && first && cq.nu >= 1) ok = wait_bar(bar(kBarOEmpty), (cq.nu - 1) & 1, wc);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t kvs = sKV + ks * kKVBytes;
-          const uint32_t ps = sP + s * C::kPBytes;
-          const uint64_t a0 = sdesc_sw128(kvs, kPanelKV, 1024), b0 = sdesc_sw128(ps, 16, 1024);
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              // A = V^T block b: rows d in [128b, 128b+128) = panels 2b, 2b+1 (MN-major);
-              //     K = slots [16kk, 16kk+16) = row groups 2kk, 2kk+1
-              const uint64_t a = sdesc_advance(a0, (2 * b) * kPanelKV + kk * 2048);
-              // B = P^T: N = NH heads (rows), K = 16 slots at byte offset 32kk (K-major)
-              const uint64_t bd = sdesc_advance(b0, kk * 32);
-              mma_bf16(tmem + C::kOCol + b * NH, a, bd, C::kIdescPV, (first && kk == 0) ? 0u : 1u);
-            }
-            if (b & 1) mma_commit(bar(pv_done(ks, b >> 1)));  // half b/2 of the stage may be refilled
-          }
-          cq.next();
         }
       }
       // drain this thread's MMAs (and the last q copy) before TMEM and smem go away
-      const int drain = qk_role ? (qh ? kBarDrainQb : kBarDrain) : kBarDrainPv;
+      const int drain = qh ? kBarDrainQb : kBarDrain;
       mma_commit(bar(drain));
       drain_bar(bar(drain), 0, wc);
-      if (qk_role && qh == 0 && q_issued >= 1) drain_bar(bar(kBarQFull), (q_issued - 1) & 1, wc);
+      if (qh == 0 && q_issued >= 1) drain_bar(bar(kBarQFull), (q_issued - 1) & 1, wc);
     }
     __syncwarp();
     }
@@ -710,7 +680,12 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
         };
         // exact path on a unit's first tile (block-uniform), else by vote (an
         // invalid head's weights are never stored, so it casts no vote)
-        const bool exact = i == 0 || named_bar_or(1, kSoftmaxThreads, weights() && vA);
+        bool exact = i == 0;
+        if (!exact) {
+          const bool over = weights() && vA;
+          fence_proxy_async_smem();  // this thread's P stores -> read by the tensor cores
+          exact = named_bar_or(1, kSoftmaxThreads, over);
+        }
         if (exact) {
           // exact path: the tile's largest scaled score per head
           float eA = -INFINITY, eB = -INFINITY;
@@ -748,6 +723,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
             mB = eB;
           }
           weights();  // against the raised reference (the scores die here)
+          fence_proxy_async_smem();
           if (i > 0) {
             // O^T already holds this unit's earlier tiles: scale its head columns
             if (tq == 0 && hc == 0) {
@@ -774,15 +750,39 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
               }
             }
             tmem_wait_st();
-            named_bar_sync(1, kSoftmaxThreads);  // s_alpha is rewritten next time
           }
+          // every warp's P (and rescaled O^T) is written; s_alpha is rewritten next time
+          tc_fence_before();
+          named_bar_sync(1, kSoftmaxThreads);
         }
         lA += sA;
         lB += sB;
-        fence_proxy_async_smem();
-        tc_fence_before();
+        // O^T += V^T P^T of this tile, issued by one thread now that the last
+        // barrier (the vote, or the exact path's) has seen every warp's P: a
+        // commit after blocks 1 and 3 releases each half of the KV stage (the
+        // second also frees the P buffer and marks O^T complete).  The same
+        // shared tile is K (K-major) for QK and V (MN-major) here.
+        if (threadIdx.x == 0) {
+          tc_fence_after();
+          const int ks = g % KS;
+          const uint32_t kvs = sKV + ks * kKVBytes;
+          const uint32_t ps = sP + s * C::kPBytes;
+          const uint64_t a0 = sdesc_sw128(kvs, kPanelKV, 1024), b0 = sdesc_sw128(ps, 16, 1024);
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              // A = V^T block b: rows d in [128b, 128b+128) = panels 2b, 2b+1 (MN-major);
+              //     K = slots [16kk, 16kk+16) = row groups 2kk, 2kk+1
+              const uint64_t a = sdesc_advance(a0, (2 * b) * kPanelKV + kk * 2048);
+              // B = P^T: N = NH heads (rows), K = 16 slots at byte offset 32kk (K-major)
+              const uint64_t bd = sdesc_advance(b0, kk * 32);
+              mma_bf16(tmem + C::kOCol + b * NH, a, bd, C::kIdescPV, (i == 0 && kk == 0) ? 0u : 1u);
+            }
+            if (b & 1) mma_commit(bar(pv_done(ks, b >> 1)));
+          }
+        }
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarPFull0 + s));
       }
       // ---------------------------------------------- epilogue of the unit
       // denominators: the quad's shares, then the two halves of the tile
@@ -911,9 +911,14 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
           }
         }
       }
+      // s_fac / s_lsum are rewritten, and O^T is overwritten by the next unit's
+      // first PV (issued by thread 0 after a later barrier)
       tc_fence_before();
-      named_bar_sync(1, kSoftmaxThreads);  // s_fac / s_lsum are rewritten by the next unit
-      if (lane == 0) mbar_arrive(bar(kBarOEmpty));
+      named_bar_sync(1, kSoftmaxThreads);
+    }
+    if (threadIdx.x == 0) {  // every PV MMA done before TMEM and shared memory go away
+      mma_commit(bar(kBarDrainPv));
+      drain_bar(bar(kBarDrainPv), 0, wc);
     }
     if (q4 == 0 && lane == 0) bulk_wait0();  // every output store has landed before the CTA exits
   }
