@@ -274,3 +274,24 @@ def test_fused_large_batch_equals_two_calls():
     w = inputs.random_small(9000, 9000, 16, 512, 1 << 16, lens, device="cuda")
     bi = w.builder_inputs("cuda")
     assert_same(fused(w, bi), two_calls(w, bi))
+
+
+@pytest.mark.parametrize("offset", [0, 1])
+def test_fused_bad_entries_unaligned(offset):
+    """Bad compressed entries in several tokens, with the entry arrays passed
+    as views that start `offset` entries into larger arrays (not 16-byte
+    aligned for offset 1): the fused call's entry check and per-token
+    re-check give exactly the two calls' lists, status and output."""
+    w = inputs.config(2, device="cuda")
+    bi = {k: v.clone() for k, v in w.builder_inputs("cuda").items()}
+    cp = bi["comp_indptr"].cpu().numpy()
+    for t in (3, 40, 41, 200):
+        if cp[t + 1] > cp[t]:
+            bi["comp_slot"][int(cp[t + 1]) - 1] = w.k_per_block      # bit 8
+    bi["comp_block"][int(cp[100])] = (w.total_pages - w.swa_pages) // w.k_per_block + 7  # bit 16
+    for k in ("comp_block", "comp_slot"):
+        pad = torch.zeros(offset, dtype=torch.int32, device="cuda")
+        bi[k] = torch.cat([pad, bi[k]])[offset:]
+    a, b = fused(w, bi), two_calls(w, bi)
+    assert_same(a, b)
+    assert int(a[3].item()) & 8
