@@ -85,7 +85,6 @@ struct RegSplit {  // the FP8 loaders dequantise in registers, so they get more
                     kThreads * kLaunchRegs,
                 "register split exceeds the launch allocation");
 };
-constexpr int kRowsPerLoader = kTileSlots / kLoaderWarps;  // 8 rows of a tile per loader warp
 constexpr int kSoftmaxThreads = kSmWarps * 32;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -281,7 +280,7 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
     mbar_init(bar(kBarQFull), 1);
     mbar_init(bar(kBarQEmpty), 2);  // both QK issuers' commits
     for (int i = 0; i < 2 * C::kStages; ++i) {
-      mbar_init(bar(kBarKVFull0 + i), FP8 ? kLoaderWarps : kLoaderGroups * kLoaderWarps);
+      mbar_init(bar(kBarKVFull0 + i), kLoaderGroups * kLoaderWarps);
       mbar_init(bar(kBarPVDone0 + i), 1);
     }
     mbar_init(bar(kBarSFull0), 2);  // S_a and S_b
@@ -314,22 +313,11 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
 
   if (warp >= kLoaderWarp0 && warp < kLoaderWarp0 + kLoaderGroups * kLoaderWarps) {
     // ===================================================== KV row loaders
-    // Two groups of 8 loader warps; warp w of a group owns rows [8w, 8w+8)
-    // of the group's 64-slot tiles (bf16 pool: group 0 the even tiles,
-    // group 1 the odd ones, so that one group waits for its rows to land
-    // while the other issues; FP8 pool: group 0 all tiles).  The rows of a
-    // later tile are brought into L2 with one bulk prefetch per row, so that
-    // their loads wait on L2, not on DRAM.
+    // All 16 loader warps share every 64-slot tile: warp v copies rows
+    // [4v, 4v+4).  The rows of the tile two ahead are brought into L2 with one
+    // bulk prefetch per row, so that their loads wait on L2, not on DRAM.
     setmaxnreg_dec<RegSplit<FP8>::kLoader>();
-    const int grp = (warp - kLoaderWarp0) / kLoaderWarps;
-    const int lw = (warp - kLoaderWarp0) % kLoaderWarps;
     const uint4* kv4 = reinterpret_cast<const uint4*>(p.kv);
-    TileCursor c{};  // the next tile whose slots are read
-    auto tile_slot = [&]() {  // lanes 0..7: slot of row 8w + lane of tile c, else -1
-      const int n = min(kTileN, c.len() - c.i * kTileN);
-      const int r = lw * kRowsPerLoader + lane;
-      return (lane < kRowsPerLoader && r < n) ? __ldg(p.kv_indices + c.u.y + c.i * kTileN + r) : -1;
-    };
     auto prefetch_rows = [&](int slot_of_lane) {
       constexpr uint32_t kRowBytes = FP8 ? kD : kD * 2;
       if (slot_of_lane >= 0) {
@@ -338,61 +326,69 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
       }
     };
     bool ok = true;
-    TileCursor t;  // this group's current tile (the groups take every other tile)
-    t.init(my_units, n_units);
-    if (grp == 1 && t.valid) t.next();
-    c = t;  // c: this group's next tile (slots read one tile early)
-    auto skip2 = [&](TileCursor& x) {
-      if (x.valid) x.next();
-      if (x.valid) x.next();
-    };
     if constexpr (FP8) {
-      // E4M3 pool: each row is 512 bytes of codes; lane l reads bytes
-      // [8l, 8l+8) of each half (one 8-byte load per row and half, 256 bytes
-      // per warp instruction), lanes 0..7 also read their row's scale one tile
-      // early; the codes are dequantised (code * scale, rounded to bf16) into
-      // the same swizzled bf16 tile as the bf16 pool's rows, half by half.
+      // E4M3 pool: all 16 loader warps share every tile, warp v rows [4v, 4v+4)
+      // (as for the bf16 pool).  Lane l reads bytes [8l, 8l+8) of each half of
+      // a row's 512 codes (one 8-byte load per row and half, both halves in
+      // flight before the stage is free) and lanes 0..3 their rows' scales one
+      // tile early; the codes are dequantised (code * scale, rounded to bf16)
+      // into the same swizzled bf16 tile as the bf16 pool's rows, half by half.
+      constexpr int kRows = kTileN / (kLoaderGroups * kLoaderWarps);  // 4 rows per warp
+      const int v = warp - kLoaderWarp0;
       const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
-      bool hv0 = t.valid;
-      int sl0 = hv0 ? tile_slot() : -1;
-      float scl0 = (lane < kRowsPerLoader && sl0 >= 0) ? __ldg(p.kv_scale + sl0) : 0.f;
-      skip2(c);
-      for (int g = grp; hv0 && ok; g += 2) {
+      auto slot_of = [&](const TileCursor& x) {  // lanes 0..3: slot of row 4v + lane of tile x, else -1
+        const int n = min(kTileN, x.len() - x.i * kTileN);
+        const int r = v * kRows + lane;
+        return (lane < kRows && r < n) ? __ldg(p.kv_indices + x.u.y + x.i * kTileN + r) : -1;
+      };
+      TileCursor cu;  // the current tile
+      cu.init(my_units, n_units);
+      TileCursor nx = cu;  // the next tile
+      if (nx.valid) nx.next();
+      TileCursor n2 = nx;  // the one after: its slots are read a tile early, its rows prefetched
+      if (n2.valid) n2.next();
+      int sl0 = cu.valid ? slot_of(cu) : -1;
+      int sl1 = nx.valid ? slot_of(nx) : -1;
+      float sc0 = (lane < kRows && sl0 >= 0) ? __ldg(p.kv_scale + sl0) : 0.f;
+      if (sl1 >= 0) prefetch_rows(sl1);
+      for (int g = 0; cu.valid && ok; ++g) {
         const int s = g % KS;  // KV stage
-        const bool hv1 = c.valid;
-        const int sl1 = hv1 ? tile_slot() : -1;
-        skip2(c);
-        int slot_r[kRowsPerLoader];
-        float sc_r[kRowsPerLoader];
+        const int sl2 = n2.valid ? slot_of(n2) : -1;
+        int slot_r[kRows];
+        float sc_r[kRows];
 #pragma unroll
-        for (int r = 0; r < kRowsPerLoader; ++r) {
+        for (int r = 0; r < kRows; ++r) {
           slot_r[r] = __shfl_sync(0xffffffffu, sl0, r);
-          sc_r[r] = __shfl_sync(0xffffffffu, scl0, r);
+          sc_r[r] = __shfl_sync(0xffffffffu, sc0, r);
         }
-        uint8_t* stage = smem + C::kOffKV + s * kKVBytes;
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-          uint2 w[kRowsPerLoader];
+        // a tail row of a partial tile is zeros (its p is forced to 0)
+        uint2 w[2][kRows];
 #pragma unroll
-          for (int r = 0; r < kRowsPerLoader; ++r) {
-            // a tail row of a partial tile is zeros (its p is forced to 0)
-            w[r] = slot_r[r] >= 0
-                       ? __ldcg(reinterpret_cast<const uint2*>(kv8 + (size_t)slot_r[r] * kD) + 32 * hh + lane)
-                       : make_uint2(0, 0);
-          }
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int r = 0; r < kRows; ++r)
+            w[hh][r] = slot_r[r] >= 0
+                           ? __ldcg(reinterpret_cast<const uint2*>(kv8 + (size_t)slot_r[r] * kD) + 32 * hh + lane)
+                           : make_uint2(0, 0);
+        const float sc1 = (lane < kRows && sl1 >= 0) ? __ldg(p.kv_scale + sl1) : 0.f;  // next tile's scales
+        uint8_t* stage = smem + C::kOffKV + s * kKVBytes;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
           if (g >= KS) {  // the tile KS back in this stage
             if (lane == 0) ok = wait_bar(bar(pv_done(s, hh)), ((g / KS) - 1) & 1, wc);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
           }
-          // 16-byte chunk q = 32*hh + lane of each row: panel q/8, chunk q%8
+          // 16-byte chunk q = 32*hh + lane of each row: panel q/8, chunk q%8;
+          // row 4v + r sits at row (4v + r) % 8 of 8-row swizzle atom (4v + r) / 8
           const int q = hh * 32 + lane, k = q & 7;
-          uint8_t* atom = stage + (q >> 3) * kPanelKV + lw * 1024;
+          uint8_t* atom = stage + (q >> 3) * kPanelKV + (v >> 1) * 1024;
 #pragma unroll
-          for (int r = 0; r < kRowsPerLoader; ++r) {
-            const uint2 c8 = w[r];
+          for (int r = 0; r < kRows; ++r) {
+            const int r8 = 4 * (v & 1) + r;
+            const uint2 c8 = w[hh][r];
             const float sr = sc_r[r];
-            *reinterpret_cast<uint4*>(atom + r * 128 + ((k ^ r) << 4)) =
+            *reinterpret_cast<uint4*>(atom + r8 * 128 + ((k ^ r8) << 4)) =
                 make_uint4(e4m3x2_to_bf16x2_scaled(c8.x & 0xffffu, sr),
                            e4m3x2_to_bf16x2_scaled(c8.x >> 16, sr),
                            e4m3x2_to_bf16x2_scaled(c8.y & 0xffffu, sr),
@@ -402,11 +398,13 @@ decode_umma_kernel(const __grid_constant__ CUtensorMap tmap_q,
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kv_full(s, hh)));
         }
-        // the next tile's scales (lanes 0..7) and rows (into L2)
-        scl0 = (lane < kRowsPerLoader && sl1 >= 0) ? __ldg(p.kv_scale + sl1) : 0.f;
-        prefetch_rows(sl1);
+        prefetch_rows(sl2);  // rows (and scales) of tile g + 2 into L2
+        cu = nx;
+        nx = n2;
+        if (n2.valid) n2.next();
         sl0 = sl1;
-        hv0 = hv1;
+        sl1 = sl2;
+        sc0 = sc1;
       }
     } else {
     // bf16 pool: all 16 loader warps share every tile, warp v (0..15) rows
