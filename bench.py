@@ -26,7 +26,10 @@ each with the fp64 oracle (`parity_sample`).
             q: token chunks over copy-engine streams, overlapped with the
             decode); other paths: one packed H2D copy in, D2H copies out
   roofline  the attention kernel alone (events recorded around it by the
-            library's timing hook): algorithmic bytes / time vs measured HBM
+            library's timing hook): algorithmic bytes / time vs measured HBM;
+            also distinct_row_bytes / frac_distinct_rows, each distinct pool
+            row counted once (the HBM figure of a prefill chunk, whose tokens
+            share most rows)
   cpu_baseline  the fp64 CPU oracle on the host cores (bounded sample)
 
 --path topk times the step in front of the index build: per token, the k
@@ -270,6 +273,18 @@ def algorithmic_bytes(w, kv="bf16"):
     L = int(w.total_len)
     row = w.D * 2 if kv == "bf16" else w.D + 4
     return L * row + 2 * w.N * w.H * w.D * 2 + L * 4 + (w.N + 1) * 4
+
+
+def distinct_row_bytes(w, kv="bf16"):
+    """algorithmic_bytes with each distinct pool row counted once, however
+    many tokens' lists hold it: the least the step could read from HBM.  The
+    decode workloads' lists barely overlap, so it is close to
+    algorithmic_bytes; a prefill chunk's neighbouring tokens share most of
+    their rows, and the fraction against these bytes is its HBM figure."""
+    n = int(np.unique(np.asarray(w.kv_indices)).size)
+    L = int(w.total_len)
+    row = w.D * 2 if kv == "bf16" else w.D + 4
+    return n * row + 2 * w.N * w.H * w.D * 2 + L * 4 + (w.N + 1) * 4
 
 
 def store_algorithmic_bytes(w, rope_dim, kv="bf16"):
@@ -697,6 +712,10 @@ def report_line(args, w, ws, ms_step, ms_kernel, ms_e2e, tokens_total, r):
     else:
         line["gathered_kv_gbs"] = (int(w.total_len) * (w.D * 2 if kv == "bf16" else w.D + 4)
                                    / (ms_step * 1e-3) / 1e9)
+        if bound == "hbm":
+            db = distinct_row_bytes(w, kv)
+            line["roofline"]["distinct_row_bytes"] = db
+            line["roofline"]["frac_distinct_rows"] = db / 1e9 / (ms_kernel * 1e-3) / hbm
     return line
 
 

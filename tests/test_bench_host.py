@@ -138,3 +138,26 @@ def test_report_line_of_every_path(path):
     assert line["metric"] == {"store": bench.STORE_METRIC, "topk": bench.TOPK_METRIC}.get(path, bench.METRIC)
     assert line["value"] == pytest.approx(w.N / 40e-6) and line["e2e"]["value"] == pytest.approx(w.N / 60e-6)
     assert line["config"]["path"] == path
+
+
+def test_distinct_row_bytes():
+    """Each distinct pool row counted once: equal to the algorithmic bytes
+    when no row repeats, smaller by the repeats' row bytes otherwise."""
+    w = inputs.random_small(3, 6, 4, 64, 1000, [7, 0, 3, 9, 1, 5])
+    assert len(set(w.kv_indices.tolist())) == w.kv_indices.size
+    assert bench.distinct_row_bytes(w) == bench.algorithmic_bytes(w)
+    d = inputs.random_small(4, 6, 4, 64, 8, [7, 0, 3, 9, 1, 5], duplicates=True)
+    repeats = d.kv_indices.size - len(set(d.kv_indices.tolist()))
+    assert repeats > 0
+    assert bench.distinct_row_bytes(d) == bench.algorithmic_bytes(d) - repeats * 64 * 2
+    assert bench.distinct_row_bytes(d, "fp8") == bench.algorithmic_bytes(d, "fp8") - repeats * (64 + 4)
+
+
+def test_report_line_distinct_rows():
+    class Args:
+        steps, warmup, config, kv, path = 10, 3, "h16", "bf16", "decode"
+    w = inputs.config(1)
+    r = {"h2d": 10, "d2h": 20, "clocks": {"sm_mhz": 2070.0}, "launches_per_step": 5}
+    rf = bench.report_line(Args, w, 1, 0.040, 0.020, 0.060, w.N, r)["roofline"]
+    assert rf["distinct_row_bytes"] == bench.distinct_row_bytes(w) <= rf["algorithmic_bytes"]
+    assert rf["frac_distinct_rows"] == pytest.approx(rf["distinct_row_bytes"] / 1e9 / 20e-6 / rf["peak"])
